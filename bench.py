@@ -1,0 +1,440 @@
+"""Benchmark: one decode step of the 32K-context GQA workload on the compressed cache.
+
+A step is the whole online path for one new token: encode (append) the new
+key/value of all 8 KV heads into the paged 4-bit cache, then decode attention
+for the 64 query heads over the 32768 cached tokens.  The metric is GB/s of
+compressed KV the decode reads (32768 tokens x 8 KV heads x 134 B = 35.13 MB per
+step) over the step time.  Prefill encode throughput (Mtokens/s) is reported
+beside it.
+
+Inputs are synthetic and seeded; caches are rotated among 16 distinct copies
+(562 MB in total, above the 129 MB L2) so that every step reads from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (under torch.distributed.run) each rank runs its own replica of the
+workload (independent sequences, no data-path collective: weak scaling); the
+reported value is the bytes all ranks read over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from online_kv_cache_encode_gb300 import workloads as W  # noqa: E402
+
+WORKLOAD = "gqa32k"
+METRIC = "compressed-KV decode-attention GB/s (% of HBM peak); KV encode Mtokens/s"
+N_COPIES = 16
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    import torch
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("tq_decode.cu", "tq_device.cuh", "tq_internal.h"):
+        with open(os.path.join(ROOT, "online_kv_cache_encode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "decode_gqa32k.md")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash()
+    for line in open(p):
+        if line.startswith("traffic_bytes_per_launch:"):
+            parts = line.split()
+            if len(parts) >= 4 and parts[2] == "source" and parts[3] == want:
+                return float(parts[1])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import torch
+    from online_kv_cache_encode_gb300 import tq
+
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[WORKLOAD]
+    T = w.lens[0]
+    hkv, hq, d = w.hkv, w.hq, w.d
+    nb = w.num_blocks()
+    bt_np = W.block_table(w)
+    bt = torch.from_numpy(bt_np).to(dev)
+    lens = torch.tensor([T], dtype=torch.int32, device=dev)
+    bpth = w.bytes_per_token_head()
+    decode_bytes = T * hkv * bpth
+
+    # ---- prefill: encode the context once (timed: encode throughput), then copy to the replicas ----
+    K = torch.from_numpy(W.kv_tokens(w, 0, 0, 0, T)).to(dev, torch.bfloat16)
+    V = torch.from_numpy(W.kv_tokens(w, 1, 0, 0, T)).to(dev, torch.bfloat16)
+    slots = torch.from_numpy(W.slots(w, bt_np, 0, 0, T)).to(dev)
+    status = tq.new_status(dev)
+    base = tq.Cache(nb, hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        base.encode(K, V, slots, status)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_enc = 10
+    e0.record(stream)
+    for _ in range(n_enc):
+        base.encode(K, V, slots, status)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    enc_ms = e0.elapsed_time(e1) / n_enc
+    copies = [base] + [tq.Cache(nb, hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed,
+                                pool=base.pool.clone()) for _ in range(N_COPIES - 1)]
+    del K, V
+
+    # ---- per-step inputs: the new token (position T-1) and the query ----
+    newK = torch.from_numpy(W.kv_tokens(w, 0, 0, T - 1, T)).to(dev, torch.bfloat16)
+    newV = torch.from_numpy(W.kv_tokens(w, 1, 0, T - 1, T)).to(dev, torch.bfloat16)
+    new_slot = torch.from_numpy(W.slots(w, bt_np, 0, T - 1, T)).to(dev)
+    q = torch.from_numpy(W.queries(w, 0)).to(dev, torch.bfloat16)
+    out = torch.empty((1, hq, d), dtype=torch.float32, device=dev)
+    wss = [c.new_workspace(1, hq, bt.shape[1]) for c in copies]
+
+    if args.profile:
+        # three warm-up decode launches, then three to capture (ncu -k regex:decode_kernel -s 3 -c 3)
+        for i in range(6):
+            copies[i % N_COPIES].decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "gqa32k decode", "device_status": int(status.item())}), flush=True)
+        return
+
+    def step(i):
+        c = copies[i % N_COPIES]
+        c.encode(newK, newV, new_slot, status)
+        c.decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    step_ms = t0.elapsed_time(t1) / args.steps
+    launches = 2 * args.steps
+
+    # ---- the decode kernel alone (roofline) ----
+    for i in range(3):
+        copies[i % N_COPIES].decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES])
+    torch.cuda.synchronize()
+    nd = max(args.steps, 20)
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for i in range(nd):
+        copies[i % N_COPIES].decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES])
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dec_ms = d0.elapsed_time(d1) / nd
+
+    # ---- end to end through the public API with host buffers ----
+    hK = newK.cpu().pin_memory()
+    hV = newV.cpu().pin_memory()
+    hq_ = q.cpu().pin_memory()
+    hout = torch.empty_like(out, device="cpu").pin_memory()
+    dK, dV, dq = torch.empty_like(newK), torch.empty_like(newV), torch.empty_like(q)
+
+    def e2e_step(i):
+        dK.copy_(hK, non_blocking=True)
+        dV.copy_(hV, non_blocking=True)
+        dq.copy_(hq_, non_blocking=True)
+        c = copies[i % N_COPIES]
+        c.encode(dK, dV, new_slot, status)
+        c.decode(dq, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
+        hout.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(dist)
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = x0.elapsed_time(x1) / args.steps
+    st = int(status.item())
+
+    step_ms = max_over_ranks(step_ms, dist)
+    e2e_ms = max_over_ranks(e2e_ms, dist)
+    dec_ms = max_over_ranks(dec_ms, dist)
+    enc_ms = max_over_ranks(enc_ms, dist)
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    value = world * decode_bytes / (step_ms * 1e-3) / 1e9
+    achieved = decode_bytes / (dec_ms * 1e-3) / 1e9
+    enc_tokens = T  # tokens (positions) per prefill encode call, all 8 KV heads each
+    enc_bytes = T * hkv * (2 * d * 2 + bpth)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "operands": "4-bit codes as exact fp16 integers, fp16 hi+lo split queries/probabilities, fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) bf16 K/V with 4 x20 outlier channels per KV head and per-token lognormal(0,0.25); N(0,1) bf16 q)",
+        "config": {
+            "workload": "gqa32k: 64 query / 8 KV heads, head_dim 128, 32768-token context, batch 1, "
+                        "4-bit keys and values, 16-token pages in a permuted block table",
+            "step": "encode 1 new token (8 KV heads) + decode attention for 64 query heads over 32768 tokens",
+            "decode_bytes_per_step": decode_bytes,
+            "l2": f"inputs larger than L2: {N_COPIES} distinct caches rotated ({N_COPIES * decode_bytes / 1e6:.0f} MB)",
+            "parallelism": f"replica per GPU x{world}",
+        },
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "roofline": {
+            "kernel": "decode_kernel<4,4,0>",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(),
+            "algorithmic_bytes_per_launch": decode_bytes,
+            "decode_ms": round(dec_ms, 5),
+        },
+        "encode": {
+            "metric": "KV encode Mtokens/s (prefill, 1 token = 8 KV heads of one position)",
+            "value": round(enc_tokens / (enc_ms * 1e-3) / 1e6, 2),
+            "tokens_per_call": enc_tokens,
+            "ms_per_call": round(enc_ms, 5),
+            "achieved_GBps": round(enc_bytes / (enc_ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(enc_bytes / (enc_ms * 1e-3) / 1e9 / peak, 4),
+        },
+        "e2e": {
+            "value": round(world * decode_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 5),
+            "h2d_bytes_per_step": int(newK.numel() * 2 + newV.numel() * 2 + q.numel() * 2),
+            "d2h_bytes_per_step": int(out.numel() * 4),
+        },
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "device_status": st,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+CPU_SAMPLE_TOKENS = 8192   # cpu_baseline: one step over an 8192-token window (about 10-20 s of CPU work)
+REF_SAMPLE_TOKENS = 1024   # reference arm: each step over a 1024-token window (a fraction of a second)
+
+
+def _oracle_sample(w, n_tokens):
+    """Oracle cache holding the first n_tokens of the workload's context, built
+    outside any timed region."""
+    import oracle
+    threads = oracle.set_threads(len(os.sched_getaffinity(0)))
+    bt = W.block_table(w)
+    oc = oracle.Cache(w.d, w.key_bits, w.value_bits, w.qjl_m, w.block_size, w.hkv, w.num_blocks(), w.seed)
+    pool = oc.new_pool()
+    oc.encode(W.kv_tokens(w, 0, 0, 0, n_tokens), W.kv_tokens(w, 1, 0, 0, n_tokens),
+              W.slots(w, bt, 0, 0, n_tokens), pool)
+    return oc, pool, bt, threads
+
+
+def _oracle_step(w, oc, pool, bt, n_tokens):
+    """The step on the oracle: append token n_tokens-1, attend all 64 query heads over n_tokens."""
+    t = n_tokens
+    oc.encode(W.kv_tokens(w, 0, 0, t - 1, t), W.kv_tokens(w, 1, 0, t - 1, t), W.slots(w, bt, 0, t - 1, t), pool)
+    q = W.queries(w, 0).astype(np.float64)
+    out, _ = oc.decode(pool, q, bt, np.array([t], dtype=np.int32), W.sm_scale(w))
+    return out
+
+
+def cpu_baseline(w):
+    n = CPU_SAMPLE_TOKENS
+    oc, pool, bt, threads = _oracle_sample(w, n)
+    t = time.perf_counter()
+    _oracle_step(w, oc, pool, bt, n)
+    dt = time.perf_counter() - t
+    nbytes = n * w.hkv * w.bytes_per_token_head()
+    return {"value": round(nbytes / dt / 1e9, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"one step (append 1 token, attend 64 query heads) over the first {n} of the 32768 "
+                      "context tokens, float64 oracle; its cache pre-encoded by the oracle outside the timing",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return  # the oracle arm runs on rank 0 only
+    w = W.WORKLOADS[WORKLOAD]
+    n = REF_SAMPLE_TOKENS
+    oc, pool, bt, threads = _oracle_sample(w, n)
+    for _ in range(args.warmup):
+        _oracle_step(w, oc, pool, bt, n)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(w, oc, pool, bt, n)
+    dt = (time.perf_counter() - t) / args.steps
+    nbytes = n * w.hkv * w.bytes_per_token_head()
+    v = nbytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": "gqa32k: 64 query / 8 KV heads, head_dim 128, 32768-token context, batch 1, "
+                               "4-bit keys and values, 16-token pages in a permuted block table",
+                   "step": f"oracle: encode 1 new token + decode attention for 64 query heads over a "
+                           f"{n}-token window of the context (bytes counted for that window)"},
+        "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: append + decode over the first {n} context tokens, float64 oracle"},
+        "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="only build the caches and launch the decode kernel 6 times (for ncu)")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,228 @@
+/*
+ * tq.h -- C ABI of the GB300 (sm_103a) online KV-cache compression library.
+ *
+ * The library compresses key/value vectors as they are produced during decode
+ * and runs decode attention straight from the compressed, paged cache.
+ *
+ * Method, as the source pages state it (cited "page title -- section"):
+ *  - Split each key into a norm and a direction, rotate the direction with a
+ *    random sign flip followed by a Walsh-Hadamard transform, and store the
+ *    index of the nearest codeword per coordinate.
+ *      ["TurboQuant: KV Cache Vector Quantization" -- the three steps;
+ *       "OCTOPUS ..." summary -- methodology steps 1-2]
+ *  - The codebook is a per-coordinate Lloyd-Max quantizer for the marginal of
+ *    the rotated direction.  ["OCTOPUS ..." -- key idea; glossary]
+ *  - Values take per-token min-max codes in the rotated frame with an fp16
+ *    scale and zero point.  [TurboQuant deep dive (cell-devlog) -- Step 3]
+ *  - Optionally a 1-bit QJL sketch of the key residual, sign(S r), plus the
+ *    residual norm, gives an unbiased correction to each logit.
+ *      ["OCTOPUS ..." -- contribution "Optional 1-bit QJL residual"; step 8]
+ *  - Attention is softmax(q K^T / sqrt(d_h)) V over the compressed cache
+ *    ["TurboQuant: KV Cache Compression" (Bit-Axon) -- attention under
+ *    quantized KV], computed in the rotated frame without reconstructing keys
+ *    ["OCTOPUS ..." -- TL;DR, step 7; deep dive -- [RHT effect]: the rotation
+ *    preserves inner products].
+ *
+ * Conventions
+ *  - Every data pointer passed to an encode/decode call is a DEVICE pointer
+ *    owned by the caller; the library never frees or reallocates it.  Host
+ *    pointers are marked "host".
+ *  - Calls are asynchronous on the given CUDA stream (`stream` is a
+ *    cudaStream_t; NULL is the legacy default stream).  Errors that the host
+ *    can see are returned at once as a tq_status and nothing is launched.
+ *  - Errors that only the device can see are OR-ed, as TQ_FLAG_* bits, into
+ *    the int32 word at `dev_status` (a device pointer; may be NULL to ignore
+ *    them).  Read it after synchronising.  Kernels never trap and never spin
+ *    without a bound.
+ *  - Tensor layouts are C-contiguous (row-major); sizes are element counts.
+ *
+ * Paged cache layout (bytes; d = head dim, kb/vb = key/value bits, m = QJL
+ * rows, bs = block size in tokens).  One page holds one block of bs token
+ * slots of one KV head; page (block n, KV head h) starts at byte
+ * (n * num_kv_heads + h) * tq_page_bytes(...).  Sections, in order:
+ *      key codes     bs rows of d*kb/8 bytes
+ *      value codes   bs rows of d*vb/8 bytes
+ *      gamma         bs binary16  (key norm)
+ *      value scale   bs binary16
+ *      value zero    bs binary16  (the rotated-frame minimum)
+ *      rho           bs binary16  (QJL residual norm; only if m > 0)
+ *      sigma         bs rows of m/8 bytes (QJL sign bits; only if m > 0)
+ * then zero padding to a multiple of 16 bytes.  Inside a row, code j takes
+ * bits [j*b, j*b + b) of the row read as a little-endian bit string (bit k is
+ * bit k%8 of byte k/8).  Key code j is the index, in increasing order, of the
+ * nearest centroid to rotated direction coordinate j (an exact tie goes to the
+ * lower index).  Sigma bit i is 1 iff (S r)_i >= 0.
+ * 4/4-bit keys/values take 134 bytes per token and KV head, 3/3-bit 102, and
+ * 2/2-bit with m = 128 take 88.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define TQ_API
+#else
+#define TQ_API __attribute__((visibility("default")))
+#endif
+
+/* Host-visible result of every call. */
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_INVALID_ARG = 1, /* a NULL pointer, a negative size, a shape that does not fit */
+    TQ_ERR_UNSUPPORTED = 2, /* valid in principle, not built (e.g. head dim != 128) */
+    TQ_ERR_CUDA = 3,        /* a CUDA runtime call failed; tq_last_error() has the text */
+    TQ_ERR_WORKSPACE = 4    /* the workspace passed to decode is too small */
+} tq_status;
+
+/* Device-detected conditions, OR-ed into *dev_status. */
+#define TQ_FLAG_OVERFLOW 1  /* a norm, scale, zero or rho exceeded the fp16 range (stored as inf) */
+#define TQ_FLAG_BAD_SLOT 2  /* a slot or block id outside the pool; that token/page was skipped */
+#define TQ_FLAG_NONFINITE 4 /* a key or value held NaN or inf; its codes are unspecified */
+#define TQ_FLAG_TIMEOUT 8   /* a bounded device wait gave up; the output is incomplete */
+
+/* Element type of K, V and q inputs. */
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
+
+/* ---------------------------------------------------------------------- */
+/* Codebook                                                                */
+/* ---------------------------------------------------------------------- */
+
+/* Opaque, library-owned Lloyd-Max codebook for one (d, bits). */
+typedef struct tq_codebook tq_codebook;
+
+/* Fit the per-coordinate Lloyd-Max codebook for the marginal density of one
+ * coordinate of a uniform point on the unit sphere S^{d-1},
+ *     f(x) proportional to (1 - x^2)^((d-3)/2) on [-1, 1],
+ * by Lloyd's iteration (boundaries at centroid midpoints, centroids at cell
+ * conditional means) from evenly spaced starting centroids until no centroid
+ * moves by 1e-14 (at most 10000 passes).  Host only; touches no GPU.
+ * ["OCTOPUS ..." -- key idea: per-coordinate Lloyd-Max over the marginals;
+ *  glossary "Lloyd-Max quantization"]
+ * d: even, 4..1024.  bits: 1..8.  *out receives a handle the caller frees
+ * with tq_codebook_free.  Returns TQ_ERR_INVALID_ARG for other d or bits. */
+TQ_API tq_status tq_codebook_init(int d, int bits, tq_codebook** out);
+
+/* Copy the codebook to host arrays: centroids[2^bits] (increasing),
+ * boundaries[2^bits - 1] (midpoints), *passes = Lloyd passes run.  Any output
+ * pointer may be NULL. */
+TQ_API tq_status tq_codebook_get(const tq_codebook* cb, double* centroids, double* boundaries,
+                                 int* passes);
+
+TQ_API void tq_codebook_free(tq_codebook* cb);
+
+/* ---------------------------------------------------------------------- */
+/* Cache                                                                   */
+/* ---------------------------------------------------------------------- */
+
+/* Opaque view over a caller-owned page pool plus the method constants (the
+ * codebook, the rotation signs s and, when qjl_m > 0, the m x d Gaussian
+ * matrix S, which the library keeps in device memory it owns). */
+typedef struct tq_cache tq_cache;
+
+/* Bytes of one page (block_size token slots of one KV head), as laid out
+ * above.  Returns -1 for an invalid combination. */
+TQ_API int64_t tq_page_bytes(int d, int key_bits, int value_bits, int qjl_m, int block_size);
+
+/* Describe a cache over `pool` (device, num_blocks * num_kv_heads *
+ * tq_page_bytes(...) bytes, 16-byte aligned, caller-owned) and derive the
+ * method constants from `seed`:
+ *   s_j  = +1 if the top bit of z_j(seed, 0) is clear, else -1   (j < d)
+ *   S_ij = sqrt(-2 ln u1) cos(2 pi u2), u1 = ((z_{2n}(seed,1) >> 11) + 1) 2^-53,
+ *          u2 = (z_{2n+1}(seed,1) >> 11) 2^-53, n = i*d + j          (i < m)
+ * where z_i(seed, tag) = mix(seed ^ tag*0xD1B54A32D192ED03 + (i+1)*0x9E3779B97F4A7C15)
+ * and mix is the SplitMix64 finaliser (Steele, Lea, Flood 2014).  The pages
+ * draw the signs from a seed [deep dive -- Step 1: RHT] with torch's
+ * generator, which is not reproduced.
+ * Supported on the GPU path: d = 128, block_size = 16, key_bits and
+ * value_bits in {2, 3, 4}, qjl_m in {0, 128}; anything else returns
+ * TQ_ERR_UNSUPPORTED.  Uses the current CUDA device. */
+TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size, int num_kv_heads,
+                                 int d, int key_bits, int value_bits, int qjl_m, uint64_t seed,
+                                 tq_cache** out);
+
+TQ_API void tq_cache_free(tq_cache* cache);
+
+/* The constants a seed defines, derived on the host without a GPU (the same
+ * derivation tq_cache_create performs): signs[d] as +-1 and, if m > 0 and S is
+ * not NULL, S[m*d] row-major in double.  d: 1..4096, m: 0..4096. */
+TQ_API tq_status tq_method_constants(int d, int m, uint64_t seed, int8_t* signs, double* S);
+
+/* Host copies of the derived constants (tests): signs[d] as +-1, S[m*d]
+ * row-major in double (the device holds it in fp32). */
+TQ_API tq_status tq_cache_signs(const tq_cache* cache, int8_t* signs);
+TQ_API tq_status tq_cache_gaussian(const tq_cache* cache, double* S);
+
+/* ---------------------------------------------------------------------- */
+/* Encode (append)                                                         */
+/* ---------------------------------------------------------------------- */
+
+/* Compress num_tokens new tokens into the cache.
+ * K, V: device, [num_tokens, num_kv_heads, d] of `dtype`.
+ * slot_mapping: device int64 [num_tokens]; slot = block * block_size + offset.
+ *   A negative slot skips the token; a slot past the pool sets
+ *   TQ_FLAG_BAD_SLOT and skips it.
+ * For each (token, KV head):
+ *   key:   gamma = ||k|| (fp32) stored as fp16; u_rot = R k / gamma with
+ *          R = H diag(s) / sqrt(d); code_j = #{boundaries < u_rot[j]};
+ *          if qjl_m > 0: r = u_rot - C[code], rho = ||r|| as fp16,
+ *          sigma_i = [(S r)_i >= 0].  A zero key stores codes 2^(kb-1) - 1,
+ *          rho 0 and all sigma bits 1.
+ *   value: v_rot = R v; mn = min, mx = max over coordinates; scale =
+ *          (mx - mn)/(2^vb - 1); code = clamp(round-half-even((v_rot - mn) /
+ *          scale), 0, 2^vb - 1) (all 0 if scale == 0); scale, mn as fp16.
+ * [three steps (split/rotate/codebook); Bit-Axon -- quantization function;
+ *  deep dive -- Step 1 (RHT), Step 3 (value codes); "OCTOPUS ..." -- step 8]
+ * Tokens that map to the same slot race; the last writer is unspecified. */
+TQ_API tq_status tq_encode_kv(const tq_cache* cache, const void* K, const void* V, tq_dtype dtype,
+                              int64_t num_tokens, const int64_t* slot_mapping, int32_t* dev_status,
+                              void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* Decode attention                                                        */
+/* ---------------------------------------------------------------------- */
+
+/* Workspace bytes tq_decode_attention needs for this batch shape (split-K
+ * partials plus one counter per sequence and KV head).  The workspace must
+ * be zero-filled once before its first use; each call leaves its counters at
+ * zero again on completion, so a workspace can be reused by later calls on
+ * the same stream without clearing.  Two calls in flight at once must not
+ * share a workspace. */
+TQ_API size_t tq_decode_workspace_bytes(const tq_cache* cache, int batch, int num_q_heads,
+                                        int max_blocks_per_seq);
+
+/* One query token per sequence over its cached tokens:
+ *   out[b, hq] = sum_t softmax_t(l_t) V^_t,  t < lens[b],
+ *   l_t = sm_scale * gamma_t * ( <R q, C[code_t]>
+ *                                + sqrt(pi/2)/m * rho_t * <S R q, 2 sigma_t - 1> )  [QJL term if m > 0]
+ *   V^_t = R^T (scale_t * vcode_t + zero_t),
+ * with the KV head of query head hq being hq / (num_q_heads / num_kv_heads)
+ * and token t in block block_table[b * max_blocks_per_seq + t / block_size],
+ * slot t % block_size.  Logits and values are formed in the rotated frame;
+ * keys are never reconstructed; one inverse rotation is applied per output.
+ * q: device [batch, num_q_heads, d] of `dtype`.  block_table: device int32.
+ * lens: device int32 [batch]; a zero length yields a zero output row.
+ * out: device fp32 [batch, num_q_heads, d].  sm_scale: normally 1/sqrt(d).
+ * workspace: device, at least tq_decode_workspace_bytes(...) bytes.
+ * num_q_heads must be a multiple of num_kv_heads with a group size <= 8.
+ * A block id outside the pool sets TQ_FLAG_BAD_SLOT and its page is skipped. */
+TQ_API tq_status tq_decode_attention(const tq_cache* cache, const void* q, tq_dtype dtype, int batch,
+                                     int num_q_heads, const int32_t* block_table,
+                                     int max_blocks_per_seq, const int32_t* lens, float sm_scale,
+                                     float* out, void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, void* stream);
+
+/* Text for a status code, and the detail of the last failure on this thread. */
+TQ_API const char* tq_status_string(tq_status s);
+TQ_API const char* tq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

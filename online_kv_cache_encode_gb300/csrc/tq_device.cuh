@@ -1,0 +1,116 @@
+// Device helpers shared by the encode and decode kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+__device__ __forceinline__ void flag(int32_t* status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// Four consecutive elements starting at element index i of a row.
+__device__ __forceinline__ void load4(const void* base, int dtype, int64_t i, float x[4]) {
+    if (dtype == TQ_F32) {
+        float4 v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i);
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+        uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + i);
+        if (dtype == TQ_BF16) {
+            x[0] = __uint_as_float(v.x << 16);
+            x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+            x[2] = __uint_as_float(v.y << 16);
+            x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+        } else {
+            __half2 a = *reinterpret_cast<__half2*>(&v.x), b = *reinterpret_cast<__half2*>(&v.y);
+            float2 fa = __half22float2(a), fb = __half22float2(b);
+            x[0] = fa.x; x[1] = fa.y; x[2] = fb.x; x[3] = fb.y;
+        }
+    }
+}
+
+// The 4 sign bits of coordinates 4*lane .. 4*lane+3 (bit i set: s = -1).
+__device__ __forceinline__ uint32_t lane_signs(const Consts& c, int lane) {
+    return (c.sign_bits[lane >> 3] >> (4 * (lane & 7))) & 0xFu;
+}
+
+__device__ __forceinline__ void apply_signs(float x[4], uint32_t sm) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if ((sm >> i) & 1u) x[i] = -x[i];
+}
+
+// Unnormalised natural-order Walsh-Hadamard transform of a 128-vector spread
+// over a warp, lane holding coordinates 4*lane .. 4*lane+3: butterflies of
+// stride 1 and 2 inside the lane, strides 4..64 across lanes (the lower index
+// takes a+b, the upper a-b).
+__device__ __forceinline__ void fwht128(float x[4], int lane) {
+    float a = x[0] + x[1], b = x[0] - x[1], c = x[2] + x[3], d = x[2] - x[3];
+    x[0] = a + c; x[2] = a - c; x[1] = b + d; x[3] = b - d;
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int m = 1 << k;
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float y = __shfl_xor_sync(0xffffffffu, x[i], m);
+            x[i] = upper ? (y - x[i]) : (x[i] + y);
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int m = 16; m; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int m = 16; m; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+    for (int m = 16; m; m >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t f16_bits(float x) {
+    __half h = __float2half_rn(x);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Write a row of 128 B-bit codes, lane holding the 4 codes of coordinates
+// 4*lane .. 4*lane+3 packed LSB-first in p (4*B bits).  Code j occupies bits
+// [j*B, j*B + B) of the row; lanes below 4*B each store one 32-bit word.
+template <int B>
+__device__ __forceinline__ void store_code_row(uint8_t* row, uint32_t p, int lane) {
+    constexpr int LB = 4 * B;  // bits per lane
+    constexpr int WORDS = 4 * B;
+    uint32_t word = 0;
+    const int src0 = (lane * 32) / LB;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int src = src0 + k;
+        const uint32_t pv = __shfl_sync(0xffffffffu, p, src < 32 ? src : 31);
+        const int shift = src * LB - lane * 32;
+        if (src < 32) {
+            if (shift >= 0 && shift < 32) word |= pv << shift;
+            else if (shift < 0 && shift > -LB) word |= pv >> (-shift);
+        }
+    }
+    if (lane < WORDS) reinterpret_cast<uint32_t*>(row)[lane] = word;
+}
+
+}  // namespace tq

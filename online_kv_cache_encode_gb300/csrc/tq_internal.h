@@ -1,0 +1,94 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int kHeadDim = 128;   // the one head dimension the kernels are built for
+constexpr int kBlockSize = 16;  // tokens per page
+constexpr int kMaxCodebook = 16;
+
+// Byte layout of one page (one block of kBlockSize slots of one KV head).
+struct Geometry {
+    int d, kb, vb, m, bs, hkv;
+    int64_t num_blocks;
+    int64_t page_bytes;
+    int kcode_off, vcode_off, gam_off, scl_off, zer_off, rho_off, sig_off;
+};
+
+Geometry make_geometry(int d, int kb, int vb, int m, int bs, int hkv, int64_t num_blocks);
+
+// Method constants the kernels take by value.
+struct Consts {
+    float boundary[kMaxCodebook];  // key decision boundaries (2^kb - 1 used)
+    float centroid[kMaxCodebook];  // key centroids (fp32), used by the QJL residual
+    // Decode splits each centroid as C[c] = alpha * (c - (2^kb - 1)/2) + rem[c]:
+    // the linear part goes through the tensor cores on the exact integer code,
+    // rem[c] (binary16 bits) is looked up.
+    float alpha;
+    uint16_t rem_f16[kMaxCodebook];
+    uint32_t sign_bits[kHeadDim / 32];  // bit j set when s_j = -1
+};
+
+struct EncodeArgs {
+    Geometry g;
+    Consts c;
+    uint8_t* pool;
+    const void* K;
+    const void* V;
+    int dtype;
+    int64_t num_tokens;
+    const int64_t* slot_mapping;
+    int32_t* status;
+    const float* S;  // m x d fp32, device (QJL only)
+};
+
+struct DecodeArgs {
+    Geometry g;
+    Consts c;
+    const uint8_t* pool;
+    const void* q;
+    int dtype;
+    int batch, hq, group;
+    const int32_t* block_table;
+    int max_blocks;
+    const int32_t* lens;
+    float sm_scale_log2;  // sm_scale * log2(e)
+    float* out;
+    float* partials;      // [batch, hkv, splits, group, 4 + d]
+    unsigned* counters;   // [batch, hkv]
+    int pages_per_split;
+    int num_splits;
+    int32_t* status;
+    const float* S;
+};
+
+// Launchers (return a cudaError_t as int).
+int launch_encode(const EncodeArgs& a, int num_sms, void* stream);
+int launch_decode(const DecodeArgs& a, void* stream);
+int decode_smem_bytes(const Geometry& g);
+
+void set_error(const char* fmt, ...);
+
+}  // namespace tq
+
+struct tq_codebook {
+    int d, bits, passes;
+    double centroid[256];
+    double boundary[255];
+};
+
+struct tq_cache {
+    void* pool;
+    tq::Geometry g;
+    tq::Consts c;
+    uint64_t seed;
+    int8_t signs[tq::kHeadDim];
+    double* S_host;   // m x d
+    float* S_dev;     // m x d, library-owned device memory
+    int device;
+    int num_sms;
+};

@@ -1,0 +1,221 @@
+"""Parity harness: run a workload through the CUDA library and through the
+oracle on the same seeded inputs, and compare at the stated tolerances.
+
+  (a) codes bit-exact, except coordinates within 1e-5 of a decision boundary
+      (rotated-direction units for keys, code steps for values, |(S r)_i| /
+      (||S_i|| rho) for QJL bits); such mismatches stay under 1e-5 of all
+      coordinates;
+  (b) fp16 norm, scale, zero and rho within 1 fp16 ulp;
+  (c) decode output: max over query heads of ||gpu - oracle||_inf /
+      ||oracle||_inf <= 2e-3, both sides reading the identical compressed cache
+      (the oracle's own encoding of the inputs).
+
+Pages are unpacked here with numpy from the layout the header documents, a
+reader independent of both implementations.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from online_kv_cache_encode_gb300 import workloads as W
+
+BOUNDARY_TOL = 1e-5
+MISMATCH_FRACTION = 1e-5
+DECODE_RTOL = 2e-3
+
+
+class Layout:
+    def __init__(self, d, kb, vb, m, bs, hkv, page_bytes):
+        self.d, self.kb, self.vb, self.m, self.bs, self.hkv = d, kb, vb, m, bs, hkv
+        self.page_bytes = page_bytes
+        off = 0
+        self.k = off; off += bs * d * kb // 8
+        self.v = off; off += bs * d * vb // 8
+        self.g = off; off += 2 * bs
+        self.s = off; off += 2 * bs
+        self.z = off; off += 2 * bs
+        if m:
+            self.r = off; off += 2 * bs
+            self.sig = off; off += bs * m // 8
+        assert (off + 15) // 16 * 16 == page_bytes
+
+
+def unpack(pool: np.ndarray, L: Layout, slots: np.ndarray, heads: np.ndarray) -> dict:
+    """Fields of the given (slot, head) pairs: codes as int arrays, fp16 as raw uint16."""
+    blk, off = slots // L.bs, slots % L.bs
+    page = (blk * L.hkv + heads) * L.page_bytes
+
+    def rows(base, nbytes):
+        idx = (page + base + off * nbytes)[:, None] + np.arange(nbytes)[None, :]
+        return pool[idx]
+
+    def codes(base, b):
+        bits = np.unpackbits(rows(base, L.d * b // 8), axis=1, bitorder="little")
+        bits = bits.reshape(len(slots), L.d, b).astype(np.int64)
+        return (bits << np.arange(b)[None, None, :]).sum(axis=2)
+
+    def f16(base):
+        idx = (page + base + 2 * off)[:, None] + np.arange(2)[None, :]
+        return pool[idx].copy().view(np.uint16)[:, 0]
+
+    out = dict(k=codes(L.k, L.kb), v=codes(L.v, L.vb), gamma=f16(L.g), scale=f16(L.s), zero=f16(L.z))
+    if L.m:
+        out["rho"] = f16(L.r)
+        out["sig"] = np.unpackbits(rows(L.sig, L.m // 8), axis=1, bitorder="little").astype(np.int64)
+    return out
+
+
+def _ordered(h: np.ndarray) -> np.ndarray:
+    """fp16 bit patterns mapped to integers that step by one per representable value."""
+    h = h.astype(np.int64)
+    return np.where(h & 0x8000, -(h & 0x7FFF), h)
+
+
+def _inputs(w):
+    K = [W.kv_tokens(w, 0, b, 0, w.lens[b]) for b in range(w.batch)]
+    V = [W.kv_tokens(w, 1, b, 0, w.lens[b]) for b in range(w.batch)]
+    return K, V
+
+
+def run_case(w, oracle, tq, q_step: int = 0, decode_gpu_pool: bool = True, decode: bool = True) -> dict:
+    """Encode the workload's prefill on both sides, compare; decode one step on both, compare."""
+    import torch
+
+    dev = torch.device("cuda")
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    bt = W.block_table(w)
+    nb = w.num_blocks()
+    K, V = _inputs(w)
+    slots = [W.slots(w, bt, b, 0, w.lens[b]) for b in range(w.batch)]
+
+    # ---- oracle ----
+    oc = oracle.Cache(w.d, w.key_bits, w.value_bits, w.qjl_m, w.block_size, w.hkv, nb, w.seed)
+    pool_o = oc.new_pool()
+    st_o = 0
+    for b in range(w.batch):
+        st_o |= oc.encode(K[b], V[b], slots[b], pool_o)
+
+    # ---- GPU encode ----
+    gc = tq.Cache(nb, w.hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed, w.block_size, w.d)
+    status = tq.new_status()
+    Kt = torch.from_numpy(np.concatenate(K)).to(dev, tdt).contiguous()
+    Vt = torch.from_numpy(np.concatenate(V)).to(dev, tdt).contiguous()
+    sm = torch.from_numpy(np.concatenate(slots)).to(dev)
+    gc.encode(Kt, Vt, sm, status)
+    torch.cuda.synchronize()
+    pool_g = gc.pool.cpu().numpy()
+    st_g = int(status.item())
+
+    L = Layout(w.d, w.key_bits, w.value_bits, w.qjl_m, w.block_size, w.hkv, oc.page_bytes)
+    all_slots = np.repeat(np.concatenate(slots), w.hkv)
+    all_heads = np.tile(np.arange(w.hkv), len(all_slots) // w.hkv)
+    fo = unpack(pool_o, L, all_slots, all_heads)
+    fg = unpack(pool_g, L, all_slots, all_heads)
+    kin = np.concatenate(K).reshape(-1, w.d).astype(np.float64)
+    vin = np.concatenate(V).reshape(-1, w.d).astype(np.float64)
+    enc = compare_encode(fo, fg, kin, vin, oc, oracle)
+    enc["status_oracle"], enc["status_gpu"] = st_o, st_g
+    # bytes outside the written slots (padding, other slots) must be equal
+    mask = np.ones(pool_o.size, dtype=bool)
+    for sl, hh in ((all_slots, all_heads),):
+        page = (sl // L.bs * L.hkv + hh) * L.page_bytes
+        for base, nbytes in [(L.k, w.d * w.key_bits // 8), (L.v, w.d * w.value_bits // 8),
+                             (L.g, 2), (L.s, 2), (L.z, 2)] + ([(L.r, 2), (L.sig, w.qjl_m // 8)] if w.qjl_m else []):
+            idx = (page + base + (sl % L.bs) * nbytes)[:, None] + np.arange(nbytes)[None, :]
+            mask[idx.ravel()] = False
+    enc["other_bytes_equal"] = bool(np.array_equal(pool_o[mask], pool_g[mask]))
+
+    if not decode:
+        return dict(enc=enc, dec=None, w=w)
+    # ---- decode one step on the oracle's cache, both sides ----
+    q = W.queries(w, q_step)
+    lens = np.array(w.lens, dtype=np.int32)
+    smv = W.sm_scale(w)
+    out_o, dst_o = oc.decode(pool_o, q.astype(np.float64), bt, lens, smv)
+    gc_o = tq.Cache(nb, w.hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed, w.block_size, w.d,
+                    pool=torch.from_numpy(pool_o).to(dev))
+    qt = torch.from_numpy(q).to(dev, tdt).contiguous()
+    btt = torch.from_numpy(bt).to(dev)
+    lt = torch.from_numpy(lens).to(dev)
+    dstatus = tq.new_status()
+    out_g = gc_o.decode(qt, btt, lt, smv, status=dstatus).cpu().numpy().astype(np.float64)
+    dec = dict(rel_err=rel_err(out_g, out_o), status_gpu=int(dstatus.item()), status_oracle=dst_o,
+               out_gpu=out_g, out_oracle=out_o)
+    if decode_gpu_pool:
+        # end to end: the GPU's own cache through the GPU decode vs the oracle end to end
+        out_gg = gc.decode(qt, btt, lt, smv).cpu().numpy().astype(np.float64)
+        dec["rel_err_end_to_end"] = rel_err(out_gg, out_o)
+    torch.cuda.synchronize()
+    return dict(enc=enc, dec=dec, w=w)
+
+
+def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
+    """max over query heads of ||got - ref||_inf / ||ref||_inf."""
+    num = np.abs(got - ref).max(axis=-1)
+    den = np.abs(ref).max(axis=-1)
+    den = np.where(den == 0, 1.0, den)
+    return float((num / den).max())
+
+
+def compare_encode(fo, fg, kin, vin, oc, oracle) -> dict:
+    n_vec, d = fo["k"].shape
+    res = {}
+    # keys
+    kmis = np.argwhere(fo["k"] != fg["k"])
+    bad_k = 0
+    for vi, j in kmis:
+        k = kin[vi]
+        u = oracle.rotate(oc.s, k / np.linalg.norm(k))
+        if np.min(np.abs(u[j] - oc.T)) > BOUNDARY_TOL:
+            bad_k += 1
+    res["key_mismatch"], res["key_mismatch_far"] = len(kmis), bad_k
+    # values
+    vmis = np.argwhere(fo["v"] != fg["v"])
+    bad_v = 0
+    for vi, j in vmis:
+        vr = oracle.rotate(oc.s, vin[vi])
+        sc = (vr.max() - vr.min()) / ((1 << oc.vb) - 1)
+        x = (vr[j] - vr.min()) / sc
+        if abs((x - math.floor(x)) - 0.5) > BOUNDARY_TOL or abs(int(fo["v"][vi, j]) - int(fg["v"][vi, j])) > 1:
+            bad_v += 1
+    res["val_mismatch"], res["val_mismatch_far"] = len(vmis), bad_v
+    res["coords"] = 2 * n_vec * d
+    # fp16 fields
+    for f in ("gamma", "scale", "zero") + (("rho",) if "rho" in fo else ()):
+        res[f + "_max_ulp"] = int(np.abs(_ordered(fo[f]) - _ordered(fg[f])).max()) if n_vec else 0
+    if "sig" in fo:
+        ok_rows = np.all(fo["k"] == fg["k"], axis=1)
+        smis = np.argwhere((fo["sig"] != fg["sig"]) & ok_rows[:, None])
+        bad_s = 0
+        for vi, i in smis:
+            k = kin[vi]
+            g = np.linalg.norm(k)
+            u = oracle.rotate(oc.s, k / g)
+            r = u - oc.C[fo["k"][vi]]
+            if abs(oc.S[i] @ r) > BOUNDARY_TOL * np.linalg.norm(oc.S[i]) * np.linalg.norm(r):
+                bad_s += 1
+        res["sig_mismatch"], res["sig_mismatch_far"] = len(smis), bad_s
+        res["sig_rows_skipped"] = int((~ok_rows).sum())
+    return res
+
+
+def assert_encode_parity(res: dict):
+    e = res["enc"]
+    assert e["status_gpu"] == e["status_oracle"], e
+    assert e["key_mismatch_far"] == 0 and e["val_mismatch_far"] == 0, e
+    assert e["key_mismatch"] + e["val_mismatch"] <= MISMATCH_FRACTION * e["coords"], e
+    for f in ("gamma", "scale", "zero", "rho"):
+        if f + "_max_ulp" in e:
+            assert e[f + "_max_ulp"] <= 1, (f, e)
+    if "sig_mismatch" in e:
+        assert e["sig_mismatch_far"] == 0, e
+    assert e["other_bytes_equal"], e
+
+
+def assert_decode_parity(res: dict):
+    d = res["dec"]
+    assert d["status_gpu"] == d["status_oracle"] == 0, d
+    assert np.all(np.isfinite(d["out_gpu"]))
+    assert d["rel_err"] <= DECODE_RTOL, d["rel_err"]
