@@ -119,7 +119,7 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.index),
                  "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "100"],
+                 "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -133,6 +133,16 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.fh.close()
+
+    def count(self) -> int:
+        if self.proc is None:
+            return 0
+        self.fh.flush()
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
 
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
@@ -220,18 +230,30 @@ def run_ours(args, rank, world, local):
         c.encode(newK, newV, new_slot, status)
         c.decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    barrier(dist)
-    torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        # the sampler sees the GPU under this same load before and after the timed region
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        deadline = time.time() + 3.0
+        while clk.count() < 3 and time.time() < deadline:
+            for i in range(50):
+                step(i)
+            torch.cuda.synchronize()
+        barrier(dist)
+        torch.cuda.synchronize()
         t0.record(stream)
         for i in range(args.steps):
             step(i)
         t1.record(stream)
         torch.cuda.synchronize()
+        n_before = clk.count()
+        deadline = time.time() + 1.0
+        while clk.count() <= n_before and time.time() < deadline:
+            for i in range(50):
+                step(i)
+            torch.cuda.synchronize()
     barrier(dist)
     torch.cuda.synchronize()
     step_ms = t0.elapsed_time(t1) / args.steps

@@ -33,7 +33,7 @@ namespace tq {
 constexpr int kNCW = 8;                       // consumer warps
 constexpr int kThreads = (kNCW + 1) * 32;     // + producer warp
 constexpr int kLutBytes = 256 * 256;          // 256 entries x 256 B (lanes use 128 B)
-constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s bound on any wait
+constexpr long long kWaitCycles = 3000000000ll;  // bound on any wait: ~1.5 s at 2 GHz
 // split partial record: max, sum, 2 pad, acc[128] (keeps the acc 16-byte aligned)
 constexpr int kPartStride = 4 + kHeadDim;
 
@@ -61,13 +61,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for the phase of the given parity; gives up after kWaitNs.
+// Wait for the phase of the given parity.  Spins on try_wait and looks at the
+// SM cycle counter only every 256 tries; gives up after kWaitCycles (about a
+// second or two at GB300 clocks).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (!mbar_try(bar, parity))
-        if (global_ns() - t0 > kWaitNs) return false;
-    return true;
+    const long long t0 = clock64();
+    for (;;) {
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try(bar, parity)) return true;
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile(
@@ -79,6 +83,26 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float lds_h2f(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return __half2float(__ushort_as_half(v));
 }
 __device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t m, uint32_t o) {
     return (a & m) | o;
@@ -141,7 +165,7 @@ __device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t f[4]) {
 // shared memory map (dynamic)
 // ---------------------------------------------------------------------------
 struct SmemMap {
-    int lut, qrot, qoff, bars, ok, ring;
+    int lut, qrot, qoff, sq, bars, ok, ring;
     int stages, stride, total;
 };
 
@@ -151,6 +175,7 @@ __host__ __device__ inline SmemMap smem_map(int page_bytes) {
     m.lut = off; off += kLutBytes;
     m.qrot = off; off += 8 * kHeadDim * 4;
     m.qoff = off; off += 8 * 4;
+    m.sq = off; off += 8 * kHeadDim * 4;
     m.stride = (page_bytes + 127) / 128 * 128;
     const int budget = 227 * 1024 - 1024;
     int fixed = off + 64;
@@ -167,11 +192,123 @@ __host__ __device__ inline SmemMap smem_map(int page_bytes) {
 int decode_smem_bytes(const Geometry& g) { return smem_map((int)g.page_bytes).total; }
 
 // ---------------------------------------------------------------------------
+// code unpacking: every key / value code becomes an exact small integer in
+// fp16 (the 0x6400 "1024 + x" bit pattern, then the 1024 removed exactly)
+// ---------------------------------------------------------------------------
+// sixteen 2-bit codes c0..c15 of w (c_i at bits 2i) -> eight fp16x2 (c_i, c_{i+8})
+__device__ __forceinline__ void crumb16_to_h2(uint32_t w, uint32_t f[8]) {
+    const uint32_t magic = 0x64006400u;
+    const uint32_t scale[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};  // 1, 1/4, 1/16, 1/64
+    const uint32_t bias[4] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u};   // -1024, -256, -64, -16
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t x = (i < 4) ? w : (w >> 8);
+        const int k = i & 3;
+        f[i] = hfma2(lop_and_or(x, 0x00030003u << (2 * k), magic), scale[k], bias[k]);
+    }
+}
+
+// bits [pos, pos + n) of a little-endian multi-word bit string (pos, n compile-time after unrolling)
+template <int NW>
+__device__ __forceinline__ uint32_t bits_at(const uint32_t (&w)[NW], int pos, int n) {
+    const int wi = pos >> 5, sh = pos & 31;
+    uint32_t x = (sh + n <= 32 || wi + 1 >= NW) ? (w[wi] >> sh) : __funnelshift_r(w[wi], w[wi + 1], sh);
+    return x & ((1u << n) - 1u);
+}
+
+__device__ __forceinline__ uint32_t int_pair_h2(uint32_t c0, uint32_t c1) {
+    return hsub2((c0 | (c1 << 16)) | 0x64006400u, 0x64006400u);
+}
+
+// Key chunk of one token (the 32 codes of dims 32qd .. 32qd+31, 4*KB bytes):
+// I[n] = codes of dims key_int_dim(n, 0/1) as exact fp16 integers,
+// R[n] = (rem[c_{2n}], rem[c_{2n+1}]) from the lane-private table.
+template <int KB>
+__host__ __device__ constexpr int key_int_dim(int n, int half) {
+    return KB == 4 ? 8 * (n >> 2) + (n & 3) + 4 * half
+         : KB == 2 ? 16 * (n >> 3) + (n & 7) + 8 * half
+                   : 2 * n + half;
+}
+
+template <int KB>
+__device__ __forceinline__ void key_chunk(uint32_t row, int qd, uint32_t lut, uint32_t lane,
+                                          uint32_t I[16], uint32_t R[16]) {
+    uint32_t w[KB];
+    if constexpr (KB == 4) {
+        const uint4 v = lds128(row + qd * 16);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) nib8_to_h2(w[i], &I[4 * i]);
+        const uint32_t lw = lane << 2;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            const uint32_t addr = lut + prmt(w[n >> 2], lw, 0x5504u | ((uint32_t)(n & 3) << 4));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(R[n]) : "r"(addr));
+        }
+    } else if constexpr (KB == 2) {
+        const uint2 v = lds64(row + qd * 8);
+        w[0] = v.x; w[1] = v.y;
+        crumb16_to_h2(w[0], &I[0]);
+        crumb16_to_h2(w[1], &I[8]);
+        const uint32_t lw = lane << 3;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t addr = lut + prmt(w[j >> 2], lw, 0x5504u | ((uint32_t)(j & 3) << 4));
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(R[2 * j]), "=r"(R[2 * j + 1]) : "r"(addr));
+        }
+    } else {
+        w[0] = lds32(row + qd * 12); w[1] = lds32(row + qd * 12 + 4); w[2] = lds32(row + qd * 12 + 8);
+        const uint32_t lw = lane << 2;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            const uint32_t t = bits_at<3>(w, 6 * n, 6);
+            I[n] = int_pair_h2(t & 7u, t >> 3);
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(R[n]) : "r"(lut + (t << 7) + lw));
+        }
+    }
+}
+
+// Value codes of dims 16r .. 16r+15 for a token pair (ta, tb): P[i] = (code_ta, code_tb)
+// of dim 16r + i as exact fp16 integers.
+template <int VB>
+__device__ __forceinline__ void value_pair(uint32_t vbase, int r, int ta, int tb, uint32_t P[16]) {
+    constexpr int ROW = kHeadDim * VB / 8;
+    if constexpr (VB == 4) {
+        const uint2 va = lds64(vbase + ta * ROW + r * 8);
+        const uint2 vb = lds64(vbase + tb * ROW + r * 8);
+        nib8_to_h2(prmt(va.x, vb.x, 0x5410u), &P[0]);
+        nib8_to_h2(prmt(va.x, vb.x, 0x7632u), &P[4]);
+        nib8_to_h2(prmt(va.y, vb.y, 0x5410u), &P[8]);
+        nib8_to_h2(prmt(va.y, vb.y, 0x7632u), &P[12]);
+    } else if constexpr (VB == 2) {
+        const uint32_t wa = lds32(vbase + ta * ROW + r * 4);
+        const uint32_t wb = lds32(vbase + tb * ROW + r * 4);
+        crumb16_to_h2(prmt(wa, wb, 0x5410u), &P[0]);
+        crumb16_to_h2(prmt(wa, wb, 0x7632u), &P[8]);
+    } else {
+        const int base = (6 * r) & ~3, sh = ((6 * r) & 3) * 8;
+        const uint32_t a0 = lds32(vbase + ta * ROW + base), a1 = lds32(vbase + ta * ROW + base + 4);
+        const uint32_t b0 = lds32(vbase + tb * ROW + base), b1 = lds32(vbase + tb * ROW + base + 4);
+        const uint32_t xa[2] = {__funnelshift_r(a0, a1, sh), a1 >> sh};
+        const uint32_t xb[2] = {__funnelshift_r(b0, b1, sh), b1 >> sh};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) P[i] = int_pair_h2(bits_at<2>(xa, 3 * i, 3), bits_at<2>(xb, 3 * i, 3));
+    }
+}
+
+// QJL sign bits of one token (bits 32qd .. 32qd+31 of its sigma row):
+// Z[n] = (+-1 for bit n, +-1 for bit n+16) in fp16.
+__device__ __forceinline__ void sign_chunk(uint32_t w, uint32_t Z[16]) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n) Z[n] = ((w << (15 - n)) & 0x80008000u) ^ 0xBC00BC00u;
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 template <int KB, int VB, int M>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
-    static_assert(KB == 4 && VB == 4 && M == 0, "only 4/4-bit pages are built so far");
+    static_assert(KB >= 2 && KB <= 4 && VB >= 2 && VB <= 4 && (M == 0 || M == 128), "unsupported page format");
     extern __shared__ __align__(128) uint8_t sm[];
     const Geometry& g = a.g;
     constexpr int D = kHeadDim;
@@ -216,51 +353,77 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     bool timed_out = false;
     if (warp == kNCW) {
         // =================== producer ===================
+        // Lane k of the warp issues page base + k of each batch of 32: it waits
+        // until the page that last used its ring slot has been consumed, then
+        // starts one bulk copy.  Block ids of the next batch are loaded ahead.
         const int32_t* bt = a.block_table + (int64_t)b * a.max_blocks + p0;
-        int issued = 0;
-        for (int base = 0; base < npages && !timed_out; base += 32) {
-            const int mine = base + lane;
-            const int blk = mine < npages ? bt[mine] : -1;
-            const int cnt = min(32, npages - base);
-            for (int k = 0; k < cnt; ++k) {
-                const int bk = __shfl_sync(0xffffffffu, blk, k);
-                if (lane == 0 && !timed_out) {
-                    const int pi = base + k, s = pi % ST;
-                    if (pi >= ST && !mbar_wait(bar_empty + 8 * s, ((pi / ST) & 1) ^ 1)) {
-                        timed_out = true;
+        int blk = lane < npages ? __ldg(bt + lane) : -1;
+        for (int base = 0; base < npages; base += 32) {
+            const int pi = base + lane;
+            const int nxt = (pi + 32 < npages) ? __ldg(bt + pi + 32) : -1;
+            if (pi < npages && !timed_out) {
+                const int s = pi % ST;
+                if (pi >= ST && !mbar_wait(bar_empty + 8 * s, ((pi / ST) & 1) ^ 1)) {
+                    timed_out = true;
+                } else {
+                    const bool ok = blk >= 0 && blk < g.num_blocks;
+                    slot_ok[s] = ok;
+                    if (ok) {
+                        mbar_arrive_tx(bar_full + 8 * s, (uint32_t)g.page_bytes);
+                        bulk_g2s(ring_base + s * mp.stride, a.pool + ((int64_t)blk * g.hkv + h) * g.page_bytes,
+                                 (uint32_t)g.page_bytes, bar_full + 8 * s);
                     } else {
-                        const bool ok = bk >= 0 && bk < g.num_blocks;
-                        slot_ok[s] = ok;
-                        if (ok) {
-                            mbar_arrive_tx(bar_full + 8 * s, (uint32_t)g.page_bytes);
-                            bulk_g2s(ring_base + s * mp.stride,
-                                     a.pool + ((int64_t)bk * g.hkv + h) * g.page_bytes,
-                                     (uint32_t)g.page_bytes, bar_full + 8 * s);
-                        } else {
-                            flag(a.status, TQ_FLAG_BAD_SLOT);
-                            mbar_arrive(bar_full + 8 * s);
-                        }
-                        ++issued;
+                        flag(a.status, TQ_FLAG_BAD_SLOT);
+                        mbar_arrive(bar_full + 8 * s);
                     }
                 }
-                timed_out = __shfl_sync(0xffffffffu, timed_out, 0);
-                if (timed_out) break;
+            }
+            blk = nxt;
+            if (__any_sync(0xffffffffu, timed_out)) {
+                timed_out = true;
+                break;
             }
         }
-        // every copy this CTA started must land before shared memory is reused
-        if (lane == 0) {
-            for (int pi = issued - ST > 0 ? issued - ST : 0; pi < issued; ++pi)
-                if (!mbar_wait(bar_full + 8 * (pi % ST), (pi / ST) & 1)) timed_out = true;
+        // every copy this CTA started must land before shared memory is reused:
+        // lane k checks the last use of ring slots k, k+32, ...
+        {
+            const int issued = npages;  // pages past a timeout were not all issued; their waits just fail fast
+            for (int s = lane; s < ST; s += 32) {
+                // the last page that used slot s
+                const int last = (issued - 1 - s) >= 0 ? s + ((issued - 1 - s) / ST) * ST : -1;
+                if (last >= 0 && !timed_out && !mbar_wait(bar_full + 8 * s, (last / ST) & 1)) timed_out = true;
+            }
         }
-        timed_out = __shfl_sync(0xffffffffu, timed_out, 0);
+        timed_out = __any_sync(0xffffffffu, timed_out);
     } else {
         // =================== consumers ===================
-        // lane-private remainder table: entry e (a byte holding two key codes)
-        // -> (rem[e & 15], rem[e >> 4]) as fp16x2, copy for lane l at e*256 + 4l
-        for (int i = tid; i < 256 * 32; i += kNCW * 32) {
-            const int e = i >> 5, l = i & 31;
-            const uint32_t v = (uint32_t)a.c.rem_f16[e & 15] | ((uint32_t)a.c.rem_f16[e >> 4] << 16);
-            *reinterpret_cast<uint32_t*>(sm + mp.lut + e * 256 + 4 * l) = v;
+        // Lane-private remainder table (copy for lane l at entry*stride + l*width):
+        //   4-bit keys: byte e (2 codes) -> (rem[e&15], rem[e>>4])              stride 256, 4 B
+        //   2-bit keys: byte e (4 codes) -> (rem[c0], rem[c1]), (rem[c2], rem[c3]) stride 256, 8 B
+        //   3-bit keys: 6 bits e (2 codes) -> (rem[e&7], rem[e>>3])              stride 128, 4 B
+        {
+            const uint16_t* rem = a.c.rem_f16;
+            if constexpr (KB == 4) {
+                for (int i = tid; i < 256 * 32; i += kNCW * 32) {
+                    const int e = i >> 5, l = i & 31;
+                    *reinterpret_cast<uint32_t*>(sm + mp.lut + e * 256 + 4 * l) =
+                        (uint32_t)rem[e & 15] | ((uint32_t)rem[e >> 4] << 16);
+                }
+            } else if constexpr (KB == 2) {
+                for (int i = tid; i < 256 * 32; i += kNCW * 32) {
+                    const int e = i >> 5, l = i & 31;
+                    uint2 v;
+                    v.x = (uint32_t)rem[e & 3] | ((uint32_t)rem[(e >> 2) & 3] << 16);
+                    v.y = (uint32_t)rem[(e >> 4) & 3] | ((uint32_t)rem[e >> 6] << 16);
+                    *reinterpret_cast<uint2*>(sm + mp.lut + e * 256 + 8 * l) = v;
+                }
+            } else {
+                for (int i = tid; i < 64 * 32; i += kNCW * 32) {
+                    const int e = i >> 5, l = i & 31;
+                    *reinterpret_cast<uint32_t*>(sm + mp.lut + e * 128 + 4 * l) =
+                        (uint32_t)rem[e & 7] | ((uint32_t)rem[e >> 3] << 16);
+                }
+            }
         }
         // q_rot = R q for query (warp) of this group, and alpha * mid * sum(q_rot)
         {
@@ -278,29 +441,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             if (lane == 0) qoff[warp] = a.c.alpha * (float)((1 << KB) - 1) * 0.5f * sq;
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kNCW * 32) : "memory");
+        float* sqv = reinterpret_cast<float*>(sm + mp.sq);  // [8][128]: S q_rot per query
+        if constexpr (M > 0) {
+            // (S q_rot)_i for every query of the group: thread -> row i, queries g0, g0+2, ...
+            const int i = tid & (M - 1), g0 = tid / M;
+            const float4* srow = reinterpret_cast<const float4*>(a.S + (int64_t)i * D);
+            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int j4 = 0; j4 < D / 4; ++j4) {
+                const float4 sv = __ldg(srow + j4);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int gq = g0 + (kNCW * 32 / M) * k;
+                    if (gq < 8) {
+                        const float4 qv = *reinterpret_cast<const float4*>(qrot + gq * D + 4 * j4);
+                        acc4[k] = fmaf(sv.x, qv.x, fmaf(sv.y, qv.y, fmaf(sv.z, qv.z, fmaf(sv.w, qv.w, acc4[k]))));
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int gq = g0 + (kNCW * 32 / M) * k;
+                if (gq < 8) sqv[gq * D + i] = acc4[k];
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kNCW * 32) : "memory");
+        }
 
         const int r = lane >> 2, qd = lane & 3;   // r: token row / query column; qd: quad index
-        // ---- B fragments (queries as columns) ----
-        // int-code MMA: word wi of the lane's 32-dim chunk covers dims 8wi..8wi+7;
-        // k-step ks uses regs 2(ks&1), 2(ks&1)+1 of word ks>>1, i.e. dim pairs
-        // (8wi+i, 8wi+i+4) with i = 2(ks&1) (b0) and i+1 (b1).
+        // ---- B fragments (queries as columns): k-step ks, slot s uses pair n = 2ks + s ----
+        //   QAh/QAl: alpha*q_rot at the integer-code dims key_int_dim<KB>(n, 0/1), hi + lo
+        //   QB:      q_rot hi at the remainder dims (2n, 2n+1)
+        //   QSh/QSl: S q_rot at sign dims (n, n+16), hi + lo (QJL)
         uint32_t QAh[8][2], QAl[8][2], QB[8][2];
+        uint32_t QSh[M > 0 ? 8 : 1][2], QSl[M > 0 ? 8 : 1][2];
         {
             const float* qr = qrot + r * D + 32 * qd;
             const float al = a.c.alpha;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const int wi = ks >> 1, i = 2 * (ks & 1);
-                const int d0 = 8 * wi + i;
-                split_h2(al * qr[d0], al * qr[d0 + 4], QAh[ks][0], QAl[ks][0]);
-                split_h2(al * qr[d0 + 1], al * qr[d0 + 5], QAh[ks][1], QAl[ks][1]);
-                QB[ks][0] = pack_h2(qr[4 * ks], qr[4 * ks + 1]);
-                QB[ks][1] = pack_h2(qr[4 * ks + 2], qr[4 * ks + 3]);
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    const int n = 2 * ks + sl;
+                    split_h2(al * qr[key_int_dim<KB>(n, 0)], al * qr[key_int_dim<KB>(n, 1)], QAh[ks][sl], QAl[ks][sl]);
+                    QB[ks][sl] = pack_h2(qr[2 * n], qr[2 * n + 1]);
+                    if constexpr (M > 0) {
+                        const float* sr = sqv + r * D + 32 * qd;
+                        split_h2(sr[n], sr[n + 16], QSh[ks][sl], QSl[ks][sl]);
+                    }
+                }
             }
         }
         const float off0 = qoff[2 * qd], off1 = qoff[2 * qd + 1];
         const float ksc = a.sm_scale_log2;
-        const uint32_t lanew = (uint32_t)lane << 2;
+        const float cq = 1.2533141373155003f / (float)(M > 0 ? M : 1);  // sqrt(pi/2) / m
+        constexpr int KROW = D * KB / 8;
 
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
         float acc[8][4];
@@ -313,49 +506,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
                 timed_out = true;
                 break;
             }
-            const uint8_t* pg = ring + s * mp.stride;
+            const uint32_t pg = ring_base + s * mp.stride;  // shared-space address of the page
             const bool pok = slot_ok[s] != 0;
 
-            // ---------- scores ----------
-            const uint4 ka = *reinterpret_cast<const uint4*>(pg + g.kcode_off + r * 64 + qd * 16);
-            const uint4 kb = *reinterpret_cast<const uint4*>(pg + g.kcode_off + (r + 8) * 64 + qd * 16);
-            const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w}, kbw[4] = {kb.x, kb.y, kb.z, kb.w};
+            // ---------- scores: tokens r (rows 0-7) and r+8 (rows 8-15) ----------
             float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f}, sC[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                uint32_t Ia[16], Ra[16], Ib[16], Rb[16];
+                key_chunk<KB>(pg + g.kcode_off + r * KROW, qd, lut_base, (uint32_t)lane, Ia, Ra);
+                key_chunk<KB>(pg + g.kcode_off + (r + 8) * KROW, qd, lut_base, (uint32_t)lane, Ib, Rb);
 #pragma unroll
-            for (int wi = 0; wi < 4; ++wi) {
-                uint32_t fa[4], fb[4];
-                nib8_to_h2(kaw[wi], fa);
-                nib8_to_h2(kbw[wi], fb);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int ks = 2 * wi + hh;
-                    mma16816(sA, fa[2 * hh], fb[2 * hh], fa[2 * hh + 1], fb[2 * hh + 1], QAh[ks][0], QAh[ks][1]);
-                    mma16816(sB, fa[2 * hh], fb[2 * hh], fa[2 * hh + 1], fb[2 * hh + 1], QAl[ks][0], QAl[ks][1]);
-                }
-                // remainder lookups: byte j of the chunk holds dims (2j, 2j+1)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int ks = 2 * wi + hh;  // bytes 2ks, 2ks+1 live in word wi
-                    const uint32_t sel0 = 0x5504u | ((uint32_t)(2 * hh) << 4);
-                    const uint32_t sel1 = 0x5504u | ((uint32_t)(2 * hh + 1) << 4);
-                    uint32_t la0, la1, lb0, lb1;
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(la0) : "r"(lut_base + prmt(kaw[wi], lanew, sel0)));
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(lb0) : "r"(lut_base + prmt(kbw[wi], lanew, sel0)));
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(la1) : "r"(lut_base + prmt(kaw[wi], lanew, sel1)));
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(lb1) : "r"(lut_base + prmt(kbw[wi], lanew, sel1)));
-                    mma16816(sC, la0, lb0, la1, lb1, QB[ks][0], QB[ks][1]);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int n = 2 * ks;
+                    mma16816(sA, Ia[n], Ib[n], Ia[n + 1], Ib[n + 1], QAh[ks][0], QAh[ks][1]);
+                    mma16816(sB, Ia[n], Ib[n], Ia[n + 1], Ib[n + 1], QAl[ks][0], QAl[ks][1]);
+                    mma16816(sC, Ra[n], Rb[n], Ra[n + 1], Rb[n + 1], QB[ks][0], QB[ks][1]);
                 }
             }
-            const uint16_t* gam = reinterpret_cast<const uint16_t*>(pg + g.gam_off);
-            const uint16_t* vsc = reinterpret_cast<const uint16_t*>(pg + g.scl_off);
-            const uint16_t* vze = reinterpret_cast<const uint16_t*>(pg + g.zer_off);
-            const float gr = h2f(gam[r]) * ksc, gr8 = h2f(gam[r + 8]) * ksc;
+            float t0 = sA[0] + sB[0] + sC[0] - off0, t1 = sA[1] + sB[1] + sC[1] - off1;
+            float t2 = sA[2] + sB[2] + sC[2] - off0, t3 = sA[3] + sB[3] + sC[3] - off1;
+            if constexpr (M > 0) {
+                float sQ[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t Za[16], Zb[16];
+                sign_chunk(lds32(pg + g.sig_off + r * (M / 8) + 4 * qd), Za);
+                sign_chunk(lds32(pg + g.sig_off + (r + 8) * (M / 8) + 4 * qd), Zb);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int n = 2 * ks;
+                    mma16816(sQ, Za[n], Zb[n], Za[n + 1], Zb[n + 1], QSh[ks][0], QSh[ks][1]);
+                    mma16816(sQ, Za[n], Zb[n], Za[n + 1], Zb[n + 1], QSl[ks][0], QSl[ks][1]);
+                }
+                const float rr = cq * lds_h2f(pg + g.rho_off + 2 * r), rr8 = cq * lds_h2f(pg + g.rho_off + 2 * (r + 8));
+                t0 = fmaf(rr, sQ[0], t0); t1 = fmaf(rr, sQ[1], t1);
+                t2 = fmaf(rr8, sQ[2], t2); t3 = fmaf(rr8, sQ[3], t3);
+            }
+            const float gr = lds_h2f(pg + g.gam_off + 2 * r) * ksc, gr8 = lds_h2f(pg + g.gam_off + 2 * (r + 8)) * ksc;
             const int tok = (p0 + pi) * g.bs;
             const bool v_r = pok && (tok + r < len), v_r8 = pok && (tok + r + 8 < len);
-            float s0 = v_r ? (sA[0] + sB[0] + sC[0] - off0) * gr : -INFINITY;
-            float s1 = v_r ? (sA[1] + sB[1] + sC[1] - off1) * gr : -INFINITY;
-            float s2 = v_r8 ? (sA[2] + sB[2] + sC[2] - off0) * gr8 : -INFINITY;
-            float s3 = v_r8 ? (sA[3] + sB[3] + sC[3] - off1) * gr8 : -INFINITY;
+            const float s0 = v_r ? t0 * gr : -INFINITY;
+            const float s1 = v_r ? t1 * gr : -INFINITY;
+            const float s2 = v_r8 ? t2 * gr8 : -INFINITY;
+            const float s3 = v_r8 ? t3 * gr8 : -INFINITY;
 
             // ---------- online softmax ----------
             float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
@@ -379,7 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             }
             const float b0 = (m0 == -INFINITY) ? 0.f : m0, b1 = (m1 == -INFINITY) ? 0.f : m1;
             const float p0v = exp2f(s0 - b0), p1v = exp2f(s1 - b1), p2v = exp2f(s2 - b0), p3v = exp2f(s3 - b1);
-            const float sr = h2f(vsc[r]), sr8 = h2f(vsc[r + 8]), zr = h2f(vze[r]), zr8 = h2f(vze[r + 8]);
+            const float sr = lds_h2f(pg + g.scl_off + 2 * r), sr8 = lds_h2f(pg + g.scl_off + 2 * (r + 8));
+            const float zr = lds_h2f(pg + g.zer_off + 2 * r), zr8 = lds_h2f(pg + g.zer_off + 2 * (r + 8));
             l0 += p0v + p2v;
             l1 += p1v + p3v;
             z0 = fmaf(p0v, zr, fmaf(p2v, zr8, z0));
@@ -390,27 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             const uint32_t bh0 = movtrans(h01), bh1 = movtrans(h23);
             const uint32_t bl0 = movtrans(l01), bl1 = movtrans(l23);
 
-            // ---------- values ----------
-            // lane (r, qd): dims 16r..16r+15 of tokens 2qd, 2qd+1, 2qd+8, 2qd+9
-            const uint8_t* vrow = pg + g.vcode_off + r * 8;
-            const uint2 va = *reinterpret_cast<const uint2*>(vrow + (2 * qd) * 64);
-            const uint2 vb = *reinterpret_cast<const uint2*>(vrow + (2 * qd + 1) * 64);
-            const uint2 vc = *reinterpret_cast<const uint2*>(vrow + (2 * qd + 8) * 64);
-            const uint2 vd = *reinterpret_cast<const uint2*>(vrow + (2 * qd + 9) * 64);
-            const uint32_t wab[4] = {prmt(va.x, vb.x, 0x5410u), prmt(va.x, vb.x, 0x7632u),
-                                     prmt(va.y, vb.y, 0x5410u), prmt(va.y, vb.y, 0x7632u)};
-            const uint32_t wcd[4] = {prmt(vc.x, vd.x, 0x5410u), prmt(vc.x, vd.x, 0x7632u),
-                                     prmt(vc.y, vd.y, 0x5410u), prmt(vc.y, vd.y, 0x7632u)};
+            // ---------- values: lane (r, qd) holds dims 16r..16r+15 of tokens 2qd, 2qd+1, 2qd+8, 2qd+9 ----------
+            {
+                uint32_t Pab[16], Pcd[16];
+                value_pair<VB>(pg + g.vcode_off, r, 2 * qd, 2 * qd + 1, Pab);
+                value_pair<VB>(pg + g.vcode_off, r, 2 * qd + 8, 2 * qd + 9, Pcd);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t fab[4], fcd[4];
-                nib8_to_h2(wab[j], fab);
-                nib8_to_h2(wcd[j], fcd);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int mt = 2 * j + hh;  // dims 16r + 2mt (row r) and 16r + 2mt + 1 (row r+8)
-                    mma16816(acc[mt], fab[2 * hh], fab[2 * hh + 1], fcd[2 * hh], fcd[2 * hh + 1], bh0, bh1);
-                    mma16816(acc[mt], fab[2 * hh], fab[2 * hh + 1], fcd[2 * hh], fcd[2 * hh + 1], bl0, bl1);
+                for (int mt = 0; mt < 8; ++mt) {  // rows: dim 16r + 2mt (row r), 16r + 2mt + 1 (row r + 8)
+                    mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bh0, bh1);
+                    mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bl0, bl1);
                 }
             }
             __syncwarp();
@@ -544,7 +724,14 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
 
 int launch_decode(const DecodeArgs& a, void* stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (a.g.kb == 4 && a.g.vb == 4 && a.g.m == 0) return launch_decode_t<4, 4, 0>(a, s);
+    const int kb = a.g.kb, vb = a.g.vb, m = a.g.m;
+#define TQ_DEC(KB_, VB_)                                                                          \
+    if (kb == KB_ && vb == VB_)                                                                   \
+        return m ? launch_decode_t<KB_, VB_, 128>(a, s) : launch_decode_t<KB_, VB_, 0>(a, s);
+    TQ_DEC(2, 2) TQ_DEC(2, 3) TQ_DEC(2, 4)
+    TQ_DEC(3, 2) TQ_DEC(3, 3) TQ_DEC(3, 4)
+    TQ_DEC(4, 2) TQ_DEC(4, 3) TQ_DEC(4, 4)
+#undef TQ_DEC
     return (int)cudaErrorNotSupported;
 }
 

@@ -51,10 +51,27 @@ def test_many_splits(tq, oracle, n):
     _check(parity.run_case(w, oracle, tq))
 
 
-@pytest.mark.parametrize("kb,vb,m", [(3, 3, 0), (2, 2, 128), (4, 2, 0), (2, 4, 128)])
-def test_encode_other_bit_widths(tq, oracle, kb, vb, m):
-    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(333, 40), hkv=3, hq=3, key_bits=kb, value_bits=vb, qjl_m=m)
-    _check(parity.run_case(w, oracle, tq, decode=False), decode=False)
+@pytest.mark.parametrize("kb,vb,m", [(3, 3, 0), (2, 2, 128), (4, 2, 0), (2, 4, 128), (3, 4, 0), (4, 3, 128),
+                                     (2, 3, 0), (3, 2, 128), (4, 4, 128)])
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_other_bit_widths_and_qjl(tq, oracle, kb, vb, m, G):
+    """Every built (key bits, value bits, QJL) page format, ragged lengths, several group sizes."""
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(333, 40, 1), hkv=2, hq=2 * G, key_bits=kb, value_bits=vb, qjl_m=m)
+    _check(parity.run_case(w, oracle, tq))
+
+
+def test_long3bit_shape_reduced(tq, oracle):
+    """The 128K / 3-bit workload's head layout (64 q / 8 KV heads) at 4 x 2500 tokens."""
+    w = W.scaled(W.WORKLOADS["long128k3"], lens=(2500, 2501, 17, 2000))
+    _check(parity.run_case(w, oracle, tq, decode_gpu_pool=False))
+
+
+def test_qjl64_shape_reduced(tq, oracle):
+    """The high-concurrency QJL workload's format (2-bit + QJL m=128, 2-bit values, G=4) with
+    its first 8 sequence lengths divided by 8."""
+    lens = tuple(max(1, x // 8) for x in W.WORKLOADS["qjl64"].lens[:8])
+    w = W.scaled(W.WORKLOADS["qjl64"], lens=lens)
+    _check(parity.run_case(w, oracle, tq, decode_gpu_pool=False))
 
 
 def test_swa_workload_full_size(tq, oracle):
