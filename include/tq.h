@@ -217,6 +217,36 @@ TQ_API tq_status tq_decode_attention(const tq_cache* cache, const void* q, tq_dt
                                      float* out, void* workspace, size_t workspace_bytes,
                                      int32_t* dev_status, void* stream);
 
+/* Bytes of the fixed decode workspace built into the library (see below). */
+#define TQ_NOALLOC_WORKSPACE_BYTES (4u << 20)
+
+/* Decode attention exactly as tq_decode_attention, but without a caller
+ * workspace and without allocating anything.  (The source pages have no
+ * counterpart to this call: it exists for callers that may not allocate.)
+ *
+ * Who needs it: callers that cannot call cudaMalloc when they decode -- an
+ * engine that plans all of its device memory ahead of time, code running in a
+ * memory pool it does not control, or a serving loop that forbids allocations
+ * because they can synchronise the device.  Instead of a workspace argument
+ * the call uses one fixed scratch area of TQ_NOALLOC_WORKSPACE_BYTES (4 MiB)
+ * that is part of the library image; every GPU that loads the library holds
+ * it until the process exits.
+ *
+ * Arguments are those of tq_decode_attention minus the workspace.  Returns
+ * TQ_ERR_WORKSPACE, launching nothing, when the batch shape would need more
+ * than TQ_NOALLOC_WORKSPACE_BYTES (tq_decode_workspace_bytes tells).
+ * Uses the current CUDA device, which must be the cache's.  The first call on
+ * a device looks up the scratch area's device address; make that first call
+ * before any stream capture.  Each call clears the area's split counters on
+ * `stream` and calls no cudaMalloc, cudaFree or other allocating routine.
+ * All calls on a device share the one area and it keeps the last call's
+ * contents: two calls whose work overlaps on the GPU (different streams, or
+ * host threads without ordering) race and corrupt each other's results. */
+TQ_API tq_status tq_decode_attention_noalloc(const tq_cache* cache, const void* q, tq_dtype dtype,
+                                             int batch, int num_q_heads, const int32_t* block_table,
+                                             int max_blocks_per_seq, const int32_t* lens, float sm_scale,
+                                             float* out, int32_t* dev_status, void* stream);
+
 /* Text for a status code, and the detail of the last failure on this thread. */
 TQ_API const char* tq_status_string(tq_status s);
 TQ_API const char* tq_last_error(void);

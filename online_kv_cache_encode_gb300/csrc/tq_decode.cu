@@ -736,3 +736,92 @@ int launch_decode(const DecodeArgs& a, void* stream) {
 }
 
 }  // namespace tq
+
+// ===========================================================================
+// Decode without any device allocation by the caller or the library.
+//
+// Some callers cannot call cudaMalloc at the point where they decode: an
+// inference engine that pre-plans all of its device memory up front, code
+// running inside a memory pool it does not own, or a host that forbids
+// allocations on the serving path because they can synchronise the device.
+// For them this entry point uses a fixed scratch area that is part of the
+// library image itself (a file-scope __device__ array), sized
+// TQ_NOALLOC_WORKSPACE_BYTES.  Every device that loads the library keeps that
+// memory until the process exits.
+// ===========================================================================
+#include <mutex>
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_workspace[TQ_NOALLOC_WORKSPACE_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  Host code only
+// holds a stand-in for the array's name; the real address comes from the
+// runtime, looked up once per device with that device current.
+tq_status noalloc_workspace(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        tq::set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+        return TQ_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        tq::set_error("device ordinal %d is beyond the %d devices this entry point tracks", dev, kMaxDevices);
+        return TQ_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_workspace);
+        if (e != cudaSuccess || !p) {
+            tq::set_error("cudaGetSymbolAddress of the fixed decode workspace: %s", cudaGetErrorString(e));
+            return TQ_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" TQ_API tq_status tq_decode_attention_noalloc(const tq_cache* cache, const void* q, tq_dtype dtype,
+                                                        int batch, int num_q_heads, const int32_t* block_table,
+                                                        int max_blocks_per_seq, const int32_t* lens, float sm_scale,
+                                                        float* out, int32_t* dev_status, void* stream) {
+    if (!cache) {
+        tq::set_error("cache is NULL");
+        return TQ_ERR_INVALID_ARG;
+    }
+    if (batch == 0) return TQ_OK;
+    const size_t need = tq_decode_workspace_bytes(cache, batch, num_q_heads, max_blocks_per_seq);
+    if (need == 0) {
+        tq::set_error("bad batch / num_q_heads / max_blocks_per_seq");
+        return TQ_ERR_INVALID_ARG;
+    }
+    if (need > (size_t)TQ_NOALLOC_WORKSPACE_BYTES) {
+        tq::set_error("this batch shape needs %zu bytes of decode workspace, more than the %zu bytes of the "
+                      "fixed workspace; use tq_decode_attention with a workspace of your own",
+                      need, (size_t)TQ_NOALLOC_WORKSPACE_BYTES);
+        return TQ_ERR_WORKSPACE;
+    }
+    void* ws = nullptr;
+    tq_status st = noalloc_workspace(&ws);
+    if (st != TQ_OK) return st;
+    // The split counters sit at the end of the workspace and must start at
+    // zero; the array keeps whatever the previous call left, so clear them.
+    const size_t counters = (size_t)batch * cache->g.hkv * sizeof(unsigned);
+    const size_t counters_region = (counters + 255) / 256 * 256;
+    cudaError_t e = cudaMemsetAsync(static_cast<unsigned char*>(ws) + (need - counters_region), 0, counters,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        tq::set_error("clearing the fixed workspace counters: %s", cudaGetErrorString(e));
+        return TQ_ERR_CUDA;
+    }
+    return tq_decode_attention(cache, q, dtype, batch, num_q_heads, block_table, max_blocks_per_seq, lens, sm_scale,
+                               out, ws, need, dev_status, stream);
+}

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libtq.so")
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_WORKSPACE = range(5)
 FLAG_OVERFLOW, FLAG_BAD_SLOT, FLAG_NONFINITE, FLAG_TIMEOUT = 1, 2, 4, 8
 TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
+NOALLOC_WORKSPACE_BYTES = 4 << 20  # TQ_NOALLOC_WORKSPACE_BYTES
 
 # every exported symbol of include/tq.h: (restype, argtypes)
 _P, _I, _I64, _U64, _F, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
@@ -37,6 +38,7 @@ SIGNATURES = {
     "tq_encode_kv": (_I, [_P, _P, _P, _I, _I64, _P, _P, _P]),
     "tq_decode_workspace_bytes": (_SZ, [_P, _I, _I, _I]),
     "tq_decode_attention": (_I, [_P, _P, _I, _I, _I, _P, _I, _P, _F, _P, _P, _SZ, _P, _P]),
+    "tq_decode_attention_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _I, _P, _F, _P, _P, _P]),
     "tq_status_string": (ctypes.c_char_p, [_I]),
     "tq_last_error": (ctypes.c_char_p, []),
 }
@@ -201,4 +203,23 @@ class Cache:
         _check(lib().tq_decode_attention(self._h, _ptr(q), _dtype_code(q), B, hq, _ptr(block_table), mb,
                                          _ptr(lens), float(sm_scale), _ptr(out), _ptr(workspace),
                                          workspace.numel(), _ptr(status), ctypes.c_void_p(_stream())))
+        return out
+
+    def decode_noalloc(self, q: torch.Tensor, block_table: torch.Tensor, lens: torch.Tensor,
+                       sm_scale: float | None = None, out: torch.Tensor = None,
+                       status: torch.Tensor | None = None) -> torch.Tensor:
+        """decode() through tq_decode_attention_noalloc: the library's fixed
+        workspace instead of a caller one (for callers that must not allocate).
+        `out` must be given: this call allocates nothing, here or in the library."""
+        assert out is not None and out.dtype == torch.float32 and out.is_contiguous()
+        assert q.is_cuda and q.dim() == 3 and q.shape[2] == self.d and q.is_contiguous()
+        B, hq, _ = q.shape
+        assert out.shape == (B, hq, self.d)
+        assert block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
+        assert lens.dtype == torch.int32 and lens.numel() == B
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.d)
+        _check(lib().tq_decode_attention_noalloc(self._h, _ptr(q), _dtype_code(q), B, hq, _ptr(block_table),
+                                                 block_table.shape[1], _ptr(lens), float(sm_scale), _ptr(out),
+                                                 _ptr(status), ctypes.c_void_p(_stream())))
         return out
