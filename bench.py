@@ -230,47 +230,59 @@ def run_ours(args, rank, world, local):
         c.encode(newK, newV, new_slot, status)
         c.decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
 
+    def capture(fn, n):
+        """CUDA graph of n calls of fn(i) (the library launches on torch's current stream)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                fn(i)
+        return g
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    steps_graph = capture(step, args.steps)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         # the sampler sees the GPU under this same load before and after the timed region
-        for i in range(args.warmup):
-            step(i)
+        steps_graph.replay()
         torch.cuda.synchronize()
         deadline = time.time() + 3.0
         while clk.count() < 3 and time.time() < deadline:
-            for i in range(50):
-                step(i)
+            steps_graph.replay()
             torch.cuda.synchronize()
         barrier(dist)
         torch.cuda.synchronize()
         t0.record(stream)
-        for i in range(args.steps):
-            step(i)
+        steps_graph.replay()
         t1.record(stream)
         torch.cuda.synchronize()
         n_before = clk.count()
         deadline = time.time() + 1.0
         while clk.count() <= n_before and time.time() < deadline:
-            for i in range(50):
-                step(i)
+            steps_graph.replay()
             torch.cuda.synchronize()
     barrier(dist)
     torch.cuda.synchronize()
     step_ms = t0.elapsed_time(t1) / args.steps
     launches = 2 * args.steps
+    del steps_graph
 
-    # ---- the decode kernel alone (roofline) ----
-    for i in range(3):
+    # ---- the decode kernel alone (roofline): a graph of back-to-back decode launches ----
+    def dec(i):
         copies[i % N_COPIES].decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES])
-    torch.cuda.synchronize()
+
     nd = max(args.steps, 20)
+    dec_graph = capture(dec, nd)
+    dec_graph.replay()
+    torch.cuda.synchronize()
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     d0.record(stream)
-    for i in range(nd):
-        copies[i % N_COPIES].decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES])
+    dec_graph.replay()
     d1.record(stream)
     torch.cuda.synchronize()
     dec_ms = d0.elapsed_time(d1) / nd
+    del dec_graph
 
     # ---- end to end through the public API with host buffers ----
     hK = newK.cpu().pin_memory()
@@ -332,6 +344,8 @@ def run_ours(args, rank, world, local):
             "step": "encode 1 new token (8 KV heads) + decode attention for 64 query heads over 32768 tokens",
             "decode_bytes_per_step": decode_bytes,
             "l2": f"inputs larger than L2: {N_COPIES} distinct caches rotated ({N_COPIES * decode_bytes / 1e6:.0f} MB)",
+            "timing": "the K steps captured in one CUDA graph, replayed once between CUDA events; "
+                      "e2e is eager per-call through the Python binding",
             "parallelism": f"replica per GPU x{world}",
         },
         "pct_of_hbm_peak": round(100 * value / peak, 2),

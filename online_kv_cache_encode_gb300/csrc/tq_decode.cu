@@ -576,11 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             l1 += p1v + p3v;
             z0 = fmaf(p0v, zr, fmaf(p2v, zr8, z0));
             z1 = fmaf(p1v, zr, fmaf(p3v, zr8, z1));
-            uint32_t h01, l01, h23, l23;
-            split_h2(p0v * sr, p1v * sr, h01, l01);
-            split_h2(p2v * sr8, p3v * sr8, h23, l23);
+            // the weights p * scale go in as single fp16 (their rounding costs ~1e-4 of output)
+            const uint32_t h01 = pack_h2(p0v * sr, p1v * sr), h23 = pack_h2(p2v * sr8, p3v * sr8);
             const uint32_t bh0 = movtrans(h01), bh1 = movtrans(h23);
-            const uint32_t bl0 = movtrans(l01), bl1 = movtrans(l23);
 
             // ---------- values: lane (r, qd) holds dims 16r..16r+15 of tokens 2qd, 2qd+1, 2qd+8, 2qd+9 ----------
             {
@@ -588,10 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
                 value_pair<VB>(pg + g.vcode_off, r, 2 * qd, 2 * qd + 1, Pab);
                 value_pair<VB>(pg + g.vcode_off, r, 2 * qd + 8, 2 * qd + 9, Pcd);
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {  // rows: dim 16r + 2mt (row r), 16r + 2mt + 1 (row r + 8)
+                for (int mt = 0; mt < 8; ++mt)  // rows: dim 16r + 2mt (row r), 16r + 2mt + 1 (row r + 8)
                     mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bh0, bh1);
-                    mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bl0, bl1);
-                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
@@ -675,21 +671,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
         __threadfence();
         finalize = true;
         if (warp < G) {
+            // Lanes load the splits' (max, sum) in parallel; the acc loads of a
+            // group of up to 32 splits are independent of each other, so they
+            // overlap instead of paying one L2 round trip per split.
             const float* base = a.partials + (unit * a.num_splits * G) * kPartStride;
+            const int ns = a.num_splits;
             Mx = -INFINITY;
-            for (int sp = 0; sp < a.num_splits; ++sp) Mx = fmaxf(Mx, __ldcg(base + (sp * G + qg) * kPartStride));
+            for (int s0 = 0; s0 < ns; s0 += 32) {
+                const int sp = s0 + lane;
+                Mx = fmaxf(Mx, sp < ns ? __ldcg(base + (sp * G + qg) * kPartStride) : -INFINITY);
+            }
+            Mx = warp_max(Mx);
             L = 0.f;
             O[0] = O[1] = O[2] = O[3] = 0.f;
             if (Mx != -INFINITY) {
-                for (int sp = 0; sp < a.num_splits; ++sp) {
-                    const float* pp = base + (sp * G + qg) * kPartStride;
-                    const float ms = __ldcg(pp);
-                    if (ms == -INFINITY) continue;
-                    const float f = exp2f(ms - Mx);
-                    L = fmaf(f, __ldcg(pp + 1), L);
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(pp + 4 + 4 * lane));
-                    O[0] = fmaf(f, v.x, O[0]); O[1] = fmaf(f, v.y, O[1]);
-                    O[2] = fmaf(f, v.z, O[2]); O[3] = fmaf(f, v.w, O[3]);
+                for (int s0 = 0; s0 < ns; s0 += 32) {
+                    const int sp = s0 + lane;
+                    float f = 0.f, lv = 0.f;
+                    if (sp < ns) {
+                        const float ms = __ldcg(base + (sp * G + qg) * kPartStride);
+                        lv = __ldcg(base + (sp * G + qg) * kPartStride + 1);
+                        f = (ms == -INFINITY) ? 0.f : exp2f(ms - Mx);
+                    }
+                    L += warp_sum(f * lv);
+                    const int n = min(32, ns - s0);
+#pragma unroll 8
+                    for (int k = 0; k < n; ++k) {
+                        const float fk = __shfl_sync(0xffffffffu, f, k);
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                            base + ((s0 + k) * G + qg) * kPartStride + 4 + 4 * lane));
+                        O[0] = fmaf(fk, v.x, O[0]); O[1] = fmaf(fk, v.y, O[1]);
+                        O[2] = fmaf(fk, v.z, O[2]); O[3] = fmaf(fk, v.w, O[3]);
+                    }
                 }
             }
         }
@@ -715,7 +728,8 @@ template <int KB, int VB, int M>
 static int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
     const int smem = smem_map((int)a.g.page_bytes).total;
     auto kern = decode_kernel<KB, VB, M>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static int done[64] = {};
+    cudaError_t e = ensure_smem_limit(kern, smem, done);
     if (e != cudaSuccess) return (int)e;
     dim3 grid((unsigned)a.num_splits, (unsigned)a.g.hkv, (unsigned)a.batch);
     kern<<<grid, kThreads, smem, s>>>(a);

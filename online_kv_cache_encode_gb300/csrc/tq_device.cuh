@@ -1,6 +1,7 @@
 // Device helpers shared by the encode and decode kernels.
 #pragma once
 
+#include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -9,6 +10,20 @@
 #include "tq_internal.h"
 
 namespace tq {
+
+// Raise a kernel's dynamic shared-memory limit once per device and size; the
+// attribute call costs host time that would otherwise be paid on every launch.
+// Concurrent first calls may both set it, which is harmless.
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kern, int bytes, int (&done)[64]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev] >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = bytes;
+    return e;
+}
 
 __device__ __forceinline__ void flag(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);

@@ -160,7 +160,8 @@ static int launch_encode_t(const EncodeArgs& a, int num_sms, cudaStream_t s) {
     const size_t smem = (size_t)(M * kSPad + (M > 0 ? kEncWarps * kHeadDim : 0)) * sizeof(float);
     auto kern = encode_kernel<KB, VB, M>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        static int done[64] = {};
+        cudaError_t e = ensure_smem_limit(kern, (int)smem, done);
         if (e != cudaSuccess) return (int)e;
     }
     const int64_t items = a.num_tokens * a.g.hkv;
