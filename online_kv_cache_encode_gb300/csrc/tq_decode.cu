@@ -26,12 +26,15 @@
 // quantized KV].
 #include <cuda_runtime.h>
 
+#include <cuda_fp8.h>
+
 #include "tq_device.cuh"
 
 namespace tq {
 
-constexpr int kNCW = 8;                       // consumer warps
-constexpr int kThreads = (kNCW + 1) * 32;     // + producer warp
+constexpr int kNCW = 8;                       // warps per CTA, each consumes (and fetches) its own pages
+constexpr int kThreads = kNCW * 32;
+constexpr int kSlotsPerWarp = 8;              // ring slots per warp: pages a warp keeps in flight
 constexpr int kLutBytes = 256 * 256;          // 256 entries x 256 B (lanes use 128 B)
 constexpr long long kWaitCycles = 3000000000ll;  // bound on any wait: ~1.5 s at 2 GHz
 // split partial record: max, sum, 2 pad, acc[128] (keeps the acc 16-byte aligned)
@@ -130,6 +133,21 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// D += A . B with A 16x32, B 32x8 of e4m3, fp32 accumulate (exact products, fp32 sums)
+__device__ __forceinline__ void mma_e4m3(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t f2e4m3(float x) {
+    return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float e4m3_2f(uint32_t b) {
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3)));
+}
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -165,7 +183,7 @@ __device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t f[4]) {
 // shared memory map (dynamic)
 // ---------------------------------------------------------------------------
 struct SmemMap {
-    int lut, qrot, qoff, sq, bars, ok, ring;
+    int lut, rem, qrot, qoff, qscale, sq, bars, ok, ring;
     int stages, stride, total;
 };
 
@@ -173,18 +191,16 @@ __host__ __device__ inline SmemMap smem_map(int page_bytes) {
     SmemMap m;
     int off = 0;
     m.lut = off; off += kLutBytes;
+    m.rem = off; off += 16 * 2;
     m.qrot = off; off += 8 * kHeadDim * 4;
     m.qoff = off; off += 8 * 4;
+    m.qscale = off; off += 8 * 4;
     m.sq = off; off += 8 * kHeadDim * 4;
     m.stride = (page_bytes + 127) / 128 * 128;
-    const int budget = 227 * 1024 - 1024;
-    int fixed = off + 64;
-    int stages = (budget - fixed) / (m.stride + 2 * 8 + 4);
-    if (stages > 64) stages = 64;
-    m.stages = stages;
-    m.bars = (off + 7) / 8 * 8; off = m.bars + 2 * 8 * stages;
-    m.ok = off; off += 4 * stages;
-    m.ring = (off + 127) / 128 * 128; off = m.ring + m.stride * stages;
+    m.stages = kNCW * kSlotsPerWarp;
+    m.bars = (off + 7) / 8 * 8; off = m.bars + 8 * m.stages;
+    m.ok = off; off += 4 * m.stages;
+    m.ring = (off + 127) / 128 * 128; off = m.ring + m.stride * m.stages;
     m.total = off;
     return m;
 }
@@ -220,51 +236,77 @@ __device__ __forceinline__ uint32_t int_pair_h2(uint32_t c0, uint32_t c1) {
     return hsub2((c0 | (c1 << 16)) | 0x64006400u, 0x64006400u);
 }
 
-// Key chunk of one token (the 32 codes of dims 32qd .. 32qd+31, 4*KB bytes):
-// I[n] = codes of dims key_int_dim(n, 0/1) as exact fp16 integers,
-// R[n] = (rem[c_{2n}], rem[c_{2n+1}]) from the lane-private table.
+// Key chunk of one token: the 32 codes of dims 32qd .. 32qd+31 (4*KB bytes).
 template <int KB>
-__host__ __device__ constexpr int key_int_dim(int n, int half) {
-    return KB == 4 ? 8 * (n >> 2) + (n & 3) + 4 * half
-         : KB == 2 ? 16 * (n >> 3) + (n & 7) + 8 * half
-                   : 2 * n + half;
-}
-
-template <int KB>
-__device__ __forceinline__ void key_chunk(uint32_t row, int qd, uint32_t lut, uint32_t lane,
-                                          uint32_t I[16], uint32_t R[16]) {
-    uint32_t w[KB];
+__device__ __forceinline__ void key_words(uint32_t row, int qd, uint32_t (&w)[KB]) {
     if constexpr (KB == 4) {
         const uint4 v = lds128(row + qd * 16);
         w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) nib8_to_h2(w[i], &I[4 * i]);
-        const uint32_t lw = lane << 2;
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            const uint32_t addr = lut + prmt(w[n >> 2], lw, 0x5504u | ((uint32_t)(n & 3) << 4));
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(R[n]) : "r"(addr));
-        }
     } else if constexpr (KB == 2) {
         const uint2 v = lds64(row + qd * 8);
         w[0] = v.x; w[1] = v.y;
-        crumb16_to_h2(w[0], &I[0]);
-        crumb16_to_h2(w[1], &I[8]);
+    } else {
+        w[0] = lds32(row + qd * 12); w[1] = lds32(row + qd * 12 + 4); w[2] = lds32(row + qd * 12 + 8);
+    }
+}
+
+// The integer codes as e4m3 operand bytes.  A code byte n < 16 read as e4m3 is
+// exactly n * 2^-9 (exponent field 0 is the subnormal n * 2^-9, field 1 is
+// (8 + m) * 2^-9), so the codes need only be spread into bytes.
+// E[e] byte i holds the code of chunk dim key_fp8_dim<KB>(e, i).
+template <int KB>
+__host__ __device__ constexpr int key_fp8_dim(int e, int i) {
+    return KB == 4 ? 8 * (e >> 1) + 2 * i + (e & 1)
+         : KB == 2 ? 16 * (e >> 2) + 4 * i + (e & 3)
+                   : 4 * e + i;
+}
+
+__device__ __forceinline__ uint32_t spread3x4(uint32_t t) {  // four 3-bit fields -> four bytes
+    return (t & 0x7u) | ((t & 0x38u) << 5) | ((t & 0x1C0u) << 10) | ((t & 0xE00u) << 15);
+}
+
+template <int KB>
+__device__ __forceinline__ void key_bytes(const uint32_t (&w)[KB], uint32_t E[8]) {
+    if constexpr (KB == 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            E[2 * i] = w[i] & 0x0F0F0F0Fu;
+            E[2 * i + 1] = (w[i] >> 4) & 0x0F0F0F0Fu;
+        }
+    } else if constexpr (KB == 2) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int sh = 0; sh < 4; ++sh) E[4 * i + sh] = (w[i] >> (2 * sh)) & 0x03030303u;
+    } else {
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+            const uint32_t x = bits_at<3>(w, 24 * gi, 24);
+            E[2 * gi] = spread3x4(x & 0xFFFu);
+            E[2 * gi + 1] = spread3x4(x >> 12);
+        }
+    }
+}
+
+// Remainder operands: R[n] = (rem[c_{2n}], rem[c_{2n+1}]) from the lane-private table.
+template <int KB>
+__device__ __forceinline__ void key_rem(const uint32_t (&w)[KB], uint32_t lut, uint32_t lane, uint32_t R[16]) {
+    if constexpr (KB == 4) {
+        const uint32_t lw = lane << 2;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) R[n] = lds32(lut + prmt(w[n >> 2], lw, 0x5504u | ((uint32_t)(n & 3) << 4)));
+    } else if constexpr (KB == 2) {
         const uint32_t lw = lane << 3;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const uint32_t addr = lut + prmt(w[j >> 2], lw, 0x5504u | ((uint32_t)(j & 3) << 4));
-            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(R[2 * j]), "=r"(R[2 * j + 1]) : "r"(addr));
+            const uint2 v = lds64(lut + prmt(w[j >> 2], lw, 0x5504u | ((uint32_t)(j & 3) << 4)));
+            R[2 * j] = v.x;
+            R[2 * j + 1] = v.y;
         }
     } else {
-        w[0] = lds32(row + qd * 12); w[1] = lds32(row + qd * 12 + 4); w[2] = lds32(row + qd * 12 + 8);
         const uint32_t lw = lane << 2;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            const uint32_t t = bits_at<3>(w, 6 * n, 6);
-            I[n] = int_pair_h2(t & 7u, t >> 3);
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(R[n]) : "r"(lut + (t << 7) + lw));
-        }
+        for (int n = 0; n < 16; ++n) R[n] = lds32(lut + (bits_at<3>(w, 6 * n, 6) << 7) + lw);
     }
 }
 
@@ -316,93 +358,75 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = a.group;
     const SmemMap mp = smem_map((int)g.page_bytes);
-    const int ST = mp.stages;
+    constexpr int SPW = kSlotsPerWarp;
 
     float* qrot = reinterpret_cast<float*>(sm + mp.qrot);
     float* qoff = reinterpret_cast<float*>(sm + mp.qoff);
+    float* qscale = reinterpret_cast<float*>(sm + mp.qscale);
     int* slot_ok = reinterpret_cast<int*>(sm + mp.ok);
     const uint32_t bar_full = smem_u32(sm + mp.bars);
-    const uint32_t bar_empty = bar_full + 8 * ST;
     const uint32_t lut_base = smem_u32(sm + mp.lut);
     const uint32_t ring_base = smem_u32(sm + mp.ring);
     uint8_t* ring = sm + mp.ring;
+    const int p0 = split * a.pages_per_split;
+
+    // ---- independent global loads first: length, this warp's block ids, the query ----
+    // Warp w handles pages w, w + 8, w + 16, ... of the split (its j-th page is
+    // w + 8 j) in its own ring slots w*SPW .. w*SPW + SPW - 1.  Lane l holds the
+    // block id of the warp's page l of the current batch of 32 (bid_cur) and of
+    // the next batch (bid_nxt).
+    int len = __ldg(a.lens + b);
+    const int32_t* btw = a.block_table + (int64_t)b * a.max_blocks + p0 + warp;
+    const int reach = min(a.pages_per_split, a.max_blocks - p0) - warp;  // pages of the split at or after this warp's first
+    int bid_cur = (8 * lane < reach) ? __ldg(btw + 8 * lane) : -1;
+    int bid_nxt = (8 * (32 + lane) < reach) ? __ldg(btw + 8 * (32 + lane)) : -1;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (warp < G) load4(a.q, a.dtype, ((int64_t)b * a.hq + (int64_t)h * G + warp) * D + 4 * lane, x);
+    if (lane == 0) {
+        for (int k = 0; k < SPW; ++k) mbar_init(bar_full + 8 * (warp * SPW + k), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
 
     // ---- sequence range of this split ----
-    int len = a.lens[b];
     if (len > a.max_blocks * g.bs) {
         if (tid == 0) flag(a.status, TQ_FLAG_BAD_SLOT);
         len = a.max_blocks * g.bs;
     }
     if (len < 0) len = 0;
     const int seq_pages = (len + g.bs - 1) / g.bs;
-    const int p0 = split * a.pages_per_split;
     int npages = seq_pages - p0;
     if (npages > a.pages_per_split) npages = a.pages_per_split;
     if (npages < 0) npages = 0;
+    const int nmine = npages > warp ? (npages - warp + kNCW - 1) / kNCW : 0;  // this warp's pages
 
-    // ---- barriers ----
-    if (tid == 0) {
-        for (int s = 0; s < ST; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+    // Start a page copy into the warp's ring slot; a bad block id arrives on the
+    // barrier without data and the page is skipped.
+    auto issue = [&](int j, int blk) {
+        const int sl = warp * SPW + (j % SPW);
+        const bool ok = blk >= 0 && blk < g.num_blocks;
+        slot_ok[sl] = ok;
+        if (ok) {
+            mbar_arrive_tx(bar_full + 8 * sl, (uint32_t)g.page_bytes);
+            bulk_g2s(ring_base + sl * mp.stride, a.pool + ((int64_t)blk * g.hkv + h) * g.page_bytes,
+                     (uint32_t)g.page_bytes, bar_full + 8 * sl);
+        } else {
+            flag(a.status, TQ_FLAG_BAD_SLOT);
+            mbar_arrive(bar_full + 8 * sl);
         }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
+    };
+    if (lane < SPW && lane < nmine) issue(lane, bid_cur);  // the first SPW pages, one lane each
 
     bool timed_out = false;
-    if (warp == kNCW) {
-        // =================== producer ===================
-        // Lane k of the warp issues page base + k of each batch of 32: it waits
-        // until the page that last used its ring slot has been consumed, then
-        // starts one bulk copy.  Block ids of the next batch are loaded ahead.
-        const int32_t* bt = a.block_table + (int64_t)b * a.max_blocks + p0;
-        int blk = lane < npages ? __ldg(bt + lane) : -1;
-        for (int base = 0; base < npages; base += 32) {
-            const int pi = base + lane;
-            const int nxt = (pi + 32 < npages) ? __ldg(bt + pi + 32) : -1;
-            if (pi < npages && !timed_out) {
-                const int s = pi % ST;
-                if (pi >= ST && !mbar_wait(bar_empty + 8 * s, ((pi / ST) & 1) ^ 1)) {
-                    timed_out = true;
-                } else {
-                    const bool ok = blk >= 0 && blk < g.num_blocks;
-                    slot_ok[s] = ok;
-                    if (ok) {
-                        mbar_arrive_tx(bar_full + 8 * s, (uint32_t)g.page_bytes);
-                        bulk_g2s(ring_base + s * mp.stride, a.pool + ((int64_t)blk * g.hkv + h) * g.page_bytes,
-                                 (uint32_t)g.page_bytes, bar_full + 8 * s);
-                    } else {
-                        flag(a.status, TQ_FLAG_BAD_SLOT);
-                        mbar_arrive(bar_full + 8 * s);
-                    }
-                }
-            }
-            blk = nxt;
-            if (__any_sync(0xffffffffu, timed_out)) {
-                timed_out = true;
-                break;
-            }
-        }
-        // every copy this CTA started must land before shared memory is reused:
-        // lane k checks the last use of ring slots k, k+32, ...
-        {
-            const int issued = npages;  // pages past a timeout were not all issued; their waits just fail fast
-            for (int s = lane; s < ST; s += 32) {
-                // the last page that used slot s
-                const int last = (issued - 1 - s) >= 0 ? s + ((issued - 1 - s) / ST) * ST : -1;
-                if (last >= 0 && !timed_out && !mbar_wait(bar_full + 8 * s, (last / ST) & 1)) timed_out = true;
-            }
-        }
-        timed_out = __any_sync(0xffffffffu, timed_out);
-    } else {
-        // =================== consumers ===================
+    {
         // Lane-private remainder table (copy for lane l at entry*stride + l*width):
         //   4-bit keys: byte e (2 codes) -> (rem[e&15], rem[e>>4])              stride 256, 4 B
         //   2-bit keys: byte e (4 codes) -> (rem[c0], rem[c1]), (rem[c2], rem[c3]) stride 256, 8 B
         //   3-bit keys: 6 bits e (2 codes) -> (rem[e&7], rem[e>>3])              stride 128, 4 B
+        uint16_t* rem = reinterpret_cast<uint16_t*>(sm + mp.rem);
+        if (tid < 16) rem[tid] = a.c.rem_f16[tid];
+        __syncthreads();
         {
-            const uint16_t* rem = a.c.rem_f16;
             if constexpr (KB == 4) {
                 for (int i = tid; i < 256 * 32; i += kNCW * 32) {
                     const int e = i >> 5, l = i & 31;
@@ -427,9 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
         }
         // q_rot = R q for query (warp) of this group, and alpha * mid * sum(q_rot)
         {
-            float x[4] = {0.f, 0.f, 0.f, 0.f};
             if (warp < G) {
-                load4(a.q, a.dtype, ((int64_t)b * a.hq + (int64_t)h * G + warp) * D + 4 * lane, x);
                 apply_signs(x, lane_signs(a.c, lane));
                 fwht128(x, lane);
 #pragma unroll
@@ -438,9 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
 #pragma unroll
             for (int i = 0; i < 4; ++i) qrot[warp * D + 4 * lane + i] = x[i];
             const float sq = warp_sum(x[0] + x[1] + x[2] + x[3]);
-            if (lane == 0) qoff[warp] = a.c.alpha * (float)((1 << KB) - 1) * 0.5f * sq;
+            // power-of-two scale putting max |alpha q_rot 2^9| / scale in (112, 224]: e4m3 range
+            const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+            const float big = fabsf(a.c.alpha) * 512.f * mx;
+            const float scl = (big > 0.f) ? exp2f(ceilf(log2f(big / 224.f))) : 1.f;
+            if (lane == 0) {
+                qoff[warp] = a.c.alpha * (float)((1 << KB) - 1) * 0.5f * sq;
+                qscale[warp] = scl;
+            }
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kNCW * 32) : "memory");
+        __syncthreads();
         float* sqv = reinterpret_cast<float*>(sm + mp.sq);  // [8][128]: S q_rot per query
         if constexpr (M > 0) {
             // (S q_rot)_i for every query of the group: thread -> row i, queries g0, g0+2, ...
@@ -463,25 +492,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
                 const int gq = g0 + (kNCW * 32 / M) * k;
                 if (gq < 8) sqv[gq * D + i] = acc4[k];
             }
-            asm volatile("bar.sync 1, %0;" ::"r"(kNCW * 32) : "memory");
+            __syncthreads();
         }
 
         const int r = lane >> 2, qd = lane & 3;   // r: token row / query column; qd: quad index
         // ---- B fragments (queries as columns): k-step ks, slot s uses pair n = 2ks + s ----
-        //   QAh/QAl: alpha*q_rot at the integer-code dims key_int_dim<KB>(n, 0/1), hi + lo
+        //   QT:      alpha*q_rot*2^9/scale at the code dims, as four e4m3 terms t_k, the
+        //            k-th carrying 16^k x the residual left by the earlier ones (~16 bits)
         //   QB:      q_rot hi at the remainder dims (2n, 2n+1)
         //   QSh/QSl: S q_rot at sign dims (n, n+16), hi + lo (QJL)
-        uint32_t QAh[8][2], QAl[8][2], QB[8][2];
+        uint32_t QT[4][4][2], QB[8][2];
         uint32_t QSh[M > 0 ? 8 : 1][2], QSl[M > 0 ? 8 : 1][2];
         {
             const float* qr = qrot + r * D + 32 * qd;
-            const float al = a.c.alpha;
+            const float al = a.c.alpha * 512.f / qscale[r];
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    uint32_t tb[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float res = al * qr[key_fp8_dim<KB>(2 * ks + sl, i)];
+                        float mul = 1.f;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t t = f2e4m3(res * mul);
+                            res -= e4m3_2f(t) / mul;
+                            mul *= 16.f;
+                            tb[k] |= t << (8 * i);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) QT[k][ks][sl] = tb[k];
+                }
+            }
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
                 for (int sl = 0; sl < 2; ++sl) {
                     const int n = 2 * ks + sl;
-                    split_h2(al * qr[key_int_dim<KB>(n, 0)], al * qr[key_int_dim<KB>(n, 1)], QAh[ks][sl], QAl[ks][sl]);
                     QB[ks][sl] = pack_h2(qr[2 * n], qr[2 * n + 1]);
                     if constexpr (M > 0) {
                         const float* sr = sqv + r * D + 32 * qd;
@@ -491,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             }
         }
         const float off0 = qoff[2 * qd], off1 = qoff[2 * qd + 1];
+        const float qs0 = qscale[2 * qd], qs1 = qscale[2 * qd + 1];
         const float ksc = a.sm_scale_log2;
         const float cq = 1.2533141373155003f / (float)(M > 0 ? M : 1);  // sqrt(pi/2) / m
         constexpr int KROW = D * KB / 8;
@@ -500,9 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-        for (int pi = warp; pi < npages; pi += kNCW) {
-            const int s = pi % ST;
-            if (!mbar_wait(bar_full + 8 * s, (pi / ST) & 1)) {
+        int jdone = 0;  // pages of this warp consumed
+        for (int j = 0; j < nmine; ++j) {
+            const int pi = warp + kNCW * j;
+            const int s = warp * SPW + (j % SPW);
+            if (!mbar_wait(bar_full + 8 * s, (j / SPW) & 1)) {
                 timed_out = true;
                 break;
             }
@@ -510,21 +563,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             const bool pok = slot_ok[s] != 0;
 
             // ---------- scores: tokens r (rows 0-7) and r+8 (rows 8-15) ----------
-            float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f}, sC[4] = {0.f, 0.f, 0.f, 0.f};
+            float sI[4][4], sC[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sI[k][0] = sI[k][1] = sI[k][2] = sI[k][3] = 0.f;
             {
-                uint32_t Ia[16], Ra[16], Ib[16], Rb[16];
-                key_chunk<KB>(pg + g.kcode_off + r * KROW, qd, lut_base, (uint32_t)lane, Ia, Ra);
-                key_chunk<KB>(pg + g.kcode_off + (r + 8) * KROW, qd, lut_base, (uint32_t)lane, Ib, Rb);
+                uint32_t wa[KB], wb[KB];
+                key_words<KB>(pg + g.kcode_off + r * KROW, qd, wa);
+                key_words<KB>(pg + g.kcode_off + (r + 8) * KROW, qd, wb);
+                uint32_t Ea[8], Eb[8];
+                key_bytes<KB>(wa, Ea);
+                key_bytes<KB>(wb, Eb);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_e4m3(sI[k], Ea[2 * ks], Eb[2 * ks], Ea[2 * ks + 1], Eb[2 * ks + 1], QT[k][ks][0], QT[k][ks][1]);
+                uint32_t Ra[16], Rb[16];
+                key_rem<KB>(wa, lut_base, (uint32_t)lane, Ra);
+                key_rem<KB>(wb, lut_base, (uint32_t)lane, Rb);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const int n = 2 * ks;
-                    mma16816(sA, Ia[n], Ib[n], Ia[n + 1], Ib[n + 1], QAh[ks][0], QAh[ks][1]);
-                    mma16816(sB, Ia[n], Ib[n], Ia[n + 1], Ib[n + 1], QAl[ks][0], QAl[ks][1]);
                     mma16816(sC, Ra[n], Rb[n], Ra[n + 1], Rb[n + 1], QB[ks][0], QB[ks][1]);
                 }
             }
-            float t0 = sA[0] + sB[0] + sC[0] - off0, t1 = sA[1] + sB[1] + sC[1] - off1;
-            float t2 = sA[2] + sB[2] + sC[2] - off0, t3 = sA[3] + sB[3] + sC[3] - off1;
+            float iv[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                iv[c] = sI[0][c] + 0.0625f * sI[1][c] + 0.00390625f * sI[2][c] + 0.000244140625f * sI[3][c];
+            float t0 = fmaf(qs0, iv[0], sC[0] - off0), t1 = fmaf(qs1, iv[1], sC[1] - off1);
+            float t2 = fmaf(qs0, iv[2], sC[2] - off0), t3 = fmaf(qs1, iv[3], sC[3] - off1);
             if constexpr (M > 0) {
                 float sQ[4] = {0.f, 0.f, 0.f, 0.f};
                 uint32_t Za[16], Zb[16];
@@ -589,8 +657,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
                 for (int mt = 0; mt < 8; ++mt)  // rows: dim 16r + 2mt (row r), 16r + 2mt + 1 (row r + 8)
                     mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bh0, bh1);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            __syncwarp();  // every lane has read the slot: refill it with the page SPW ahead
+            jdone = j + 1;
+            const int jn = j + SPW;
+            if (jn < nmine) {
+                if ((jn & 31) == 0) {  // next batch of block ids; prefetch the one after it
+                    bid_cur = bid_nxt;
+                    const int k = 8 * (jn + 32 + lane);
+                    bid_nxt = (k < reach) ? __ldg(btw + k) : -1;
+                }
+                const int bk = __shfl_sync(0xffffffffu, bid_cur, jn & 31);
+                if (lane == 0) issue(jn, bk);
+            }
+        }
+        if (timed_out) {
+            // copies this warp started must land before its shared memory goes away;
+            // one shared deadline for all of them
+            const long long t0 = clock64();
+            for (int jj = jdone; jj < min(jdone + SPW, nmine); ++jj) {
+                const uint32_t bar = bar_full + 8 * (warp * SPW + (jj % SPW));
+                while (!mbar_try(bar, (jj / SPW) & 1) && clock64() - t0 < kWaitCycles) {
+                }
+            }
         }
 
         // ---- reduce l, z over the 8 token rows, publish warp state ----
@@ -621,7 +709,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             wacc[(warp * 8 + 2 * qd + 1) * D + dim + 1] = acc[mt][3];
         }
     }
-    if (warp == kNCW) __syncthreads();  // producer's side of (A)
     timed_out = __syncthreads_or(timed_out);  // (B)
     if (timed_out) {
         if (tid == 0) flag(a.status, TQ_FLAG_TIMEOUT);
@@ -662,49 +749,57 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             if (lane == 0) { pp[0] = Mx; pp[1] = L; }
             *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(O[0], O[1], O[2], O[3]);
         }
-        __threadfence();
+        // The CTA barrier orders every thread's partial writes before thread 0's
+        // gpu-scope release (cumulativity); the acquire side pairs with the other
+        // CTAs' releases before the last one reads their partials.
         __syncthreads();
         __shared__ int s_last;
-        if (tid == 0) s_last = (atomicAdd(a.counters + unit, 1u) == (unsigned)a.num_splits - 1);
+        if (tid == 0) {
+            unsigned old;
+            asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + unit) : "memory");
+            s_last = (old == (unsigned)a.num_splits - 1);
+        }
         __syncthreads();
         if (!s_last) return;
-        __threadfence();
         finalize = true;
         if (warp < G) {
-            // Lanes load the splits' (max, sum) in parallel; the acc loads of a
-            // group of up to 32 splits are independent of each other, so they
-            // overlap instead of paying one L2 round trip per split.
+            // All loads of a chunk of up to kMergeChunk splits are issued before
+            // any is used, so a chunk costs one L2 round trip; chunks merge with
+            // a running max.
+            constexpr int kMergeChunk = 20;
             const float* base = a.partials + (unit * a.num_splits * G) * kPartStride;
             const int ns = a.num_splits;
-            Mx = -INFINITY;
-            for (int s0 = 0; s0 < ns; s0 += 32) {
-                const int sp = s0 + lane;
-                Mx = fmaxf(Mx, sp < ns ? __ldcg(base + (sp * G + qg) * kPartStride) : -INFINITY);
-            }
-            Mx = warp_max(Mx);
-            L = 0.f;
+            float runM = -INFINITY, runL = 0.f;
             O[0] = O[1] = O[2] = O[3] = 0.f;
-            if (Mx != -INFINITY) {
-                for (int s0 = 0; s0 < ns; s0 += 32) {
-                    const int sp = s0 + lane;
-                    float f = 0.f, lv = 0.f;
-                    if (sp < ns) {
-                        const float ms = __ldcg(base + (sp * G + qg) * kPartStride);
-                        lv = __ldcg(base + (sp * G + qg) * kPartStride + 1);
-                        f = (ms == -INFINITY) ? 0.f : exp2f(ms - Mx);
-                    }
-                    L += warp_sum(f * lv);
-                    const int n = min(32, ns - s0);
-#pragma unroll 8
-                    for (int k = 0; k < n; ++k) {
-                        const float fk = __shfl_sync(0xffffffffu, f, k);
-                        const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                            base + ((s0 + k) * G + qg) * kPartStride + 4 + 4 * lane));
-                        O[0] = fmaf(fk, v.x, O[0]); O[1] = fmaf(fk, v.y, O[1]);
-                        O[2] = fmaf(fk, v.z, O[2]); O[3] = fmaf(fk, v.w, O[3]);
-                    }
+            for (int s0 = 0; s0 < ns; s0 += kMergeChunk) {
+                const int n = min(kMergeChunk, ns - s0);
+                float ms = -INFINITY, ls = 0.f;
+                if (lane < n) {
+                    ms = __ldcg(base + ((s0 + lane) * G + qg) * kPartStride);
+                    ls = __ldcg(base + ((s0 + lane) * G + qg) * kPartStride + 1);
                 }
+                float4 v[kMergeChunk];
+#pragma unroll
+                for (int k = 0; k < kMergeChunk; ++k)
+                    v[k] = (k < n) ? __ldcg(reinterpret_cast<const float4*>(base + ((s0 + k) * G + qg) * kPartStride + 4 + 4 * lane))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float nm = fmaxf(runM, warp_max(ms));
+                if (nm == -INFINITY) continue;
+                const float fr = (runM == -INFINITY) ? 0.f : exp2f(runM - nm);
+                const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - nm);
+                runL = fmaf(runL, fr, warp_sum(f * ls));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) O[i] *= fr;
+#pragma unroll
+                for (int k = 0; k < kMergeChunk; ++k) {
+                    const float fk = __shfl_sync(0xffffffffu, f, k);
+                    O[0] = fmaf(fk, v[k].x, O[0]); O[1] = fmaf(fk, v[k].y, O[1]);
+                    O[2] = fmaf(fk, v[k].z, O[2]); O[3] = fmaf(fk, v[k].w, O[3]);
+                }
+                runM = nm;
             }
+            Mx = runM;
+            L = runL;
         }
         if (tid == 0) a.counters[unit] = 0u;
     }
