@@ -85,6 +85,7 @@ typedef enum {
 #define TQ_FLAG_BAD_SLOT 2  /* a slot or block id outside the pool; that token/page was skipped */
 #define TQ_FLAG_NONFINITE 4 /* a key or value held NaN or inf; its codes are unspecified */
 #define TQ_FLAG_TIMEOUT 8   /* a bounded device wait gave up; the output is incomplete */
+#define TQ_FLAG_INTERNAL 16 /* the kernel could not lay out its shared memory; no output was written */
 
 /* Element type of K, V and q inputs. */
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;

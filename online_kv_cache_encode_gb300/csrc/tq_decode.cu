@@ -1,21 +1,25 @@
 // Decode attention over the compressed paged cache (split-K flash decode).
 //
-// Grid (split, KV head, sequence); one CTA per SM (shared memory bound).
-//  - Producer warp: reads block ids, streams whole pages (one page = 16
-//    tokens of one KV head, contiguous) into a shared-memory ring with 1-D
-//    bulk async copies (cp.async.bulk) completing on mbarriers.
-//  - 8 consumer warps: each takes whole pages and keeps its own online-softmax
-//    state for the G <= 8 query heads of the group.  Per page:
-//      scores  S[16 tok x 8 q] = A[16 tok x 128] . B[128 x 8 q]  (mma.sync m16n8k16,
-//              tokens as rows) where the key centroid is split as
-//              C[c] = alpha (c - mid) + rem[c]: the integer code c is exact in
-//              fp16 and multiplies alpha*q_rot split into fp16 hi + lo; rem[c]
-//              comes from a lane-private shared-memory table and multiplies
-//              q_rot's hi part.  logit = gamma_t * sm_scale * (S - alpha*mid*sum q_rot)
-//      softmax running max / sum per query (exp2 domain)
-//      values  O^T[128 x 8 q] += Vcode^T[128 x 16 tok] . (p * scale)^T[16 tok x 8 q],
-//              value codes exact in fp16, p*scale split into hi + lo; the
-//              zero-point term sum_t p_t zero_t is accumulated in fp32.
+// Grid (split, KV head, sequence); one CTA per SM.
+//  - Every warp takes every NW-th page of its split (one page = 16 tokens of
+//    one KV head, contiguous) and streams it into its own shared-memory ring
+//    slots with 1-D bulk async copies (cp.async.bulk) completing on mbarriers.
+//  - Per page, for the G <= 8 query heads of the group (queries as the n8 side
+//    of mma.sync, tokens as rows):
+//      scores  the key centroid is split as C[c] = alpha (c - mid) + rem[c].
+//              The integer code c, masked in place inside a 16-bit lane, is the
+//              exact fp16 subnormal c * 2^-e; it multiplies alpha*q_rot split
+//              into fp16 hi + lo parts that carry the matching 2^(e-24), so all
+//              products share one scale (m16n8k16, fp32 accumulate).  rem[c]
+//              comes in fp16 from a lane-private shared-memory table and
+//              multiplies q_rot (m16n8k16).
+//              logit = gamma_t * sm_scale * (sum_j C[c_j] q_rot[j]) [+ QJL term]
+//      softmax running max / sum per query in the exp2 domain; the page max is
+//              reduced across lanes only when some score beats the running max
+//      values  O^T[128 x 8 q] += Vcode^T[128 x 16 tok] . (p * scale)^T[16 tok x 8 q]
+//              (m16n8k16).  A value code masked in place inside a 16-bit lane is
+//              an exact fp16 subnormal c * 2^-e; the power of two is removed once
+//              at the end.  The zero-point term sum_t p_t zero_t is kept in fp32.
 //    Keys are never reconstructed; everything stays in the rotated frame
 //    ["OCTOPUS ..." -- TL;DR / step 7; deep dive -- [RHT effect]: inner
 //    products are preserved by the rotation].
@@ -26,17 +30,17 @@
 // quantized KV].
 #include <cuda_runtime.h>
 
-#include <cuda_fp8.h>
-
 #include "tq_device.cuh"
 
 namespace tq {
 
-constexpr int kNCW = 8;                       // warps per CTA, each consumes (and fetches) its own pages
-constexpr int kThreads = kNCW * 32;
-constexpr int kSlotsPerWarp = 8;              // ring slots per warp: pages a warp keeps in flight
-constexpr int kLutBytes = 256 * 256;          // 256 entries x 256 B (lanes use 128 B)
+constexpr int kMaxSlotsPerWarp = 8;            // ring slots per warp: pages a warp keeps in flight
+constexpr uint32_t kLutAddr = 0x10000;         // shared-window address of the remainder table
+constexpr int kLutBytes = 0x10000;
+constexpr int kMaxSmemBase = 4096;             // dynamic shared memory must start below this address
+constexpr int kSmemLimit = 227 * 1024;         // opt-in dynamic shared memory per CTA
 constexpr long long kWaitCycles = 3000000000ll;  // bound on any wait: ~1.5 s at 2 GHz
+constexpr float kMinusBig = -1.0e30f;          // running max before any token (finite: no inf - inf)
 // split partial record: max, sum, 2 pad, acc[128] (keeps the acc 16-byte aligned)
 constexpr int kPartStride = 4 + kHeadDim;
 
@@ -107,24 +111,12 @@ __device__ __forceinline__ float lds_h2f(uint32_t addr) {
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
     return __half2float(__ushort_as_half(v));
 }
-__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t m, uint32_t o) {
-    return (a & m) | o;
-}
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
 __device__ __forceinline__ uint32_t movtrans(uint32_t a) {
     uint32_t d;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
     return d;
 }
+// D = A . B + C, m16n8k16, fp16 operands, fp32 accumulate
 __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -133,97 +125,94 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// D += A . B with A 16x32, B 32x8 of e4m3, fp32 accumulate (exact products, fp32 sums)
-__device__ __forceinline__ void mma_e4m3(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
+// the same with the accumulator's starting value given separately
+__device__ __forceinline__ void mma16816_c(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3) {
     asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
-__device__ __forceinline__ uint32_t f2e4m3(float x) {
-    return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-}
-__device__ __forceinline__ float e4m3_2f(uint32_t b) {
-    return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3)));
+// 2^x with the hardware approximation (relative error ~2^-22; -inf gives 0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ float2 unpack_h2(uint32_t v) {
-    return __half22float2(*reinterpret_cast<__half2*>(&v));
-}
-// x ~= hi + lo, both binary16
-__device__ __forceinline__ void split_h2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-    hi = pack_h2(x0, x1);
-    float2 h = unpack_h2(hi);
-    lo = pack_h2(x0 - h.x, x1 - h.y);
-}
-__device__ __forceinline__ float h2f(uint16_t b) {
-    return __half2float(*reinterpret_cast<__half*>(&b));
-}
-
-// Four fp16x2 registers from one word of eight 4-bit codes n0..n7 (n_i at
-// bits 4i): reg i holds (n_i, n_{i+4}) as exact small integers.
-__device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t f[4]) {
-    const uint32_t magic = 0x64006400u;           // fp16 1024.0 in both halves
-    const uint32_t k1024 = 0x64006400u;
-    const uint32_t k16 = 0x2C002C00u;             // 1/16
-    const uint32_t km64 = 0xD400D400u;            // -64
-    const uint32_t w8 = w >> 8;
-    f[0] = hsub2(lop_and_or(w, 0x000F000Fu, magic), k1024);
-    f[1] = hfma2(lop_and_or(w, 0x00F000F0u, magic), k16, km64);
-    f[2] = hsub2(lop_and_or(w8, 0x000F000Fu, magic), k1024);
-    f[3] = hfma2(lop_and_or(w8, 0x00F000F0u, magic), k16, km64);
-}
 
 // ---------------------------------------------------------------------------
-// shared memory map (dynamic)
+// page format and shared memory map, both fixed at compile time per format
 // ---------------------------------------------------------------------------
-struct SmemMap {
-    int lut, rem, qrot, qoff, qscale, sq, bars, ok, ring;
-    int stages, stride, total;
+template <int KB, int VB, int M>
+struct PageFmt {
+    static constexpr int kcode = 0;
+    static constexpr int vcode = kBlockSize * kHeadDim * KB / 8;
+    static constexpr int gam = vcode + kBlockSize * kHeadDim * VB / 8;
+    static constexpr int scl = gam + 2 * kBlockSize;
+    static constexpr int zer = scl + 2 * kBlockSize;
+    static constexpr int rho = zer + 2 * kBlockSize;
+    static constexpr int sig = rho + (M ? 2 * kBlockSize : 0);
+    static constexpr int bytes = (sig + kBlockSize * M / 8 + 15) / 16 * 16;
+    static constexpr int stride = (bytes + 127) / 128 * 128;  // ring slot size
 };
 
-__host__ __device__ inline SmemMap smem_map(int page_bytes) {
-    SmemMap m;
+// Warps per CTA: the QJL sign term needs 32 more registers of query fragments.
+template <int M>
+__host__ __device__ constexpr int decode_warps() { return M ? 8 : 12; }
+
+// Per-lane query fragments (uint4 vectors): 8 of fp16 hi/lo alpha q_rot at the
+// code dims, 4 of fp16 q_rot at the remainder dims, 8 of fp16 hi/lo S q_rot for
+// the QJL term.
+template <int M>
+__host__ __device__ constexpr int frag_vecs() { return 8 + 4 + (M ? 8 : 0); }
+
+struct Layout {
+    int frag, qrot, sq, qoff, qscale, bars, ok;  // small fixed region at the start
+    int ringA, nwA;   // ring slots of warps 0 .. nwA-1 sit below the remainder table
+    int spw;          // ring slots per warp
+    int total;        // dynamic bytes to request: enough for any start address up to kMaxSmemBase
+};
+
+// The remainder table must sit at shared address kLutAddr (its entry index then
+// drops straight into bits 8..15 of the lookup address).  Ring slots of the
+// first warps fill the space below it, the rest follow it.
+template <int KB, int VB, int M>
+__host__ __device__ constexpr Layout decode_layout() {
+    constexpr int NW = decode_warps<M>();
+    Layout L{};
     int off = 0;
-    m.lut = off; off += kLutBytes;
-    m.rem = off; off += 16 * 2;
-    m.qrot = off; off += 8 * kHeadDim * 4;
-    m.qoff = off; off += 8 * 4;
-    m.qscale = off; off += 8 * 4;
-    m.sq = off; off += 8 * kHeadDim * 4;
-    m.stride = (page_bytes + 127) / 128 * 128;
-    m.stages = kNCW * kSlotsPerWarp;
-    m.bars = (off + 7) / 8 * 8; off = m.bars + 8 * m.stages;
-    m.ok = off; off += 4 * m.stages;
-    m.ring = (off + 127) / 128 * 128; off = m.ring + m.stride * m.stages;
-    m.total = off;
-    return m;
-}
-
-int decode_smem_bytes(const Geometry& g) { return smem_map((int)g.page_bytes).total; }
-
-// ---------------------------------------------------------------------------
-// code unpacking: every key / value code becomes an exact small integer in
-// fp16 (the 0x6400 "1024 + x" bit pattern, then the 1024 removed exactly)
-// ---------------------------------------------------------------------------
-// sixteen 2-bit codes c0..c15 of w (c_i at bits 2i) -> eight fp16x2 (c_i, c_{i+8})
-__device__ __forceinline__ void crumb16_to_h2(uint32_t w, uint32_t f[8]) {
-    const uint32_t magic = 0x64006400u;
-    const uint32_t scale[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};  // 1, 1/4, 1/16, 1/64
-    const uint32_t bias[4] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u};   // -1024, -256, -64, -16
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t x = (i < 4) ? w : (w >> 8);
-        const int k = i & 3;
-        f[i] = hfma2(lop_and_or(x, 0x00030003u << (2 * k), magic), scale[k], bias[k]);
+    L.frag = off; off += 32 * 16 * frag_vecs<M>();
+    L.qrot = off; off += 8 * kHeadDim * 4;
+    L.sq = off; off += M ? 8 * kHeadDim * 4 : 0;
+    L.qoff = off; off += 8 * 4;
+    L.qscale = off; off += 8 * 4;
+    L.bars = off; off += 8 * NW * kMaxSlotsPerWarp;
+    L.ok = off; off += 4 * NW * kMaxSlotsPerWarp;
+    L.ringA = (off + 127) / 128 * 128;
+    const int stride = PageFmt<KB, VB, M>::stride;
+    const int capA = (int)kLutAddr - kMaxSmemBase - L.ringA;
+    for (int spw = kMaxSlotsPerWarp; spw >= 1; --spw) {
+        const int per = spw * stride;
+        const int nA = capA / per < NW ? capA / per : NW;
+        const int total = (int)kLutAddr + kLutBytes + (NW - nA) * per;  // start address 0 is the worst case
+        if (total <= kSmemLimit) {
+            L.spw = spw;
+            L.nwA = nA;
+            L.total = total;
+            return L;
+        }
     }
+    return L;  // spw == 0: does not fit
 }
 
+// ---------------------------------------------------------------------------
+// code unpacking
+// ---------------------------------------------------------------------------
 // bits [pos, pos + n) of a little-endian multi-word bit string (pos, n compile-time after unrolling)
 template <int NW>
 __device__ __forceinline__ uint32_t bits_at(const uint32_t (&w)[NW], int pos, int n) {
@@ -232,101 +221,129 @@ __device__ __forceinline__ uint32_t bits_at(const uint32_t (&w)[NW], int pos, in
     return x & ((1u << n) - 1u);
 }
 
-__device__ __forceinline__ uint32_t int_pair_h2(uint32_t c0, uint32_t c1) {
-    return hsub2((c0 | (c1 << 16)) | 0x64006400u, 0x64006400u);
-}
-
-// Key chunk of one token: the 32 codes of dims 32qd .. 32qd+31 (4*KB bytes).
+// Key chunk of one token: the 32 codes of one 32-dim chunk (4*KB bytes).
 template <int KB>
-__device__ __forceinline__ void key_words(uint32_t row, int qd, uint32_t (&w)[KB]) {
+__device__ __forceinline__ void key_words(uint32_t addr, uint32_t (&w)[KB]) {
     if constexpr (KB == 4) {
-        const uint4 v = lds128(row + qd * 16);
+        const uint4 v = lds128(addr);
         w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
     } else if constexpr (KB == 2) {
-        const uint2 v = lds64(row + qd * 8);
+        const uint2 v = lds64(addr);
         w[0] = v.x; w[1] = v.y;
     } else {
-        w[0] = lds32(row + qd * 12); w[1] = lds32(row + qd * 12 + 4); w[2] = lds32(row + qd * 12 + 8);
+        w[0] = lds32(addr); w[1] = lds32(addr + 4); w[2] = lds32(addr + 8);
     }
 }
 
-// The integer codes as e4m3 operand bytes.  A code byte n < 16 read as e4m3 is
-// exactly n * 2^-9 (exponent field 0 is the subnormal n * 2^-9, field 1 is
-// (8 + m) * 2^-9), so the codes need only be spread into bytes.
-// E[e] byte i holds the code of chunk dim key_fp8_dim<KB>(e, i).
+// The integer codes as fp16 A operands.  A code c masked in place inside a
+// 16-bit half, below bit 10, is the exact subnormal c * 2^-24 shifted by its
+// bit position, so only masks (and one shift per word) are needed.  X[n] holds
+// two codes of the lane's 32-dim chunk: element h (0 low, 1 high) is chunk dim
+// key_dim<KB>(n, h), scaled by 2^-key_exp<KB>(n).  MMA k-step ks uses X[2ks]
+// (k = 2qd, 2qd+1) and X[2ks+1] (k = 8+2qd, 8+2qd+1).
 template <int KB>
-__host__ __device__ constexpr int key_fp8_dim(int e, int i) {
-    return KB == 4 ? 8 * (e >> 1) + 2 * i + (e & 1)
-         : KB == 2 ? 16 * (e >> 2) + 4 * i + (e & 3)
-                   : 4 * e + i;
+__host__ __device__ constexpr int key_dim(int n, int h) {
+    return KB == 4 ? 8 * (n >> 2) + (n & 3) + 4 * h : KB == 2 ? 16 * (n >> 3) + (n & 7) + 8 * h : 2 * n + h;
+}
+template <int KB>
+__host__ __device__ constexpr int key_exp(int n) {
+    return KB == 4 ? ((n & 1) ? 20 : 24) : KB == 2 ? 24 - 2 * (n & 3) : 24;
+}
+// inverse of key_dim: the register holding chunk dim c (its half is key_half)
+template <int KB>
+__host__ __device__ constexpr int key_reg(int c) {
+    return KB == 4 ? 4 * (c >> 3) + (c & 3) : KB == 2 ? 8 * (c >> 4) + (c & 7) : c >> 1;
+}
+template <int KB>
+__host__ __device__ constexpr int key_half(int c) {
+    return KB == 4 ? (c >> 2) & 1 : KB == 2 ? (c >> 3) & 1 : c & 1;
 }
 
-__device__ __forceinline__ uint32_t spread3x4(uint32_t t) {  // four 3-bit fields -> four bytes
-    return (t & 0x7u) | ((t & 0x38u) << 5) | ((t & 0x1C0u) << 10) | ((t & 0xE00u) << 15);
-}
-
 template <int KB>
-__device__ __forceinline__ void key_bytes(const uint32_t (&w)[KB], uint32_t E[8]) {
+__device__ __forceinline__ void key_halves(const uint32_t (&w)[KB], uint32_t X[16]) {
     if constexpr (KB == 4) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            E[2 * i] = w[i] & 0x0F0F0F0Fu;
-            E[2 * i + 1] = (w[i] >> 4) & 0x0F0F0F0Fu;
+            const uint32_t y = w[i] >> 8;
+            X[4 * i + 0] = w[i] & 0x000F000Fu;
+            X[4 * i + 1] = w[i] & 0x00F000F0u;
+            X[4 * i + 2] = y & 0x000F000Fu;
+            X[4 * i + 3] = y & 0x00F000F0u;
         }
     } else if constexpr (KB == 2) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t y = w[i] >> 8;
 #pragma unroll
-            for (int sh = 0; sh < 4; ++sh) E[4 * i + sh] = (w[i] >> (2 * sh)) & 0x03030303u;
+            for (int m = 0; m < 4; ++m) {
+                X[8 * i + m] = w[i] & (0x00030003u << (2 * m));
+                X[8 * i + 4 + m] = y & (0x00030003u << (2 * m));
+            }
+        }
     } else {
 #pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-            const uint32_t x = bits_at<3>(w, 24 * gi, 24);
-            E[2 * gi] = spread3x4(x & 0xFFFu);
-            E[2 * gi + 1] = spread3x4(x >> 12);
+        for (int n = 0; n < 16; ++n) {
+            const uint32_t x = bits_at<3>(w, 6 * n, 6);
+            X[n] = (x & 7u) | ((x << 13) & 0x70000u);
         }
     }
 }
 
-// Remainder operands: R[n] = (rem[c_{2n}], rem[c_{2n+1}]) from the lane-private table.
+// Remainder operands R[n] = (rem[c_{2n}], rem[c_{2n+1}]) from the lane-private
+// table at kLutAddr.  lw = kLutAddr | lane offset; for 2- and 4-bit keys a code
+// byte is the entry index and is dropped into bits 8..15 of the address with
+// one byte permute.
 template <int KB>
-__device__ __forceinline__ void key_rem(const uint32_t (&w)[KB], uint32_t lut, uint32_t lane, uint32_t R[16]) {
+__device__ __forceinline__ void key_rem(const uint32_t (&w)[KB], uint32_t lw, uint32_t R[16]) {
     if constexpr (KB == 4) {
-        const uint32_t lw = lane << 2;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) R[n] = lds32(lut + prmt(w[n >> 2], lw, 0x5504u | ((uint32_t)(n & 3) << 4)));
+        for (int n = 0; n < 16; ++n) R[n] = lds32(prmt(w[n >> 2], lw, 0x7604u | ((uint32_t)(n & 3) << 4)));
     } else if constexpr (KB == 2) {
-        const uint32_t lw = lane << 3;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const uint2 v = lds64(lut + prmt(w[j >> 2], lw, 0x5504u | ((uint32_t)(j & 3) << 4)));
+            const uint2 v = lds64(prmt(w[j >> 2], lw, 0x7604u | ((uint32_t)(j & 3) << 4)));
             R[2 * j] = v.x;
             R[2 * j + 1] = v.y;
         }
     } else {
-        const uint32_t lw = lane << 2;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) R[n] = lds32(lut + (bits_at<3>(w, 6 * n, 6) << 7) + lw);
+        for (int n = 0; n < 16; ++n) R[n] = lds32(lw | (bits_at<3>(w, 6 * n, 6) << 7));
     }
 }
 
-// Value codes of dims 16r .. 16r+15 for a token pair (ta, tb): P[i] = (code_ta, code_tb)
-// of dim 16r + i as exact fp16 integers.
+// Value codes of dims 16r .. 16r+15 for a token pair (ta, tb): P[i] holds the
+// codes of dim 16r + i for ta (low half) and tb (high half) as fp16 subnormals
+// code * 2^-value_exp<VB>(i), exact.
 template <int VB>
-__device__ __forceinline__ void value_pair(uint32_t vbase, int r, int ta, int tb, uint32_t P[16]) {
+__host__ __device__ constexpr int value_exp(int i) {
+    return VB == 4 ? ((i & 1) ? 20 : 24) : VB == 2 ? 24 - 2 * (i & 3) : 24;
+}
+template <int VB>
+__device__ __forceinline__ void value_codes(uint32_t vbase, int r, int ta, int tb, uint32_t P[16]) {
     constexpr int ROW = kHeadDim * VB / 8;
     if constexpr (VB == 4) {
         const uint2 va = lds64(vbase + ta * ROW + r * 8);
         const uint2 vb = lds64(vbase + tb * ROW + r * 8);
-        nib8_to_h2(prmt(va.x, vb.x, 0x5410u), &P[0]);
-        nib8_to_h2(prmt(va.x, vb.x, 0x7632u), &P[4]);
-        nib8_to_h2(prmt(va.y, vb.y, 0x5410u), &P[8]);
-        nib8_to_h2(prmt(va.y, vb.y, 0x7632u), &P[12]);
+        const uint32_t x[4] = {prmt(va.x, vb.x, 0x5410u), prmt(va.x, vb.x, 0x7632u), prmt(va.y, vb.y, 0x5410u),
+                               prmt(va.y, vb.y, 0x7632u)};
+#pragma unroll
+        for (int hq = 0; hq < 4; ++hq) {
+            P[4 * hq + 0] = x[hq] & 0x000F000Fu;
+            P[4 * hq + 1] = x[hq] & 0x00F000F0u;
+            P[4 * hq + 2] = (x[hq] >> 8) & 0x000F000Fu;
+            P[4 * hq + 3] = (x[hq] >> 8) & 0x00F000F0u;
+        }
     } else if constexpr (VB == 2) {
         const uint32_t wa = lds32(vbase + ta * ROW + r * 4);
         const uint32_t wb = lds32(vbase + tb * ROW + r * 4);
-        crumb16_to_h2(prmt(wa, wb, 0x5410u), &P[0]);
-        crumb16_to_h2(prmt(wa, wb, 0x7632u), &P[8]);
+        const uint32_t x[2] = {prmt(wa, wb, 0x5410u), prmt(wa, wb, 0x7632u)};
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t y = (i < 4) ? x[hq] : (x[hq] >> 8);
+                P[8 * hq + i] = y & (0x00030003u << (2 * (i & 3)));
+            }
     } else {
         const int base = (6 * r) & ~3, sh = ((6 * r) & 3) * 8;
         const uint32_t a0 = lds32(vbase + ta * ROW + base), a1 = lds32(vbase + ta * ROW + base + 4);
@@ -334,7 +351,7 @@ __device__ __forceinline__ void value_pair(uint32_t vbase, int r, int ta, int tb
         const uint32_t xa[2] = {__funnelshift_r(a0, a1, sh), a1 >> sh};
         const uint32_t xb[2] = {__funnelshift_r(b0, b1, sh), b1 >> sh};
 #pragma unroll
-        for (int i = 0; i < 16; ++i) P[i] = int_pair_h2(bits_at<2>(xa, 3 * i, 3), bits_at<2>(xb, 3 * i, 3));
+        for (int i = 0; i < 16; ++i) P[i] = bits_at<2>(xa, 3 * i, 3) | (bits_at<2>(xb, 3 * i, 3) << 16);
     }
 }
 
@@ -349,41 +366,53 @@ __device__ __forceinline__ void sign_chunk(uint32_t w, uint32_t Z[16]) {
 // the kernel
 // ---------------------------------------------------------------------------
 template <int KB, int VB, int M>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const DecodeArgs a) {
     static_assert(KB >= 2 && KB <= 4 && VB >= 2 && VB <= 4 && (M == 0 || M == 128), "unsupported page format");
+    using F = PageFmt<KB, VB, M>;
+    constexpr int NW = decode_warps<M>();
+    constexpr int NT = NW * 32;
+    constexpr Layout LY = decode_layout<KB, VB, M>();
+    constexpr int SPW = LY.spw;
+    static_assert(SPW >= 1, "page format does not fit in shared memory");
+    constexpr int D = kHeadDim;
+    constexpr int KROW = D * KB / 8;
     extern __shared__ __align__(128) uint8_t sm[];
     const Geometry& g = a.g;
-    constexpr int D = kHeadDim;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = a.group;
-    const SmemMap mp = smem_map((int)g.page_bytes);
-    constexpr int SPW = kSlotsPerWarp;
 
-    float* qrot = reinterpret_cast<float*>(sm + mp.qrot);
-    float* qoff = reinterpret_cast<float*>(sm + mp.qoff);
-    float* qscale = reinterpret_cast<float*>(sm + mp.qscale);
-    int* slot_ok = reinterpret_cast<int*>(sm + mp.ok);
-    const uint32_t bar_full = smem_u32(sm + mp.bars);
-    const uint32_t lut_base = smem_u32(sm + mp.lut);
-    const uint32_t ring_base = smem_u32(sm + mp.ring);
-    uint8_t* ring = sm + mp.ring;
+    // The layout assumes dynamic shared memory starts below kMaxSmemBase.
+    const uint32_t sbase = smem_u32(sm);
+    if (sbase > (uint32_t)kMaxSmemBase) {
+        if (tid == 0) flag(a.status, TQ_FLAG_INTERNAL);
+        return;
+    }
+    const int lut_off = (int)kLutAddr - (int)sbase;  // byte offset of the remainder table in sm[]
+    const uint32_t ring_w = (warp < LY.nwA) ? sbase + LY.ringA + warp * SPW * F::stride
+                                           : kLutAddr + kLutBytes + (warp - LY.nwA) * SPW * F::stride;
+    const uint32_t bar_w = sbase + LY.bars + 8 * warp * kMaxSlotsPerWarp;
+    int* slot_ok = reinterpret_cast<int*>(sm + LY.ok) + warp * kMaxSlotsPerWarp;
+    float* qrot = reinterpret_cast<float*>(sm + LY.qrot);
+    float* qoff = reinterpret_cast<float*>(sm + LY.qoff);
+    float* qscale = reinterpret_cast<float*>(sm + LY.qscale);
     const int p0 = split * a.pages_per_split;
+    const float ksc = a.sm_scale_log2;
 
     // ---- independent global loads first: length, this warp's block ids, the query ----
-    // Warp w handles pages w, w + 8, w + 16, ... of the split (its j-th page is
-    // w + 8 j) in its own ring slots w*SPW .. w*SPW + SPW - 1.  Lane l holds the
-    // block id of the warp's page l of the current batch of 32 (bid_cur) and of
-    // the next batch (bid_nxt).
+    // Warp w handles pages w, w + NW, w + 2 NW, ... of the split (its j-th page
+    // is w + NW j) in its own SPW ring slots.  Lane l holds the block id of the
+    // warp's page l of the current batch of 32 (bid_cur) and of the next batch
+    // (bid_nxt).
     int len = __ldg(a.lens + b);
     const int32_t* btw = a.block_table + (int64_t)b * a.max_blocks + p0 + warp;
     const int reach = min(a.pages_per_split, a.max_blocks - p0) - warp;  // pages of the split at or after this warp's first
-    int bid_cur = (8 * lane < reach) ? __ldg(btw + 8 * lane) : -1;
-    int bid_nxt = (8 * (32 + lane) < reach) ? __ldg(btw + 8 * (32 + lane)) : -1;
+    int bid_cur = (NW * lane < reach) ? __ldg(btw + NW * lane) : -1;
+    int bid_nxt = (NW * (32 + lane) < reach) ? __ldg(btw + NW * (32 + lane)) : -1;
     float x[4] = {0.f, 0.f, 0.f, 0.f};
     if (warp < G) load4(a.q, a.dtype, ((int64_t)b * a.hq + (int64_t)h * G + warp) * D + 4 * lane, x);
     if (lane == 0) {
-        for (int k = 0; k < SPW; ++k) mbar_init(bar_full + 8 * (warp * SPW + k), 1);
+        for (int k = 0; k < SPW; ++k) mbar_init(bar_w + 8 * k, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
@@ -398,59 +427,60 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     int npages = seq_pages - p0;
     if (npages > a.pages_per_split) npages = a.pages_per_split;
     if (npages < 0) npages = 0;
-    const int nmine = npages > warp ? (npages - warp + kNCW - 1) / kNCW : 0;  // this warp's pages
+    const int nmine = npages > warp ? (npages - warp + NW - 1) / NW : 0;  // this warp's pages
 
-    // Start a page copy into the warp's ring slot; a bad block id arrives on the
-    // barrier without data and the page is skipped.
-    auto issue = [&](int j, int blk) {
-        const int sl = warp * SPW + (j % SPW);
+    // Start a page copy into ring slot `slot` of this warp; a bad block id
+    // arrives on the barrier without data and the page is skipped.
+    auto issue = [&](int slot, int blk) {
         const bool ok = blk >= 0 && blk < g.num_blocks;
-        slot_ok[sl] = ok;
+        const uint32_t bar = bar_w + 8 * slot;
+        slot_ok[slot] = ok;
         if (ok) {
-            mbar_arrive_tx(bar_full + 8 * sl, (uint32_t)g.page_bytes);
-            bulk_g2s(ring_base + sl * mp.stride, a.pool + ((int64_t)blk * g.hkv + h) * g.page_bytes,
-                     (uint32_t)g.page_bytes, bar_full + 8 * sl);
+            mbar_arrive_tx(bar, (uint32_t)F::bytes);
+            bulk_g2s(ring_w + slot * F::stride, a.pool + ((int64_t)blk * g.hkv + h) * F::bytes, (uint32_t)F::bytes,
+                     bar);
         } else {
             flag(a.status, TQ_FLAG_BAD_SLOT);
-            mbar_arrive(bar_full + 8 * sl);
+            mbar_arrive(bar);
         }
     };
     if (lane < SPW && lane < nmine) issue(lane, bid_cur);  // the first SPW pages, one lane each
 
     bool timed_out = false;
     {
-        // Lane-private remainder table (copy for lane l at entry*stride + l*width):
+        // Lane-private remainder table at shared address kLutAddr (copy for
+        // lane l at entry*stride + l*width):
         //   4-bit keys: byte e (2 codes) -> (rem[e&15], rem[e>>4])              stride 256, 4 B
         //   2-bit keys: byte e (4 codes) -> (rem[c0], rem[c1]), (rem[c2], rem[c3]) stride 256, 8 B
         //   3-bit keys: 6 bits e (2 codes) -> (rem[e&7], rem[e>>3])              stride 128, 4 B
-        uint16_t* rem = reinterpret_cast<uint16_t*>(sm + mp.rem);
-        if (tid < 16) rem[tid] = a.c.rem_f16[tid];
-        __syncthreads();
         {
+            uint8_t* lut = sm + lut_off;
+            const uint16_t* rem = a.c.rem_f16;
             if constexpr (KB == 4) {
-                for (int i = tid; i < 256 * 32; i += kNCW * 32) {
-                    const int e = i >> 5, l = i & 31;
-                    *reinterpret_cast<uint32_t*>(sm + mp.lut + e * 256 + 4 * l) =
-                        (uint32_t)rem[e & 15] | ((uint32_t)rem[e >> 4] << 16);
+                for (int i = tid; i < 256 * 8; i += NT) {   // entry e, lanes 4k..4k+3
+                    const int e = i >> 3, k = i & 7;
+                    const uint32_t v = (uint32_t)rem[e & 15] | ((uint32_t)rem[e >> 4] << 16);
+                    *reinterpret_cast<uint4*>(lut + e * 256 + 16 * k) = make_uint4(v, v, v, v);
                 }
             } else if constexpr (KB == 2) {
-                for (int i = tid; i < 256 * 32; i += kNCW * 32) {
-                    const int e = i >> 5, l = i & 31;
-                    uint2 v;
-                    v.x = (uint32_t)rem[e & 3] | ((uint32_t)rem[(e >> 2) & 3] << 16);
-                    v.y = (uint32_t)rem[(e >> 4) & 3] | ((uint32_t)rem[e >> 6] << 16);
-                    *reinterpret_cast<uint2*>(sm + mp.lut + e * 256 + 8 * l) = v;
+                for (int i = tid; i < 256 * 16; i += NT) {  // entry e, lanes 2k, 2k+1
+                    const int e = i >> 4, k = i & 15;
+                    const uint32_t xx = (uint32_t)rem[e & 3] | ((uint32_t)rem[(e >> 2) & 3] << 16);
+                    const uint32_t yy = (uint32_t)rem[(e >> 4) & 3] | ((uint32_t)rem[e >> 6] << 16);
+                    *reinterpret_cast<uint4*>(lut + e * 256 + 16 * k) = make_uint4(xx, yy, xx, yy);
                 }
             } else {
-                for (int i = tid; i < 64 * 32; i += kNCW * 32) {
-                    const int e = i >> 5, l = i & 31;
-                    *reinterpret_cast<uint32_t*>(sm + mp.lut + e * 128 + 4 * l) =
-                        (uint32_t)rem[e & 7] | ((uint32_t)rem[e >> 3] << 16);
+                for (int i = tid; i < 64 * 8; i += NT) {    // entry e, lanes 4k..4k+3
+                    const int e = i >> 3, k = i & 7;
+                    const uint32_t v = (uint32_t)rem[e & 7] | ((uint32_t)rem[e >> 3] << 16);
+                    *reinterpret_cast<uint4*>(lut + e * 128 + 16 * k) = make_uint4(v, v, v, v);
                 }
             }
         }
-        // q_rot = R q for query (warp) of this group, and alpha * mid * sum(q_rot)
-        {
+        // q_rot = R q for query (warp) of this group; its per-query constants:
+        //   qoff   = sm_scale log2(e) alpha mid sum(q_rot)
+        //   qscale = power of two putting max |ksc alpha q_rot| / qscale in (256, 512]
+        if (warp < 8) {
             if (warp < G) {
                 apply_signs(x, lane_signs(a.c, lane));
                 fwht128(x, lane);
@@ -460,27 +490,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
 #pragma unroll
             for (int i = 0; i < 4; ++i) qrot[warp * D + 4 * lane + i] = x[i];
             const float sq = warp_sum(x[0] + x[1] + x[2] + x[3]);
-            // power-of-two scale putting max |alpha q_rot 2^9| / scale in (112, 224]: e4m3 range
             const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
-            const float big = fabsf(a.c.alpha) * 512.f * mx;
-            const float scl = (big > 0.f) ? exp2f(ceilf(log2f(big / 224.f))) : 1.f;
+            const float big = fabsf(a.c.alpha) * ksc * mx;
+            const float scl = (big > 0.f) ? exp2f(ceilf(log2f(big / 512.f))) : 1.f;
             if (lane == 0) {
-                qoff[warp] = a.c.alpha * (float)((1 << KB) - 1) * 0.5f * sq;
+                qoff[warp] = ksc * a.c.alpha * (float)((1 << KB) - 1) * 0.5f * sq;
                 qscale[warp] = scl;
             }
         }
         __syncthreads();
-        float* sqv = reinterpret_cast<float*>(sm + mp.sq);  // [8][128]: S q_rot per query
+        float* sqv = reinterpret_cast<float*>(sm + LY.sq);  // [8][128]: sm_scale log2(e) S q_rot per query
         if constexpr (M > 0) {
-            // (S q_rot)_i for every query of the group: thread -> row i, queries g0, g0+2, ...
+            // thread -> row i of S, queries g0, g0 + NT/M, ...
             const int i = tid & (M - 1), g0 = tid / M;
+            constexpr int GS = NT / M;
             const float4* srow = reinterpret_cast<const float4*>(a.S + (int64_t)i * D);
-            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc4[(8 + GS - 1) / GS];
+#pragma unroll
+            for (int k = 0; k < (8 + GS - 1) / GS; ++k) acc4[k] = 0.f;
             for (int j4 = 0; j4 < D / 4; ++j4) {
                 const float4 sv = __ldg(srow + j4);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int gq = g0 + (kNCW * 32 / M) * k;
+                for (int k = 0; k < (8 + GS - 1) / GS; ++k) {
+                    const int gq = g0 + GS * k;
                     if (gq < 8) {
                         const float4 qv = *reinterpret_cast<const float4*>(qrot + gq * D + 4 * j4);
                         acc4[k] = fmaf(sv.x, qv.x, fmaf(sv.y, qv.y, fmaf(sv.z, qv.z, fmaf(sv.w, qv.w, acc4[k]))));
@@ -488,145 +520,161 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
                 }
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int gq = g0 + (kNCW * 32 / M) * k;
-                if (gq < 8) sqv[gq * D + i] = acc4[k];
+            for (int k = 0; k < (8 + GS - 1) / GS; ++k) {
+                const int gq = g0 + GS * k;
+                if (gq < 8) sqv[gq * D + i] = ksc * acc4[k];
             }
             __syncthreads();
         }
 
-        const int r = lane >> 2, qd = lane & 3;   // r: token row / query column; qd: quad index
-        // ---- B fragments (queries as columns): k-step ks, slot s uses pair n = 2ks + s ----
-        //   QT:      alpha*q_rot*2^9/scale at the code dims, as four e4m3 terms t_k, the
-        //            k-th carrying 16^k x the residual left by the earlier ones (~16 bits)
-        //   QB:      q_rot hi at the remainder dims (2n, 2n+1)
-        //   QSh/QSl: S q_rot at sign dims (n, n+16), hi + lo (QJL)
-        uint32_t QT[4][4][2], QB[8][2];
-        uint32_t QSh[M > 0 ? 8 : 1][2], QSl[M > 0 ? 8 : 1][2];
+        // ---- per-lane query fragments, written once per CTA in lane-major order ----
+        // (word w of lane l at ((w / 4) * 32 + l) * 16 + (w % 4) * 4, so that a
+        // warp reads each group of four words with one conflict-free 16-byte load)
+        //   words  0..31  QI: x = ksc alpha q_rot / qscale in fp16 hi + lo; word
+        //                 4 ks + 2 part + slot holds part (0 hi, 1 lo) of x 2^(e-24)
+        //                 at the dims of key register X[2 ks + slot] (e its scale)
+        //   words 32..47  QB: sm_scale log2(e) q_rot in fp16 at remainder dims (2n, 2n+1)
+        //   words 48..79  QSh / QSl: sqv hi + lo in fp16 at sign dims (n, n + 16)
         {
-            const float* qr = qrot + r * D + 32 * qd;
-            const float al = a.c.alpha * 512.f / qscale[r];
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-                for (int sl = 0; sl < 2; ++sl) {
-                    uint32_t tb[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float res = al * qr[key_fp8_dim<KB>(2 * ks + sl, i)];
-                        float mul = 1.f;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t t = f2e4m3(res * mul);
-                            res -= e4m3_2f(t) / mul;
-                            mul *= 16.f;
-                            tb[k] |= t << (8 * i);
-                        }
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) QT[k][ks][sl] = tb[k];
+            uint8_t* fr = sm + LY.frag;
+            for (int t = tid; t < 8 * D; t += NT) {
+                const int gq = t >> 7, dim = t & (D - 1);
+                const int ln = gq * 4 + (dim >> 5), c = dim & 31;
+                auto word = [&](int w) -> uint8_t* { return fr + (((w >> 2) * 32 + ln) * 16 + (w & 3) * 4); };
+                const float q = qrot[gq * D + dim];
+                const int n = key_reg<KB>(c), hh = key_half<KB>(c);
+                const float xs = ksc * a.c.alpha / qscale[gq] * q * exp2f((float)(key_exp<KB>(n) - 24));
+                const __half xh = __float2half_rn(xs);
+                reinterpret_cast<__half*>(word(4 * (n >> 1) + (n & 1)))[hh] = xh;
+                reinterpret_cast<__half*>(word(4 * (n >> 1) + 2 + (n & 1)))[hh] = __float2half_rn(xs - __half2float(xh));
+                reinterpret_cast<__half*>(word(32 + (c >> 1)))[c & 1] = __float2half_rn(q * ksc);
+                if constexpr (M > 0) {
+                    const float v = sqv[gq * D + dim];
+                    const __half hi = __float2half_rn(v);
+                    const __half lo = __float2half_rn(v - __half2float(hi));
+                    reinterpret_cast<__half*>(word(48 + (c & 15)))[c >> 4] = hi;
+                    reinterpret_cast<__half*>(word(64 + (c & 15)))[c >> 4] = lo;
                 }
             }
+        }
+        __syncthreads();
+        const int r = lane >> 2, qd = lane & 3;   // r: token row / query column; qd: quad index
+        uint32_t QI[8][4], QB[16];
+        uint32_t QSh[M > 0 ? 16 : 1], QSl[M > 0 ? 16 : 1];
+        {
+            const uint4* fv = reinterpret_cast<const uint4*>(sm + LY.frag) + lane;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
+            for (int v = 0; v < 8; ++v) {
+                const uint4 t = fv[v * 32];
+                QI[v][0] = t.x; QI[v][1] = t.y; QI[v][2] = t.z; QI[v][3] = t.w;
+            }
 #pragma unroll
-                for (int sl = 0; sl < 2; ++sl) {
-                    const int n = 2 * ks + sl;
-                    QB[ks][sl] = pack_h2(qr[2 * n], qr[2 * n + 1]);
-                    if constexpr (M > 0) {
-                        const float* sr = sqv + r * D + 32 * qd;
-                        split_h2(sr[n], sr[n + 16], QSh[ks][sl], QSl[ks][sl]);
-                    }
+            for (int v = 0; v < 4; ++v) {
+                const uint4 t = fv[(8 + v) * 32];
+                QB[4 * v] = t.x; QB[4 * v + 1] = t.y; QB[4 * v + 2] = t.z; QB[4 * v + 3] = t.w;
+            }
+            if constexpr (M > 0) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint4 t = fv[(12 + v) * 32], u = fv[(16 + v) * 32];
+                    QSh[4 * v] = t.x; QSh[4 * v + 1] = t.y; QSh[4 * v + 2] = t.z; QSh[4 * v + 3] = t.w;
+                    QSl[4 * v] = u.x; QSl[4 * v + 1] = u.y; QSl[4 * v + 2] = u.z; QSl[4 * v + 3] = u.w;
                 }
             }
         }
         const float off0 = qoff[2 * qd], off1 = qoff[2 * qd + 1];
-        const float qs0 = qscale[2 * qd], qs1 = qscale[2 * qd + 1];
-        const float ksc = a.sm_scale_log2;
+        const float qs0 = qscale[2 * qd] * 16777216.f, qs1 = qscale[2 * qd + 1] * 16777216.f;  // 2^24 qscale
         const float cq = 1.2533141373155003f / (float)(M > 0 ? M : 1);  // sqrt(pi/2) / m
-        constexpr int KROW = D * KB / 8;
+        const uint32_t lw = kLutAddr | ((uint32_t)lane << (KB == 2 ? 3 : 2));
+        const int koff = F::kcode + r * KROW + qd * 4 * KB;  // this lane's key chunk in a page
 
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+        float m0 = kMinusBig, m1 = kMinusBig, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
         float acc[8][4];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-        int jdone = 0;  // pages of this warp consumed
+        int slot = 0;
+        uint32_t phase = 0;
+        int issued = min(SPW, nmine);   // pages of this warp whose copies were started
+        int jfail = nmine;              // first page whose wait gave up
         for (int j = 0; j < nmine; ++j) {
-            const int pi = warp + kNCW * j;
-            const int s = warp * SPW + (j % SPW);
-            if (!mbar_wait(bar_full + 8 * s, (j / SPW) & 1)) {
+            if (!mbar_wait(bar_w + 8 * slot, phase)) {
                 timed_out = true;
+                jfail = j;
                 break;
             }
-            const uint32_t pg = ring_base + s * mp.stride;  // shared-space address of the page
-            const bool pok = slot_ok[s] != 0;
+            const uint32_t pg = ring_w + slot * F::stride;  // shared-space address of the page
+            const bool pok = slot_ok[slot] != 0;
 
             // ---------- scores: tokens r (rows 0-7) and r+8 (rows 8-15) ----------
-            float sI[4][4], sC[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) sI[k][0] = sI[k][1] = sI[k][2] = sI[k][3] = 0.f;
+            uint32_t wa[KB], wb[KB];
+            key_words<KB>(pg + koff, wa);
+            key_words<KB>(pg + koff + 8 * KROW, wb);
+            float I0[4], I1[4], R0[4], R1[4];
             {
-                uint32_t wa[KB], wb[KB];
-                key_words<KB>(pg + g.kcode_off + r * KROW, qd, wa);
-                key_words<KB>(pg + g.kcode_off + (r + 8) * KROW, qd, wb);
-                uint32_t Ea[8], Eb[8];
-                key_bytes<KB>(wa, Ea);
-                key_bytes<KB>(wb, Eb);
+                uint32_t Xa[16], Xb[16];
+                key_halves<KB>(wa, Xa);
+                key_halves<KB>(wb, Xb);
+                mma16816_c(I0, Xa[0], Xb[0], Xa[1], Xb[1], QI[0][0], QI[0][1], 0.f, 0.f, 0.f, 0.f);
+                mma16816(I0, Xa[0], Xb[0], Xa[1], Xb[1], QI[0][2], QI[0][3]);
+                mma16816_c(I1, Xa[2], Xb[2], Xa[3], Xb[3], QI[1][0], QI[1][1], 0.f, 0.f, 0.f, 0.f);
+                mma16816(I1, Xa[2], Xb[2], Xa[3], Xb[3], QI[1][2], QI[1][3]);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_e4m3(sI[k], Ea[2 * ks], Eb[2 * ks], Ea[2 * ks + 1], Eb[2 * ks + 1], QT[k][ks][0], QT[k][ks][1]);
-                uint32_t Ra[16], Rb[16];
-                key_rem<KB>(wa, lut_base, (uint32_t)lane, Ra);
-                key_rem<KB>(wb, lut_base, (uint32_t)lane, Rb);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int n = 2 * ks;
-                    mma16816(sC, Ra[n], Rb[n], Ra[n + 1], Rb[n + 1], QB[ks][0], QB[ks][1]);
+                for (int ks = 2; ks < 8; ++ks) {
+                    float* I = (ks & 1) ? I1 : I0;
+                    mma16816(I, Xa[2 * ks], Xb[2 * ks], Xa[2 * ks + 1], Xb[2 * ks + 1], QI[ks][0], QI[ks][1]);
+                    mma16816(I, Xa[2 * ks], Xb[2 * ks], Xa[2 * ks + 1], Xb[2 * ks + 1], QI[ks][2], QI[ks][3]);
                 }
             }
-            float iv[4];
+            {
+                uint32_t Ra[16], Rb[16];
+                key_rem<KB>(wa, lw, Ra);
+                key_rem<KB>(wb, lw, Rb);
+                mma16816_c(R0, Ra[0], Rb[0], Ra[1], Rb[1], QB[0], QB[1], -off0, -off1, -off0, -off1);
+                mma16816_c(R1, Ra[2], Rb[2], Ra[3], Rb[3], QB[2], QB[3], 0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                iv[c] = sI[0][c] + 0.0625f * sI[1][c] + 0.00390625f * sI[2][c] + 0.000244140625f * sI[3][c];
-            float t0 = fmaf(qs0, iv[0], sC[0] - off0), t1 = fmaf(qs1, iv[1], sC[1] - off1);
-            float t2 = fmaf(qs0, iv[2], sC[2] - off0), t3 = fmaf(qs1, iv[3], sC[3] - off1);
-            if constexpr (M > 0) {
-                float sQ[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t Za[16], Zb[16];
-                sign_chunk(lds32(pg + g.sig_off + r * (M / 8) + 4 * qd), Za);
-                sign_chunk(lds32(pg + g.sig_off + (r + 8) * (M / 8) + 4 * qd), Zb);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
+                for (int ks = 2; ks < 8; ++ks) {
                     const int n = 2 * ks;
-                    mma16816(sQ, Za[n], Zb[n], Za[n + 1], Zb[n + 1], QSh[ks][0], QSh[ks][1]);
-                    mma16816(sQ, Za[n], Zb[n], Za[n + 1], Zb[n + 1], QSl[ks][0], QSl[ks][1]);
+                    mma16816((ks & 1) ? R1 : R0, Ra[n], Rb[n], Ra[n + 1], Rb[n + 1], QB[n], QB[n + 1]);
                 }
-                const float rr = cq * lds_h2f(pg + g.rho_off + 2 * r), rr8 = cq * lds_h2f(pg + g.rho_off + 2 * (r + 8));
+            }
+            float t0 = fmaf(qs0, I0[0] + I1[0], R0[0] + R1[0]), t1 = fmaf(qs1, I0[1] + I1[1], R0[1] + R1[1]);
+            float t2 = fmaf(qs0, I0[2] + I1[2], R0[2] + R1[2]), t3 = fmaf(qs1, I0[3] + I1[3], R0[3] + R1[3]);
+            if constexpr (M > 0) {
+                float sQ[4];
+                uint32_t Za[16], Zb[16];
+                sign_chunk(lds32(pg + F::sig + r * (M / 8) + 4 * qd), Za);
+                sign_chunk(lds32(pg + F::sig + (r + 8) * (M / 8) + 4 * qd), Zb);
+                mma16816_c(sQ, Za[0], Zb[0], Za[1], Zb[1], QSh[0], QSh[1], 0.f, 0.f, 0.f, 0.f);
+                mma16816(sQ, Za[0], Zb[0], Za[1], Zb[1], QSl[0], QSl[1]);
+#pragma unroll
+                for (int ks = 1; ks < 8; ++ks) {
+                    const int n = 2 * ks;
+                    mma16816(sQ, Za[n], Zb[n], Za[n + 1], Zb[n + 1], QSh[n], QSh[n + 1]);
+                    mma16816(sQ, Za[n], Zb[n], Za[n + 1], Zb[n + 1], QSl[n], QSl[n + 1]);
+                }
+                const float rr = cq * lds_h2f(pg + F::rho + 2 * r), rr8 = cq * lds_h2f(pg + F::rho + 2 * (r + 8));
                 t0 = fmaf(rr, sQ[0], t0); t1 = fmaf(rr, sQ[1], t1);
                 t2 = fmaf(rr8, sQ[2], t2); t3 = fmaf(rr8, sQ[3], t3);
             }
-            const float gr = lds_h2f(pg + g.gam_off + 2 * r) * ksc, gr8 = lds_h2f(pg + g.gam_off + 2 * (r + 8)) * ksc;
-            const int tok = (p0 + pi) * g.bs;
-            const bool v_r = pok && (tok + r < len), v_r8 = pok && (tok + r + 8 < len);
-            const float s0 = v_r ? t0 * gr : -INFINITY;
-            const float s1 = v_r ? t1 * gr : -INFINITY;
-            const float s2 = v_r8 ? t2 * gr8 : -INFINITY;
-            const float s3 = v_r8 ? t3 * gr8 : -INFINITY;
-
-            // ---------- online softmax ----------
-            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            const float gr = lds_h2f(pg + F::gam + 2 * r), gr8 = lds_h2f(pg + F::gam + 2 * (r + 8));
+            float s0 = t0 * gr, s1 = t1 * gr, s2 = t2 * gr8, s3 = t3 * gr8;
+            const int tok = (p0 + warp + NW * j) * kBlockSize;
+            if (!pok || tok + kBlockSize > len) {  // the sequence's last page or a skipped one (warp-uniform)
+                if (!(pok && tok + r < len)) s0 = s1 = -INFINITY;
+                if (!(pok && tok + r + 8 < len)) s2 = s3 = -INFINITY;
             }
-            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-            if (__any_sync(0xffffffffu, n0 > m0 || n1 > m1)) {
-                const float f0 = (n0 > m0) ? exp2f(m0 - n0) : 1.f;
-                const float f1 = (n1 > m1) ? exp2f(m1 - n1) : 1.f;
+
+            // ---------- online softmax; the page max matters only if it beats the running max ----------
+            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+            if (__any_sync(0xffffffffu, mx0 > m0 || mx1 > m1)) {
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+                const float f0 = ex2(m0 - n0), f1 = ex2(m1 - n1);
                 l0 *= f0; z0 *= f0; l1 *= f1; z1 *= f1;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -636,47 +684,50 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
                 m0 = n0;
                 m1 = n1;
             }
-            const float b0 = (m0 == -INFINITY) ? 0.f : m0, b1 = (m1 == -INFINITY) ? 0.f : m1;
-            const float p0v = exp2f(s0 - b0), p1v = exp2f(s1 - b1), p2v = exp2f(s2 - b0), p3v = exp2f(s3 - b1);
-            const float sr = lds_h2f(pg + g.scl_off + 2 * r), sr8 = lds_h2f(pg + g.scl_off + 2 * (r + 8));
-            const float zr = lds_h2f(pg + g.zer_off + 2 * r), zr8 = lds_h2f(pg + g.zer_off + 2 * (r + 8));
+            const float p0v = ex2(s0 - m0), p1v = ex2(s1 - m1), p2v = ex2(s2 - m0), p3v = ex2(s3 - m1);
+            const float sr = lds_h2f(pg + F::scl + 2 * r), sr8 = lds_h2f(pg + F::scl + 2 * (r + 8));
+            const float zr = lds_h2f(pg + F::zer + 2 * r), zr8 = lds_h2f(pg + F::zer + 2 * (r + 8));
             l0 += p0v + p2v;
             l1 += p1v + p3v;
             z0 = fmaf(p0v, zr, fmaf(p2v, zr8, z0));
             z1 = fmaf(p1v, zr, fmaf(p3v, zr8, z1));
-            // the weights p * scale go in as single fp16 (their rounding costs ~1e-4 of output)
-            const uint32_t h01 = pack_h2(p0v * sr, p1v * sr), h23 = pack_h2(p2v * sr8, p3v * sr8);
-            const uint32_t bh0 = movtrans(h01), bh1 = movtrans(h23);
 
             // ---------- values: lane (r, qd) holds dims 16r..16r+15 of tokens 2qd, 2qd+1, 2qd+8, 2qd+9 ----------
+            // the weights p * scale go in as single fp16 (their rounding costs ~1e-4 of output)
             {
+                const uint32_t bh0 = movtrans(pack_h2(p0v * sr, p1v * sr));
+                const uint32_t bh1 = movtrans(pack_h2(p2v * sr8, p3v * sr8));
                 uint32_t Pab[16], Pcd[16];
-                value_pair<VB>(pg + g.vcode_off, r, 2 * qd, 2 * qd + 1, Pab);
-                value_pair<VB>(pg + g.vcode_off, r, 2 * qd + 8, 2 * qd + 9, Pcd);
+                value_codes<VB>(pg + F::vcode, r, 2 * qd, 2 * qd + 1, Pab);
+                value_codes<VB>(pg + F::vcode, r, 2 * qd + 8, 2 * qd + 9, Pcd);
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt)  // rows: dim 16r + 2mt (row r), 16r + 2mt + 1 (row r + 8)
                     mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bh0, bh1);
             }
+
             __syncwarp();  // every lane has read the slot: refill it with the page SPW ahead
-            jdone = j + 1;
             const int jn = j + SPW;
             if (jn < nmine) {
                 if ((jn & 31) == 0) {  // next batch of block ids; prefetch the one after it
                     bid_cur = bid_nxt;
-                    const int k = 8 * (jn + 32 + lane);
+                    const int k = NW * (jn + 32 + lane);
                     bid_nxt = (k < reach) ? __ldg(btw + k) : -1;
                 }
-                const int bk = __shfl_sync(0xffffffffu, bid_cur, jn & 31);
-                if (lane == 0) issue(jn, bk);
+                if (lane == (jn & 31)) issue(slot, bid_cur);
+                ++issued;
+            }
+            if (++slot == SPW) {
+                slot = 0;
+                phase ^= 1u;
             }
         }
         if (timed_out) {
             // copies this warp started must land before its shared memory goes away;
             // one shared deadline for all of them
             const long long t0 = clock64();
-            for (int jj = jdone; jj < min(jdone + SPW, nmine); ++jj) {
-                const uint32_t bar = bar_full + 8 * (warp * SPW + (jj % SPW));
-                while (!mbar_try(bar, (jj / SPW) & 1) && clock64() - t0 < kWaitCycles) {
+            for (int jj = jfail; jj < issued; ++jj) {
+                const uint32_t bar = bar_w + 8 * (jj % SPW);
+                while (!mbar_try(bar, (uint32_t)((jj / SPW) & 1)) && clock64() - t0 < kWaitCycles) {
                 }
             }
         }
@@ -689,9 +740,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             z0 += __shfl_xor_sync(0xffffffffu, z0, o);
             z1 += __shfl_xor_sync(0xffffffffu, z1, o);
         }
-        __syncthreads();  // (A) ring is free: all copies landed, all pages consumed
-        float* wst = reinterpret_cast<float*>(ring);                 // [kNCW][8][3]
-        float* wacc = reinterpret_cast<float*>(ring) + kNCW * 8 * 3;  // [kNCW][8][128]
+        __syncthreads();  // (A) every warp is past its pages: the remainder table is free
+        // warp states [NW][8][3] and accumulators [NW][8][128] over the table; a
+        // query's dims are stored XOR-swizzled by 4 * (query / 2) so that both
+        // these stores and the merge's 16-byte loads stay clear of bank conflicts
+        float* wst = reinterpret_cast<float*>(sm + lut_off);
+        float* wacc = reinterpret_cast<float*>(sm + lut_off + 2048);
         if (r == 0) {
             wst[(warp * 8 + 2 * qd) * 3 + 0] = m0;
             wst[(warp * 8 + 2 * qd) * 3 + 1] = l0;
@@ -702,11 +756,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
         }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            const int dim = 16 * r + 2 * mt;
-            wacc[(warp * 8 + 2 * qd) * D + dim] = acc[mt][0];
-            wacc[(warp * 8 + 2 * qd + 1) * D + dim] = acc[mt][1];
-            wacc[(warp * 8 + 2 * qd) * D + dim + 1] = acc[mt][2];
-            wacc[(warp * 8 + 2 * qd + 1) * D + dim + 1] = acc[mt][3];
+            // undo the fp16-subnormal scaling of the value codes of dims d, d + 1
+            const float e0 = (float)(1u << value_exp<VB>(2 * mt)), e1 = (float)(1u << value_exp<VB>(2 * mt + 1));
+            const int d = (16 * r + 2 * mt) ^ (4 * qd);
+            *reinterpret_cast<float2*>(wacc + (warp * 8 + 2 * qd) * D + d) = make_float2(acc[mt][0] * e0, acc[mt][2] * e1);
+            *reinterpret_cast<float2*>(wacc + (warp * 8 + 2 * qd + 1) * D + d) =
+                make_float2(acc[mt][1] * e0, acc[mt][3] * e1);
         }
     }
     timed_out = __syncthreads_or(timed_out);  // (B)
@@ -716,27 +771,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     }
 
     // ---- merge the warps: thread (query warp, lane) owns dims 4 lane .. 4 lane + 3 ----
-    const float* wst = reinterpret_cast<const float*>(ring);
-    const float* wacc = reinterpret_cast<const float*>(ring) + kNCW * 8 * 3;
-    const int qg = warp;  // query of this warp (consumer warps only)
-    float Mx = -INFINITY, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-    if (warp < kNCW) {
-        for (int w = 0; w < kNCW; ++w) Mx = fmaxf(Mx, wst[(w * 8 + qg) * 3]);
-        if (Mx != -INFINITY) {
-            float Z = 0.f;
-            for (int w = 0; w < kNCW; ++w) {
-                const float mw = wst[(w * 8 + qg) * 3];
-                if (mw == -INFINITY) continue;
-                const float f = exp2f(mw - Mx);
-                L = fmaf(f, wst[(w * 8 + qg) * 3 + 1], L);
-                Z = fmaf(f, wst[(w * 8 + qg) * 3 + 2], Z);
-                const float4 v = *reinterpret_cast<const float4*>(wacc + (w * 8 + qg) * D + 4 * lane);
-                O[0] = fmaf(f, v.x, O[0]); O[1] = fmaf(f, v.y, O[1]);
-                O[2] = fmaf(f, v.z, O[2]); O[3] = fmaf(f, v.w, O[3]);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) O[i] += Z;
+    const float* wst = reinterpret_cast<const float*>(sm + lut_off);
+    const float* wacc = reinterpret_cast<const float*>(sm + lut_off + 2048);
+    const int qg = warp;  // query of this warp (warps 0..7)
+    float Mx = kMinusBig, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
+    if (warp < 8) {
+        for (int w = 0; w < NW; ++w) Mx = fmaxf(Mx, wst[(w * 8 + qg) * 3]);
+        float Z = 0.f;
+        const int dsw = (4 * lane) ^ (4 * (qg >> 1));
+        for (int w = 0; w < NW; ++w) {
+            const float f = exp2f(wst[(w * 8 + qg) * 3] - Mx);
+            L = fmaf(f, wst[(w * 8 + qg) * 3 + 1], L);
+            Z = fmaf(f, wst[(w * 8 + qg) * 3 + 2], Z);
+            const float4 v = *reinterpret_cast<const float4*>(wacc + (w * 8 + qg) * D + dsw);
+            O[0] = fmaf(f, v.x, O[0]); O[1] = fmaf(f, v.y, O[1]);
+            O[2] = fmaf(f, v.z, O[2]); O[3] = fmaf(f, v.w, O[3]);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) O[i] += Z;
     }
 
     const int64_t unit = (int64_t)b * g.hkv + h;
@@ -769,11 +821,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
             constexpr int kMergeChunk = 20;
             const float* base = a.partials + (unit * a.num_splits * G) * kPartStride;
             const int ns = a.num_splits;
-            float runM = -INFINITY, runL = 0.f;
+            float runM = kMinusBig, runL = 0.f;
             O[0] = O[1] = O[2] = O[3] = 0.f;
             for (int s0 = 0; s0 < ns; s0 += kMergeChunk) {
                 const int n = min(kMergeChunk, ns - s0);
-                float ms = -INFINITY, ls = 0.f;
+                float ms = kMinusBig, ls = 0.f;
                 if (lane < n) {
                     ms = __ldcg(base + ((s0 + lane) * G + qg) * kPartStride);
                     ls = __ldcg(base + ((s0 + lane) * G + qg) * kPartStride + 1);
@@ -784,9 +836,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
                     v[k] = (k < n) ? __ldcg(reinterpret_cast<const float4*>(base + ((s0 + k) * G + qg) * kPartStride + 4 + 4 * lane))
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
                 const float nm = fmaxf(runM, warp_max(ms));
-                if (nm == -INFINITY) continue;
-                const float fr = (runM == -INFINITY) ? 0.f : exp2f(runM - nm);
-                const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - nm);
+                const float fr = exp2f(runM - nm);
+                const float f = exp2f(ms - nm);
                 runL = fmaf(runL, fr, warp_sum(f * ls));
 #pragma unroll
                 for (int i = 0; i < 4; ++i) O[i] *= fr;
@@ -806,29 +857,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     if (finalize && warp < G) {
         // out = R^T (acc / l) = s (.) H (acc / l) / sqrt(d)
         const float inv = (L > 0.f) ? 1.f / L : 0.f;
-        float x[4] = {O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv};
-        fwht128(x, lane);
+        float y[4] = {O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv};
+        fwht128(y, lane);
         const uint32_t sg = lane_signs(a.c, lane);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            x[i] *= 0.08838834764831845f;
-            if ((sg >> i) & 1u) x[i] = -x[i];
+            y[i] *= 0.08838834764831845f;
+            if ((sg >> i) & 1u) y[i] = -y[i];
         }
         float* o = a.out + ((int64_t)b * a.hq + (int64_t)h * G + qg) * D;
-        *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(y[0], y[1], y[2], y[3]);
     }
 }
 
 template <int KB, int VB, int M>
 static int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
-    const int smem = smem_map((int)a.g.page_bytes).total;
+    using F = PageFmt<KB, VB, M>;
+    const Geometry& g = a.g;
+    if (g.page_bytes != F::bytes || g.vcode_off != F::vcode || g.gam_off != F::gam || g.scl_off != F::scl ||
+        g.zer_off != F::zer || (M && (g.rho_off != F::rho || g.sig_off != F::sig)) || g.bs != kBlockSize ||
+        g.d != kHeadDim)
+        return (int)cudaErrorInvalidValue;  // the cache's geometry is not the format this kernel was built for
+    constexpr Layout L = decode_layout<KB, VB, M>();
     auto kern = decode_kernel<KB, VB, M>;
     static int done[64] = {};
-    cudaError_t e = ensure_smem_limit(kern, smem, done);
+    cudaError_t e = ensure_smem_limit(kern, L.total, done);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid((unsigned)a.num_splits, (unsigned)a.g.hkv, (unsigned)a.batch);
-    kern<<<grid, kThreads, smem, s>>>(a);
+    dim3 grid((unsigned)a.num_splits, (unsigned)g.hkv, (unsigned)a.batch);
+    kern<<<grid, decode_warps<M>() * 32, L.total, s>>>(a);
     return (int)cudaGetLastError();
+}
+
+int decode_smem_bytes(const Geometry& g) {
+#define TQ_SMEM(KB_, VB_)                                                                         \
+    if (g.kb == KB_ && g.vb == VB_)                                                               \
+        return g.m ? decode_layout<KB_, VB_, 128>().total : decode_layout<KB_, VB_, 0>().total;
+    TQ_SMEM(2, 2) TQ_SMEM(2, 3) TQ_SMEM(2, 4)
+    TQ_SMEM(3, 2) TQ_SMEM(3, 3) TQ_SMEM(3, 4)
+    TQ_SMEM(4, 2) TQ_SMEM(4, 3) TQ_SMEM(4, 4)
+#undef TQ_SMEM
+    return -1;
 }
 
 int launch_decode(const DecodeArgs& a, void* stream) {

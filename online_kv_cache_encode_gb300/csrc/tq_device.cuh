@@ -70,11 +70,11 @@ __device__ __forceinline__ void fwht128(float x[4], int lane) {
 #pragma unroll
     for (int k = 0; k < 5; ++k) {
         const int m = 1 << k;
-        const bool upper = (lane & m) != 0;
+        const float sg = (lane & m) ? -1.f : 1.f;  // upper: y - x, lower: x + y (one exact-sign fma)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float y = __shfl_xor_sync(0xffffffffu, x[i], m);
-            x[i] = upper ? (y - x[i]) : (x[i] + y);
+            const float y = __shfl_xor_sync(0xffffffffu, x[i], m);
+            x[i] = fmaf(sg, x[i], y);
         }
     }
 }

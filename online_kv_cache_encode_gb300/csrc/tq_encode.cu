@@ -19,6 +19,16 @@ namespace tq {
 constexpr int kEncWarps = 8;
 constexpr int kSPad = kHeadDim + 1;  // padded row stride of S in shared memory
 
+// One 128-code row, lane holding the 4*B bits of codes 4 lane .. 4 lane + 3:
+// 2- and 4-bit rows are plain byte / halfword stores, 3-bit rows go through
+// the shuffle packer.
+template <int B>
+__device__ __forceinline__ void store_codes(uint8_t* row, uint32_t p, int lane) {
+    if constexpr (B == 4) reinterpret_cast<uint16_t*>(row)[lane] = (uint16_t)p;
+    else if constexpr (B == 2) row[lane] = (uint8_t)p;
+    else store_code_row<B>(row, p, lane);
+}
+
 template <int KB, int VB, int M>
 __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs a) {
     extern __shared__ float smem[];
@@ -27,6 +37,7 @@ __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs
     constexpr int D = kHeadDim;
     constexpr int NB = (1 << KB) - 1;
     constexpr int VMAX = (1 << VB) - 1;
+    constexpr int HALF = 1 << (KB - 1);
     float* Ss = smem;                       // [M][kSPad]
     float* rbuf = smem + M * kSPad + warp * D;
     if constexpr (M > 0) {
@@ -55,9 +66,11 @@ __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs
         float k[4], v[4];
         load4(a.K, a.dtype, it * D + 4 * lane, k);
         load4(a.V, a.dtype, it * D + 4 * lane, v);
-        bool finite = true;
+        // x * 0 is 0 for every finite x and NaN for inf / NaN
+        float z = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) finite = finite && isfinite(k[i]) && isfinite(v[i]);
+        for (int i = 0; i < 4; ++i) z = fmaf(k[i], 0.f, fmaf(v[i], 0.f, z));
+        const bool finite = (z == 0.f);
         if (!__all_sync(0xffffffffu, finite) && lane == 0) flag(a.status, TQ_FLAG_NONFINITE);
 
         // ---- key ----
@@ -72,15 +85,23 @@ __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs
         if (gamma > 0.f) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float u = (k[i] * inv_sqrt_d) / gamma;
-                int c = 0;
+                const float u = (k[i] * inv_sqrt_d) / gamma;  // correctly rounded: keeps ties with the codebook rare
+                // The codebook is symmetric (t_b = -t_{NB-1-b}, middle boundary 0), so
+                // code = #{t_b < u} is HALF + #{positive t_b < |u|} for u > 0 and
+                // HALF - 1 - #{positive t_b <= |u|} otherwise; the two differ from the
+                // plain count only at a tie with a boundary.
+                const float au = fabsf(u);
+                int n = 0;
 #pragma unroll
-                for (int b = 0; b < NB; ++b) c += (a.c.boundary[b] < u) ? 1 : 0;
+                for (int b = HALF; b < NB; ++b) n += (a.c.boundary[b] < au) ? 1 : 0;
+                const int c = (u > 0.f) ? HALF + n : HALF - 1 - n;
                 kp |= (uint32_t)c << (KB * i);
-                float cv = 0.f;
+                if constexpr (M > 0) {
+                    float cv = 0.f;
 #pragma unroll
-                for (int b = 0; b <= NB; ++b) cv = (c == b) ? a.c.centroid[b] : cv;
-                r[i] = u - cv;
+                    for (int b = 0; b <= NB; ++b) cv = (c == b) ? a.c.centroid[b] : cv;
+                    r[i] = u - cv;
+                }
             }
         } else {
 #pragma unroll
@@ -89,7 +110,7 @@ __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs
                 r[i] = 0.f;
             }
         }
-        store_code_row<KB>(page + g.kcode_off + off * (D * KB / 8), kp, lane);
+        store_codes<KB>(page + g.kcode_off + off * (D * KB / 8), kp, lane);
 
         float rho = 0.f;
         if constexpr (M > 0) {
@@ -129,15 +150,10 @@ __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs
         uint32_t vp = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            int c = 0;
-            if (scale > 0.f) {
-                float qv = rintf((v[i] - mn) / scale);
-                qv = fminf(fmaxf(qv, 0.f), (float)VMAX);
-                c = (int)qv;
-            }
-            vp |= (uint32_t)c << (VB * i);
+            const float qv = (scale > 0.f) ? fminf(fmaxf(rintf((v[i] - mn) / scale), 0.f), (float)VMAX) : 0.f;
+            vp |= (uint32_t)qv << (VB * i);
         }
-        store_code_row<VB>(page + g.vcode_off + off * (D * VB / 8), vp, lane);
+        store_codes<VB>(page + g.vcode_off + off * (D * VB / 8), vp, lane);
 
         if (lane == 0) {
             const uint16_t hg = f16_bits(gamma), hs = f16_bits(scale), hz = f16_bits(mn);

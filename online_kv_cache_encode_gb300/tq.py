@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtq.so")
 
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_WORKSPACE = range(5)
-FLAG_OVERFLOW, FLAG_BAD_SLOT, FLAG_NONFINITE, FLAG_TIMEOUT = 1, 2, 4, 8
+FLAG_OVERFLOW, FLAG_BAD_SLOT, FLAG_NONFINITE, FLAG_TIMEOUT, FLAG_INTERNAL = 1, 2, 4, 8, 16
 TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
 NOALLOC_WORKSPACE_BYTES = 4 << 20  # TQ_NOALLOC_WORKSPACE_BYTES
 
