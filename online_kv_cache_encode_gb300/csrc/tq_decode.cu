@@ -14,8 +14,9 @@
 //              comes in fp16 from a lane-private shared-memory table and
 //              multiplies q_rot (m16n8k16).
 //              logit = gamma_t * sm_scale * (sum_j C[c_j] q_rot[j]) [+ QJL term]
-//      softmax running max / sum per query in the exp2 domain; the page max is
-//              reduced across lanes only when some score beats the running max
+//      softmax running max / sum per query in the exp2 domain; the max is
+//              raised (and the state rescaled) only when a score beats it by
+//              more than 8 (log2), which after the first page is rare
 //      values  O^T[128 x 8 q] += Vcode^T[128 x 16 tok] . (p * scale)^T[16 tok x 8 q]
 //              (m16n8k16).  A value code masked in place inside a 16-bit lane is
 //              an exact fp16 subnormal c * 2^-e; the power of two is removed once
@@ -35,12 +36,19 @@
 namespace tq {
 
 constexpr int kMaxSlotsPerWarp = 8;            // ring slots per warp: pages a warp keeps in flight
+constexpr int kFirstPages = 2;                 // pages per warp requested before the query is prepared
 constexpr uint32_t kLutAddr = 0x10000;         // shared-window address of the remainder table
 constexpr int kLutBytes = 0x10000;
 constexpr int kMaxSmemBase = 4096;             // dynamic shared memory must start below this address
 constexpr int kSmemLimit = 227 * 1024;         // opt-in dynamic shared memory per CTA
 constexpr long long kWaitCycles = 3000000000ll;  // bound on any wait: ~1.5 s at 2 GHz
 constexpr float kMinusBig = -1.0e30f;          // running max before any token (finite: no inf - inf)
+// The running max is raised only when a score beats it by more than kLazy (log2
+// units), so weights stay below 2^kLazy (any reference max gives the same
+// softmax).  A page whose value scale exceeds kBigScale takes the exact max, so
+// that p * scale stays inside the fp16 range of the PV operand.
+constexpr float kLazy = 8.f;
+constexpr float kBigScale = 255.f;
 // split partial record: max, sum, 2 pad, acc[128] (keeps the acc 16-byte aligned)
 constexpr int kPartStride = 4 + kHeadDim;
 
@@ -86,6 +94,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
+// Programmatic dependent launch: wait for the grid this one depends on (a
+// no-op when launched without the attribute); allow the next grid to launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -172,7 +184,7 @@ template <int M>
 __host__ __device__ constexpr int frag_vecs() { return 8 + 4 + (M ? 8 : 0); }
 
 struct Layout {
-    int frag, qrot, sq, qoff, qscale, bars, ok;  // small fixed region at the start
+    int frag, qrot, sq, qoff, qscale, rem, bars, ok;  // small fixed region at the start
     int ringA, nwA;   // ring slots of warps 0 .. nwA-1 sit below the remainder table
     int spw;          // ring slots per warp
     int total;        // dynamic bytes to request: enough for any start address up to kMaxSmemBase
@@ -191,6 +203,7 @@ __host__ __device__ constexpr Layout decode_layout() {
     L.sq = off; off += M ? 8 * kHeadDim * 4 : 0;
     L.qoff = off; off += 8 * 4;
     L.qscale = off; off += 8 * 4;
+    L.rem = off; off += 16 * 2;
     L.bars = off; off += 8 * NW * kMaxSlotsPerWarp;
     L.ok = off; off += 4 * NW * kMaxSlotsPerWarp;
     L.ringA = (off + 127) / 128 * 128;
@@ -385,6 +398,7 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     // The layout assumes dynamic shared memory starts below kMaxSmemBase.
     const uint32_t sbase = smem_u32(sm);
     if (sbase > (uint32_t)kMaxSmemBase) {
+        grid_dependency_wait();
         if (tid == 0) flag(a.status, TQ_FLAG_INTERNAL);
         return;
     }
@@ -399,7 +413,48 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     const int p0 = split * a.pages_per_split;
     const float ksc = a.sm_scale_log2;
 
-    // ---- independent global loads first: length, this warp's block ids, the query ----
+    // ---- shared-memory-only setup: it may overlap the previous kernel's tail ----
+    if (lane == 0) {
+        for (int k = 0; k < SPW; ++k) mbar_init(bar_w + 8 * k, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    uint16_t* rem = reinterpret_cast<uint16_t*>(sm + LY.rem);
+    if (tid < 16) rem[tid] = a.c.rem_f16[tid];
+    __syncthreads();
+    // Lane-private remainder table at shared address kLutAddr (copy for
+    // lane l at entry*stride + l*width):
+    //   4-bit keys: byte e (2 codes) -> (rem[e&15], rem[e>>4])              stride 256, 4 B
+    //   2-bit keys: byte e (4 codes) -> (rem[c0], rem[c1]), (rem[c2], rem[c3]) stride 256, 8 B
+    //   3-bit keys: 6 bits e (2 codes) -> (rem[e&7], rem[e>>3])              stride 128, 4 B
+    {
+        uint8_t* lut = sm + lut_off;
+        if constexpr (KB == 4) {
+            for (int i = tid; i < 256 * 8; i += NT) {   // entry e, lanes 4k..4k+3
+                const int e = i >> 3, k = i & 7;
+                const uint32_t v = (uint32_t)rem[e & 15] | ((uint32_t)rem[e >> 4] << 16);
+                *reinterpret_cast<uint4*>(lut + e * 256 + 16 * k) = make_uint4(v, v, v, v);
+            }
+        } else if constexpr (KB == 2) {
+            for (int i = tid; i < 256 * 16; i += NT) {  // entry e, lanes 2k, 2k+1
+                const int e = i >> 4, k = i & 15;
+                const uint32_t xx = (uint32_t)rem[e & 3] | ((uint32_t)rem[(e >> 2) & 3] << 16);
+                const uint32_t yy = (uint32_t)rem[(e >> 4) & 3] | ((uint32_t)rem[e >> 6] << 16);
+                *reinterpret_cast<uint4*>(lut + e * 256 + 16 * k) = make_uint4(xx, yy, xx, yy);
+            }
+        } else {
+            for (int i = tid; i < 64 * 8; i += NT) {    // entry e, lanes 4k..4k+3
+                const int e = i >> 3, k = i & 7;
+                const uint32_t v = (uint32_t)rem[e & 7] | ((uint32_t)rem[e >> 3] << 16);
+                *reinterpret_cast<uint4*>(lut + e * 128 + 16 * k) = make_uint4(v, v, v, v);
+            }
+        }
+    }
+    // Launched as a programmatic dependent of the previous kernel in the stream:
+    // nothing in global memory is touched before that grid has completed.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    // ---- global loads: length, this warp's block ids, the query ----
     // Warp w handles pages w, w + NW, w + 2 NW, ... of the split (its j-th page
     // is w + NW j) in its own SPW ring slots.  Lane l holds the block id of the
     // warp's page l of the current batch of 32 (bid_cur) and of the next batch
@@ -411,11 +466,6 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     int bid_nxt = (NW * (32 + lane) < reach) ? __ldg(btw + NW * (32 + lane)) : -1;
     float x[4] = {0.f, 0.f, 0.f, 0.f};
     if (warp < G) load4(a.q, a.dtype, ((int64_t)b * a.hq + (int64_t)h * G + warp) * D + 4 * lane, x);
-    if (lane == 0) {
-        for (int k = 0; k < SPW; ++k) mbar_init(bar_w + 8 * k, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
 
     // ---- sequence range of this split ----
     if (len > a.max_blocks * g.bs) {
@@ -444,39 +494,14 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             mbar_arrive(bar);
         }
     };
-    if (lane < SPW && lane < nmine) issue(lane, bid_cur);  // the first SPW pages, one lane each
+    // The first kFirstPages pages of every warp now, one lane each; the rest of
+    // the ring once the query is prepared, so that the first pages of all warps
+    // are not queued behind the whole initial burst.
+    constexpr int kFirst = SPW < kFirstPages ? SPW : kFirstPages;
+    if (lane < kFirst && lane < nmine) issue(lane, bid_cur);
 
     bool timed_out = false;
     {
-        // Lane-private remainder table at shared address kLutAddr (copy for
-        // lane l at entry*stride + l*width):
-        //   4-bit keys: byte e (2 codes) -> (rem[e&15], rem[e>>4])              stride 256, 4 B
-        //   2-bit keys: byte e (4 codes) -> (rem[c0], rem[c1]), (rem[c2], rem[c3]) stride 256, 8 B
-        //   3-bit keys: 6 bits e (2 codes) -> (rem[e&7], rem[e>>3])              stride 128, 4 B
-        {
-            uint8_t* lut = sm + lut_off;
-            const uint16_t* rem = a.c.rem_f16;
-            if constexpr (KB == 4) {
-                for (int i = tid; i < 256 * 8; i += NT) {   // entry e, lanes 4k..4k+3
-                    const int e = i >> 3, k = i & 7;
-                    const uint32_t v = (uint32_t)rem[e & 15] | ((uint32_t)rem[e >> 4] << 16);
-                    *reinterpret_cast<uint4*>(lut + e * 256 + 16 * k) = make_uint4(v, v, v, v);
-                }
-            } else if constexpr (KB == 2) {
-                for (int i = tid; i < 256 * 16; i += NT) {  // entry e, lanes 2k, 2k+1
-                    const int e = i >> 4, k = i & 15;
-                    const uint32_t xx = (uint32_t)rem[e & 3] | ((uint32_t)rem[(e >> 2) & 3] << 16);
-                    const uint32_t yy = (uint32_t)rem[(e >> 4) & 3] | ((uint32_t)rem[e >> 6] << 16);
-                    *reinterpret_cast<uint4*>(lut + e * 256 + 16 * k) = make_uint4(xx, yy, xx, yy);
-                }
-            } else {
-                for (int i = tid; i < 64 * 8; i += NT) {    // entry e, lanes 4k..4k+3
-                    const int e = i >> 3, k = i & 7;
-                    const uint32_t v = (uint32_t)rem[e & 7] | ((uint32_t)rem[e >> 3] << 16);
-                    *reinterpret_cast<uint4*>(lut + e * 128 + 16 * k) = make_uint4(v, v, v, v);
-                }
-            }
-        }
         // q_rot = R q for query (warp) of this group; its per-query constants:
         //   qoff   = sm_scale log2(e) alpha mid sum(q_rot)
         //   qscale = power of two putting max |ksc alpha q_rot| / qscale in (256, 512]
@@ -558,6 +583,7 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             }
         }
         __syncthreads();
+        if (lane >= kFirst && lane < SPW && lane < nmine) issue(lane, bid_cur);
         const int r = lane >> 2, qd = lane & 3;   // r: token row / query column; qd: quad index
         uint32_t QI[8][4], QB[16];
         uint32_t QSh[M > 0 ? 16 : 1], QSl[M > 0 ? 16 : 1];
@@ -665,9 +691,11 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 if (!(pok && tok + r + 8 < len)) s2 = s3 = -INFINITY;
             }
 
-            // ---------- online softmax; the page max matters only if it beats the running max ----------
+            // ---------- online softmax; the max moves only when a score beats it by kLazy ----------
+            const float sr = lds_h2f(pg + F::scl + 2 * r), sr8 = lds_h2f(pg + F::scl + 2 * (r + 8));
             float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-            if (__any_sync(0xffffffffu, mx0 > m0 || mx1 > m1)) {
+            const bool exact = fmaxf(sr, sr8) > kBigScale;
+            if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy || (exact && (mx0 > m0 || mx1 > m1)))) {
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -685,18 +713,25 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 m1 = n1;
             }
             const float p0v = ex2(s0 - m0), p1v = ex2(s1 - m1), p2v = ex2(s2 - m0), p3v = ex2(s3 - m1);
-            const float sr = lds_h2f(pg + F::scl + 2 * r), sr8 = lds_h2f(pg + F::scl + 2 * (r + 8));
             const float zr = lds_h2f(pg + F::zer + 2 * r), zr8 = lds_h2f(pg + F::zer + 2 * (r + 8));
             l0 += p0v + p2v;
             l1 += p1v + p3v;
-            z0 = fmaf(p0v, zr, fmaf(p2v, zr8, z0));
-            z1 = fmaf(p1v, zr, fmaf(p3v, zr8, z1));
 
             // ---------- values: lane (r, qd) holds dims 16r..16r+15 of tokens 2qd, 2qd+1, 2qd+8, 2qd+9 ----------
-            // the weights p * scale go in as single fp16 (their rounding costs ~1e-4 of output)
+            // The weights w = p * scale (p <= 2^kLazy) go in as single fp16 w'.  The
+            // codes are not centred, so the rounding w - w' is also added back times
+            // the mid code through the fp32 zero-point sum; what is left is
+            // (w - w') (c - mid), a few 1e-4 of the output at most.
             {
-                const uint32_t bh0 = movtrans(pack_h2(p0v * sr, p1v * sr));
-                const uint32_t bh1 = movtrans(pack_h2(p2v * sr8, p3v * sr8));
+                const float w0 = p0v * sr, w1 = p1v * sr, w2 = p2v * sr8, w3 = p3v * sr8;
+                const uint32_t h01 = pack_h2(w0, w1), h23 = pack_h2(w2, w3);
+                const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+                const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+                constexpr float kMid = 0.5f * (float)((1 << VB) - 1);
+                z0 = fmaf(p0v, zr, fmaf(p2v, zr8, fmaf(kMid, (w0 - r01.x) + (w2 - r23.x), z0)));
+                z1 = fmaf(p1v, zr, fmaf(p3v, zr8, fmaf(kMid, (w1 - r01.y) + (w3 - r23.y), z1)));
+                const uint32_t bh0 = movtrans(h01);
+                const uint32_t bh1 = movtrans(h23);
                 uint32_t Pab[16], Pcd[16];
                 value_codes<VB>(pg + F::vcode, r, 2 * qd, 2 * qd + 1, Pab);
                 value_codes<VB>(pg + F::vcode, r, 2 * qd + 8, 2 * qd + 9, Pcd);
@@ -791,83 +826,85 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
         for (int i = 0; i < 4; ++i) O[i] += Z;
     }
 
-    const int64_t unit = (int64_t)b * g.hkv + h;
-    bool finalize = (a.num_splits == 1);
-    if (!finalize) {
-        // publish this split's partial (max, sum, acc with the zero term folded in)
-        float* part = a.partials + ((unit * a.num_splits + split) * G) * kPartStride;
-        if (warp < G) {
-            float* pp = part + qg * kPartStride;
-            if (lane == 0) { pp[0] = Mx; pp[1] = L; }
-            *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(O[0], O[1], O[2], O[3]);
-        }
-        // The CTA barrier orders every thread's partial writes before thread 0's
-        // gpu-scope release (cumulativity); the acquire side pairs with the other
-        // CTAs' releases before the last one reads their partials.
-        __syncthreads();
-        __shared__ int s_last;
-        if (tid == 0) {
-            unsigned old;
-            asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + unit) : "memory");
-            s_last = (old == (unsigned)a.num_splits - 1);
-        }
-        __syncthreads();
-        if (!s_last) return;
-        finalize = true;
-        if (warp < G) {
-            // All loads of a chunk of up to kMergeChunk splits are issued before
-            // any is used, so a chunk costs one L2 round trip; chunks merge with
-            // a running max.
-            constexpr int kMergeChunk = 20;
-            const float* base = a.partials + (unit * a.num_splits * G) * kPartStride;
-            const int ns = a.num_splits;
-            float runM = kMinusBig, runL = 0.f;
-            O[0] = O[1] = O[2] = O[3] = 0.f;
-            for (int s0 = 0; s0 < ns; s0 += kMergeChunk) {
-                const int n = min(kMergeChunk, ns - s0);
-                float ms = kMinusBig, ls = 0.f;
-                if (lane < n) {
-                    ms = __ldcg(base + ((s0 + lane) * G + qg) * kPartStride);
-                    ls = __ldcg(base + ((s0 + lane) * G + qg) * kPartStride + 1);
-                }
-                float4 v[kMergeChunk];
-#pragma unroll
-                for (int k = 0; k < kMergeChunk; ++k)
-                    v[k] = (k < n) ? __ldcg(reinterpret_cast<const float4*>(base + ((s0 + k) * G + qg) * kPartStride + 4 + 4 * lane))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                const float nm = fmaxf(runM, warp_max(ms));
-                const float fr = exp2f(runM - nm);
-                const float f = exp2f(ms - nm);
-                runL = fmaf(runL, fr, warp_sum(f * ls));
-#pragma unroll
-                for (int i = 0; i < 4; ++i) O[i] *= fr;
-#pragma unroll
-                for (int k = 0; k < kMergeChunk; ++k) {
-                    const float fk = __shfl_sync(0xffffffffu, f, k);
-                    O[0] = fmaf(fk, v[k].x, O[0]); O[1] = fmaf(fk, v[k].y, O[1]);
-                    O[2] = fmaf(fk, v[k].z, O[2]); O[3] = fmaf(fk, v[k].w, O[3]);
-                }
-                runM = nm;
-            }
-            Mx = runM;
-            L = runL;
-        }
-        if (tid == 0) a.counters[unit] = 0u;
-    }
-    if (finalize && warp < G) {
-        // out = R^T (acc / l) = s (.) H (acc / l) / sqrt(d)
-        const float inv = (L > 0.f) ? 1.f / L : 0.f;
-        float y[4] = {O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv};
-        fwht128(y, lane);
+    // Rotate this CTA's unnormalised accumulator back now, R^T O = s (.) H O / sqrt(d):
+    // R^T is linear, so the split merge below is then a plain weighted sum.
+    if (warp < G) {
+        fwht128(O, lane);
         const uint32_t sg = lane_signs(a.c, lane);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            y[i] *= 0.08838834764831845f;
-            if ((sg >> i) & 1u) y[i] = -y[i];
+            O[i] *= 0.08838834764831845f;
+            if ((sg >> i) & 1u) O[i] = -O[i];
         }
-        float* o = a.out + ((int64_t)b * a.hq + (int64_t)h * G + qg) * D;
-        *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(y[0], y[1], y[2], y[3]);
     }
+    float* o = a.out + ((int64_t)b * a.hq + (int64_t)h * G + qg) * D;
+    if (a.num_splits == 1) {
+        if (warp < G) {
+            const float inv = (L > 0.f) ? 1.f / L : 0.f;
+            *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
+        }
+        return;
+    }
+
+    // publish this split's partial (max, sum, rotated acc with the zero term folded in)
+    const int64_t unit = (int64_t)b * g.hkv + h;
+    float* part = a.partials + ((unit * a.num_splits + split) * G) * kPartStride;
+    if (warp < G) {
+        float* pp = part + qg * kPartStride;
+        if (lane == 0) { pp[0] = Mx; pp[1] = L; }
+        *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(O[0], O[1], O[2], O[3]);
+    }
+    // The CTA barrier orders every thread's partial writes before thread 0's
+    // gpu-scope release (cumulativity); the acquire side pairs with the other
+    // CTAs' releases before the last one reads their partials.
+    __syncthreads();
+    __shared__ int s_last;
+    if (tid == 0) {
+        unsigned old;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + unit) : "memory");
+        s_last = (old == (unsigned)a.num_splits - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    if (warp < G) {
+        // Lane k loads (max, sum) of split s0 + k and every lane its 4 dims of all
+        // kChunk splits, all before any use: one L2 round trip per chunk.
+        constexpr int kChunk = 20;
+        const float* base = a.partials + (unit * a.num_splits * G + qg) * kPartStride;
+        const int ns = a.num_splits;
+        float runM = kMinusBig, runL = 0.f;
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s0 = 0; s0 < ns; s0 += kChunk) {
+            const int n = min(kChunk, ns - s0);
+            float ms = kMinusBig, ls = 0.f;
+            if (lane < n) {
+                ms = __ldcg(base + (int64_t)(s0 + lane) * G * kPartStride);
+                ls = __ldcg(base + (int64_t)(s0 + lane) * G * kPartStride + 1);
+            }
+            float4 v[kChunk];
+#pragma unroll
+            for (int k = 0; k < kChunk; ++k)
+                v[k] = (k < n) ? __ldcg(reinterpret_cast<const float4*>(base + (int64_t)(s0 + k) * G * kPartStride + 4 + 4 * lane))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float cm = fmaxf(runM, warp_max(ms));
+            const float fr = exp2f(runM - cm);
+            const float f = exp2f(ms - cm);
+            runL = fmaf(runL, fr, warp_sum(f * ls));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc4[i] *= fr;
+#pragma unroll
+            for (int k = 0; k < kChunk; ++k) {
+                const float fk = __shfl_sync(0xffffffffu, f, k);
+                acc4[0] = fmaf(fk, v[k].x, acc4[0]); acc4[1] = fmaf(fk, v[k].y, acc4[1]);
+                acc4[2] = fmaf(fk, v[k].z, acc4[2]); acc4[3] = fmaf(fk, v[k].w, acc4[3]);
+            }
+            runM = cm;
+        }
+        const float inv = (runL > 0.f) ? 1.f / runL : 0.f;
+        *reinterpret_cast<float4*>(o + 4 * lane) =
+            make_float4(acc4[0] * inv, acc4[1] * inv, acc4[2] * inv, acc4[3] * inv);
+    }
+    if (tid == 0) a.counters[unit] = 0u;
 }
 
 template <int KB, int VB, int M>
@@ -883,9 +920,8 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
     static int done[64] = {};
     cudaError_t e = ensure_smem_limit(kern, L.total, done);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid((unsigned)a.num_splits, (unsigned)g.hkv, (unsigned)a.batch);
-    kern<<<grid, decode_warps<M>() * 32, L.total, s>>>(a);
-    return (int)cudaGetLastError();
+    return (int)launch_programmatic(kern, dim3((unsigned)a.num_splits, (unsigned)g.hkv, (unsigned)a.batch),
+                                    dim3(decode_warps<M>() * 32), (size_t)L.total, s, a);
 }
 
 int decode_smem_bytes(const Geometry& g) {

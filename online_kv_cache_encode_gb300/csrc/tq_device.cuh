@@ -25,6 +25,25 @@ inline cudaError_t ensure_smem_limit(Kernel kern, int bytes, int (&done)[64]) {
     return e;
 }
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel in the stream drains, and must execute griddepcontrol.wait
+// before it touches global memory.
+template <typename Kernel, typename Args>
+inline cudaError_t launch_programmatic(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                       const Args& args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
 __device__ __forceinline__ void flag(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }

@@ -40,6 +40,10 @@ __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs
     constexpr int HALF = 1 << (KB - 1);
     float* Ss = smem;                       // [M][kSPad]
     float* rbuf = smem + M * kSPad + warp * D;
+    // launched as a programmatic dependent: wait for the previous grid before
+    // touching global memory, and let the next one start launching
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if constexpr (M > 0) {
         for (int i = threadIdx.x; i < M * D; i += blockDim.x) Ss[(i / D) * kSPad + (i % D)] = a.S[i];
         __syncthreads();
@@ -184,8 +188,7 @@ static int launch_encode_t(const EncodeArgs& a, int num_sms, cudaStream_t s) {
     int64_t blocks = (items + kEncWarps - 1) / kEncWarps;
     const int64_t cap = (int64_t)num_sms * (M > 0 ? 2 : 8);
     if (blocks > cap) blocks = cap;
-    kern<<<(unsigned)blocks, kEncWarps * 32, smem, s>>>(a);
-    return (int)cudaGetLastError();
+    return (int)launch_programmatic(kern, dim3((unsigned)blocks), dim3(kEncWarps * 32), smem, s, a);
 }
 
 int launch_encode(const EncodeArgs& a, int num_sms, void* stream) {
