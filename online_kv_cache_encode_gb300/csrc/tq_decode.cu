@@ -37,6 +37,7 @@ namespace tq {
 
 constexpr int kMaxSlotsPerWarp = 8;            // ring slots per warp: pages a warp keeps in flight
 constexpr int kFirstPages = 2;                 // pages per warp requested before the query is prepared
+constexpr int kQStride = kHeadDim + 4;         // padded row of q_rot / S q_rot in shared memory (float4-aligned)
 constexpr uint32_t kLutAddr = 0x10000;         // shared-window address of the remainder table
 constexpr int kLutBytes = 0x10000;
 constexpr int kMaxSmemBase = 4096;             // dynamic shared memory must start below this address
@@ -199,8 +200,8 @@ __host__ __device__ constexpr Layout decode_layout() {
     Layout L{};
     int off = 0;
     L.frag = off; off += 32 * 16 * frag_vecs<M>();
-    L.qrot = off; off += 8 * kHeadDim * 4;
-    L.sq = off; off += M ? 8 * kHeadDim * 4 : 0;
+    L.qrot = off; off += 8 * kQStride * 4;
+    L.sq = off; off += M ? 8 * kQStride * 4 : 0;
     L.qoff = off; off += 8 * 4;
     L.qscale = off; off += 8 * 4;
     L.rem = off; off += 16 * 2;
@@ -213,10 +214,13 @@ __host__ __device__ constexpr Layout decode_layout() {
         const int per = spw * stride;
         const int nA = capA / per < NW ? capA / per : NW;
         const int total = (int)kLutAddr + kLutBytes + (NW - nA) * per;  // start address 0 is the worst case
-        if (total <= kSmemLimit) {
+        // the warp merge reuses the space from the table on: states + accumulators
+        const int merge_end = (int)kLutAddr + 2048 + NW * 8 * kHeadDim * 4;
+        const int need = total > merge_end ? total : merge_end;
+        if (need <= kSmemLimit) {
             L.spw = spw;
             L.nwA = nA;
-            L.total = total;
+            L.total = need;
             return L;
         }
     }
@@ -513,7 +517,7 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 for (int i = 0; i < 4; ++i) x[i] *= 0.08838834764831845f;
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) qrot[warp * D + 4 * lane + i] = x[i];
+            for (int i = 0; i < 4; ++i) qrot[warp * kQStride + 4 * lane + i] = x[i];
             const float sq = warp_sum(x[0] + x[1] + x[2] + x[3]);
             const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
             const float big = fabsf(a.c.alpha) * ksc * mx;
@@ -539,7 +543,7 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 for (int k = 0; k < (8 + GS - 1) / GS; ++k) {
                     const int gq = g0 + GS * k;
                     if (gq < 8) {
-                        const float4 qv = *reinterpret_cast<const float4*>(qrot + gq * D + 4 * j4);
+                        const float4 qv = *reinterpret_cast<const float4*>(qrot + gq * kQStride + 4 * j4);
                         acc4[k] = fmaf(sv.x, qv.x, fmaf(sv.y, qv.y, fmaf(sv.z, qv.z, fmaf(sv.w, qv.w, acc4[k]))));
                     }
                 }
@@ -547,39 +551,57 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
 #pragma unroll
             for (int k = 0; k < (8 + GS - 1) / GS; ++k) {
                 const int gq = g0 + GS * k;
-                if (gq < 8) sqv[gq * D + i] = ksc * acc4[k];
+                if (gq < 8) sqv[gq * kQStride + i] = ksc * acc4[k];
             }
             __syncthreads();
         }
 
         // ---- per-lane query fragments, written once per CTA in lane-major order ----
         // (word w of lane l at ((w / 4) * 32 + l) * 16 + (w % 4) * 4, so that a
-        // warp reads each group of four words with one conflict-free 16-byte load)
+        // warp reads each group of four words with one conflict-free 16-byte load;
+        // thread (vector v, lane l) computes and stores one such group)
         //   words  0..31  QI: x = ksc alpha q_rot / qscale in fp16 hi + lo; word
         //                 4 ks + 2 part + slot holds part (0 hi, 1 lo) of x 2^(e-24)
         //                 at the dims of key register X[2 ks + slot] (e its scale)
         //   words 32..47  QB: sm_scale log2(e) q_rot in fp16 at remainder dims (2n, 2n+1)
         //   words 48..79  QSh / QSl: sqv hi + lo in fp16 at sign dims (n, n + 16)
         {
-            uint8_t* fr = sm + LY.frag;
-            for (int t = tid; t < 8 * D; t += NT) {
-                const int gq = t >> 7, dim = t & (D - 1);
-                const int ln = gq * 4 + (dim >> 5), c = dim & 31;
-                auto word = [&](int w) -> uint8_t* { return fr + (((w >> 2) * 32 + ln) * 16 + (w & 3) * 4); };
-                const float q = qrot[gq * D + dim];
-                const int n = key_reg<KB>(c), hh = key_half<KB>(c);
-                const float xs = ksc * a.c.alpha / qscale[gq] * q * exp2f((float)(key_exp<KB>(n) - 24));
-                const __half xh = __float2half_rn(xs);
-                reinterpret_cast<__half*>(word(4 * (n >> 1) + (n & 1)))[hh] = xh;
-                reinterpret_cast<__half*>(word(4 * (n >> 1) + 2 + (n & 1)))[hh] = __float2half_rn(xs - __half2float(xh));
-                reinterpret_cast<__half*>(word(32 + (c >> 1)))[c & 1] = __float2half_rn(q * ksc);
-                if constexpr (M > 0) {
-                    const float v = sqv[gq * D + dim];
-                    const __half hi = __float2half_rn(v);
-                    const __half lo = __float2half_rn(v - __half2float(hi));
-                    reinterpret_cast<__half*>(word(48 + (c & 15)))[c >> 4] = hi;
-                    reinterpret_cast<__half*>(word(64 + (c & 15)))[c >> 4] = lo;
+            uint4* fr = reinterpret_cast<uint4*>(sm + LY.frag);
+            for (int t = tid; t < 32 * frag_vecs<M>(); t += NT) {
+                const int v = t >> 5, ln = t & 31;
+                const int gq = ln >> 2, ch = 32 * (ln & 3);  // query, first dim of the lane's chunk
+                const float* qr = qrot + gq * kQStride + ch;
+                uint32_t wv[4];
+                if (v < 8) {
+                    const float xs = ksc * a.c.alpha / qscale[gq];
+#pragma unroll
+                    for (int sl = 0; sl < 2; ++sl) {
+                        const int n = 2 * v + sl;
+                        const float e = xs * exp2f((float)(key_exp<KB>(n) - 24));
+                        const float x0 = e * qr[key_dim<KB>(n, 0)], x1 = e * qr[key_dim<KB>(n, 1)];
+                        const uint32_t hi = pack_h2(x0, x1);
+                        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+                        wv[sl] = hi;
+                        wv[2 + sl] = pack_h2(x0 - hf.x, x1 - hf.y);
+                    }
+                } else if (v < 12) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int n = 4 * (v - 8) + i;
+                        wv[i] = pack_h2(qr[2 * n] * ksc, qr[2 * n + 1] * ksc);
+                    }
+                } else {
+                    const float* sr = sqv + gq * kQStride + ch;
+                    const int lo = v >= 16;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int n = 4 * (v - (lo ? 16 : 12)) + i;
+                        const uint32_t hi = pack_h2(sr[n], sr[n + 16]);
+                        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+                        wv[i] = lo ? pack_h2(sr[n] - hf.x, sr[n + 16] - hf.y) : hi;
+                    }
                 }
+                fr[v * 32 + ln] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
         }
         __syncthreads();
@@ -612,7 +634,13 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
         const float qs0 = qscale[2 * qd] * 16777216.f, qs1 = qscale[2 * qd + 1] * 16777216.f;  // 2^24 qscale
         const float cq = 1.2533141373155003f / (float)(M > 0 ? M : 1);  // sqrt(pi/2) / m
         const uint32_t lw = kLutAddr | ((uint32_t)lane << (KB == 2 ? 3 : 2));
-        const int koff = F::kcode + r * KROW + qd * 4 * KB;  // this lane's key chunk in a page
+        // Score row r holds token tr = r ^ ((r >> 1) & 1) (and row r + 8 token tr + 8):
+        // tokens 2 and 3, 6 and 7 trade rows, so that the value loads below (tokens
+        // of rows 2qd, 2qd+1 for qd = 0..3) alternate between the two halves of the
+        // bank space instead of colliding four ways.
+        const int tr = r ^ ((r >> 1) & 1);
+        const int ta = (2 * qd) ^ (qd & 1), tb = (2 * qd + 1) ^ (qd & 1);  // tokens of rows 2qd, 2qd+1
+        const int koff = F::kcode + tr * KROW + qd * 4 * KB;  // this lane's key chunk in a page
 
         float m0 = kMinusBig, m1 = kMinusBig, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
         float acc[8][4];
@@ -669,8 +697,8 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             if constexpr (M > 0) {
                 float sQ[4];
                 uint32_t Za[16], Zb[16];
-                sign_chunk(lds32(pg + F::sig + r * (M / 8) + 4 * qd), Za);
-                sign_chunk(lds32(pg + F::sig + (r + 8) * (M / 8) + 4 * qd), Zb);
+                sign_chunk(lds32(pg + F::sig + tr * (M / 8) + 4 * qd), Za);
+                sign_chunk(lds32(pg + F::sig + (tr + 8) * (M / 8) + 4 * qd), Zb);
                 mma16816_c(sQ, Za[0], Zb[0], Za[1], Zb[1], QSh[0], QSh[1], 0.f, 0.f, 0.f, 0.f);
                 mma16816(sQ, Za[0], Zb[0], Za[1], Zb[1], QSl[0], QSl[1]);
 #pragma unroll
@@ -679,20 +707,20 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                     mma16816(sQ, Za[n], Zb[n], Za[n + 1], Zb[n + 1], QSh[n], QSh[n + 1]);
                     mma16816(sQ, Za[n], Zb[n], Za[n + 1], Zb[n + 1], QSl[n], QSl[n + 1]);
                 }
-                const float rr = cq * lds_h2f(pg + F::rho + 2 * r), rr8 = cq * lds_h2f(pg + F::rho + 2 * (r + 8));
+                const float rr = cq * lds_h2f(pg + F::rho + 2 * tr), rr8 = cq * lds_h2f(pg + F::rho + 2 * (tr + 8));
                 t0 = fmaf(rr, sQ[0], t0); t1 = fmaf(rr, sQ[1], t1);
                 t2 = fmaf(rr8, sQ[2], t2); t3 = fmaf(rr8, sQ[3], t3);
             }
-            const float gr = lds_h2f(pg + F::gam + 2 * r), gr8 = lds_h2f(pg + F::gam + 2 * (r + 8));
+            const float gr = lds_h2f(pg + F::gam + 2 * tr), gr8 = lds_h2f(pg + F::gam + 2 * (tr + 8));
             float s0 = t0 * gr, s1 = t1 * gr, s2 = t2 * gr8, s3 = t3 * gr8;
             const int tok = (p0 + warp + NW * j) * kBlockSize;
             if (!pok || tok + kBlockSize > len) {  // the sequence's last page or a skipped one (warp-uniform)
-                if (!(pok && tok + r < len)) s0 = s1 = -INFINITY;
-                if (!(pok && tok + r + 8 < len)) s2 = s3 = -INFINITY;
+                if (!(pok && tok + tr < len)) s0 = s1 = -INFINITY;
+                if (!(pok && tok + tr + 8 < len)) s2 = s3 = -INFINITY;
             }
 
             // ---------- online softmax; the max moves only when a score beats it by kLazy ----------
-            const float sr = lds_h2f(pg + F::scl + 2 * r), sr8 = lds_h2f(pg + F::scl + 2 * (r + 8));
+            const float sr = lds_h2f(pg + F::scl + 2 * tr), sr8 = lds_h2f(pg + F::scl + 2 * (tr + 8));
             float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
             const bool exact = fmaxf(sr, sr8) > kBigScale;
             if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy || (exact && (mx0 > m0 || mx1 > m1)))) {
@@ -713,11 +741,11 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 m1 = n1;
             }
             const float p0v = ex2(s0 - m0), p1v = ex2(s1 - m1), p2v = ex2(s2 - m0), p3v = ex2(s3 - m1);
-            const float zr = lds_h2f(pg + F::zer + 2 * r), zr8 = lds_h2f(pg + F::zer + 2 * (r + 8));
+            const float zr = lds_h2f(pg + F::zer + 2 * tr), zr8 = lds_h2f(pg + F::zer + 2 * (tr + 8));
             l0 += p0v + p2v;
             l1 += p1v + p3v;
 
-            // ---------- values: lane (r, qd) holds dims 16r..16r+15 of tokens 2qd, 2qd+1, 2qd+8, 2qd+9 ----------
+            // ---------- values: lane (r, qd) holds dims 16r..16r+15 of the tokens of rows 2qd, 2qd+1, 2qd+8, 2qd+9 ----------
             // The weights w = p * scale (p <= 2^kLazy) go in as single fp16 w'.  The
             // codes are not centred, so the rounding w - w' is also added back times
             // the mid code through the fp32 zero-point sum; what is left is
@@ -733,8 +761,8 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 const uint32_t bh0 = movtrans(h01);
                 const uint32_t bh1 = movtrans(h23);
                 uint32_t Pab[16], Pcd[16];
-                value_codes<VB>(pg + F::vcode, r, 2 * qd, 2 * qd + 1, Pab);
-                value_codes<VB>(pg + F::vcode, r, 2 * qd + 8, 2 * qd + 9, Pcd);
+                value_codes<VB>(pg + F::vcode, r, ta, tb, Pab);
+                value_codes<VB>(pg + F::vcode, r, ta + 8, tb + 8, Pcd);
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt)  // rows: dim 16r + 2mt (row r), 16r + 2mt + 1 (row r + 8)
                     mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bh0, bh1);

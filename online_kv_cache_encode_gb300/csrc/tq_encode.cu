@@ -50,26 +50,50 @@ __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs
     }
     const uint32_t sm = lane_signs(a.c, lane);
     const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
-    const int64_t items = a.num_tokens * g.hkv;
-    const int64_t cap = g.num_blocks * g.bs;
+    const int hkv = g.hkv;
+    const int64_t items = a.num_tokens * hkv;
+    const int64_t cap = g.num_blocks * kBlockSize;
 
-    for (int64_t it = (int64_t)blockIdx.x * kEncWarps + warp; it < items;
-         it += (int64_t)gridDim.x * kEncWarps) {
-        const int64_t t = it / g.hkv;
-        const int h = (int)(it - t * g.hkv);
-        const int64_t slot = a.slot_mapping[t];
+    // Item it = t * hkv + h.  The grid-stride loop keeps (t, h) incrementally
+    // (no 64-bit division per item) and loads the next item's K, V and slot
+    // while the current one is coded.
+    const int64_t stride = (int64_t)gridDim.x * kEncWarps;
+    const int64_t st_t = stride / hkv;
+    const int st_h = (int)(stride - st_t * hkv);
+    int64_t it = (int64_t)blockIdx.x * kEncWarps + warp;
+    int64_t t = it / hkv;
+    int h = (int)(it - t * hkv);
+    float kn[4] = {0.f, 0.f, 0.f, 0.f}, vn[4] = {0.f, 0.f, 0.f, 0.f};
+    int64_t slot_n = -1;
+    if (it < items) {
+        load4(a.K, a.dtype, it * D + 4 * lane, kn);
+        load4(a.V, a.dtype, it * D + 4 * lane, vn);
+        slot_n = a.slot_mapping[t];
+    }
+    for (; it < items; it += stride) {
+        float k[4], v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { k[i] = kn[i]; v[i] = vn[i]; }
+        const int64_t slot = slot_n;
+        const int hc = h;
+        // advance to the next item and start its loads
+        t += st_t;
+        h += st_h;
+        if (h >= hkv) { h -= hkv; ++t; }
+        if (it + stride < items) {
+            load4(a.K, a.dtype, (it + stride) * D + 4 * lane, kn);
+            load4(a.V, a.dtype, (it + stride) * D + 4 * lane, vn);
+            slot_n = a.slot_mapping[t];
+        }
         if (slot < 0) continue;
         if (slot >= cap) {
             if (lane == 0) flag(a.status, TQ_FLAG_BAD_SLOT);
             continue;
         }
-        const int64_t blk = slot / g.bs;
-        const int off = (int)(slot - blk * g.bs);
-        uint8_t* page = a.pool + (blk * g.hkv + h) * g.page_bytes;
-
-        float k[4], v[4];
-        load4(a.K, a.dtype, it * D + 4 * lane, k);
-        load4(a.V, a.dtype, it * D + 4 * lane, v);
+        static_assert(kBlockSize == 16, "page index by shift");
+        const int64_t blk = slot >> 4;
+        const int off = (int)(slot & (kBlockSize - 1));
+        uint8_t* page = a.pool + (blk * hkv + hc) * g.page_bytes;
         // x * 0 is 0 for every finite x and NaN for inf / NaN
         float z = 0.f;
 #pragma unroll

@@ -56,6 +56,8 @@ class TQError(RuntimeError):
 def lib():
     """Load libtq.so (raises if it has not been built)."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -75,8 +77,11 @@ def _check(st: int):
         raise TQError(st, lib().tq_last_error().decode())
 
 
+_DTYPE_CODES = {torch.float32: TQ_F32, torch.bfloat16: TQ_BF16, torch.float16: TQ_F16}
+
+
 def _dtype_code(t: torch.Tensor) -> int:
-    return {torch.float32: TQ_F32, torch.bfloat16: TQ_BF16, torch.float16: TQ_F16}[t.dtype]
+    return _DTYPE_CODES[t.dtype]
 
 
 def _stream() -> int:
@@ -84,7 +89,8 @@ def _stream() -> int:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: the c_void_p argtypes convert it
+    return None if t is None else t.data_ptr()
 
 
 def page_bytes(d: int, key_bits: int, value_bits: int, qjl_m: int = 0, block_size: int = 16) -> int:
@@ -172,7 +178,7 @@ class Cache:
         assert slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous()
         assert slot_mapping.numel() == K.shape[0]
         _check(lib().tq_encode_kv(self._h, _ptr(K), _ptr(V), _dtype_code(K), K.shape[0],
-                                  _ptr(slot_mapping), _ptr(status), ctypes.c_void_p(_stream())))
+                                  _ptr(slot_mapping), _ptr(status), _stream()))
 
     # ---- decode ----
     def workspace_bytes(self, batch: int, num_q_heads: int, max_blocks_per_seq: int) -> int:
@@ -202,7 +208,7 @@ class Cache:
             workspace = self._ws[1]
         _check(lib().tq_decode_attention(self._h, _ptr(q), _dtype_code(q), B, hq, _ptr(block_table), mb,
                                          _ptr(lens), float(sm_scale), _ptr(out), _ptr(workspace),
-                                         workspace.numel(), _ptr(status), ctypes.c_void_p(_stream())))
+                                         workspace.numel(), _ptr(status), _stream()))
         return out
 
     def decode_noalloc(self, q: torch.Tensor, block_table: torch.Tensor, lens: torch.Tensor,
@@ -221,5 +227,5 @@ class Cache:
             sm_scale = 1.0 / math.sqrt(self.d)
         _check(lib().tq_decode_attention_noalloc(self._h, _ptr(q), _dtype_code(q), B, hq, _ptr(block_table),
                                                  block_table.shape[1], _ptr(lens), float(sm_scale), _ptr(out),
-                                                 _ptr(status), ctypes.c_void_p(_stream())))
+                                                 _ptr(status), _stream()))
         return out
