@@ -164,7 +164,7 @@ TQ_API tq_status tq_cache_gaussian(const tq_cache* cache, double* S);
 /* ---------------------------------------------------------------------- */
 
 /* Compress num_tokens new tokens into the cache.
- * K, V: device, [num_tokens, num_kv_heads, d] of `dtype`.
+ * K, V: device, [num_tokens, num_kv_heads, d] of `dtype`, 16-byte aligned.
  * slot_mapping: device int64 [num_tokens]; slot = block * block_size + offset.
  *   A negative slot skips the token; a slot past the pool sets
  *   TQ_FLAG_BAD_SLOT and skips it.

@@ -125,26 +125,4 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Write a row of 128 B-bit codes, lane holding the 4 codes of coordinates
-// 4*lane .. 4*lane+3 packed LSB-first in p (4*B bits).  Code j occupies bits
-// [j*B, j*B + B) of the row; lanes below 4*B each store one 32-bit word.
-template <int B>
-__device__ __forceinline__ void store_code_row(uint8_t* row, uint32_t p, int lane) {
-    constexpr int LB = 4 * B;  // bits per lane
-    constexpr int WORDS = 4 * B;
-    uint32_t word = 0;
-    const int src0 = (lane * 32) / LB;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int src = src0 + k;
-        const uint32_t pv = __shfl_sync(0xffffffffu, p, src < 32 ? src : 31);
-        const int shift = src * LB - lane * 32;
-        if (src < 32) {
-            if (shift >= 0 && shift < 32) word |= pv << shift;
-            else if (shift < 0 && shift > -LB) word |= pv >> (-shift);
-        }
-    }
-    if (lane < WORDS) reinterpret_cast<uint32_t*>(row)[lane] = word;
-}
-
 }  // namespace tq

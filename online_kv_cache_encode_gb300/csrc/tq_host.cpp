@@ -361,9 +361,8 @@ TQ_API tq_status tq_encode_kv(const tq_cache* c, const void* K, const void* V, t
     if (num_tokens == 0) return TQ_OK;
     if (!K || !V || !slot_mapping) return fail(TQ_ERR_INVALID_ARG, "K, V and slot_mapping must be non-NULL");
     if (dtype != TQ_F32 && dtype != TQ_BF16 && dtype != TQ_F16) return fail(TQ_ERR_INVALID_ARG, "bad dtype");
-    const int64_t elem = dtype == TQ_F32 ? 4 : 2;
-    if ((reinterpret_cast<uintptr_t>(K) % (4 * elem)) || (reinterpret_cast<uintptr_t>(V) % (4 * elem)))
-        return fail(TQ_ERR_INVALID_ARG, "K and V must be aligned to 4 elements");
+    if ((reinterpret_cast<uintptr_t>(K) % 16) || (reinterpret_cast<uintptr_t>(V) % 16))
+        return fail(TQ_ERR_INVALID_ARG, "K and V must be 16-byte aligned");
     EncodeArgs a{};
     a.g = c->g;
     a.c = c->c;
