@@ -226,9 +226,9 @@ def run_ours(args, rank, world, local):
         return
 
     def step(i):
+        # the decode step in one launch: append the new token, then attend
         c = copies[i % N_COPIES]
-        c.encode(newK, newV, new_slot, status)
-        c.decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
+        c.decode_append(newK, newV, q, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
 
     def capture(fn, n):
         """CUDA graph of n calls of fn(i) (the library launches on torch's current stream)."""
@@ -265,7 +265,7 @@ def run_ours(args, rank, world, local):
     barrier(dist)
     torch.cuda.synchronize()
     step_ms = t0.elapsed_time(t1) / args.steps
-    launches = 2 * args.steps
+    launches = args.steps
     del steps_graph
 
     # ---- the decode kernel alone (roofline): a graph of back-to-back decode launches ----
@@ -301,8 +301,7 @@ def run_ours(args, rank, world, local):
     def e2e_step(i):
         din.copy_(hin, non_blocking=True)
         c = copies[i % N_COPIES]
-        c.encode(dK, dV, new_slot, status)
-        c.decode(dq, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
+        c.decode_append(dK, dV, dq, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
         hout.copy_(out, non_blocking=True)
 
     for i in range(3):
@@ -346,7 +345,7 @@ def run_ours(args, rank, world, local):
         "config": {
             "workload": "gqa32k: 64 query / 8 KV heads, head_dim 128, 32768-token context, batch 1, "
                         "4-bit keys and values, 16-token pages in a permuted block table",
-            "step": "encode 1 new token (8 KV heads) + decode attention for 64 query heads over 32768 tokens",
+            "step": "append 1 new token (8 KV heads) + decode attention for 64 query heads over 32768 tokens, one launch (tq_decode_attention_append)",
             "decode_bytes_per_step": decode_bytes,
             "l2": f"inputs larger than L2: {N_COPIES} distinct caches rotated ({N_COPIES * decode_bytes / 1e6:.0f} MB)",
             "timing": "the K steps captured in one CUDA graph, replayed once between CUDA events; "

@@ -218,6 +218,25 @@ TQ_API tq_status tq_decode_attention(const tq_cache* cache, const void* q, tq_dt
                                      float* out, void* workspace, size_t workspace_bytes,
                                      int32_t* dev_status, void* stream);
 
+/* One decode step in one launch: append, then attend.  For every sequence b
+ * with lens[b] >= 1 the new token (rows k_new[b], v_new[b] of
+ * [batch, num_kv_heads, d], `kv_dtype`, device, 16-byte aligned) is encoded
+ * exactly as tq_encode_kv encodes it into position lens[b] - 1, i.e. slot
+ * block_table[b][(lens[b]-1) / block_size] * block_size + (lens[b]-1) % block_size,
+ * and attended to together with the lens[b] - 1 tokens before it; all other
+ * arguments and results are those of tq_decode_attention.  This is the order
+ * of the pages' decode step -- the new key/value enters the compressed cache,
+ * then the query reads it ["TurboQuant: KV Cache Vector Quantization" -- three
+ * steps; Bit-Axon -- KV cache memory model] -- without a separate encode
+ * launch between the two.  Caches with a QJL sketch (qjl_m > 0) return
+ * TQ_ERR_UNSUPPORTED: use tq_encode_kv, then tq_decode_attention. */
+TQ_API tq_status tq_decode_attention_append(const tq_cache* cache, const void* k_new, const void* v_new,
+                                            tq_dtype kv_dtype, const void* q, tq_dtype dtype, int batch,
+                                            int num_q_heads, const int32_t* block_table,
+                                            int max_blocks_per_seq, const int32_t* lens, float sm_scale,
+                                            float* out, void* workspace, size_t workspace_bytes,
+                                            int32_t* dev_status, void* stream);
+
 /* Bytes of the fixed decode workspace built into the library (see below). */
 #define TQ_NOALLOC_WORKSPACE_BYTES (4u << 20)
 

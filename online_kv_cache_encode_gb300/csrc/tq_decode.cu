@@ -185,7 +185,7 @@ template <int M>
 __host__ __device__ constexpr int frag_vecs() { return 8 + 4 + (M ? 8 : 0); }
 
 struct Layout {
-    int frag, qrot, sq, qoff, qscale, rem, bars, ok;  // small fixed region at the start
+    int frag, qrot, sq, qoff, qscale, rem, stage, bars, ok;  // small fixed region at the start
     int ringA, nwA;   // ring slots of warps 0 .. nwA-1 sit below the remainder table
     int spw;          // ring slots per warp
     int total;        // dynamic bytes to request: enough for any start address up to kMaxSmemBase
@@ -205,6 +205,7 @@ __host__ __device__ constexpr Layout decode_layout() {
     L.qoff = off; off += 8 * 4;
     L.qscale = off; off += 8 * 4;
     L.rem = off; off += 16 * 2;
+    L.stage = off; off += 192;  // appended token: key row | value row | gamma, scale, zero | barrier at 176
     L.bars = off; off += 8 * NW * kMaxSlotsPerWarp;
     L.ok = off; off += 4 * NW * kMaxSlotsPerWarp;
     L.ringA = (off + 127) / 128 * 128;
@@ -380,6 +381,166 @@ __device__ __forceinline__ void sign_chunk(uint32_t w, uint32_t Z[16]) {
 }
 
 // ---------------------------------------------------------------------------
+// append: one warp encodes the new token of (sequence, KV head) exactly as the
+// encode kernel does with one warp per token (lane l holds coordinates
+// 4l .. 4l+3), writes it into its page in the pool and keeps a staged copy
+// (key row at 0, value row at 64, gamma / scale / zero at 128) that the warp
+// patches into its shared-memory copy of the page before consuming it.
+// ["TurboQuant: KV Cache Vector Quantization" -- three steps; deep dive --
+//  Step 1 (RHT), Step 3 (value codes); "OCTOPUS ..." -- methodology step 8]
+// ---------------------------------------------------------------------------
+// A 128-code row of 3-bit codes, lane holding 12 bits (codes 4 lane .. 4 lane+3):
+// lanes below 12 gather one 32-bit word of the row each.
+__device__ __forceinline__ uint32_t row3_word(uint32_t p, int lane) {
+    constexpr int LB = 12;
+    uint32_t word = 0;
+    const int src0 = (lane * 32) / LB;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int src = src0 + k;
+        const uint32_t pv = __shfl_sync(0xffffffffu, p, src < 32 ? src : 31);
+        const int shift = src * LB - lane * 32;
+        if (src < 32) {
+            if (shift >= 0 && shift < 32) word |= pv << shift;
+            else if (shift < 0 && shift > -LB) word |= pv >> (-shift);
+        }
+    }
+    return word;
+}
+
+template <int B>
+__device__ __forceinline__ void store_row_both(uint8_t* g, uint8_t* st, uint32_t p, int lane) {
+    if constexpr (B == 4) {
+        reinterpret_cast<uint16_t*>(g)[lane] = (uint16_t)p;
+        reinterpret_cast<uint16_t*>(st)[lane] = (uint16_t)p;
+    } else if constexpr (B == 2) {
+        g[lane] = (uint8_t)p;
+        st[lane] = (uint8_t)p;
+    } else {
+        const uint32_t w = row3_word(p, lane);
+        if (lane < 12) {
+            reinterpret_cast<uint32_t*>(g)[lane] = w;
+            reinterpret_cast<uint32_t*>(st)[lane] = w;
+        }
+    }
+}
+
+// Raw bits of elements i .. i+3 of a row: one 8-byte load for 16-bit types,
+// two for fp32.  Nothing here uses the loaded registers, so the warp does not
+// wait for them until cvt4 converts them.
+__device__ __forceinline__ void raw4(const void* base, int dtype, int64_t i, uint32_t r[4]) {
+    const int f32 = dtype == TQ_F32;
+    const char* p = reinterpret_cast<const char*>(base) + i * (f32 ? 4 : 2);
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.s32 q, %5, 0;\n"
+        " ld.global.nc.v2.u32 {%0, %1}, [%4];\n"
+        " @q ld.global.nc.v2.u32 {%2, %3}, [%4+8];\n}\n"
+        : "=r"(r[0]), "=r"(r[1]), "+r"(r[2]), "+r"(r[3])
+        : "l"(p), "r"(f32));
+}
+__device__ __forceinline__ void cvt4(const uint32_t r[4], int dtype, float x[4]) {
+    if (dtype == TQ_F32) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = __uint_as_float(r[i]);
+    } else if (dtype == TQ_BF16) {
+        x[0] = __uint_as_float(r[0] << 16);
+        x[1] = __uint_as_float(r[0] & 0xFFFF0000u);
+        x[2] = __uint_as_float(r[1] << 16);
+        x[3] = __uint_as_float(r[1] & 0xFFFF0000u);
+    } else {
+        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&r[0]));
+        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&r[1]));
+        x[0] = fa.x; x[1] = fa.y; x[2] = fb.x; x[3] = fb.y;
+    }
+}
+
+// kraw, vraw: raw4 bits of this lane's coordinates 4 lane .. 4 lane + 3 of the new token
+template <int KB, int VB, int M>
+__device__ void append_token(const DecodeArgs& a, uint8_t* page, int off, uint8_t* stage, int lane,
+                             const uint32_t kraw[4], const uint32_t vraw[4]) {
+    using F = PageFmt<KB, VB, M>;
+    constexpr int D = kHeadDim;
+    constexpr int NB = (1 << KB) - 1, HALF = 1 << (KB - 1), VMAX = (1 << VB) - 1;
+    float k[4], v[4];
+    cvt4(kraw, a.kv_dtype, k);
+    cvt4(vraw, a.kv_dtype, v);
+    float z = 0.f, ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        z = fmaf(k[i], 0.f, fmaf(v[i], 0.f, z));  // x * 0 is 0 for finite x, NaN for inf / NaN
+        ss = fmaf(k[i], k[i], ss);
+    }
+    const bool finite = (warp_sum(z) == 0.f);
+    if (!finite && lane == 0) flag(a.status, TQ_FLAG_NONFINITE);
+    const float gamma = sqrtf(warp_sum(ss));
+    const uint32_t sg = lane_signs(a.c, lane);
+    apply_signs(k, sg);
+    fwht128(k, lane);
+    uint32_t kp = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int c = HALF - 1;
+        if (gamma > 0.f) {
+            const float u = (k[i] * 0.08838834764831845f) / gamma;
+            const float au = fabsf(u);
+            int n = 0;
+#pragma unroll
+            for (int bb = HALF; bb < NB; ++bb) n += (a.c.boundary[bb] < au) ? 1 : 0;
+            c = (u > 0.f) ? HALF + n : HALF - 1 - n;
+        }
+        kp |= (uint32_t)c << (KB * i);
+    }
+    apply_signs(v, sg);
+    fwht128(v, lane);
+    float lo = 3.4e38f, hi = -3.4e38f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] *= 0.08838834764831845f;
+        lo = fminf(lo, v[i]);
+        hi = fmaxf(hi, v[i]);
+    }
+    const float mn = warp_min(lo), mx = warp_max(hi);
+    const float scale = (mx - mn) / (float)VMAX;
+    uint32_t vp = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float qv = (scale > 0.f) ? fminf(fmaxf(rintf((v[i] - mn) / scale), 0.f), (float)VMAX) : 0.f;
+        vp |= (uint32_t)qv << (VB * i);
+    }
+    store_row_both<KB>(page + F::kcode + off * (D * KB / 8), stage, kp, lane);
+    store_row_both<VB>(page + F::vcode + off * (D * VB / 8), stage + 64, vp, lane);
+    if (lane == 0) {
+        const uint16_t hg = f16_bits(gamma), hs = f16_bits(scale), hz = f16_bits(mn);
+        reinterpret_cast<uint16_t*>(page + F::gam)[off] = hg;
+        reinterpret_cast<uint16_t*>(page + F::scl)[off] = hs;
+        reinterpret_cast<uint16_t*>(page + F::zer)[off] = hz;
+        uint16_t* sm3 = reinterpret_cast<uint16_t*>(stage + 128);
+        sm3[0] = hg; sm3[1] = hs; sm3[2] = hz;
+        const bool ovf = ((hg & 0x7FFF) == 0x7C00) || ((hs & 0x7FFF) == 0x7C00) || ((hz & 0x7FFF) == 0x7C00);
+        if (ovf && finite) flag(a.status, TQ_FLAG_OVERFLOW);
+    }
+    __syncwarp();
+}
+
+// Copy the staged token into slot `off` of the shared-memory page at `pg`.
+template <int KB, int VB, int M>
+__device__ __forceinline__ void patch_page(uint8_t* pg, int off, const uint8_t* stage, int lane) {
+    using F = PageFmt<KB, VB, M>;
+    constexpr int KROW = kHeadDim * KB / 8, VROW = kHeadDim * VB / 8;
+    if (lane < KROW / 4)
+        reinterpret_cast<uint32_t*>(pg + F::kcode + off * KROW)[lane] = reinterpret_cast<const uint32_t*>(stage)[lane];
+    if (lane < VROW / 4)
+        reinterpret_cast<uint32_t*>(pg + F::vcode + off * VROW)[lane] = reinterpret_cast<const uint32_t*>(stage + 64)[lane];
+    if (lane == 0) {
+        const uint16_t* sm3 = reinterpret_cast<const uint16_t*>(stage + 128);
+        reinterpret_cast<uint16_t*>(pg + F::gam)[off] = sm3[0];
+        reinterpret_cast<uint16_t*>(pg + F::scl)[off] = sm3[1];
+        reinterpret_cast<uint16_t*>(pg + F::zer)[off] = sm3[2];
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 template <int KB, int VB, int M>
@@ -418,8 +579,10 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     const float ksc = a.sm_scale_log2;
 
     // ---- shared-memory-only setup: it may overlap the previous kernel's tail ----
+    const uint32_t stage_bar = sbase + LY.stage + 176;
     if (lane == 0) {
         for (int k = 0; k < SPW; ++k) mbar_init(bar_w + 8 * k, 1);
+        if (warp == 0) mbar_init(stage_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     uint16_t* rem = reinterpret_cast<uint16_t*>(sm + LY.rem);
@@ -498,6 +661,36 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             mbar_arrive(bar);
         }
     };
+    // The appended token (position len - 1) lies in the sequence's last page,
+    // the split's last page pi = npages - 1.  The warp that owns that page
+    // patches the token into its shared-memory copy when it gets there.  The
+    // encoding is done right after the query is prepared by warp npages % NW
+    // when that warp has one page fewer than the owner (by the owner itself
+    // otherwise) and handed over through the stage barrier.  Its inputs are
+    // requested now, ahead of the page copies, and waited on only when used.
+    int jnew = -1;        // owner: its index of the page that takes the token
+    bool enc = false;     // this warp encodes the token
+    int blknew = -1;
+    const int offnew = (len - 1) & (kBlockSize - 1);
+    uint32_t kraw[4] = {0u, 0u, 0u, 0u}, vraw[4] = {0u, 0u, 0u, 0u};
+    if constexpr (M == 0) {
+        if (a.knew != nullptr && len > 0) {
+            const int pi = (len - 1) / kBlockSize - p0;
+            if (pi >= 0 && pi < npages) {
+                const int owner = pi % NW, rest = npages % NW;
+                const int encoder = (rest != 0 && pi == npages - 1) ? rest : owner;
+                if (warp == owner) jnew = pi / NW;
+                if (warp == encoder) {
+                    enc = true;
+                    const int64_t e = ((int64_t)b * g.hkv + h) * D + 4 * lane;
+                    raw4(a.knew, a.kv_dtype, e, kraw);
+                    raw4(a.vnew, a.kv_dtype, e, vraw);
+                    blknew = __ldg(a.block_table + (int64_t)b * a.max_blocks + p0 + pi);
+                }
+            }
+        }
+    }
+
     // The first kFirstPages pages of every warp now, one lane each; the rest of
     // the ring once the query is prepared, so that the first pages of all warps
     // are not queued behind the whole initial burst.
@@ -606,6 +799,15 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
         }
         __syncthreads();
         if (lane >= kFirst && lane < SPW && lane < nmine) issue(lane, bid_cur);
+        if (enc) {
+            // a bad block id leaves the pool alone; the owner's copy of that
+            // page is flagged and skipped, so what it patches in is never used
+            if (blknew >= 0 && blknew < g.num_blocks) {
+                uint8_t* page = const_cast<uint8_t*>(a.pool) + ((int64_t)blknew * g.hkv + h) * F::bytes;
+                append_token<KB, VB, M>(a, page, offnew, sm + LY.stage, lane, kraw, vraw);
+            }
+            if (lane == 0) mbar_arrive(stage_bar);
+        }
         const int r = lane >> 2, qd = lane & 3;   // r: token row / query column; qd: quad index
         uint32_t QI[8][4], QB[16];
         uint32_t QSh[M > 0 ? 16 : 1], QSl[M > 0 ? 16 : 1];
@@ -659,6 +861,17 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             }
             const uint32_t pg = ring_w + slot * F::stride;  // shared-space address of the page
             const bool pok = slot_ok[slot] != 0;
+            if (j == jnew) {
+                if (!mbar_wait(stage_bar, 0)) {
+                    timed_out = true;
+                    jfail = j;
+                    break;
+                }
+                patch_page<KB, VB, M>(sm + (pg - sbase), offnew, sm + LY.stage, lane);
+                // the slot is refilled later by a bulk copy: order these generic
+                // writes before that async-proxy write
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
 
             // ---------- scores: tokens r (rows 0-7) and r+8 (rows 8-15) ----------
             uint32_t wa[KB], wb[KB];

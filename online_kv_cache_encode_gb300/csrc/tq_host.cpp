@@ -405,11 +405,11 @@ TQ_API size_t tq_decode_workspace_bytes(const tq_cache* c, int batch, int num_q_
     return align_up(part, 256) + align_up((size_t)batch * c->g.hkv * sizeof(unsigned), 256);
 }
 
-TQ_API tq_status tq_decode_attention(const tq_cache* c, const void* q, tq_dtype dtype, int batch,
-                                     int num_q_heads, const int32_t* block_table,
-                                     int max_blocks_per_seq, const int32_t* lens, float sm_scale,
-                                     float* out, void* workspace, size_t workspace_bytes,
-                                     int32_t* dev_status, void* stream) {
+static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype, int batch, int num_q_heads,
+                               const int32_t* block_table, int max_blocks_per_seq, const int32_t* lens,
+                               float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream, const void* knew, const void* vnew,
+                               tq_dtype kv_dtype) {
     if (!c) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
     if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0)
         return fail(TQ_ERR_INVALID_ARG, "bad batch / num_q_heads / max_blocks_per_seq");
@@ -453,9 +453,39 @@ TQ_API tq_status tq_decode_attention(const tq_cache* c, const void* q, tq_dtype 
     a.num_splits = splits;
     a.status = dev_status;
     a.S = c->S_dev;
+    a.knew = knew;
+    a.vnew = vnew;
+    a.kv_dtype = (int)kv_dtype;
     int e = launch_decode(a, stream);
     if (e != 0) return cuda_fail((cudaError_t)e, "decode launch");
     return TQ_OK;
+}
+
+TQ_API tq_status tq_decode_attention(const tq_cache* c, const void* q, tq_dtype dtype, int batch,
+                                     int num_q_heads, const int32_t* block_table,
+                                     int max_blocks_per_seq, const int32_t* lens, float sm_scale,
+                                     float* out, void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, void* stream) {
+    return decode_common(c, q, dtype, batch, num_q_heads, block_table, max_blocks_per_seq, lens, sm_scale, out,
+                         workspace, workspace_bytes, dev_status, stream, nullptr, nullptr, TQ_BF16);
+}
+
+TQ_API tq_status tq_decode_attention_append(const tq_cache* c, const void* k_new, const void* v_new,
+                                            tq_dtype kv_dtype, const void* q, tq_dtype dtype, int batch,
+                                            int num_q_heads, const int32_t* block_table,
+                                            int max_blocks_per_seq, const int32_t* lens, float sm_scale,
+                                            float* out, void* workspace, size_t workspace_bytes,
+                                            int32_t* dev_status, void* stream) {
+    if (!c) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
+    if (c->g.m > 0)
+        return fail(TQ_ERR_UNSUPPORTED, "appending inside decode is built for caches without QJL; "
+                                        "use tq_encode_kv then tq_decode_attention");
+    if (batch > 0 && (!k_new || !v_new)) return fail(TQ_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
+    if (kv_dtype != TQ_F32 && kv_dtype != TQ_BF16 && kv_dtype != TQ_F16) return fail(TQ_ERR_INVALID_ARG, "bad kv dtype");
+    if ((reinterpret_cast<uintptr_t>(k_new) % 16) || (reinterpret_cast<uintptr_t>(v_new) % 16))
+        return fail(TQ_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    return decode_common(c, q, dtype, batch, num_q_heads, block_table, max_blocks_per_seq, lens, sm_scale, out,
+                         workspace, workspace_bytes, dev_status, stream, k_new, v_new, kv_dtype);
 }
 
 }  // extern "C"

@@ -64,6 +64,11 @@ struct DecodeArgs {
     int num_splits;
     int32_t* status;
     const float* S;
+    // append (optional): the new token of every sequence, written at position
+    // lens[b] - 1 before it is attended to; null when nothing is appended
+    const void* knew;     // [batch, hkv, d]
+    const void* vnew;
+    int kv_dtype;
 };
 
 // Launchers (return a cudaError_t as int).

@@ -39,6 +39,7 @@ SIGNATURES = {
     "tq_decode_workspace_bytes": (_SZ, [_P, _I, _I, _I]),
     "tq_decode_attention": (_I, [_P, _P, _I, _I, _I, _P, _I, _P, _F, _P, _P, _SZ, _P, _P]),
     "tq_decode_attention_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _I, _P, _F, _P, _P, _P]),
+    "tq_decode_attention_append": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _F, _P, _P, _SZ, _P, _P]),
     "tq_status_string": (ctypes.c_char_p, [_I]),
     "tq_last_error": (ctypes.c_char_p, []),
 }
@@ -209,6 +210,35 @@ class Cache:
         _check(lib().tq_decode_attention(self._h, _ptr(q), _dtype_code(q), B, hq, _ptr(block_table), mb,
                                          _ptr(lens), float(sm_scale), _ptr(out), _ptr(workspace),
                                          workspace.numel(), _ptr(status), _stream()))
+        return out
+
+    def decode_append(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
+                      lens: torch.Tensor, sm_scale: float | None = None, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, status: torch.Tensor | None = None) -> torch.Tensor:
+        """One decode step: append the new token of every sequence (k_new, v_new:
+        [B, num_kv_heads, d], position lens[b] - 1) and attend over lens[b] tokens."""
+        assert k_new.is_cuda and k_new.shape == v_new.shape and k_new.dtype == v_new.dtype
+        assert k_new.dim() == 3 and k_new.shape[1] == self.hkv and k_new.shape[2] == self.d
+        assert k_new.is_contiguous() and v_new.is_contiguous()
+        assert q.is_cuda and q.dim() == 3 and q.shape[2] == self.d and q.is_contiguous()
+        B, hq, _ = q.shape
+        assert k_new.shape[0] == B
+        assert block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.shape[0] == B
+        assert block_table.is_contiguous() and lens.dtype == torch.int32 and lens.numel() == B
+        mb = block_table.shape[1]
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.d)
+        if out is None:
+            out = torch.empty((B, hq, self.d), dtype=torch.float32, device=q.device)
+        if workspace is None:
+            key = (B, hq, mb)
+            if self._ws is None or self._ws[0] != key:
+                self._ws = (key, self.new_workspace(B, hq, mb))
+            workspace = self._ws[1]
+        _check(lib().tq_decode_attention_append(self._h, _ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(q),
+                                                _dtype_code(q), B, hq, _ptr(block_table), mb, _ptr(lens),
+                                                float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                                _ptr(status), _stream()))
         return out
 
     def decode_noalloc(self, q: torch.Tensor, block_table: torch.Tensor, lens: torch.Tensor,

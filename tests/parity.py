@@ -201,6 +201,64 @@ def compare_encode(fo, fg, kin, vin, oc, oracle) -> dict:
     return res
 
 
+def run_append_case(w, oracle, tq, q_step: int = 0) -> dict:
+    """The fused decode step: the GPU encodes each sequence's first lens[b] - 1
+    tokens, then tq_decode_attention_append appends token lens[b] - 1 and
+    attends.  The resulting cache is compared with the oracle's encoding of all
+    lens[b] tokens, the output with the oracle's decode, and with the plain GPU
+    decode of the same cache (which must agree bit for bit)."""
+    import torch
+
+    dev = torch.device("cuda")
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    bt = W.block_table(w)
+    nb = w.num_blocks()
+    K, V = _inputs(w)
+    slots = [W.slots(w, bt, b, 0, w.lens[b]) for b in range(w.batch)]
+
+    oc = oracle.Cache(w.d, w.key_bits, w.value_bits, w.qjl_m, w.block_size, w.hkv, nb, w.seed)
+    pool_o = oc.new_pool()
+    st_o = 0
+    for b in range(w.batch):
+        st_o |= oc.encode(K[b], V[b], slots[b], pool_o)
+    q = W.queries(w, q_step)
+    lens = np.array(w.lens, dtype=np.int32)
+    smv = W.sm_scale(w)
+    out_o, dst_o = oc.decode(pool_o, q.astype(np.float64), bt, lens, smv)
+
+    gc = tq.Cache(nb, w.hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed, w.block_size, w.d)
+    status = tq.new_status()
+    Kp = torch.from_numpy(np.concatenate([k[:-1] for k in K])).to(dev, tdt).contiguous()
+    Vp = torch.from_numpy(np.concatenate([v[:-1] for v in V])).to(dev, tdt).contiguous()
+    sp = torch.from_numpy(np.concatenate([sl[:-1] for sl in slots])).to(dev)
+    if Kp.shape[0]:
+        gc.encode(Kp, Vp, sp, status)
+    kn = torch.from_numpy(np.stack([k[-1] for k in K])).to(dev, tdt).contiguous()
+    vn = torch.from_numpy(np.stack([v[-1] for v in V])).to(dev, tdt).contiguous()
+    qt = torch.from_numpy(q).to(dev, tdt).contiguous()
+    btt = torch.from_numpy(bt).to(dev)
+    lt = torch.from_numpy(lens).to(dev)
+    out_a = gc.decode_append(kn, vn, qt, btt, lt, smv, status=status).cpu().numpy().astype(np.float64)
+    torch.cuda.synchronize()
+    pool_g = gc.pool.cpu().numpy()
+    st_g = int(status.item())
+    out_p = gc.decode(qt, btt, lt, smv).cpu().numpy().astype(np.float64)
+
+    L = Layout(w.d, w.key_bits, w.value_bits, w.qjl_m, w.block_size, w.hkv, oc.page_bytes)
+    all_slots = np.repeat(np.concatenate(slots), w.hkv)
+    all_heads = np.tile(np.arange(w.hkv), len(all_slots) // w.hkv)
+    fo = unpack(pool_o, L, all_slots, all_heads)
+    fg = unpack(pool_g, L, all_slots, all_heads)
+    kin = np.concatenate(K).reshape(-1, w.d).astype(np.float64)
+    vin = np.concatenate(V).reshape(-1, w.d).astype(np.float64)
+    enc = compare_encode(fo, fg, kin, vin, oc, oracle)
+    enc["status_oracle"], enc["status_gpu"] = st_o | dst_o, st_g
+    enc["other_bytes_equal"] = True
+    return dict(enc=enc, dec=dict(rel_err=rel_err(out_a, out_o), status_gpu=st_g, status_oracle=st_o | dst_o,
+                                  out_gpu=out_a, out_oracle=out_o,
+                                  same_as_plain_decode=bool(np.array_equal(out_a, out_p))), w=w)
+
+
 def assert_encode_parity(res: dict):
     e = res["enc"]
     assert e["status_gpu"] == e["status_oracle"], e
