@@ -460,7 +460,7 @@ __device__ void append_token(const DecodeArgs& a, uint8_t* page, int off, uint8_
                              const uint32_t kraw[4], const uint32_t vraw[4]) {
     using F = PageFmt<KB, VB, M>;
     constexpr int D = kHeadDim;
-    constexpr int NB = (1 << KB) - 1, HALF = 1 << (KB - 1), VMAX = (1 << VB) - 1;
+    constexpr int HALF = 1 << (KB - 1), VMAX = (1 << VB) - 1;
     float k[4], v[4];
     cvt4(kraw, a.kv_dtype, k);
     cvt4(vraw, a.kv_dtype, v);
@@ -477,17 +477,10 @@ __device__ void append_token(const DecodeArgs& a, uint8_t* page, int off, uint8_
     apply_signs(k, sg);
     fwht128(k, lane);
     uint32_t kp = 0;
+    const KeyThresholds<KB> kt(a.c, gamma);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        int c = HALF - 1;
-        if (gamma > 0.f) {
-            const float u = (k[i] * 0.08838834764831845f) / gamma;
-            const float au = fabsf(u);
-            int n = 0;
-#pragma unroll
-            for (int bb = HALF; bb < NB; ++bb) n += (a.c.boundary[bb] < au) ? 1 : 0;
-            c = (u > 0.f) ? HALF + n : HALF - 1 - n;
-        }
+        const int c = (gamma > 0.f) ? kt.code(k[i]) : HALF - 1;
         kp |= (uint32_t)c << (KB * i);
     }
     apply_signs(v, sg);

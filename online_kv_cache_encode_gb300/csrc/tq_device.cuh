@@ -68,6 +68,30 @@ __device__ __forceinline__ void load4(const void* base, int dtype, int64_t i, fl
     }
 }
 
+// Key codes without a division.  With x a coordinate of H (s . k) (not yet
+// divided by sqrt(d)) and gamma = ||k|| > 0, the code #{t_b < x / (sqrt(d) gamma)}
+// is decided by comparing |x| with thr_b = (sqrt(d) t_b) gamma over the positive
+// boundaries: the codebook is symmetric (t_b = -t_{n-2-b}, middle boundary 0),
+// so the code is HALF + #{thr_b < |x|} for x > 0 and HALF - 1 - #{thr_b < |x|}
+// otherwise.  This differs from dividing first only within a few fp32 roundings
+// of a boundary, and from the plain count only at a tie.
+template <int KB>
+struct KeyThresholds {
+    static constexpr int HALF = 1 << (KB - 1);
+    float thr[HALF - 1 > 0 ? HALF - 1 : 1];
+    __device__ __forceinline__ KeyThresholds(const Consts& c, float gamma) {
+#pragma unroll
+        for (int b = 0; b < HALF - 1; ++b) thr[b] = c.boundary_sd[HALF + b] * gamma;
+    }
+    __device__ __forceinline__ int code(float x) const {
+        const float ax = fabsf(x);
+        int n = 0;
+#pragma unroll
+        for (int b = 0; b < HALF - 1; ++b) n += (thr[b] < ax) ? 1 : 0;
+        return (x > 0.f) ? HALF + n : HALF - 1 - n;
+    }
+};
+
 // The 4 sign bits of coordinates 4*lane .. 4*lane+3 (bit i set: s = -1).
 __device__ __forceinline__ uint32_t lane_signs(const Consts& c, int lane) {
     return (c.sign_bits[lane >> 3] >> (4 * (lane & 7))) & 0xFu;

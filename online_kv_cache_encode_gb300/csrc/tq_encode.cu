@@ -155,7 +155,7 @@ __device__ __forceinline__ void pack_codes(const int c[E], uint32_t& lo, uint32_
 }
 
 template <int KB, int VB, int M, int GRP>
-__global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs a) {
+__global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncodeArgs a) {
     constexpr int E = kHeadDim / GRP;   // coordinates per lane
     constexpr int IPW = 32 / GRP;       // items per warp
     extern __shared__ float smem[];
@@ -231,19 +231,12 @@ __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs
         int kc[E];
         float r[E];
         if (gamma > 0.f) {
+            const KeyThresholds<KB> kt(a.c, gamma);
 #pragma unroll
             for (int i = 0; i < E; ++i) {
-                const float u = (k[i] * inv_sqrt_d) / gamma;  // correctly rounded: keeps ties with the codebook rare
-                // The codebook is symmetric (t_b = -t_{NB-1-b}, middle boundary 0), so
-                // code = #{t_b < u} is HALF + #{positive t_b < |u|} for u > 0 and
-                // HALF - 1 - #{positive t_b <= |u|} otherwise; the two differ from the
-                // plain count only at a tie with a boundary.
-                const float au = fabsf(u);
-                int n = 0;
-#pragma unroll
-                for (int b = HALF; b < NB; ++b) n += (a.c.boundary[b] < au) ? 1 : 0;
-                kc[i] = (u > 0.f) ? HALF + n : HALF - 1 - n;
+                kc[i] = kt.code(k[i]);
                 if constexpr (M > 0) {
+                    const float u = (k[i] * inv_sqrt_d) / gamma;
                     float cv = 0.f;
 #pragma unroll
                     for (int b = 0; b <= NB; ++b) cv = (kc[i] == b) ? a.c.centroid[b] : cv;
@@ -344,8 +337,10 @@ __global__ void __launch_bounds__(kEncWarps * 32) encode_kernel(const EncodeArgs
     }
 }
 
+// The grid is at most one wave: the CTAs that fit on every SM at once (from
+// the occupancy calculator, once per kernel) loop over the items.
 template <int KB, int VB, int M, int GRP>
-static int launch_encode_g(const EncodeArgs& a, int64_t blocks, cudaStream_t s) {
+static int launch_encode_g(const EncodeArgs& a, int64_t items, int num_sms, cudaStream_t s) {
     constexpr int IPW = 32 / GRP;
     const size_t smem = (size_t)(M * kSPad + (M > 0 ? kEncWarps * IPW * kRPad : 0)) * sizeof(float);
     auto kern = encode_kernel<KB, VB, M, GRP>;
@@ -354,20 +349,27 @@ static int launch_encode_g(const EncodeArgs& a, int64_t blocks, cudaStream_t s) 
         cudaError_t e = ensure_smem_limit(kern, (int)smem, done);
         if (e != cudaSuccess) return (int)e;
     }
+    static int per_sm = 0;  // same value from any thread that computes it
+    if (per_sm == 0) {
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kEncWarps * 32, smem);
+        if (e != cudaSuccess) return (int)e;
+        per_sm = n > 0 ? n : 1;
+    }
+    const int64_t cap = (int64_t)num_sms * per_sm;
+    int64_t blocks = (items + kEncWarps * IPW - 1) / (kEncWarps * IPW);
+    if (blocks > cap) blocks = cap;
     return (int)launch_programmatic(kern, dim3((unsigned)blocks), dim3(kEncWarps * 32), smem, s, a);
 }
 
 template <int KB, int VB, int M>
 static int launch_encode_t(const EncodeArgs& a, int num_sms, cudaStream_t s) {
     const int64_t items = a.num_tokens * a.g.hkv;
-    const int64_t cap = (int64_t)num_sms * (M > 0 ? 2 : 8);
-    // four items per warp once they fill every SM's warps; one per warp below that
-    if (items >= cap * kEncWarps * 4) {
-        int64_t blocks = (items + kEncWarps * 4 - 1) / (kEncWarps * 4);
-        return launch_encode_g<KB, VB, M, 8>(a, blocks < cap ? blocks : cap, s);
-    }
-    int64_t blocks = (items + kEncWarps - 1) / kEncWarps;
-    return launch_encode_g<KB, VB, M, 32>(a, blocks < cap ? blocks : cap, s);
+    // four items per warp once there are enough to give every warp slot of
+    // the GPU four; one item per warp (lower latency) below that
+    if (items >= (int64_t)num_sms * (M > 0 ? 2 : 8) * kEncWarps * 4)
+        return launch_encode_g<KB, VB, M, 8>(a, items, num_sms, s);
+    return launch_encode_g<KB, VB, M, 32>(a, items, num_sms, s);
 }
 
 int launch_encode(const EncodeArgs& a, int num_sms, void* stream) {

@@ -288,7 +288,10 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
         // the device multiplies the code by (float)alpha; the remainder is taken
         // against exactly that product
         c->c.rem_f16[i] = half_bits_from_double(cb->centroid[i] - (double)c->c.alpha * (i - mid));
-        if (i + 1 < n) c->c.boundary[i] = (float)cb->boundary[i];
+        if (i + 1 < n) {
+            c->c.boundary[i] = (float)cb->boundary[i];
+            c->c.boundary_sd[i] = (float)(cb->boundary[i] * std::sqrt((double)d));
+        }
     }
     tq_codebook_free(cb);
 

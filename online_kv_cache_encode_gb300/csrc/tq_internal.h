@@ -24,6 +24,7 @@ Geometry make_geometry(int d, int kb, int vb, int m, int bs, int hkv, int64_t nu
 // Method constants the kernels take by value.
 struct Consts {
     float boundary[kMaxCodebook];  // key decision boundaries (2^kb - 1 used)
+    float boundary_sd[kMaxCodebook];  // sqrt(d) * boundary, rounded once from double
     float centroid[kMaxCodebook];  // key centroids (fp32), used by the QJL residual
     // Decode splits each centroid as C[c] = alpha * (c - (2^kb - 1)/2) + rem[c]:
     // the linear part goes through the tensor cores on the exact integer code,

@@ -206,7 +206,9 @@ def run_append_case(w, oracle, tq, q_step: int = 0) -> dict:
     tokens, then tq_decode_attention_append appends token lens[b] - 1 and
     attends.  The resulting cache is compared with the oracle's encoding of all
     lens[b] tokens, the output with the oracle's decode, and with the plain GPU
-    decode of the same cache (which must agree bit for bit)."""
+    decode of the same cache (which must agree bit for bit).  The cache must
+    also equal, byte for byte, what tq_encode_kv of the new tokens makes of the
+    cache as it was before the step."""
     import torch
 
     dev = torch.device("cuda")
@@ -238,9 +240,13 @@ def run_append_case(w, oracle, tq, q_step: int = 0) -> dict:
     qt = torch.from_numpy(q).to(dev, tdt).contiguous()
     btt = torch.from_numpy(bt).to(dev)
     lt = torch.from_numpy(lens).to(dev)
+    pool_pre = gc.pool.clone()
     out_a = gc.decode_append(kn, vn, qt, btt, lt, smv, status=status).cpu().numpy().astype(np.float64)
     torch.cuda.synchronize()
     pool_g = gc.pool.cpu().numpy()
+    ge = tq.Cache(nb, w.hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed, w.block_size, w.d, pool=pool_pre)
+    ge.encode(kn, vn, torch.from_numpy(np.array([sl[-1] for sl in slots])).to(dev))
+    same_as_encode = bool(np.array_equal(pool_g, pool_pre.cpu().numpy()))
     st_g = int(status.item())
     out_p = gc.decode(qt, btt, lt, smv).cpu().numpy().astype(np.float64)
 
@@ -256,7 +262,8 @@ def run_append_case(w, oracle, tq, q_step: int = 0) -> dict:
     enc["other_bytes_equal"] = True
     return dict(enc=enc, dec=dict(rel_err=rel_err(out_a, out_o), status_gpu=st_g, status_oracle=st_o | dst_o,
                                   out_gpu=out_a, out_oracle=out_o,
-                                  same_as_plain_decode=bool(np.array_equal(out_a, out_p))), w=w)
+                                  same_as_plain_decode=bool(np.array_equal(out_a, out_p)),
+                                  same_as_encode_call=same_as_encode), w=w)
 
 
 def assert_encode_parity(res: dict):

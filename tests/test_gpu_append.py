@@ -26,6 +26,7 @@ def _check(res):
     assert d["status_gpu"] == d["status_oracle"] == 0, d
     assert d["rel_err"] <= parity.DECODE_RTOL, d["rel_err"]
     assert d["same_as_plain_decode"]
+    assert d["same_as_encode_call"]
 
 
 @pytest.mark.parametrize("kb,vb", [(4, 4), (3, 3), (2, 4), (4, 2)])
