@@ -38,6 +38,9 @@ from online_kv_cache_encode_gb300 import workloads as W  # noqa: E402
 WORKLOAD = "gqa32k"
 METRIC = "compressed-KV decode-attention GB/s (% of HBM peak); KV encode Mtokens/s"
 N_COPIES = 16
+# other key / value widths measured on the same workload shape (the widths a
+# cache may choose per layer); each row: encode and decode-only throughput
+WIDTHS = [(1, 1), (3, 3), (5, 5), (6, 6), (8, 8)]
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -82,7 +85,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("tq_decode.cu", "tq_device.cuh", "tq_internal.h"):
+    for f in ("tq_decode_impl.cuh", "tq_device.cuh", "tq_internal.h"):
         with open(os.path.join(ROOT, "online_kv_cache_encode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -207,6 +210,8 @@ def run_ours(args, rank, world, local):
     enc_ms = e0.elapsed_time(e1) / n_enc
     copies = [base] + [tq.Cache(nb, hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed,
                                 pool=base.pool.clone()) for _ in range(N_COPIES - 1)]
+    q_w = torch.from_numpy(W.queries(w, 0)).to(dev, torch.bfloat16)
+    widths = [] if args.profile or args.no_widths else width_sweep(tq, w, K, V, slots, bt, q_w, measured_peaks()[0])
     del K, V
 
     # ---- per-step inputs: the new token (position T-1) and the query ----
@@ -380,6 +385,7 @@ def run_ours(args, rank, world, local):
             "h2d_bytes_per_step": int(newK.numel() * 2 + newV.numel() * 2 + q.numel() * 2),
             "d2h_bytes_per_step": int(out.numel() * 4),
         },
+        "widths": widths,
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "device_status": st,
@@ -387,6 +393,60 @@ def run_ours(args, rank, world, local):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)
+
+
+def width_sweep(tq, w, K, V, slots, bt, q, peak):
+    """Encode and decode-only throughput of the workload at the other widths in
+    WIDTHS: the same seeded K/V encoded at each width, decodes timed as one CUDA
+    graph over enough distinct cache copies to exceed L2 (about 512 MB)."""
+    import torch
+
+    T, hkv, hq, d = w.lens[0], w.hkv, w.hq, w.d
+    nb = w.num_blocks()
+    lens = torch.tensor([T], dtype=torch.int32, device=K.device)
+    out = torch.empty((1, hq, d), dtype=torch.float32, device=K.device)
+    rows = []
+    for kb, vb in WIDTHS:
+        base = tq.Cache(nb, hkv, kb, vb, 0, w.seed)
+        for _ in range(3):
+            base.encode(K, V, slots)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            base.encode(K, V, slots)
+        e1.record()
+        torch.cuda.synchronize()
+        enc_ms = e0.elapsed_time(e1) / 10
+        bpth = tq.page_bytes(d, kb, vb, 0, w.block_size) // w.block_size
+        dec_bytes = T * hkv * bpth
+        n = max(2, -(-512_000_000 // dec_bytes))
+        caches = [base] + [tq.Cache(nb, hkv, kb, vb, 0, w.seed, pool=base.pool.clone()) for _ in range(n - 1)]
+        wss = [c.new_workspace(1, hq, bt.shape[1]) for c in caches]
+        reps = max(20, n)
+        for i in range(3):
+            caches[i % n].decode(q, bt, lens, out=out, workspace=wss[i % n])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                caches[i % n].decode(q, bt, lens, out=out, workspace=wss[i % n])
+        g.replay()
+        torch.cuda.synchronize()
+        best = 1e9
+        for _ in range(3):
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / reps)
+        gbps = dec_bytes / (best * 1e-3) / 1e9
+        enc_gbps = T * hkv * (2 * d * 2 + bpth) / (enc_ms * 1e-3) / 1e9
+        rows.append({"key_bits": kb, "value_bits": vb, "bytes_per_token_head": bpth,
+                     "decode_GBps": round(gbps, 1), "decode_frac": round(gbps / peak, 4),
+                     "decode_us": round(best * 1e3, 2), "decode_copies": n,
+                     "encode_Mtok_s": round(T / (enc_ms * 1e-3) / 1e6, 1), "encode_frac": round(enc_gbps / peak, 4)})
+        del g, caches, wss, base
+        torch.cuda.empty_cache()
+    return rows
 
 
 # --------------------------------------------------------------------------- oracle (CPU)
@@ -472,6 +532,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-widths", action="store_true", help="skip the other-widths measurements")
     ap.add_argument("--profile", action="store_true",
                     help="only build the caches and launch the decode kernel 6 times (for ncu)")
     args = ap.parse_args()

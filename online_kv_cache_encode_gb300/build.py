@@ -17,7 +17,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtq.so")
-SOURCES = ["tq_host.cpp", "tq_encode.cu", "tq_decode.cu"]
+# (source, extra flags, object name); the kernels of each key width 1 .. 8 are
+# one compilation of tq_inst.cu, so the widths build in parallel
+SOURCES = [("tq_host.cpp", [], "tq_host.o"), ("tq_encode.cu", [], "tq_encode.o"), ("tq_decode.cu", [], "tq_decode.o")]
+SOURCES += [("tq_inst.cu", [f"-DTQ_KB={kb}"], f"tq_inst_k{kb}.o") for kb in range(1, 9)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -52,10 +55,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-I", INCLUDE, "-Xcompiler", "-fPIC,-fvisibility=hidden"]
     procs = []
     objs = []
-    for src in SOURCES:
-        obj = os.path.join(BUILD, src + ".o")
+    for src, flags, name in SOURCES:
+        obj = os.path.join(BUILD, name)
         objs.append(obj)
-        cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc] + common + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))

@@ -92,6 +92,56 @@ struct KeyThresholds {
     }
 };
 
+// Key widths above 4 bits: the same decision by binary search over the
+// positive boundaries (monotone, so it finds the same count as the linear
+// comparison); bsd_pos[b] = sqrt(d) t_{HALF + b}.
+template <int KB>
+__device__ __forceinline__ int key_code_search(float x, float gamma, const float* bsd_pos) {
+    constexpr int HALF = 1 << (KB - 1);
+    const float ax = fabsf(x);
+    int n = 0;
+#pragma unroll
+    for (int step = HALF / 2; step >= 1; step >>= 1)
+        if (bsd_pos[n + step - 1] * gamma < ax) n += step;
+    return (x > 0.f) ? HALF + n : HALF - 1 - n;
+}
+
+// E B-bit codes packed LSB-first into words (code i at bits B i ..).
+template <int B, int E>
+__device__ __forceinline__ void pack_words(const int c[E], uint32_t (&w)[(E * B + 31) / 32]) {
+#pragma unroll
+    for (int k = 0; k < (E * B + 31) / 32; ++k) w[k] = 0u;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        const int pos = B * i, wi = pos >> 5, sh = pos & 31;
+        w[wi] |= (uint32_t)c[i] << sh;
+        if (sh + B > 32) w[wi + 1] |= (uint32_t)c[i] >> (32 - sh);
+    }
+}
+
+// Word `lane` of a row of 128 B-bit codes whose lane l holds the codes of
+// coordinates 4l .. 4l+3 packed LSB-first in p (4B bits), gathered from the
+// lanes that hold its bits.  Every lane of the warp must call it; the row has
+// 4B words, so lanes from 4B on get nothing useful.
+template <int B>
+__device__ __forceinline__ uint32_t row_word(uint32_t p, int lane) {
+    constexpr int LB = 4 * B;
+    constexpr int K = 32 / LB + 2;  // lanes that can hold bits of one word
+    uint32_t word = 0;
+    const int src0 = (lane * 32) / LB;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int src = src0 + k;
+        const uint32_t pv = __shfl_sync(0xffffffffu, p, src < 32 ? src : 31);
+        const int shift = src * LB - lane * 32;
+        if (src < 32) {
+            if (shift >= 0 && shift < 32) word |= pv << shift;
+            else if (shift < 0 && shift > -LB) word |= pv >> (-shift);
+        }
+    }
+    return word;
+}
+
 // The 4 sign bits of coordinates 4*lane .. 4*lane+3 (bit i set: s = -1).
 __device__ __forceinline__ uint32_t lane_signs(const Consts& c, int lane) {
     return (c.sign_bits[lane >> 3] >> (4 * (lane & 7))) & 0xFu;

@@ -257,9 +257,11 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
         return fail(TQ_ERR_INVALID_ARG, "invalid d / bits / qjl_m combination");
     if (d != kHeadDim) return fail(TQ_ERR_UNSUPPORTED, "head dim must be 128");
     if (block_size != kBlockSize) return fail(TQ_ERR_UNSUPPORTED, "block_size must be 16");
-    if (key_bits < 2 || key_bits > 4 || value_bits < 2 || value_bits > 4)
-        return fail(TQ_ERR_UNSUPPORTED, "key_bits and value_bits must be 2, 3 or 4");
+    if (key_bits < 1 || key_bits > 8 || value_bits < 1 || value_bits > 8)
+        return fail(TQ_ERR_UNSUPPORTED, "key_bits and value_bits must be 1 .. 8");
     if (qjl_m != 0 && qjl_m != 128) return fail(TQ_ERR_UNSUPPORTED, "qjl_m must be 0 or 128");
+    if (qjl_m != 0 && (key_bits < 2 || key_bits > 4 || value_bits < 2 || value_bits > 4))
+        return fail(TQ_ERR_UNSUPPORTED, "the QJL sketch is built for 2-, 3- and 4-bit keys and values");
 
     tq_cache* c = new (std::nothrow) tq_cache();
     if (!c) return fail(TQ_ERR_INVALID_ARG, "out of host memory");
@@ -283,14 +285,22 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
     const double alpha = num / den;  // least-squares slope of the centroids in the code
     std::memset(&c->c, 0, sizeof(c->c));
     c->c.alpha = (float)alpha;
+    CodeTables tab;
+    std::memset(&tab, 0, sizeof(tab));
     for (int i = 0; i < n; ++i) {
-        c->c.centroid[i] = (float)cb->centroid[i];
         // the device multiplies the code by (float)alpha; the remainder is taken
         // against exactly that product
-        c->c.rem_f16[i] = half_bits_from_double(cb->centroid[i] - (double)c->c.alpha * (i - mid));
-        if (i + 1 < n) {
-            c->c.boundary[i] = (float)cb->boundary[i];
-            c->c.boundary_sd[i] = (float)(cb->boundary[i] * std::sqrt((double)d));
+        const uint16_t rem = half_bits_from_double(cb->centroid[i] - (double)c->c.alpha * (i - mid));
+        const float bsd = (i + 1 < n) ? (float)(cb->boundary[i] * std::sqrt((double)d)) : 0.f;
+        tab.rem_f16[i] = rem;
+        if (i >= n / 2 && i + 1 < n) tab.boundary_sd_pos[i - n / 2] = bsd;
+        if (n <= kMaxCodebook) {
+            c->c.centroid[i] = (float)cb->centroid[i];
+            c->c.rem_f16[i] = rem;
+            if (i + 1 < n) {
+                c->c.boundary[i] = (float)cb->boundary[i];
+                c->c.boundary_sd[i] = bsd;
+            }
         }
     }
     tq_codebook_free(cb);
@@ -310,6 +320,14 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
         return cuda_fail(e, "cudaDeviceGetAttribute");
     }
 
+    e = cudaMalloc(&c->tab_dev, sizeof(CodeTables));
+    if (e == cudaSuccess) e = cudaMemcpy(c->tab_dev, &tab, sizeof(CodeTables), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        if (c->tab_dev) cudaFree(c->tab_dev);
+        delete c;
+        return cuda_fail(e, "uploading the code tables");
+    }
+
     if (qjl_m > 0) {
         const int64_t cnt = (int64_t)qjl_m * d;
         c->S_host = new (std::nothrow) double[cnt];
@@ -327,6 +345,7 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
         delete[] tmp;
         if (e != cudaSuccess) {
             if (c->S_dev) cudaFree(c->S_dev);
+            cudaFree(c->tab_dev);
             delete[] c->S_host;
             delete c;
             return cuda_fail(e, "uploading the QJL matrix");
@@ -339,6 +358,7 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
 TQ_API void tq_cache_free(tq_cache* c) {
     if (!c) return;
     if (c->S_dev) cudaFree(c->S_dev);
+    if (c->tab_dev) cudaFree(c->tab_dev);
     delete[] c->S_host;
     delete c;
 }
@@ -377,6 +397,7 @@ TQ_API tq_status tq_encode_kv(const tq_cache* c, const void* K, const void* V, t
     a.slot_mapping = slot_mapping;
     a.status = dev_status;
     a.S = c->S_dev;
+    a.tab = c->tab_dev;
     int e = launch_encode(a, c->num_sms, stream);
     if (e != 0) return cuda_fail((cudaError_t)e, "encode launch");
     return TQ_OK;
@@ -456,6 +477,7 @@ static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype,
     a.num_splits = splits;
     a.status = dev_status;
     a.S = c->S_dev;
+    a.tab = c->tab_dev;
     a.knew = knew;
     a.vnew = vnew;
     a.kv_dtype = (int)kv_dtype;

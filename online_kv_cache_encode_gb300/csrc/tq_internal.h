@@ -9,7 +9,8 @@ namespace tq {
 
 constexpr int kHeadDim = 128;   // the one head dimension the kernels are built for
 constexpr int kBlockSize = 16;  // tokens per page
-constexpr int kMaxCodebook = 16;
+constexpr int kMaxCodebook = 16;   // levels held in the by-value constants (widths up to 4 bits)
+constexpr int kMaxLevels = 256;    // levels of the widest codes (8 bits)
 
 // Byte layout of one page (one block of kBlockSize slots of one KV head).
 struct Geometry {
@@ -34,9 +35,17 @@ struct Consts {
     uint32_t sign_bits[kHeadDim / 32];  // bit j set when s_j = -1
 };
 
+// Tables for key codes of any width, in device memory written once when the
+// cache is created (the by-value constants only hold widths up to 4 bits).
+struct CodeTables {
+    float boundary_sd_pos[kMaxLevels / 2];  // sqrt(d) t_{HALF + b}, b = 0 .. HALF - 2 (HALF = 2^(kb-1))
+    uint16_t rem_f16[kMaxLevels];           // rem[c] = C[c] - alpha (c - mid) in binary16
+};
+
 struct EncodeArgs {
     Geometry g;
     Consts c;
+    const CodeTables* tab;
     uint8_t* pool;
     const void* K;
     const void* V;
@@ -50,6 +59,7 @@ struct EncodeArgs {
 struct DecodeArgs {
     Geometry g;
     Consts c;
+    const CodeTables* tab;
     const uint8_t* pool;
     const void* q;
     int dtype;
@@ -72,10 +82,17 @@ struct DecodeArgs {
     int kv_dtype;
 };
 
-// Launchers (return a cudaError_t as int).
+// Launchers (return a cudaError_t as int).  The per-key-width ones are
+// explicitly instantiated, one key width per translation unit.
 int launch_encode(const EncodeArgs& a, int num_sms, void* stream);
 int launch_decode(const DecodeArgs& a, void* stream);
 int decode_smem_bytes(const Geometry& g);
+template <int KB>
+int launch_encode_kb(const EncodeArgs& a, int num_sms, void* stream);
+template <int KB>
+int launch_decode_kb(const DecodeArgs& a, void* stream);
+template <int KB>
+int decode_smem_kb(const Geometry& g);
 
 void set_error(const char* fmt, ...);
 
@@ -95,6 +112,7 @@ struct tq_cache {
     int8_t signs[tq::kHeadDim];
     double* S_host;   // m x d
     float* S_dev;     // m x d, library-owned device memory
+    tq::CodeTables* tab_dev;  // library-owned device memory
     int device;
     int num_sms;
 };

@@ -82,7 +82,10 @@ def test_argument_checks_need_no_gpu(tq):
     fake = ctypes.c_void_p(0x100000)
     assert L.tq_cache_create(fake, 4, 16, 1, 64, 4, 4, 0, 0, ctypes.byref(h)) == tq.TQ_ERR_UNSUPPORTED
     assert L.tq_cache_create(fake, 4, 8, 1, 128, 4, 4, 0, 0, ctypes.byref(h)) == tq.TQ_ERR_UNSUPPORTED
-    assert L.tq_cache_create(fake, 4, 16, 1, 128, 5, 4, 0, 0, ctypes.byref(h)) == tq.TQ_ERR_UNSUPPORTED
+    # widths 1 .. 8 are built; the QJL sketch only for 2- to 4-bit keys and values
+    assert L.tq_cache_create(fake, 4, 16, 1, 128, 5, 4, 128, 0, ctypes.byref(h)) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_cache_create(fake, 4, 16, 1, 128, 4, 1, 128, 0, ctypes.byref(h)) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_cache_create(fake, 4, 16, 1, 128, 9, 4, 0, 0, ctypes.byref(h)) == tq.TQ_ERR_INVALID_ARG
     assert L.tq_cache_create(fake, 4, 16, 1, 128, 4, 4, 64, 0, ctypes.byref(h)) == tq.TQ_ERR_UNSUPPORTED
     assert L.tq_cache_create(fake, 0, 16, 1, 128, 4, 4, 0, 0, ctypes.byref(h)) == tq.TQ_ERR_INVALID_ARG
     assert L.tq_encode_kv(None, None, None, 0, 1, None, None, None) == tq.TQ_ERR_INVALID_ARG
