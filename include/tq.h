@@ -141,8 +141,11 @@ TQ_API int64_t tq_page_bytes(int d, int key_bits, int value_bits, int qjl_m, int
  * draw the signs from a seed [deep dive -- Step 1: RHT] with torch's
  * generator, which is not reproduced.
  * Supported on the GPU path: d = 128, block_size = 16, key_bits and
- * value_bits in {2, 3, 4}, qjl_m in {0, 128}; anything else returns
- * TQ_ERR_UNSUPPORTED.  Uses the current CUDA device. */
+ * value_bits each 1..8 (chosen per cache, e.g. per layer [deep dive --
+ * per-layer bit allocation]), qjl_m in {0, 128} with the QJL sketch only for
+ * key and value bits 2..4; anything else returns TQ_ERR_UNSUPPORTED.  The
+ * library allocates a small device table (codebook remainders and
+ * boundaries) per cache.  Uses the current CUDA device. */
 TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size, int num_kv_heads,
                                  int d, int key_bits, int value_bits, int qjl_m, uint64_t seed,
                                  tq_cache** out);
@@ -236,6 +239,30 @@ TQ_API tq_status tq_decode_attention_append(const tq_cache* cache, const void* k
                                             int max_blocks_per_seq, const int32_t* lens, float sm_scale,
                                             float* out, void* workspace, size_t workspace_bytes,
                                             int32_t* dev_status, void* stream);
+
+/* The same decode step over a sliding window kept as a ring buffer: each
+ * sequence owns `window` slots (window / block_size blocks of its block table,
+ * window a positive multiple of block_size, at most max_blocks_per_seq *
+ * block_size) and token t lives in slot t mod window, so the ring always holds
+ * the last `window` tokens [Bit-Axon -- KV cache memory model: a sliding-
+ * window layer keeps the K and V of W tokens].  lens[b] counts all of sequence b's tokens, the new one
+ * included: the new token is encoded into slot (lens[b] - 1) mod window,
+ * replacing the token that leaves the window, and the query attends over the
+ * min(lens[b], window) tokens the ring holds (attention does not depend on
+ * their order).  To fill a ring, encode only the last `window` tokens, each
+ * at slot block_table[b][(t mod window) / block_size] * block_size + t mod
+ * block_size; tokens of one tq_encode_kv call that map to one slot race.
+ * A plain tq_decode_attention over a ring is the same attention with
+ * lens[b] replaced by min(lens[b], window).  Returns TQ_ERR_INVALID_ARG for a
+ * window that is not a positive multiple of block_size or does not fit the
+ * block table; other arguments and results are those of
+ * tq_decode_attention_append. */
+TQ_API tq_status tq_decode_attention_ring_append(const tq_cache* cache, const void* k_new, const void* v_new,
+                                                 tq_dtype kv_dtype, const void* q, tq_dtype dtype, int batch,
+                                                 int num_q_heads, const int32_t* block_table,
+                                                 int max_blocks_per_seq, const int32_t* lens, int window,
+                                                 float sm_scale, float* out, void* workspace,
+                                                 size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /* Bytes of the fixed decode workspace built into the library (see below). */
 #define TQ_NOALLOC_WORKSPACE_BYTES (4u << 20)

@@ -208,7 +208,7 @@ __host__ __device__ constexpr Layout decode_layout() {
     L.sq = off; off += M ? 8 * kQStride * 4 : 0;
     L.qoff = off; off += 8 * 4;
     L.qscale = off; off += 8 * 4;
-    L.rem = off; off += 16 * 2;
+    L.rem = off; off += 3 * 16 * 2;  // rem | N | rem2 (4-bit keys) in binary16
     L.stage = off; off += kStageBytes;  // appended token (see kStage*)
     L.bars = off; off += 8 * NW * kMaxSlotsPerWarp;
     L.ok = off; off += 4 * NW * kMaxSlotsPerWarp;
@@ -268,36 +268,30 @@ __device__ __forceinline__ void key_words(uint32_t addr, uint32_t (&w)[KB]) {
 // two codes of the lane's 32-dim chunk: element h (0 low, 1 high) is chunk dim
 // key_dim<KB>(n, h), scaled by 2^-key_exp<KB>(n).  MMA k-step ks uses X[2ks]
 // (k = 2qd, 2qd+1) and X[2ks+1] (k = 8+2qd, 8+2qd+1).
+//
+// 4-bit keys instead take the centroid's integer part N[c] (C[c] = delta N[c]
+// + rem2[c], |N| <= 2047, exact in fp16 at unit scale) from the lookup table
+// together with rem2, for the code pair of one code byte: X[n] holds chunk
+// dims (2n, 2n+1) (key_lut4 below).
 template <int KB>
 __host__ __device__ constexpr int key_dim(int n, int h) {
-    return KB == 4 ? 8 * (n >> 2) + (n & 3) + 4 * h : KB == 2 ? 16 * (n >> 3) + (n & 7) + 8 * h : 2 * n + h;
+    return KB == 2 ? 16 * (n >> 3) + (n & 7) + 8 * h : 2 * n + h;
 }
 template <int KB>
 __host__ __device__ constexpr int key_exp(int n) {
-    return KB == 4 ? ((n & 1) ? 20 : 24) : KB == 2 ? 24 - 2 * (n & 3) : 24;
+    return KB == 2 ? 24 - 2 * (n & 3) : 24;
 }
-// inverse of key_dim: the register holding chunk dim c (its half is key_half)
+// Scale of the integer part's MMA result: 2^24 undoes the subnormal code
+// operands, 4-bit integer parts are unit-scale fp16.
 template <int KB>
-__host__ __device__ constexpr int key_reg(int c) {
-    return KB == 4 ? 4 * (c >> 3) + (c & 3) : KB == 2 ? 8 * (c >> 4) + (c & 7) : c >> 1;
-}
-template <int KB>
-__host__ __device__ constexpr int key_half(int c) {
-    return KB == 4 ? (c >> 2) & 1 : KB == 2 ? (c >> 3) & 1 : c & 1;
+__host__ __device__ constexpr float key_int_scale() {
+    return KB == 4 ? 1.f : 16777216.f;
 }
 
 template <int KB>
 __device__ __forceinline__ void key_halves(const uint32_t (&w)[KB], uint32_t X[16]) {
-    if constexpr (KB == 4) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t y = w[i] >> 8;
-            X[4 * i + 0] = w[i] & 0x000F000Fu;
-            X[4 * i + 1] = w[i] & 0x00F000F0u;
-            X[4 * i + 2] = y & 0x000F000Fu;
-            X[4 * i + 3] = y & 0x00F000F0u;
-        }
-    } else if constexpr (KB == 2) {
+    static_assert(KB != 4, "4-bit keys take their operands from key_lut4");
+    if constexpr (KB == 2) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const uint32_t y = w[i] >> 8;
@@ -328,10 +322,8 @@ __device__ __forceinline__ void key_halves(const uint32_t (&w)[KB], uint32_t X[1
 // one byte permute.
 template <int KB>
 __device__ __forceinline__ void key_rem(const uint32_t (&w)[KB], uint32_t lw, uint32_t R[16]) {
-    if constexpr (KB == 4) {
-#pragma unroll
-        for (int n = 0; n < 16; ++n) R[n] = lds32(prmt(w[n >> 2], lw, 0x7604u | ((uint32_t)(n & 3) << 4)));
-    } else if constexpr (KB == 2) {
+    static_assert(KB != 4, "4-bit keys take their operands from key_lut4");
+    if constexpr (KB == 2) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint2 v = lds64(prmt(w[j >> 2], lw, 0x7604u | ((uint32_t)(j & 3) << 4)));
@@ -361,6 +353,14 @@ __device__ __forceinline__ void key_rem(const uint32_t (&w)[KB], uint32_t lw, ui
 #pragma unroll
         for (int n = 0; n < 16; ++n) R[n] = lds32(lw | (bits_at<KB>(w, 2 * KB * n, 2 * KB) << 7));
     }
+}
+
+// 4-bit keys: both operands of code byte n of the lane's chunk (codes 2n, 2n+1)
+// with one 8-byte load: (N[c0], N[c1]) and (rem2[c0], rem2[c1]) in fp16.  The
+// table has 256-byte entries (8 bytes per lane), so the code byte is the
+// address's bits 8..15, put there with one byte permute.
+__device__ __forceinline__ uint2 key_lut4(const uint32_t (&w)[4], uint32_t lw, int n) {
+    return lds64(prmt(w[n >> 2], lw, 0x7604u | ((uint32_t)(n & 3) << 4)));
 }
 
 // Value codes of dims 16r .. 16r+15 for a token pair (ta, tb): P[i] holds the
@@ -625,10 +625,12 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     }
     uint16_t* rem = reinterpret_cast<uint16_t*>(sm + LY.rem);
     if (tid < 16) rem[tid] = a.c.rem_f16[tid];
+    else if (tid < 32) rem[tid] = a.c.cint_f16[tid - 16];
+    else if (tid < 48) rem[tid] = a.c.crem_f16[tid - 32];
     __syncthreads();
     // Lane-private remainder table at shared address kLutAddr (copy for
     // lane l at entry*stride + l*width):
-    //   4-bit keys: byte e (2 codes) -> (rem[e&15], rem[e>>4])              stride 256, 4 B
+    //   4-bit keys: byte e (2 codes) -> (N[e&15], N[e>>4]), (rem2[e&15], rem2[e>>4])  stride 256, 8 B
     //   2-bit keys: byte e (4 codes) -> (rem[c0], rem[c1]), (rem[c2], rem[c3]) stride 256, 8 B
     //   3-bit keys: 6 bits e (2 codes) -> (rem[e&7], rem[e>>3])              stride 128, 4 B
     //   1-bit keys: 2 bits e (2 codes) -> (rem[e&1], rem[e>>1])              stride 128, 4 B
@@ -639,10 +641,13 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     auto build_lut = [&](const uint16_t* rsrc) {
         uint8_t* lut = sm + lut_off;
         if constexpr (KB == 4) {
-            for (int i = tid; i < 256 * 8; i += NT) {   // entry e, lanes 4k..4k+3
-                const int e = i >> 3, k = i & 7;
-                const uint32_t v = (uint32_t)rsrc[e & 15] | ((uint32_t)rsrc[e >> 4] << 16);
-                *reinterpret_cast<uint4*>(lut + e * 256 + 16 * k) = make_uint4(v, v, v, v);
+            const uint16_t* ni = rsrc + 16;  // N, then rem2
+            const uint16_t* r2 = rsrc + 32;
+            for (int i = tid; i < 256 * 16; i += NT) {  // entry e, lanes 2k, 2k+1
+                const int e = i >> 4, k = i & 15;
+                const uint32_t xx = (uint32_t)ni[e & 15] | ((uint32_t)ni[e >> 4] << 16);
+                const uint32_t yy = (uint32_t)r2[e & 15] | ((uint32_t)r2[e >> 4] << 16);
+                *reinterpret_cast<uint4*>(lut + e * 256 + 16 * k) = make_uint4(xx, yy, xx, yy);
             }
         } else if constexpr (KB == 2) {
             for (int i = tid; i < 256 * 16; i += NT) {  // entry e, lanes 2k, 2k+1
@@ -695,11 +700,19 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     if (warp < G) load4(a.q, a.dtype, ((int64_t)b * a.hq + (int64_t)h * G + warp) * D + 4 * lane, x);
 
     // ---- sequence range of this split ----
+    // len counts the sequence's tokens (the appended one included).  A ring of
+    // `window` slots holds the last `window` of them, token t in slot t mod
+    // window; attention runs over the slots that hold tokens, in any order.
+    if (len < 0) len = 0;
+    int pos_new = len - 1;  // slot of the appended token
+    if (a.window > 0) {
+        if (len > 0) pos_new = (len - 1) % a.window;
+        if (len > a.window) len = a.window;
+    }
     if (len > a.max_blocks * g.bs) {
         if (tid == 0) flag(a.status, TQ_FLAG_BAD_SLOT);
         len = a.max_blocks * g.bs;
     }
-    if (len < 0) len = 0;
     const int seq_pages = (len + g.bs - 1) / g.bs;
     int npages = seq_pages - p0;
     if (npages > a.pages_per_split) npages = a.pages_per_split;
@@ -721,24 +734,25 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             mbar_arrive(bar);
         }
     };
-    // The appended token (position len - 1) lies in the sequence's last page,
-    // the split's last page pi = npages - 1.  The warp that owns that page
-    // patches the token into its shared-memory copy when it gets there.  The
-    // encoding is done right after the query is prepared by warp npages % NW
-    // when that warp has one page fewer than the owner (by the owner itself
-    // otherwise) and handed over through the stage barrier.  Its inputs are
-    // requested now, ahead of the page copies, and waited on only when used.
+    // The appended token lies in page pos_new / 16 of the sequence (without a
+    // ring: its last page, the split's last page pi = npages - 1).  The warp
+    // that owns that page patches the token into its shared-memory copy when
+    // it gets there.  When the owner is one of the warps with an extra page,
+    // the encoding is done by warp npages % NW (one page fewer), otherwise by
+    // the owner, right after the query is prepared, and handed over through
+    // the stage barrier.  Its inputs are requested now, ahead of the page
+    // copies, and waited on only when used.
     int jnew = -1;        // owner: its index of the page that takes the token
     bool enc = false;     // this warp encodes the token
     int blknew = -1;
-    const int offnew = (len - 1) & (kBlockSize - 1);
+    const int offnew = pos_new & (kBlockSize - 1);
     uint32_t kraw[4] = {0u, 0u, 0u, 0u}, vraw[4] = {0u, 0u, 0u, 0u};
     if constexpr (M == 0) {
         if (a.knew != nullptr && len > 0) {
-            const int pi = (len - 1) / kBlockSize - p0;
+            const int pi = pos_new / kBlockSize - p0;
             if (pi >= 0 && pi < npages) {
                 const int owner = pi % NW, rest = npages % NW;
-                const int encoder = (rest != 0 && pi == npages - 1) ? rest : owner;
+                const int encoder = (rest != 0 && owner < rest) ? rest : owner;
                 if (warp == owner) jnew = pi / NW;
                 if (warp == encoder) {
                     enc = true;
@@ -773,10 +787,11 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             for (int i = 0; i < 4; ++i) qrot[warp * kQStride + 4 * lane + i] = x[i];
             const float sq = warp_sum(x[0] + x[1] + x[2] + x[3]);
             const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
-            const float big = fabsf(a.c.alpha) * ksc * mx;
+            const float slope = (KB == 4) ? a.c.delta : a.c.alpha;  // scale of the integer part
+            const float big = fabsf(slope) * ksc * mx;
             const float scl = (big > 0.f) ? exp2f(ceilf(log2f(big / 512.f))) : 1.f;
             if (lane == 0) {
-                qoff[warp] = ksc * a.c.alpha * (float)((1 << KB) - 1) * 0.5f * sq;
+                qoff[warp] = (KB == 4) ? 0.f : ksc * a.c.alpha * (float)((1 << KB) - 1) * 0.5f * sq;
                 qscale[warp] = scl;
             }
         }
@@ -826,7 +841,7 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 const float* qr = qrot + gq * kQStride + ch;
                 uint32_t wv[4];
                 if (v < 8) {
-                    const float xs = ksc * a.c.alpha / qscale[gq];
+                    const float xs = ksc * ((KB == 4) ? a.c.delta : a.c.alpha) / qscale[gq];
 #pragma unroll
                     for (int sl = 0; sl < 2; ++sl) {
                         const int n = 2 * v + sl;
@@ -893,9 +908,9 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             }
         }
         const float off0 = qoff[2 * qd], off1 = qoff[2 * qd + 1];
-        const float qs0 = qscale[2 * qd] * 16777216.f, qs1 = qscale[2 * qd + 1] * 16777216.f;  // 2^24 qscale
+        const float qs0 = qscale[2 * qd] * key_int_scale<KB>(), qs1 = qscale[2 * qd + 1] * key_int_scale<KB>();
         const float cq = 1.2533141373155003f / (float)(M > 0 ? M : 1);  // sqrt(pi/2) / m
-        const uint32_t lw = kLutAddr | ((uint32_t)lane << (KB == 2 ? 3 : 2));
+        const uint32_t lw = kLutAddr | ((uint32_t)lane << ((KB == 2 || KB == 4) ? 3 : 2));
         // Score row r holds token tr = r ^ ((r >> 1) & 1) (and row r + 8 token tr + 8):
         // tokens 2 and 3, 6 and 7 trade rows, so that the value loads below (tokens
         // of rows 2qd, 2qd+1 for qd = 0..3) alternate between the two halves of the
@@ -938,6 +953,25 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             key_words<KB>(pg + koff, wa);
             key_words<KB>(pg + koff + 8 * KROW, wb);
             float I0[4], I1[4], R0[4], R1[4];
+            if constexpr (KB == 4) {
+                // per k-step: the operands of code bytes 2ks, 2ks+1 of both tokens,
+                // then the integer part (hi and lo query) and the remainder
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint2 a0 = key_lut4(wa, lw, 2 * ks), b0 = key_lut4(wb, lw, 2 * ks);
+                    const uint2 a1 = key_lut4(wa, lw, 2 * ks + 1), b1 = key_lut4(wb, lw, 2 * ks + 1);
+                    float* I = (ks & 1) ? I1 : I0;
+                    float* Rr = (ks & 1) ? R1 : R0;
+                    if (ks < 2) {
+                        mma16816_c(I, a0.x, b0.x, a1.x, b1.x, QI[ks][0], QI[ks][1], 0.f, 0.f, 0.f, 0.f);
+                        mma16816_c(Rr, a0.y, b0.y, a1.y, b1.y, QB[2 * ks], QB[2 * ks + 1], 0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        mma16816(I, a0.x, b0.x, a1.x, b1.x, QI[ks][0], QI[ks][1]);
+                        mma16816(Rr, a0.y, b0.y, a1.y, b1.y, QB[2 * ks], QB[2 * ks + 1]);
+                    }
+                    mma16816(I, a0.x, b0.x, a1.x, b1.x, QI[ks][2], QI[ks][3]);
+                }
+            } else {
             {
                 uint32_t Xa[16], Xb[16];
                 key_halves<KB>(wa, Xa);
@@ -964,6 +998,7 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                     const int n = 2 * ks;
                     mma16816((ks & 1) ? R1 : R0, Ra[n], Rb[n], Ra[n + 1], Rb[n + 1], QB[n], QB[n + 1]);
                 }
+            }
             }
             float t0 = fmaf(qs0, I0[0] + I1[0], R0[0] + R1[0]), t1 = fmaf(qs1, I0[1] + I1[1], R0[1] + R1[1]);
             float t2 = fmaf(qs0, I0[2] + I1[2], R0[2] + R1[2]), t3 = fmaf(qs1, I0[3] + I1[3], R0[3] + R1[3]);

@@ -303,6 +303,21 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
             }
         }
     }
+    if (n == 16) {
+        // two-level split of the 4-bit centroids: N[c] = round(C[c] / delta)
+        // with delta = max|C| / 2047, the remainder taken against the fp32 delta
+        double cmax = 0.0;
+        for (int i = 0; i < n; ++i) cmax = std::fmax(cmax, std::fabs(cb->centroid[i]));
+        const float fd = (float)(cmax / 2047.0);
+        c->c.delta = fd;
+        for (int i = 0; i < n; ++i) {
+            double nq = std::nearbyint(cb->centroid[i] / (double)fd);
+            if (nq > 2047.0) nq = 2047.0;
+            if (nq < -2047.0) nq = -2047.0;
+            c->c.cint_f16[i] = half_bits_from_double(nq);
+            c->c.crem_f16[i] = half_bits_from_double(cb->centroid[i] - (double)fd * nq);
+        }
+    }
     tq_codebook_free(cb);
 
     derive_signs(seed, d, c->signs);
@@ -403,14 +418,34 @@ TQ_API tq_status tq_encode_kv(const tq_cache* c, const void* K, const void* V, t
     return TQ_OK;
 }
 
+// Splits per (sequence, KV head).  The decode kernel keeps one CTA per SM, so
+// a launch runs in waves of num_sms CTAs.  The split count minimises a simple
+// time model: waves x (page rounds of one CTA x 1.2 us + 6 us), a page round
+// being one page per warp (12 warps, 8 with QJL).  The constants are the
+// measured per-page and fixed (prologue, merge) costs on the 32K GQA
+// workload: 9 rounds in ~10.9 us plus ~6 us.  At most ceil(max_blocks / 8)
+// splits (8 pages or more each) and four times the count that fills the SMs.
 static void decode_split_plan(const tq_cache* c, int batch, int max_blocks, int* splits, int* pps) {
-    const int units = batch * c->g.hkv;
-    const int min_pages = 8;
-    int want = (c->num_sms + units - 1) / units;
-    int cap = (max_blocks + min_pages - 1) / min_pages;
-    int s = want < cap ? want : cap;
-    if (s < 1) s = 1;
-    int p = (max_blocks + s - 1) / s;
+    const int64_t units = (int64_t)batch * c->g.hkv;
+    const int nw = c->g.m ? 8 : 12;
+    const int64_t sms = c->num_sms > 0 ? c->num_sms : 1;
+    int64_t lim = 4 * ((sms + units - 1) / units);
+    const int64_t cap = (max_blocks + 7) / 8;
+    if (lim > cap) lim = cap;
+    if (lim < 1) lim = 1;
+    int best_s = 1;
+    double best = 1e300;
+    for (int64_t s = 1; s <= lim; ++s) {
+        const int64_t p = (max_blocks + s - 1) / s;
+        const int64_t se = (max_blocks + p - 1) / p;
+        const int64_t waves = (units * se + sms - 1) / sms;
+        const double cost = (double)waves * ((double)((p + nw - 1) / nw) * 1.2 + 6.0);
+        if (cost < best) {
+            best = cost;
+            best_s = (int)s;
+        }
+    }
+    int p = (max_blocks + best_s - 1) / best_s;
     if (p < 1) p = 1;
     *pps = p;
     *splits = (max_blocks + p - 1) / p;
@@ -433,7 +468,7 @@ static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype,
                                const int32_t* block_table, int max_blocks_per_seq, const int32_t* lens,
                                float sm_scale, float* out, void* workspace, size_t workspace_bytes,
                                int32_t* dev_status, void* stream, const void* knew, const void* vnew,
-                               tq_dtype kv_dtype) {
+                               tq_dtype kv_dtype, int window) {
     if (!c) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
     if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0)
         return fail(TQ_ERR_INVALID_ARG, "bad batch / num_q_heads / max_blocks_per_seq");
@@ -481,6 +516,7 @@ static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype,
     a.knew = knew;
     a.vnew = vnew;
     a.kv_dtype = (int)kv_dtype;
+    a.window = window;
     int e = launch_decode(a, stream);
     if (e != 0) return cuda_fail((cudaError_t)e, "decode launch");
     return TQ_OK;
@@ -492,15 +528,14 @@ TQ_API tq_status tq_decode_attention(const tq_cache* c, const void* q, tq_dtype 
                                      float* out, void* workspace, size_t workspace_bytes,
                                      int32_t* dev_status, void* stream) {
     return decode_common(c, q, dtype, batch, num_q_heads, block_table, max_blocks_per_seq, lens, sm_scale, out,
-                         workspace, workspace_bytes, dev_status, stream, nullptr, nullptr, TQ_BF16);
+                         workspace, workspace_bytes, dev_status, stream, nullptr, nullptr, TQ_BF16, 0);
 }
 
-TQ_API tq_status tq_decode_attention_append(const tq_cache* c, const void* k_new, const void* v_new,
-                                            tq_dtype kv_dtype, const void* q, tq_dtype dtype, int batch,
-                                            int num_q_heads, const int32_t* block_table,
-                                            int max_blocks_per_seq, const int32_t* lens, float sm_scale,
-                                            float* out, void* workspace, size_t workspace_bytes,
-                                            int32_t* dev_status, void* stream) {
+static tq_status append_common(const tq_cache* c, const void* k_new, const void* v_new, tq_dtype kv_dtype,
+                               const void* q, tq_dtype dtype, int batch, int num_q_heads,
+                               const int32_t* block_table, int max_blocks_per_seq, const int32_t* lens, int window,
+                               float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream) {
     if (!c) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
     if (c->g.m > 0)
         return fail(TQ_ERR_UNSUPPORTED, "appending inside decode is built for caches without QJL; "
@@ -510,7 +545,31 @@ TQ_API tq_status tq_decode_attention_append(const tq_cache* c, const void* k_new
     if ((reinterpret_cast<uintptr_t>(k_new) % 16) || (reinterpret_cast<uintptr_t>(v_new) % 16))
         return fail(TQ_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
     return decode_common(c, q, dtype, batch, num_q_heads, block_table, max_blocks_per_seq, lens, sm_scale, out,
-                         workspace, workspace_bytes, dev_status, stream, k_new, v_new, kv_dtype);
+                         workspace, workspace_bytes, dev_status, stream, k_new, v_new, kv_dtype, window);
+}
+
+TQ_API tq_status tq_decode_attention_append(const tq_cache* c, const void* k_new, const void* v_new,
+                                            tq_dtype kv_dtype, const void* q, tq_dtype dtype, int batch,
+                                            int num_q_heads, const int32_t* block_table,
+                                            int max_blocks_per_seq, const int32_t* lens, float sm_scale,
+                                            float* out, void* workspace, size_t workspace_bytes,
+                                            int32_t* dev_status, void* stream) {
+    return append_common(c, k_new, v_new, kv_dtype, q, dtype, batch, num_q_heads, block_table, max_blocks_per_seq,
+                         lens, 0, sm_scale, out, workspace, workspace_bytes, dev_status, stream);
+}
+
+TQ_API tq_status tq_decode_attention_ring_append(const tq_cache* c, const void* k_new, const void* v_new,
+                                                 tq_dtype kv_dtype, const void* q, tq_dtype dtype, int batch,
+                                                 int num_q_heads, const int32_t* block_table,
+                                                 int max_blocks_per_seq, const int32_t* lens, int window,
+                                                 float sm_scale, float* out, void* workspace,
+                                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (window <= 0 || window % kBlockSize)
+        return fail(TQ_ERR_INVALID_ARG, "window must be a positive multiple of the block size (16)");
+    if (max_blocks_per_seq <= 0 || (int64_t)window > (int64_t)max_blocks_per_seq * kBlockSize)
+        return fail(TQ_ERR_INVALID_ARG, "the block table holds fewer than window slots per sequence");
+    return append_common(c, k_new, v_new, kv_dtype, q, dtype, batch, num_q_heads, block_table, max_blocks_per_seq,
+                         lens, window, sm_scale, out, workspace, workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

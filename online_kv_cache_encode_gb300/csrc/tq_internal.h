@@ -32,6 +32,12 @@ struct Consts {
     // rem[c] (binary16 bits) is looked up.
     float alpha;
     uint16_t rem_f16[kMaxCodebook];
+    // 4-bit keys use a finer two-level split instead: C[c] = delta * N[c] +
+    // rem2[c] with N[c] an integer of magnitude <= 2047 (exact in binary16)
+    // and |rem2[c]| <= delta / 2, both looked up per code pair.
+    float delta;
+    uint16_t cint_f16[kMaxCodebook];   // N[c] in binary16
+    uint16_t crem_f16[kMaxCodebook];   // rem2[c] in binary16
     uint32_t sign_bits[kHeadDim / 32];  // bit j set when s_j = -1
 };
 
@@ -80,6 +86,9 @@ struct DecodeArgs {
     const void* knew;     // [batch, hkv, d]
     const void* vnew;
     int kv_dtype;
+    // ring of `window` slots per sequence (0: no ring): the appended token goes
+    // to slot (lens[b] - 1) mod window, attention runs over min(lens[b], window) slots
+    int window;
 };
 
 // Launchers (return a cudaError_t as int).  The per-key-width ones are

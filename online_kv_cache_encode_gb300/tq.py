@@ -40,6 +40,8 @@ SIGNATURES = {
     "tq_decode_attention": (_I, [_P, _P, _I, _I, _I, _P, _I, _P, _F, _P, _P, _SZ, _P, _P]),
     "tq_decode_attention_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _I, _P, _F, _P, _P, _P]),
     "tq_decode_attention_append": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _F, _P, _P, _SZ, _P, _P]),
+    "tq_decode_attention_ring_append": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _I, _F, _P, _P, _SZ, _P,
+                                             _P]),
     "tq_status_string": (ctypes.c_char_p, [_I]),
     "tq_last_error": (ctypes.c_char_p, []),
 }
@@ -92,6 +94,13 @@ def _stream() -> int:
 def _ptr(t):
     # a plain int: the c_void_p argtypes convert it
     return None if t is None else t.data_ptr()
+
+
+def ring_slots(block_row, positions, window: int, block_size: int = 16):
+    """Slots of token positions in a sequence's ring of `window` slots (its
+    block-table row block_row): position t lives in slot t % window."""
+    r = positions % window
+    return block_row[r // block_size] * block_size + r % block_size
 
 
 def page_bytes(d: int, key_bits: int, value_bits: int, qjl_m: int = 0, block_size: int = 16) -> int:
@@ -214,9 +223,13 @@ class Cache:
 
     def decode_append(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
                       lens: torch.Tensor, sm_scale: float | None = None, out: torch.Tensor | None = None,
-                      workspace: torch.Tensor | None = None, status: torch.Tensor | None = None) -> torch.Tensor:
+                      workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                      window: int | None = None) -> torch.Tensor:
         """One decode step: append the new token of every sequence (k_new, v_new:
-        [B, num_kv_heads, d], position lens[b] - 1) and attend over lens[b] tokens."""
+        [B, num_kv_heads, d], position lens[b] - 1) and attend over lens[b] tokens.
+        With `window`, each sequence's blocks form a ring of `window` slots: the
+        token goes to slot (lens[b] - 1) % window and the query attends over the
+        min(lens[b], window) tokens the ring holds."""
         assert k_new.is_cuda and k_new.shape == v_new.shape and k_new.dtype == v_new.dtype
         assert k_new.dim() == 3 and k_new.shape[1] == self.hkv and k_new.shape[2] == self.d
         assert k_new.is_contiguous() and v_new.is_contiguous()
@@ -235,10 +248,17 @@ class Cache:
             if self._ws is None or self._ws[0] != key:
                 self._ws = (key, self.new_workspace(B, hq, mb))
             workspace = self._ws[1]
-        _check(lib().tq_decode_attention_append(self._h, _ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(q),
-                                                _dtype_code(q), B, hq, _ptr(block_table), mb, _ptr(lens),
-                                                float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
-                                                _ptr(status), _stream()))
+        if window is None:
+            _check(lib().tq_decode_attention_append(self._h, _ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(q),
+                                                    _dtype_code(q), B, hq, _ptr(block_table), mb, _ptr(lens),
+                                                    float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                                    _ptr(status), _stream()))
+        else:
+            _check(lib().tq_decode_attention_ring_append(self._h, _ptr(k_new), _ptr(v_new), _dtype_code(k_new),
+                                                         _ptr(q), _dtype_code(q), B, hq, _ptr(block_table), mb,
+                                                         _ptr(lens), int(window), float(sm_scale), _ptr(out),
+                                                         _ptr(workspace), workspace.numel(), _ptr(status),
+                                                         _stream()))
         return out
 
     def decode_noalloc(self, q: torch.Tensor, block_table: torch.Tensor, lens: torch.Tensor,

@@ -181,6 +181,14 @@ def slots(w: Workload, bt: np.ndarray, seq: int, t0: int, t1: int) -> np.ndarray
     return bt[seq, t // w.block_size].astype(np.int64) * w.block_size + t % w.block_size
 
 
+def ring_slots(w: Workload, bt: np.ndarray, seq: int, t0: int, t1: int, window: int) -> np.ndarray:
+    """Physical slots of tokens [t0, t1) of a sequence kept in a ring of `window`
+    slots (the first window / block_size blocks of its block-table row): token t
+    lives in slot t mod window."""
+    r = np.arange(t0, t1) % window
+    return bt[seq, r // w.block_size].astype(np.int64) * w.block_size + r % w.block_size
+
+
 def scaled(w: Workload, **changes) -> Workload:
     """The same workload with some fields changed (smaller parity cases)."""
     return dataclasses.replace(w, **changes)

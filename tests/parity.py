@@ -228,7 +228,10 @@ def run_append_case(w, oracle, tq, q_step: int = 0) -> dict:
     lens[b] tokens, the output with the oracle's decode, and with the plain GPU
     decode of the same cache (which must agree bit for bit).  The cache must
     also equal, byte for byte, what tq_encode_kv of the new tokens makes of the
-    cache as it was before the step."""
+    cache as it was before the step.  Decode parity (c) is taken on identical
+    caches: the GPU decodes the oracle's cache and is compared with the
+    oracle's decode (a code within rounding of a boundary may legitimately
+    differ between the two encodings and move a logit)."""
     import torch
 
     dev = torch.device("cuda")
@@ -269,6 +272,9 @@ def run_append_case(w, oracle, tq, q_step: int = 0) -> dict:
     same_as_encode = bool(np.array_equal(pool_g, pool_pre.cpu().numpy()))
     st_g = int(status.item())
     out_p = gc.decode(qt, btt, lt, smv).cpu().numpy().astype(np.float64)
+    go = tq.Cache(nb, w.hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed, w.block_size, w.d,
+                  pool=torch.from_numpy(pool_o).to(dev))
+    out_go = go.decode(qt, btt, lt, smv).cpu().numpy().astype(np.float64)
 
     L = Layout(w.d, w.key_bits, w.value_bits, w.qjl_m, w.block_size, w.hkv, oc.page_bytes)
     all_slots = np.repeat(np.concatenate(slots), w.hkv)
@@ -280,8 +286,8 @@ def run_append_case(w, oracle, tq, q_step: int = 0) -> dict:
     enc = compare_encode(fo, fg, kin, vin, oc, oracle)
     enc["status_oracle"], enc["status_gpu"] = st_o | dst_o, st_g
     enc["other_bytes_equal"] = True
-    return dict(enc=enc, dec=dict(rel_err=rel_err(out_a, out_o), status_gpu=st_g, status_oracle=st_o | dst_o,
-                                  out_gpu=out_a, out_oracle=out_o,
+    return dict(enc=enc, dec=dict(rel_err=rel_err(out_go, out_o), status_gpu=st_g, status_oracle=st_o | dst_o,
+                                  out_gpu=out_go, out_oracle=out_o, rel_err_own_cache=rel_err(out_a, out_o),
                                   same_as_plain_decode=bool(np.array_equal(out_a, out_p)),
                                   same_as_encode_call=same_as_encode), w=w)
 
@@ -304,3 +310,90 @@ def assert_decode_parity(res: dict):
     assert d["status_gpu"] == d["status_oracle"] == 0, d
     assert np.all(np.isfinite(d["out_gpu"]))
     assert d["rel_err"] <= DECODE_RTOL, d["rel_err"]
+
+
+def run_ring_stream(w, oracle, tq, window: int, t0s, steps: int, checks) -> list:
+    """Sliding-window decode through rings of `window` slots per sequence.
+
+    Both sides encode the last `window` of each sequence's first t0s[b] tokens
+    into its ring (token t in slot t mod window).  Then, for `steps` steps, the
+    GPU runs one tq_decode_attention_ring_append launch per step: it appends
+    token t0s[b] + i and attends.  The oracle encodes the same token into the
+    same slot and decodes over the min(len, window) slots the ring holds.  At
+    the steps in `checks`, the ring contents are compared field by field
+    (every slot that holds a token), and the output against the oracle and
+    against a plain GPU decode of the same ring.  Decode parity (c) is taken
+    on identical caches: the GPU decodes the oracle's ring and is compared
+    with the oracle's decode."""
+    import torch
+
+    dev = torch.device("cuda")
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    bt = W.block_table(w)
+    nb = w.num_blocks()
+    B = w.batch
+    t0s = np.asarray(t0s, dtype=np.int64)
+    oc = oracle.Cache(w.d, w.key_bits, w.value_bits, w.qjl_m, w.block_size, w.hkv, nb, w.seed)
+    pool_o = oc.new_pool()
+    gc = tq.Cache(nb, w.hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed, w.block_size, w.d)
+    status = tq.new_status()
+    st_o = 0
+    for b in range(B):
+        lo = max(0, int(t0s[b]) - window)
+        if lo == t0s[b]:
+            continue
+        K = W.kv_tokens(w, 0, b, lo, int(t0s[b]))
+        V = W.kv_tokens(w, 1, b, lo, int(t0s[b]))
+        sl = W.ring_slots(w, bt, b, lo, int(t0s[b]), window)
+        st_o |= oc.encode(K, V, sl, pool_o)
+        gc.encode(torch.from_numpy(K).to(dev, tdt).contiguous(), torch.from_numpy(V).to(dev, tdt).contiguous(),
+                  torch.from_numpy(sl).to(dev), status)
+    btt = torch.from_numpy(bt).to(dev)
+    smv = W.sm_scale(w)
+    L = Layout(w.d, w.key_bits, w.value_bits, w.qjl_m, w.block_size, w.hkv, oc.page_bytes)
+    results = []
+    for i in range(steps):
+        lens = (t0s + i + 1).astype(np.int32)
+        kn = np.stack([W.kv_tokens(w, 0, b, int(lens[b]) - 1, int(lens[b]))[0] for b in range(B)])
+        vn = np.stack([W.kv_tokens(w, 1, b, int(lens[b]) - 1, int(lens[b]))[0] for b in range(B)])
+        q = W.queries(w, i)
+        for b in range(B):
+            st_o |= oc.encode(kn[b:b + 1], vn[b:b + 1],
+                              W.ring_slots(w, bt, b, int(lens[b]) - 1, int(lens[b]), window), pool_o)
+        qt = torch.from_numpy(q).to(dev, tdt).contiguous()
+        lt = torch.from_numpy(lens).to(dev)
+        out_g = gc.decode_append(torch.from_numpy(kn).to(dev, tdt).contiguous(),
+                                 torch.from_numpy(vn).to(dev, tdt).contiguous(), qt, btt, lt, smv,
+                                 status=status, window=window)
+        if i not in checks:
+            continue
+        held = np.minimum(lens, window).astype(np.int32)
+        out_a = out_g.cpu().numpy().astype(np.float64)
+        out_p = gc.decode(qt, btt, torch.from_numpy(held).to(dev), smv).cpu().numpy().astype(np.float64)
+        torch.cuda.synchronize()
+        st_g = int(status.item())
+        out_o, dst_o = oc.decode(pool_o, q.astype(np.float64), bt, held, smv)
+        go = tq.Cache(nb, w.hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed, w.block_size, w.d,
+                      pool=torch.from_numpy(pool_o).to(dev))
+        out_go = go.decode(qt, btt, torch.from_numpy(held).to(dev), smv).cpu().numpy().astype(np.float64)
+        pool_g = gc.pool.cpu().numpy()
+        sl, kin, vin = [], [], []
+        for b in range(B):
+            lo = int(lens[b]) - int(held[b])
+            sl.append(W.ring_slots(w, bt, b, lo, int(lens[b]), window))
+            kin.append(W.kv_tokens(w, 0, b, lo, int(lens[b])))
+            vin.append(W.kv_tokens(w, 1, b, lo, int(lens[b])))
+        all_slots = np.repeat(np.concatenate(sl), w.hkv)
+        all_heads = np.tile(np.arange(w.hkv), len(all_slots) // w.hkv)
+        fo = unpack(pool_o, L, all_slots, all_heads)
+        fg = unpack(pool_g, L, all_slots, all_heads)
+        kin = np.concatenate(kin).reshape(-1, w.d).astype(np.float64)
+        vin = np.concatenate(vin).reshape(-1, w.d).astype(np.float64)
+        enc = compare_encode(fo, fg, kin, vin, oc, oracle)
+        enc["status_oracle"], enc["status_gpu"] = st_o | dst_o, st_g
+        enc["other_bytes_equal"] = True
+        results.append(dict(step=i, enc=enc,
+                            dec=dict(rel_err=rel_err(out_go, out_o), status_gpu=st_g, status_oracle=st_o | dst_o,
+                                     out_gpu=out_go, out_oracle=out_o, rel_err_own_cache=rel_err(out_a, out_o),
+                                     same_as_plain_decode=bool(np.array_equal(out_a, out_p)))))
+    return results

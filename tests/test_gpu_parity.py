@@ -79,6 +79,13 @@ def test_swa_workload_full_size(tq, oracle):
     _check(parity.run_case(W.WORKLOADS["swa8x4096"], oracle, tq, decode_gpu_pool=False))
 
 
+@pytest.mark.parametrize("q_step", [1, 2, 3, 4])
+def test_swa_workload_other_queries(tq, oracle, q_step):
+    """The same workload with the queries of later decode steps (160 heads with one
+    query each: the widest spread of per-head errors among the workloads)."""
+    _check(parity.run_case(W.WORKLOADS["swa8x4096"], oracle, tq, q_step=q_step, decode_gpu_pool=False))
+
+
 def test_gqa32k_workload_full_size(tq, oracle):
     """64 q / 8 KV heads, 32768 tokens, permuted 16-token blocks, bf16, 4/4."""
     _check(parity.run_case(W.WORKLOADS["gqa32k"], oracle, tq, decode_gpu_pool=False))

@@ -546,3 +546,35 @@ def test_encode_then_unpack_roundtrip(oracle, kb, vb, m):
             if m:
                 np.testing.assert_array_equal(r["sig"], sig)
                 assert r["rho"] == oracle.fp16_round(rho)
+
+
+@pytest.mark.parametrize("T", [40, 64, 112, 208])
+def test_ring_window_equals_linear_window(oracle, T):
+    """A sliding window kept as a ring of W slots (token t in slot t mod W)
+    holds the last W tokens; since attention does not depend on token order,
+    decoding the ring over min(T, W) slots equals decoding a linear cache of
+    all T tokens over its last W tokens (T - W is a whole number of blocks
+    here, so those tokens are whole pages of the linear cache)."""
+    d, hkv, bs, W_ = 16, 2, 16, 64
+    rng = np.random.default_rng(T)
+    K = rng.standard_normal((T, hkv, d)) * 2
+    V = rng.standard_normal((T, hkv, d))
+    q = rng.standard_normal((1, 2 * hkv, d))
+    lin = oracle.Cache(d, 4, 4, 0, bs, hkv, 32, seed=3)
+    ring = oracle.Cache(d, 4, 4, 0, bs, hkv, 32, seed=3)
+    blocks = rng.permutation(32)
+    lin_bt = blocks[: (T + bs - 1) // bs].astype(np.int32)[None, :]
+    ring_bt = blocks[16: 16 + W_ // bs].astype(np.int32)[None, :]
+    pool_l, pool_r = lin.new_pool(), ring.new_pool()
+    t = np.arange(T)
+    assert lin.encode(K, V, lin_bt[0, t // bs].astype(np.int64) * bs + t % bs, pool_l) == 0
+    for c0 in range(0, T, W_):  # in order, one window at a time, so no two tokens of a call share a slot
+        tc = t[c0: c0 + W_]
+        assert ring.encode(K[tc], V[tc], ring_bt[0, (tc % W_) // bs].astype(np.int64) * bs + tc % bs, pool_r) == 0
+    n = min(T, W_)
+    out_r, st = ring.decode(pool_r, q, ring_bt, np.array([n]), 0.25)
+    assert st == 0
+    first = (T - n) // bs
+    out_l, st = lin.decode(pool_l, q, np.ascontiguousarray(lin_bt[:, first:]), np.array([n]), 0.25)
+    assert st == 0
+    np.testing.assert_allclose(out_r, out_l, rtol=0, atol=1e-12 * np.abs(out_l).max())
