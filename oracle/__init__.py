@@ -75,6 +75,19 @@ def _load():
             "orc_encode": (i32, [i32, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P, i64, P, P]),
             "orc_unpack_slot": (None, [i32, i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P]),
             "orc_decode": (i32, [i32, i32, i32, i32, i32, i32, i64, P, P, P, P, P, i32, i32, P, i32, P, f64, P]),
+            "orc_oct_map": (None, [P, P, P]),
+            "orc_oct_inverse": (None, [f64, f64, P]),
+            "orc_oct_density": (f64, [f64, f64]),
+            "orc_oct_marginal": (f64, [f64]),
+            "orc_rho_density": (f64, [i32, f64]),
+            "orc_oct_cell_mass": (f64, [i32, i32, f64, f64]),
+            "orc_lloyd_density": (i32, [i32, i32, i32, f64, i32, P, P]),
+            "orc_oct_encode_triplet": (f64, [P, P, P, i32, P, P, i32, P, P, P]),
+            "orc_oct_page_bytes": (i64, [i32, i32, i32, i32]),
+            "orc_oct_encode_key_vector": (None, [i32, P, P, i32, P, P, i32, P, P, P, P, P, P]),
+            "orc_oct_encode": (i32, [i32, i32, i32, i32, i32, i64, P, P, P, P, P, P, P, i64, P, P]),
+            "orc_oct_unpack_slot": (None, [i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P]),
+            "orc_oct_decode": (i32, [i32, i32, i32, i32, i32, i64, P, P, P, P, P, i32, i32, P, i32, P, f64, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -259,4 +272,127 @@ class Cache:
                                 self.num_blocks, _p(self.C), _p(self.s), _p(_f64(self.S)),
                                 _p(pool), _p(q), B, hq, _p(bt), bt.shape[1], _p(ln),
                                 float(sm_scale), _p(out))
+        return out, st
+
+
+# --- OCTOPUS triplet codec ------------------------------------------------------
+
+def oct_map(n) -> tuple:
+    n = _f64(n)
+    xi, eta = ctypes.c_double(), ctypes.c_double()
+    _load().orc_oct_map(_p(n), ctypes.byref(xi), ctypes.byref(eta))
+    return xi.value, eta.value
+
+
+def oct_inverse(xi: float, eta: float) -> np.ndarray:
+    n = np.empty(3)
+    _load().orc_oct_inverse(float(xi), float(eta), _p(n))
+    return n
+
+
+def oct_density(xi: float, eta: float) -> float:
+    return _load().orc_oct_density(float(xi), float(eta))
+
+
+def oct_marginal(xi: float) -> float:
+    return _load().orc_oct_marginal(float(xi))
+
+
+def rho_density(d: int, rho: float) -> float:
+    return _load().orc_rho_density(d, float(rho))
+
+
+def oct_cell_mass(kind: int, d: int, a: float, b: float) -> float:
+    return _load().orc_oct_cell_mass(kind, d, float(a), float(b))
+
+
+_oct_cb = {}
+
+
+def oct_codebook(kind: int, d: int, bits: int, tol: float = 1e-13, max_iter: int = 20000):
+    """Lloyd-Max codebook of the xi marginal (kind 0) or the triplet norm (kind 1):
+    (centroids, boundaries, passes); cached per (kind, d, bits)."""
+    key = (kind, d if kind == 1 else 0, bits)
+    if key not in _oct_cb:
+        n = 1 << bits
+        c, t = np.empty(n), np.empty(max(n - 1, 1))
+        it = _load().orc_lloyd_density(kind, d, bits, tol, max_iter, _p(c), _p(t))
+        _oct_cb[key] = (c, t[: n - 1], it)
+    return _oct_cb[key]
+
+
+def oct_page_bytes(d: int, b: int, vb: int, bs: int) -> int:
+    return int(_load().orc_oct_page_bytes(d, b, vb, bs))
+
+
+class OctCache:
+    """An OCTOPUS cache (triplet keys, min-max values), oracle side."""
+
+    def __init__(self, d: int, bits: int, value_bits: int, block_size: int, num_kv_heads: int,
+                 num_blocks: int, seed: int):
+        assert bits >= 2
+        self.d, self.b, self.vb, self.bs, self.hkv = d, bits, value_bits, block_size, num_kv_heads
+        self.num_blocks, self.seed = num_blocks, seed
+        self.ntri = (d + 2) // 3
+        self.Cxi, self.Txi, _ = oct_codebook(0, d, bits + 1)
+        self.Crho, self.Trho, _ = oct_codebook(1, d, bits - 1)
+        self.s = signs(seed, d)
+        self.page_bytes = oct_page_bytes(d, bits, value_bits, block_size)
+        self.pool_bytes = self.page_bytes * num_kv_heads * num_blocks
+
+    def new_pool(self) -> np.ndarray:
+        return np.zeros(self.pool_bytes, dtype=np.uint8)
+
+    def encode_triplet(self, t):
+        t = _f64(t)
+        a, b, r = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        sc = _load().orc_oct_encode_triplet(_p(t), _p(self.Cxi), _p(self.Txi), len(self.Cxi), _p(self.Crho),
+                                            _p(self.Trho), len(self.Crho), ctypes.byref(a), ctypes.byref(b),
+                                            ctypes.byref(r))
+        return a.value, b.value, r.value, sc
+
+    def encode_key_vector(self, k):
+        k = _f64(k)
+        ixi, ieta, irho = (np.empty(self.ntri, dtype=np.int32) for _ in range(3))
+        g = ctypes.c_double()
+        _load().orc_oct_encode_key_vector(self.d, _p(self.Cxi), _p(self.Txi), len(self.Cxi), _p(self.Crho),
+                                          _p(self.Trho), len(self.Crho), _p(self.s), _p(k), ctypes.byref(g),
+                                          _p(ixi), _p(ieta), _p(irho))
+        return g.value, ixi, ieta, irho
+
+    def direction(self, ixi, ieta, irho) -> np.ndarray:
+        """The rotated unit key the codes stand for (rebuilt from the triplets)."""
+        u = np.zeros(3 * self.ntri)
+        for i in range(self.ntri):
+            u[3 * i: 3 * i + 3] = self.Crho[irho[i]] * oct_inverse(self.Cxi[ixi[i]], self.Cxi[ieta[i]])
+        return u[: self.d]
+
+    def encode(self, K, V, slot_mapping, pool: np.ndarray) -> int:
+        K, V = _f64(K), _f64(V)
+        T = K.shape[0]
+        assert K.shape == (T, self.hkv, self.d) and V.shape == K.shape
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        assert pool.dtype == np.uint8 and pool.flags.c_contiguous and pool.size == self.pool_bytes
+        return _load().orc_oct_encode(self.d, self.b, self.vb, self.bs, self.hkv, self.num_blocks,
+                                      _p(self.Cxi), _p(self.Txi), _p(self.Crho), _p(self.Trho), _p(self.s),
+                                      _p(K), _p(V), T, _p(sm), _p(pool))
+
+    def unpack_slot(self, pool: np.ndarray, block: int, head: int, off: int):
+        page = np.ascontiguousarray(pool[(block * self.hkv + head) * self.page_bytes:][: self.page_bytes])
+        ixi, ieta, irho = (np.empty(self.ntri, dtype=np.int32) for _ in range(3))
+        vq = np.empty(self.d, dtype=np.int32)
+        g, sc, zr = (ctypes.c_double() for _ in range(3))
+        _load().orc_oct_unpack_slot(self.d, self.b, self.vb, self.bs, _p(page), off, _p(ixi), _p(ieta), _p(irho),
+                                    _p(vq), ctypes.byref(g), ctypes.byref(sc), ctypes.byref(zr))
+        return dict(ixi=ixi, ieta=ieta, irho=irho, vq=vq, gamma=g.value, scale=sc.value, zero=zr.value)
+
+    def decode(self, pool: np.ndarray, q, block_table, lens, sm_scale: float):
+        q = _f64(q)
+        B, hq, d = q.shape
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        ln = np.ascontiguousarray(lens, dtype=np.int32)
+        out = np.empty_like(q)
+        st = _load().orc_oct_decode(self.d, self.b, self.vb, self.bs, self.hkv, self.num_blocks, _p(self.Cxi),
+                                    _p(self.Crho), _p(self.s), _p(pool), _p(q), B, hq, _p(bt), bt.shape[1],
+                                    _p(ln), float(sm_scale), _p(out))
         return out, st

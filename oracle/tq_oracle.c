@@ -673,3 +673,415 @@ ORC_API int orc_decode(int d, int kb, int vb, int m, int bs, int hkv, int64_t nu
     }
     return status;
 }
+
+/* ======================================================================== */
+/* OCTOPUS: triplet key codec with an octahedral direction code             */
+/* [P3 key contribution "Octahedral triplet direction quantizer with norm   */
+/*  marginals"; methodology steps 1-7; bit split (b+1, b-1)].               */
+/*                                                                          */
+/* The rotated unit key u is cut into ntri = ceil(d/3) triplets t_i (the    */
+/* last one padded with zeros).  Each triplet is its norm rho_i and its     */
+/* direction n_i on S^2; the direction is mapped to the square by the       */
+/* octahedral map, (xi, eta) = Oct(n_i).  xi and eta take (b+1)-bit codes   */
+/* from one Lloyd-Max codebook fitted to the marginal of xi, rho takes a    */
+/* (b-1)-bit code from a Lloyd-Max codebook fitted to the marginal of the   */
+/* norm of three coordinates of a uniform point on S^{d-1}.  The page names */
+/* the map and the "3x3 joint rounding" without formulas; the readings      */
+/* taken are stated at each function.                                       */
+/* ======================================================================== */
+
+static double orc_sgn(double x) { return x < 0.0 ? -1.0 : 1.0; }
+
+/* Octahedral map: p = n / (|n_x| + |n_y| + |n_z|); for n_z >= 0 the upper
+ * half of the octahedron projects straight down, (xi, eta) = (p_x, p_y);
+ * for n_z < 0 the lower half is folded out over the square's corners,
+ * (xi, eta) = ((1 - |p_y|) sgn p_x, (1 - |p_x|) sgn p_y), sgn(0) = +1.
+ * (The standard octahedral parametrisation of the sphere.) */
+ORC_API void orc_oct_map(const double* n, double* xi, double* eta) {
+    double l1 = fabs(n[0]) + fabs(n[1]) + fabs(n[2]);
+    double px = n[0] / l1, py = n[1] / l1;
+    if (n[2] >= 0.0) {
+        *xi = px;
+        *eta = py;
+    } else {
+        *xi = (1.0 - fabs(py)) * orc_sgn(px);
+        *eta = (1.0 - fabs(px)) * orc_sgn(py);
+    }
+}
+
+/* The octahedron point of (xi, eta): z = 1 - |xi| - |eta|; where z < 0 the
+ * fold is undone, (x, y) = ((1 - |eta|) sgn xi, (1 - |xi|) sgn eta). */
+static void orc_oct_point(double xi, double eta, double* p) {
+    double z = 1.0 - fabs(xi) - fabs(eta);
+    if (z >= 0.0) {
+        p[0] = xi;
+        p[1] = eta;
+    } else {
+        p[0] = (1.0 - fabs(eta)) * orc_sgn(xi);
+        p[1] = (1.0 - fabs(xi)) * orc_sgn(eta);
+    }
+    p[2] = z;
+}
+
+/* Inverse map: the unit direction of the octahedron point. */
+ORC_API void orc_oct_inverse(double xi, double eta, double* n) {
+    double p[3];
+    orc_oct_point(xi, eta, p);
+    double r = sqrt(p[0] * p[0] + p[1] * p[1] + p[2] * p[2]);
+    n[0] = p[0] / r;
+    n[1] = p[1] / r;
+    n[2] = p[2] / r;
+}
+
+/* Density of (xi, eta) in [-1,1]^2 for n uniform on S^2.  Radial projection
+ * of an octahedron face (normal (1,1,1)/sqrt 3 in the first octant, area
+ * element sqrt(3) dxi deta over the square) onto the sphere has solid angle
+ * element (p . N) dA / |p|^3 = dxi deta / |p|^3, and the fold of the lower
+ * half is area preserving, so f = 1 / (4 pi |p|^3) with p the octahedron
+ * point of (xi, eta). */
+ORC_API double orc_oct_density(double xi, double eta) {
+    double p[3];
+    orc_oct_point(xi, eta, p);
+    double r2 = p[0] * p[0] + p[1] * p[1] + p[2] * p[2];
+    return 1.0 / (4.0 * M_PI * r2 * sqrt(r2));
+}
+
+/* composite Gauss-Legendre of g over [a, b] in pieces no wider than w */
+static double orc_gl_integrate(double (*g)(double, const void*), const void* ctx, double a, double b, double w) {
+    orc_gl_init();
+    if (b <= a) return 0.0;
+    int pieces = (int)ceil((b - a) / w);
+    if (pieces < 1) pieces = 1;
+    double h = (b - a) / pieces, sum = 0.0;
+    for (int p = 0; p < pieces; ++p) {
+        double mid = a + (p + 0.5) * h, part = 0.0;
+        for (int i = 0; i < ORC_GL_N; ++i) part += orc_gl_w[i] * g(mid + 0.5 * h * orc_gl_x[i], ctx);
+        sum += 0.5 * h * part;
+    }
+    return sum;
+}
+
+static double orc_oct_density_eta(double eta, const void* ctx) {
+    return orc_oct_density(*(const double*)ctx, eta);
+}
+
+/* Marginal of xi: int f(xi, eta) d eta over [-1, 1], in the four pieces on
+ * which the integrand is smooth (split at eta = 0 and |eta| = 1 - |xi|). */
+ORC_API double orc_oct_marginal(double xi) {
+    if (xi < -1.0 || xi > 1.0) return 0.0;
+    double e = 1.0 - fabs(xi);
+    return orc_gl_integrate(orc_oct_density_eta, &xi, -1.0, -e, 0.05) +
+           orc_gl_integrate(orc_oct_density_eta, &xi, -e, 0.0, 0.05) +
+           orc_gl_integrate(orc_oct_density_eta, &xi, 0.0, e, 0.05) +
+           orc_gl_integrate(orc_oct_density_eta, &xi, e, 1.0, 0.05);
+}
+
+/* Norm of three coordinates of a uniform point on S^{d-1}: rho^2 follows
+ * Beta(3/2, (d-3)/2) (the squared coordinates of a uniform point are a
+ * Dirichlet(1/2, ..., 1/2) vector), so
+ * f(rho) = 2 rho^2 (1 - rho^2)^((d-5)/2) / B(3/2, (d-3)/2) on [0, 1]. */
+ORC_API double orc_rho_density(int d, double rho) {
+    if (rho <= 0.0 || rho >= 1.0) return 0.0;
+    double lb = lgamma(1.5) + lgamma((d - 3) / 2.0) - lgamma(d / 2.0);
+    return 2.0 * rho * rho * pow(1.0 - rho * rho, (d - 5) / 2.0) * exp(-lb);
+}
+
+typedef struct { int kind, d, moment; } orc_dens_ctx;
+
+static double orc_dens_eval(double x, const void* vctx) {
+    const orc_dens_ctx* c = (const orc_dens_ctx*)vctx;
+    double f = (c->kind == 0) ? orc_oct_marginal(x) : orc_rho_density(c->d, x);
+    return c->moment ? x * f : f;
+}
+
+/* mass (moment = 0) or first moment (1) of density `kind` over [a, b]; the
+ * xi marginal has a kink at 0, where cells are split */
+static double orc_dens_integral(int kind, int d, int moment, double a, double b) {
+    orc_dens_ctx c = {kind, d, moment};
+    double w = (kind == 0) ? 0.05 : 0.01;
+    if (kind == 0 && a < 0.0 && b > 0.0)
+        return orc_gl_integrate(orc_dens_eval, &c, a, 0.0, w) + orc_gl_integrate(orc_dens_eval, &c, 0.0, b, w);
+    return orc_gl_integrate(orc_dens_eval, &c, a, b, w);
+}
+
+ORC_API double orc_oct_cell_mass(int kind, int d, double a, double b) {
+    return orc_dens_integral(kind, d, 0, a, b);
+}
+
+/* Lloyd-Max on density `kind` (0: the xi marginal on [-1, 1]; 1: the triplet
+ * norm on [0, 1] for dimension d), the same iteration as orc_lloyd_max:
+ * boundaries at midpoints, centroids the cells' conditional means, from
+ * evenly spaced starting levels (over [-1, 1] for xi, over [0, 4 sqrt(3/d)]
+ * for rho), until max |change| < tol or max_iter passes.  Writes n = 2^bits
+ * centroids and n - 1 boundaries; returns the passes taken. */
+ORC_API int orc_lloyd_density(int kind, int d, int bits, double tol, int max_iter, double* c, double* t) {
+    const int n = 1 << bits;
+    const double lo = (kind == 0) ? -1.0 : 0.0, hi = 1.0;
+    const double span = (kind == 0) ? 2.0 : 4.0 * sqrt(3.0 / d);
+    for (int i = 0; i < n; ++i) c[i] = lo + (i + 0.5) * span / n;
+    int it = 0;
+    for (; it < max_iter; ++it) {
+        for (int i = 0; i + 1 < n; ++i) t[i] = 0.5 * (c[i] + c[i + 1]);
+        double delta = 0.0;
+        for (int i = 0; i < n; ++i) {
+            double a = (i == 0) ? lo : t[i - 1];
+            double b = (i == n - 1) ? hi : t[i];
+            double mass = orc_dens_integral(kind, d, 0, a, b);
+            double cn = (mass > 0.0) ? orc_dens_integral(kind, d, 1, a, b) / mass : 0.5 * (a + b);
+            double dd = fabs(cn - c[i]);
+            if (dd > delta) delta = dd;
+            c[i] = cn;
+        }
+        if (delta < tol) { ++it; break; }
+    }
+    for (int i = 0; i + 1 < n; ++i) t[i] = 0.5 * (c[i] + c[i + 1]);
+    return it;
+}
+
+/* nearest level: #{boundaries < x}, ties to the lower index */
+static int orc_nearest(const double* t, int n, double x) {
+    int k = 0;
+    for (int i = 0; i + 1 < n; ++i) k += (t[i] < x) ? 1 : 0;
+    return k;
+}
+
+/* One triplet [P3 methodology steps 3-5].  rho = ||t||, n = t / rho
+ * ((0, 0, 1) when rho = 0).  Norm code: the nearest level of C_rho.
+ * Direction codes, the "3 x 3 joint rounding": with a, b the nearest levels
+ * of C_xi to xi and to eta, the candidates are a' in {a-1, a, a+1} and
+ * b' in {b-1, b, b+1} (inside the codebook); the pair whose direction
+ * n^ = Oct^{-1}(C_xi[a'], C_xi[b']) has the largest <n, n^> is kept (for the
+ * fixed rho^ this is the smallest ||t - rho^ n^||), ties to the first pair in
+ * (a', b') order.  Returns <n, n^> of the pair kept. */
+ORC_API double orc_oct_encode_triplet(const double* tr, const double* Cxi, const double* Txi, int nxi,
+                                      const double* Crho, const double* Trho, int nrho,
+                                      int* ixi, int* ieta, int* irho) {
+    double rho = sqrt(tr[0] * tr[0] + tr[1] * tr[1] + tr[2] * tr[2]);
+    double n[3] = {0.0, 0.0, 1.0};
+    if (rho > 0.0) {
+        n[0] = tr[0] / rho;
+        n[1] = tr[1] / rho;
+        n[2] = tr[2] / rho;
+    }
+    *irho = orc_nearest(Trho, nrho, rho);
+    double xi, eta;
+    orc_oct_map(n, &xi, &eta);
+    int a = orc_nearest(Txi, nxi, xi), b = orc_nearest(Txi, nxi, eta);
+    double best = -INFINITY;
+    int ba = a, bb = b;
+    for (int da = -1; da <= 1; ++da) {
+        int aa = a + da;
+        if (aa < 0 || aa >= nxi) continue;
+        for (int db = -1; db <= 1; ++db) {
+            int bq = b + db;
+            if (bq < 0 || bq >= nxi) continue;
+            double nh[3];
+            orc_oct_inverse(Cxi[aa], Cxi[bq], nh);
+            double sc = n[0] * nh[0] + n[1] * nh[1] + n[2] * nh[2];
+            if (sc > best) {
+                best = sc;
+                ba = aa;
+                bb = bq;
+            }
+        }
+    }
+    *ixi = ba;
+    *ieta = bb;
+    return best;
+}
+
+/* OCTOPUS page: per block of bs slots of one KV head,
+ *   key rows   bs rows of KR bytes, KR = 4 ceil(ntri (3b + 1) / 32); triplet i's
+ *              fields at bit i (3b + 1) of the row: xi code (b + 1 bits), eta
+ *              code (b + 1 bits), rho code (b - 1 bits), LSB first
+ *   value codes, gamma, scale, zero as in the page above (no QJL),
+ * then zero padding to a multiple of 16 bytes.  The bit budget per triplet,
+ * 2 (b + 1) + (b - 1), is the page's B_tri = 2 b_dir + b_nrm with
+ * (b_dir, b_nrm) = (b + 1, b - 1) [P3 "MSE-optimal non-uniform bit allocation"]. */
+static int64_t orc_oct_key_row(int d, int b) {
+    int ntri = (d + 2) / 3;
+    return 4LL * ((ntri * (3 * b + 1) + 31) / 32);
+}
+
+ORC_API int64_t orc_oct_page_bytes(int d, int b, int vb, int bs) {
+    int64_t off = (int64_t)bs * orc_oct_key_row(d, b);
+    off += (int64_t)bs * d * vb / 8;
+    off += 6LL * bs;
+    return (off + 15) / 16 * 16;
+}
+
+/* Key vector [P3 methodology steps 1-6]: gamma = ||k||, u = R (k / gamma),
+ * triplets of u (zeros past d), each coded by orc_oct_encode_triplet.  A zero
+ * key takes u = 0 (every triplet rho = 0, n = (0, 0, 1)). */
+ORC_API void orc_oct_encode_key_vector(int d, const double* Cxi, const double* Txi, int nxi,
+                                       const double* Crho, const double* Trho, int nrho, const double* s,
+                                       const double* k, double* gamma, int* ixi, int* ieta, int* irho) {
+    double g = 0.0;
+    for (int j = 0; j < d; ++j) g += k[j] * k[j];
+    g = sqrt(g);
+    *gamma = g;
+    double* u = (double*)calloc((size_t)d, sizeof(double));
+    double* ur = (double*)calloc((size_t)d + 3, sizeof(double));
+    if (g > 0.0)
+        for (int j = 0; j < d; ++j) u[j] = k[j] / g;
+    orc_rotate(d, s, u, ur);
+    for (int i = 0; i < (d + 2) / 3; ++i) orc_oct_encode_triplet(ur + 3 * i, Cxi, Txi, nxi, Crho, Trho, nrho,
+                                                                ixi + i, ieta + i, irho + i);
+    free(u);
+    free(ur);
+}
+
+/* Encode tokens into OCTOPUS pages: keys as above, values as orc_encode does.
+ * Same slot and status conventions as orc_encode.  b: the page's b (xi codes
+ * b + 1 bits, rho codes b - 1 bits; b >= 2). */
+ORC_API int orc_oct_encode(int d, int b, int vb, int bs, int hkv, int64_t num_blocks,
+                           const double* Cxi, const double* Txi, const double* Crho, const double* Trho,
+                           const double* s, const double* K, const double* V, int64_t T,
+                           const int64_t* slots, uint8_t* pool) {
+    const int ntri = (d + 2) / 3, nxi = 1 << (b + 1), nrho = 1 << (b - 1);
+    const int64_t KR = orc_oct_key_row(d, b), VR = (int64_t)d * vb / 8;
+    const int64_t PB = orc_oct_page_bytes(d, b, vb, bs);
+    const int64_t vcode = (int64_t)bs * KR, gam = vcode + (int64_t)bs * VR, scl = gam + 2 * bs, zer = scl + 2 * bs;
+    int status = 0;
+#pragma omp parallel for schedule(static) reduction(| : status)
+    for (int64_t th = 0; th < T * hkv; ++th) {
+        int64_t t = th / hkv;
+        int h = (int)(th % hkv);
+        int64_t slot = slots[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * bs) { status |= ORC_FLAG_BAD_SLOT; continue; }
+        const double* k = K + th * d;
+        const double* v = V + th * d;
+        int finite = 1;
+        for (int j = 0; j < d; ++j) finite &= isfinite(k[j]) && isfinite(v[j]);
+        if (!finite) status |= ORC_FLAG_NONFINITE;
+        int64_t blk = slot / bs, off = slot % bs;
+        uint8_t* page = pool + (blk * hkv + h) * PB;
+        int* ixi = (int*)malloc(sizeof(int) * ntri);
+        int* ieta = (int*)malloc(sizeof(int) * ntri);
+        int* irho = (int*)malloc(sizeof(int) * ntri);
+        int* vq = (int*)malloc(sizeof(int) * d);
+        double gamma, scale, zero;
+        orc_oct_encode_key_vector(d, Cxi, Txi, nxi, Crho, Trho, nrho, s, k, &gamma, ixi, ieta, irho);
+        orc_encode_value_vector(d, vb, s, v, &scale, &zero, vq);
+        uint8_t* krow = page + off * KR;
+        memset(krow, 0, (size_t)KR);
+        for (int i = 0; i < ntri; ++i) {
+            int64_t p = (int64_t)i * (3 * b + 1);
+            orc_put_bits(krow, p, b + 1, (unsigned)ixi[i]);
+            orc_put_bits(krow, p + b + 1, b + 1, (unsigned)ieta[i]);
+            orc_put_bits(krow, p + 2 * (b + 1), b - 1, (unsigned)irho[i]);
+        }
+        uint8_t* vrow = page + vcode + off * VR;
+        for (int j = 0; j < d; ++j) orc_put_bits(vrow, (int64_t)j * vb, vb, (unsigned)vq[j]);
+        orc_put_f16(page + gam + 2 * off, gamma);
+        orc_put_f16(page + scl + 2 * off, scale);
+        orc_put_f16(page + zer + 2 * off, zero);
+        if (finite && (isinf(orc_fp16_round(gamma)) || isinf(orc_fp16_round(scale)) || isinf(orc_fp16_round(zero))))
+            status |= ORC_FLAG_OVERFLOW;
+        free(ixi); free(ieta); free(irho); free(vq);
+    }
+    return status;
+}
+
+/* Read back one OCTOPUS slot: codes and fp16 fields widened. */
+ORC_API void orc_oct_unpack_slot(int d, int b, int vb, int bs, const uint8_t* page, int off, int* ixi,
+                                 int* ieta, int* irho, int* vq, double* gamma, double* scale, double* zero) {
+    const int ntri = (d + 2) / 3;
+    const int64_t KR = orc_oct_key_row(d, b), VR = (int64_t)d * vb / 8;
+    const int64_t vcode = (int64_t)bs * KR, gam = vcode + (int64_t)bs * VR, scl = gam + 2 * bs, zer = scl + 2 * bs;
+    const uint8_t* krow = page + off * KR;
+    for (int i = 0; i < ntri; ++i) {
+        int64_t p = (int64_t)i * (3 * b + 1);
+        ixi[i] = (int)orc_get_bits(krow, p, b + 1);
+        ieta[i] = (int)orc_get_bits(krow, p + b + 1, b + 1);
+        irho[i] = (int)orc_get_bits(krow, p + 2 * (b + 1), b - 1);
+    }
+    const uint8_t* vrow = page + vcode + off * VR;
+    for (int j = 0; j < d; ++j) vq[j] = (int)orc_get_bits(vrow, (int64_t)j * vb, vb);
+    *gamma = orc_get_f16(page + gam + 2 * off);
+    *scale = orc_get_f16(page + scl + 2 * off);
+    *zero = orc_get_f16(page + zer + 2 * off);
+}
+
+/* The rotated unit key of one slot [P3 methodology step 7: triplets rebuilt
+ * from the codes]: u^[3i + c] = C_rho[irho_i] n^_i[c] with
+ * n^_i = Oct^{-1}(C_xi[ixi_i], C_xi[ieta_i]), for 3i + c < d. */
+static void orc_oct_direction(int d, const double* Cxi, const double* Crho, const int* ixi, const int* ieta,
+                              const int* irho, double* u) {
+    for (int i = 0; i < (d + 2) / 3; ++i) {
+        double nh[3];
+        orc_oct_inverse(Cxi[ixi[i]], Cxi[ieta[i]], nh);
+        for (int c = 0; c < 3; ++c)
+            if (3 * i + c < d) u[3 * i + c] = Crho[irho[i]] * nh[c];
+    }
+}
+
+/* Decode attention over OCTOPUS pages, plain definition (as orc_decode):
+ *   K^_t = gamma_t R^T u^_t, V^_t = R^T (scale_t q_t + zero_t),
+ *   out = softmax_t(sm_scale <q, K^_t>) V^_t over t < lens[b]. */
+ORC_API int orc_oct_decode(int d, int b, int vb, int bs, int hkv, int64_t num_blocks, const double* Cxi,
+                           const double* Crho, const double* s, const uint8_t* pool, const double* Q, int B,
+                           int hq, const int32_t* block_table, int max_blocks, const int32_t* lens,
+                           double sm_scale, double* out) {
+    const int G = hq / hkv, ntri = (d + 2) / 3;
+    const int64_t PB = orc_oct_page_bytes(d, b, vb, bs);
+    int status = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : status)
+    for (int bh = 0; bh < B * hkv; ++bh) {
+        int bi = bh / hkv, h = bh % hkv;
+        int len = lens[bi];
+        for (int g = 0; g < G; ++g) {
+            double* o = out + ((int64_t)bi * hq + (int64_t)h * G + g) * d;
+            for (int j = 0; j < d; ++j) o[j] = 0.0;
+        }
+        if (len <= 0) continue;
+        double* Kh = (double*)calloc((size_t)len * d, sizeof(double));
+        double* Vh = (double*)calloc((size_t)len * d, sizeof(double));
+        char* valid = (char*)calloc((size_t)len, 1);
+        int* ixi = (int*)malloc(sizeof(int) * ntri);
+        int* ieta = (int*)malloc(sizeof(int) * ntri);
+        int* irho = (int*)malloc(sizeof(int) * ntri);
+        int* vq = (int*)malloc(sizeof(int) * d);
+        double* tmp = (double*)malloc(sizeof(double) * d);
+        for (int t = 0; t < len; ++t) {
+            int32_t blk = block_table[(int64_t)bi * max_blocks + t / bs];
+            if (blk < 0 || blk >= num_blocks) { status |= ORC_FLAG_BAD_SLOT; continue; }
+            valid[t] = 1;
+            const uint8_t* page = pool + ((int64_t)blk * hkv + h) * PB;
+            double g, sc, zr;
+            orc_oct_unpack_slot(d, b, vb, bs, page, t % bs, ixi, ieta, irho, vq, &g, &sc, &zr);
+            orc_oct_direction(d, Cxi, Crho, ixi, ieta, irho, tmp);
+            orc_rotate_inverse(d, s, tmp, Kh + (int64_t)t * d);
+            for (int j = 0; j < d; ++j) Kh[(int64_t)t * d + j] *= g;
+            for (int j = 0; j < d; ++j) tmp[j] = sc * vq[j] + zr;
+            orc_rotate_inverse(d, s, tmp, Vh + (int64_t)t * d);
+        }
+        double* logit = (double*)malloc(sizeof(double) * len);
+        for (int g = 0; g < G; ++g) {
+            int64_t qh = (int64_t)bi * hq + (int64_t)h * G + g;
+            const double* qv = Q + qh * d;
+            double mx = -INFINITY;
+            for (int t = 0; t < len; ++t) {
+                if (!valid[t]) continue;
+                double a = 0.0;
+                for (int j = 0; j < d; ++j) a += qv[j] * Kh[(int64_t)t * d + j];
+                logit[t] = sm_scale * a;
+                if (logit[t] > mx) mx = logit[t];
+            }
+            if (mx == -INFINITY) continue;
+            double* o = out + qh * d;
+            double den = 0.0;
+            for (int t = 0; t < len; ++t) {
+                if (!valid[t]) continue;
+                double p = exp(logit[t] - mx);
+                den += p;
+                for (int j = 0; j < d; ++j) o[j] += p * Vh[(int64_t)t * d + j];
+            }
+            for (int j = 0; j < d; ++j) o[j] /= den;
+        }
+        free(logit);
+        free(Kh); free(Vh); free(valid); free(ixi); free(ieta); free(irho); free(vq); free(tmp);
+    }
+    return status;
+}
