@@ -213,6 +213,7 @@ def run_ours(args, rank, world, local):
     q_w = torch.from_numpy(W.queries(w, 0)).to(dev, torch.bfloat16)
     widths = [] if args.profile or args.no_widths else width_sweep(tq, w, K, V, slots, bt, q_w, measured_peaks()[0])
     ring = {} if args.profile or args.no_widths else ring_stream(tq, dev, measured_peaks()[0])
+    octopus = [] if args.profile or args.no_widths else octopus_sweep(tq, w, K, V, slots, bt, q_w, measured_peaks()[0])
     del K, V
 
     # ---- per-step inputs: the new token (position T-1) and the query ----
@@ -388,6 +389,7 @@ def run_ours(args, rank, world, local):
         },
         "widths": widths,
         "ring": ring,
+        "octopus": octopus,
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "device_status": st,
@@ -446,6 +448,58 @@ def width_sweep(tq, w, K, V, slots, bt, q, peak):
                      "decode_GBps": round(gbps, 1), "decode_frac": round(gbps / peak, 4),
                      "decode_us": round(best * 1e3, 2), "decode_copies": n,
                      "encode_Mtok_s": round(T / (enc_ms * 1e-3) / 1e6, 1), "encode_frac": round(enc_gbps / peak, 4)})
+        del g, caches, wss, base
+        torch.cuda.empty_cache()
+    return rows
+
+
+def octopus_sweep(tq, w, K, V, slots, bt, q, peak):
+    """The OCTOPUS triplet key codec on the same workload and inputs: encode
+    Mtokens/s and decode GB/s of compressed bytes read (one decode launch plus
+    its merge launch, timed as a CUDA graph over caches larger than L2)."""
+    import torch
+
+    T, hkv, hq, d = w.lens[0], w.hkv, w.hq, w.d
+    nb = w.num_blocks()
+    lens = torch.tensor([T], dtype=torch.int32, device=K.device)
+    out = torch.empty((1, hq, d), dtype=torch.float32, device=K.device)
+    rows = []
+    for b, vb in ((4, 4), (2, 2)):
+        base = tq.OctopusCache(nb, hkv, b, vb, w.seed)
+        for _ in range(3):
+            base.encode(K, V, slots)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            base.encode(K, V, slots)
+        e1.record()
+        torch.cuda.synchronize()
+        enc_ms = e0.elapsed_time(e1) / 10
+        pb = base.page_bytes
+        dec_bytes = (T // w.block_size) * hkv * pb
+        n = max(2, -(-512_000_000 // dec_bytes))
+        caches = [base] + [tq.OctopusCache(nb, hkv, b, vb, w.seed, pool=base.pool.clone()) for _ in range(n - 1)]
+        wss = [c.new_workspace(1, hq, bt.shape[1]) for c in caches]
+        reps = max(20, n)
+        for i in range(3):
+            caches[i % n].decode(q, bt, lens, out=out, workspace=wss[i % n])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                caches[i % n].decode(q, bt, lens, out=out, workspace=wss[i % n])
+        g.replay()
+        torch.cuda.synchronize()
+        best = 1e9
+        for _ in range(3):
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / reps)
+        gbps = dec_bytes / (best * 1e-3) / 1e9
+        rows.append({"bits": b, "value_bits": vb, "page_bytes": pb, "decode_us": round(best * 1e3, 2),
+                     "decode_GBps": round(gbps, 1), "decode_frac": round(gbps / peak, 4),
+                     "encode_Mtok_s": round(T / (enc_ms * 1e-3) / 1e6, 1), "launches_per_decode": 2})
         del g, caches, wss, base
         torch.cuda.empty_cache()
     return rows

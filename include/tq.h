@@ -152,6 +152,51 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
 
 TQ_API void tq_cache_free(tq_cache* cache);
 
+/* ---------------------------------------------------------------------- */
+/* OCTOPUS triplet key codec                                               */
+/* ---------------------------------------------------------------------- */
+
+/* A cache whose keys use the OCTOPUS triplet codec ["OCTOPUS: Optimized KV
+ * Cache for Transformers via Octahedral Parametrization ..." -- key
+ * contribution "Octahedral triplet direction quantizer with norm marginals",
+ * methodology steps 1-7]; values keep their min-max codes.  For a key:
+ *   gamma = ||k|| (fp16), u = R (k / gamma) as for the main codec;
+ *   u is cut into ceil(d/3) triplets t_i (the last padded with zeros);
+ *   rho_i = ||t_i|| takes a (bits - 1)-bit code: the nearest level of a
+ *     Lloyd-Max codebook for the norm of three coordinates of a uniform point
+ *     on S^{d-1} (rho^2 ~ Beta(3/2, (d-3)/2));
+ *   the direction n_i = t_i / rho_i ((0, 0, 1) if rho_i = 0) goes through the
+ *     octahedral map Oct(n) = (xi, eta) (p = n / |n|_1; the lower half folded
+ *     over the square's corners), and xi, eta take (bits + 1)-bit codes of one
+ *     Lloyd-Max codebook for the marginal of xi of a uniform direction; among
+ *     the nearest levels of xi and of eta and their neighbours (3 x 3 pairs)
+ *     the pair whose unit direction is closest to n_i is kept.
+ * The split (bits + 1, bits - 1) is the page's (b_dir, b_nrm) = (b + 1, b - 1).
+ * Page (per block of block_size slots of one KV head): block_size key rows of
+ * KR = 4 ceil(ceil(d/3) (3 bits + 1) / 32) bytes (triplet i's fields at bit
+ * i (3 bits + 1): xi code, eta code, rho code, LSB first), then value codes,
+ * gamma, scale, zero as in the main layout, padded to 16 bytes.
+ * Decode: logit_t = sm_scale gamma_t sum_i rho^_i <(R q)_{3i..3i+2}, n^_i>, with
+ * n^_i the unit direction of the stored level pair; values and the inverse
+ * rotation as for the main codec.
+ * tq_encode_kv, tq_decode_attention and tq_decode_workspace_bytes accept such
+ * a cache (its decode runs on CUDA cores, one partial per warp merged by a
+ * second kernel); the one-launch append entry points return
+ * TQ_ERR_UNSUPPORTED.  Supported: d = 128, block_size = 16, bits 2..4,
+ * value_bits 1..8.  The library allocates its codebooks and direction table
+ * in device memory. */
+TQ_API tq_status tq_cache_create_octopus(void* pool, int64_t num_blocks, int block_size, int num_kv_heads,
+                                         int d, int bits, int value_bits, uint64_t seed, tq_cache** out);
+
+/* Bytes of one OCTOPUS page, or -1 for an invalid combination (bits 2..4,
+ * value_bits 1..8, d a positive multiple of 8). */
+TQ_API int64_t tq_octopus_page_bytes(int d, int bits, int value_bits, int block_size);
+
+/* The OCTOPUS codebooks the library computes on the host (tests): kind 0 gives
+ * the 2^bits levels for xi and eta, kind 1 the 2^bits levels for the triplet
+ * norm at dimension d, each increasing.  d 6..1024, bits 1..5. */
+TQ_API tq_status tq_octopus_codebook(int d, int bits, int kind, double* levels);
+
 /* The constants a seed defines, derived on the host without a GPU (the same
  * derivation tq_cache_create performs): signs[d] as +-1 and, if m > 0 and S is
  * not NULL, S[m*d] row-major in double.  d: 1..4096, m: 0..4096. */

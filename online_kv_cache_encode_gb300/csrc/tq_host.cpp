@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "tq_internal.h"
 
@@ -164,6 +165,136 @@ Geometry make_geometry(int d, int kb, int vb, int m, int bs, int hkv, int64_t nu
     } else {
         g.rho_off = g.sig_off = -1;
     }
+    g.page_bytes = (off + 15) / 16 * 16;
+    return g;
+}
+
+// ---------------------------------------------------------------------------
+// OCTOPUS codebooks (host).  Two densities: the xi coordinate of the
+// octahedral map of a uniform direction on S^2, and the norm of three
+// coordinates of a uniform point on S^{d-1}.  Lloyd-Max on each, with the cell
+// integrals read from cumulative tables on a fine grid (Simpson's rule per
+// grid interval, and on the partial interval up to a boundary), started from
+// the equal-mass levels.
+// ---------------------------------------------------------------------------
+namespace {
+
+// density of (xi, eta) on the square: 1 / (4 pi |p|^3), p the point of the
+// octahedron |x| + |y| + |z| = 1 that (xi, eta) stands for (the lower half
+// folded over the square's corners)
+double oct_joint_density(double xi, double eta) {
+    double x = xi, y = eta, z = 1.0 - std::fabs(xi) - std::fabs(eta);
+    if (z < 0.0) {
+        x = (1.0 - std::fabs(eta)) * (xi < 0.0 ? -1.0 : 1.0);
+        y = (1.0 - std::fabs(xi)) * (eta < 0.0 ? -1.0 : 1.0);
+    }
+    const double r2 = x * x + y * y + z * z;
+    return 1.0 / (4.0 * M_PI * r2 * std::sqrt(r2));
+}
+
+template <typename F>
+double simpson(F f, double a, double b, int n) {  // n even
+    const double h = (b - a) / n;
+    double s = f(a) + f(b);
+    for (int i = 1; i < n; ++i) s += f(a + i * h) * ((i & 1) ? 4.0 : 2.0);
+    return s * h / 3.0;
+}
+
+double oct_xi_density(double xi) {
+    if (xi < -1.0 || xi > 1.0) return 0.0;  // positive up to the ends (f(+-1) = f(0))
+    const double e = 1.0 - std::fabs(xi);
+    auto f = [xi](double eta) { return oct_joint_density(xi, eta); };
+    return simpson(f, -1.0, -e, 64) + simpson(f, -e, 0.0, 64) + simpson(f, 0.0, e, 64) + simpson(f, e, 1.0, 64);
+}
+
+double oct_rho_density(int d, double r) {
+    if (r <= 0.0 || r >= 1.0) return 0.0;
+    const double lb = std::lgamma(1.5) + std::lgamma((d - 3) / 2.0) - std::lgamma(d / 2.0);
+    return 2.0 * r * r * std::pow(1.0 - r * r, (d - 5) / 2.0) * std::exp(-lb);
+}
+
+struct CumTable {
+    int kind, d, n;
+    double lo, h;
+    std::vector<double> F0, F1;  // mass and first moment from lo to grid point k
+    double f(double x) const { return kind == 0 ? oct_xi_density(x) : oct_rho_density(d, x); }
+    void build(int kind_, int d_, double lo_, double hi_, int n_) {
+        kind = kind_; d = d_; n = n_; lo = lo_; h = (hi_ - lo_) / n_;
+        F0.assign(n + 1, 0.0);
+        F1.assign(n + 1, 0.0);
+        for (int k = 0; k < n; ++k) {
+            const double a = lo + k * h, m = a + 0.5 * h, b = a + h;
+            const double fa = f(a), fm = f(m), fb = f(b);
+            F0[k + 1] = F0[k] + h / 6.0 * (fa + 4.0 * fm + fb);
+            F1[k + 1] = F1[k] + h / 6.0 * (a * fa + 4.0 * m * fm + b * fb);
+        }
+    }
+    // integral from lo to x of f (moment 0) or x f (moment 1)
+    double cum(double x, int moment) const {
+        if (x <= lo) return 0.0;
+        int k = (int)std::floor((x - lo) / h);
+        if (k >= n) return moment ? F1[n] : F0[n];
+        const double a = lo + k * h, m = 0.5 * (a + x);
+        const double fa = f(a), fm = f(m), fx = f(x);
+        const double part = moment ? (x - a) / 6.0 * (a * fa + 4.0 * m * fm + x * fx)
+                                   : (x - a) / 6.0 * (fa + 4.0 * fm + fx);
+        return (moment ? F1[k] : F0[k]) + part;
+    }
+};
+
+// Lloyd-Max on a tabulated density over [lo, hi]; levels c[0..nl), boundaries
+// at their midpoints
+void oct_lloyd(const CumTable& T, double hi, int nl, double* c) {
+    const double total = T.cum(hi, 0);
+    // start: the levels that split the mass equally (bisection on the table)
+    for (int i = 0; i < nl; ++i) {
+        const double target = total * (i + 0.5) / nl;
+        double a = T.lo, b = hi;
+        for (int it = 0; it < 200; ++it) {
+            const double m = 0.5 * (a + b);
+            if (T.cum(m, 0) < target) a = m;
+            else b = m;
+        }
+        c[i] = 0.5 * (a + b);
+    }
+    std::vector<double> t(nl > 1 ? nl - 1 : 1);
+    for (int it = 0; it < 100000; ++it) {
+        for (int i = 0; i + 1 < nl; ++i) t[i] = 0.5 * (c[i] + c[i + 1]);
+        double delta = 0.0;
+        for (int i = 0; i < nl; ++i) {
+            const double a = i == 0 ? T.lo : t[i - 1], b = i == nl - 1 ? hi : t[i];
+            const double mass = T.cum(b, 0) - T.cum(a, 0);
+            const double cn = mass > 0.0 ? (T.cum(b, 1) - T.cum(a, 1)) / mass : 0.5 * (a + b);
+            delta = std::fmax(delta, std::fabs(cn - c[i]));
+            c[i] = cn;
+        }
+        if (delta < 1e-14) break;
+    }
+}
+
+}  // namespace
+
+// xi levels (kind 0, 2^bits of them) or triplet-norm levels (kind 1) for dimension d
+void octopus_levels(int kind, int d, int bits, double* c) {
+    CumTable T;
+    if (kind == 0) T.build(0, d, -1.0, 1.0, 8192);
+    else T.build(1, d, 0.0, 1.0, 8192);
+    oct_lloyd(T, 1.0, 1 << bits, c);
+}
+
+int octopus_key_row(int d, int b) { return 4 * ((((d + 2) / 3) * (3 * b + 1) + 31) / 32); }
+
+Geometry make_oct_geometry(int d, int b, int vb, int bs, int hkv, int64_t num_blocks) {
+    Geometry g{};
+    g.d = d; g.kb = b; g.vb = vb; g.m = 0; g.bs = bs; g.hkv = hkv;
+    g.num_blocks = num_blocks;
+    int off = 0;
+    g.kcode_off = off; off += bs * octopus_key_row(d, b);
+    g.vcode_off = off; off += bs * d * vb / 8;
+    g.gam_off = off; off += 2 * bs;
+    g.scl_off = off; off += 2 * bs;
+    g.zer_off = off; off += 2 * bs;
+    g.rho_off = g.sig_off = -1;
     g.page_bytes = (off + 15) / 16 * 16;
     return g;
 }
@@ -374,8 +505,90 @@ TQ_API void tq_cache_free(tq_cache* c) {
     if (!c) return;
     if (c->S_dev) cudaFree(c->S_dev);
     if (c->tab_dev) cudaFree(c->tab_dev);
+    if (c->oct_dev) cudaFree(c->oct_dev);
     delete[] c->S_host;
     delete c;
+}
+
+TQ_API int64_t tq_octopus_page_bytes(int d, int bits, int value_bits, int block_size) {
+    if (d <= 0 || d % 8 || bits < 2 || bits > 4 || value_bits < 1 || value_bits > 8 || block_size <= 0) return -1;
+    return make_oct_geometry(d, bits, value_bits, block_size, 1, 1).page_bytes;
+}
+
+TQ_API tq_status tq_octopus_codebook(int d, int bits, int kind, double* levels) {
+    if (!levels) return fail(TQ_ERR_INVALID_ARG, "levels is NULL");
+    if (d < 6 || d > 1024 || kind < 0 || kind > 1 || bits < 1 || bits > 5)
+        return fail(TQ_ERR_INVALID_ARG, "d 6..1024, kind 0 or 1, bits 1..5");
+    octopus_levels(kind, d, bits, levels);
+    return TQ_OK;
+}
+
+TQ_API tq_status tq_cache_create_octopus(void* pool, int64_t num_blocks, int block_size, int num_kv_heads, int d,
+                                         int bits, int value_bits, uint64_t seed, tq_cache** out) {
+    if (!out) return fail(TQ_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!pool) return fail(TQ_ERR_INVALID_ARG, "pool is NULL");
+    if ((reinterpret_cast<uintptr_t>(pool) & 15) != 0) return fail(TQ_ERR_INVALID_ARG, "pool must be 16-byte aligned");
+    if (num_blocks <= 0 || num_kv_heads <= 0 || block_size <= 0 || d <= 0)
+        return fail(TQ_ERR_INVALID_ARG, "sizes must be positive");
+    if (tq_octopus_page_bytes(d, bits, value_bits, block_size) < 0)
+        return fail(TQ_ERR_INVALID_ARG, "invalid d / bits / value_bits combination (bits 2..4, value bits 1..8)");
+    if (d != kHeadDim) return fail(TQ_ERR_UNSUPPORTED, "head dim must be 128");
+    if (block_size != kBlockSize) return fail(TQ_ERR_UNSUPPORTED, "block_size must be 16");
+    tq_cache* c = new (std::nothrow) tq_cache();
+    if (!c) return fail(TQ_ERR_INVALID_ARG, "out of host memory");
+    c->pool = pool;
+    c->seed = seed;
+    c->octopus = 1;
+    c->g = make_oct_geometry(d, bits, value_bits, block_size, num_kv_heads, num_blocks);
+    c->oct_key_row = octopus_key_row(d, bits);
+    std::memset(&c->c, 0, sizeof(c->c));
+    derive_signs(seed, d, c->signs);
+    for (int j = 0; j < d; ++j)
+        if (c->signs[j] < 0) c->c.sign_bits[j / 32] |= 1u << (j % 32);
+    // codebooks and the direction table of the level pairs
+    OctTables& T = c->oct_host;
+    std::memset(&T, 0, sizeof(T));
+    const int nxi = 1 << (bits + 1), nrho = 1 << (bits - 1);
+    double cx[kOctMaxDir], cr[8];
+    octopus_levels(0, d, bits + 1, cx);
+    octopus_levels(1, d, bits - 1, cr);
+    for (int i = 0; i < nxi; ++i) {
+        T.cxi[i] = (float)cx[i];
+        if (i + 1 < nxi) T.bxi[i] = (float)(0.5 * (cx[i] + cx[i + 1]));
+    }
+    for (int i = 0; i < nrho; ++i) {
+        T.crho[i] = (float)cr[i];
+        if (i + 1 < nrho) T.brho[i] = (float)(0.5 * (cr[i] + cr[i + 1]));
+    }
+    for (int a = 0; a < nxi; ++a)
+        for (int b = 0; b < nxi; ++b) {
+            // the unit direction of the octahedron point of (cx[a], cx[b])
+            double x = cx[a], y = cx[b], z = 1.0 - std::fabs(x) - std::fabs(y);
+            if (z < 0.0) {
+                const double xf = (1.0 - std::fabs(cx[b])) * (cx[a] < 0.0 ? -1.0 : 1.0);
+                const double yf = (1.0 - std::fabs(cx[a])) * (cx[b] < 0.0 ? -1.0 : 1.0);
+                x = xf;
+                y = yf;
+            }
+            const double r = std::sqrt(x * x + y * y + z * z);
+            float* dd = T.dir[a * kOctMaxDir + b];
+            dd[0] = (float)(x / r);
+            dd[1] = (float)(y / r);
+            dd[2] = (float)(z / r);
+            dd[3] = 0.f;
+        }
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e == cudaSuccess) e = cudaMalloc(&c->oct_dev, sizeof(OctTables));
+    if (e == cudaSuccess) e = cudaMemcpy(c->oct_dev, &T, sizeof(OctTables), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        if (c->oct_dev) cudaFree(c->oct_dev);
+        delete c;
+        return cuda_fail(e, "creating the OCTOPUS cache");
+    }
+    *out = c;
+    return TQ_OK;
 }
 
 TQ_API tq_status tq_cache_signs(const tq_cache* c, int8_t* signs) {
@@ -401,6 +614,23 @@ TQ_API tq_status tq_encode_kv(const tq_cache* c, const void* K, const void* V, t
     if (dtype != TQ_F32 && dtype != TQ_BF16 && dtype != TQ_F16) return fail(TQ_ERR_INVALID_ARG, "bad dtype");
     if ((reinterpret_cast<uintptr_t>(K) % 16) || (reinterpret_cast<uintptr_t>(V) % 16))
         return fail(TQ_ERR_INVALID_ARG, "K and V must be 16-byte aligned");
+    if (c->octopus) {
+        OctArgs o{};
+        o.g = c->g;
+        o.key_row = c->oct_key_row;
+        o.tab = c->oct_dev;
+        std::memcpy(o.sign_bits, c->c.sign_bits, sizeof(o.sign_bits));
+        o.pool = (uint8_t*)c->pool;
+        o.status = dev_status;
+        o.K = K;
+        o.V = V;
+        o.dtype = (int)dtype;
+        o.num_tokens = num_tokens;
+        o.slot_mapping = slot_mapping;
+        int e = launch_oct_encode(o, c->num_sms, stream);
+        if (e != 0) return cuda_fail((cudaError_t)e, "OCTOPUS encode launch");
+        return TQ_OK;
+    }
     EncodeArgs a{};
     a.g = c->g;
     a.c = c->c;
@@ -427,7 +657,21 @@ TQ_API tq_status tq_encode_kv(const tq_cache* c, const void* K, const void* V, t
 // splits (8 pages or more each) and four times the count that fills the SMs.
 static void decode_split_plan(const tq_cache* c, int batch, int max_blocks, int* splits, int* pps) {
     const int64_t units = (int64_t)batch * c->g.hkv;
-    const int nw = c->g.m ? 8 : 12;
+    if (c->octopus) {
+        // the OCTOPUS decode keeps ~35 KB of shared memory per CTA, so several
+        // CTAs share an SM: aim at four per SM to hide the page loads, with at
+        // least four pages per split
+        const int64_t sms = c->num_sms > 0 ? c->num_sms : 1;
+        int64_t s = (4 * sms + units - 1) / units;
+        const int64_t cap = (max_blocks + 3) / 4;
+        if (s > cap) s = cap;
+        if (s < 1) s = 1;
+        int p = (int)((max_blocks + s - 1) / s);
+        *pps = p;
+        *splits = (max_blocks + p - 1) / p;
+        return;
+    }
+    const int nw = (c->g.m || c->octopus) ? 8 : 12;
     const int64_t sms = c->num_sms > 0 ? c->num_sms : 1;
     int64_t lim = 4 * ((sms + units - 1) / units);
     const int64_t cap = (max_blocks + 7) / 8;
@@ -460,6 +704,10 @@ TQ_API size_t tq_decode_workspace_bytes(const tq_cache* c, int batch, int num_q_
     int splits, pps;
     decode_split_plan(c, batch, max_blocks_per_seq, &splits, &pps);
     const int group = num_q_heads / c->g.hkv;
+    if (c->octopus) {
+        // one partial per split: (max, sum, 2 pad, acc[d]) per query
+        return align_up((size_t)batch * c->g.hkv * splits * group * (4 + c->g.d) * sizeof(float), 256);
+    }
     size_t part = (size_t)batch * c->g.hkv * splits * group * (4 + c->g.d) * sizeof(float);
     return align_up(part, 256) + align_up((size_t)batch * c->g.hkv * sizeof(unsigned), 256);
 }
@@ -491,6 +739,32 @@ static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype,
     if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(TQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     int splits, pps;
     decode_split_plan(c, batch, max_blocks_per_seq, &splits, &pps);
+    if (c->octopus) {
+        if (knew) return fail(TQ_ERR_UNSUPPORTED, "appending inside decode is not built for OCTOPUS caches");
+        OctArgs o{};
+        o.g = c->g;
+        o.key_row = c->oct_key_row;
+        o.tab = c->oct_dev;
+        std::memcpy(o.sign_bits, c->c.sign_bits, sizeof(o.sign_bits));
+        o.pool = (uint8_t*)c->pool;
+        o.status = dev_status;
+        o.q = q;
+        o.dtype = (int)dtype;
+        o.batch = batch;
+        o.hq = num_q_heads;
+        o.group = group;
+        o.block_table = block_table;
+        o.max_blocks = max_blocks_per_seq;
+        o.lens = lens;
+        o.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+        o.out = out;
+        o.partials = (float*)workspace;
+        o.pages_per_split = pps;
+        o.num_splits = splits;
+        int e = launch_oct_decode(o, stream);
+        if (e != 0) return cuda_fail((cudaError_t)e, "OCTOPUS decode launch");
+        return TQ_OK;
+    }
     DecodeArgs a{};
     a.g = c->g;
     a.c = c->c;
@@ -537,6 +811,9 @@ static tq_status append_common(const tq_cache* c, const void* k_new, const void*
                                float sm_scale, float* out, void* workspace, size_t workspace_bytes,
                                int32_t* dev_status, void* stream) {
     if (!c) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
+    if (c->octopus)
+        return fail(TQ_ERR_UNSUPPORTED, "appending inside decode is not built for OCTOPUS caches; "
+                                        "use tq_encode_kv then tq_decode_attention");
     if (c->g.m > 0)
         return fail(TQ_ERR_UNSUPPORTED, "appending inside decode is built for caches without QJL; "
                                         "use tq_encode_kv then tq_decode_attention");

@@ -91,6 +91,51 @@ struct DecodeArgs {
     int window;
 };
 
+// ---------------------------------------------------------------------------
+// OCTOPUS triplet key codec (second codec of a cache; values keep min-max codes)
+// ---------------------------------------------------------------------------
+constexpr int kOctTri = (kHeadDim + 2) / 3;   // triplets per key (the last one padded)
+constexpr int kOctMaxDir = 32;                // direction levels per axis at b = 4
+
+// Codebooks and the direction table, in device memory written once when the
+// cache is created.  dir[a * n + b] is the unit direction of level pair (a, b)
+// (n = 2^(b+1) levels per axis), w unused.
+struct OctTables {
+    float cxi[kOctMaxDir], bxi[kOctMaxDir];   // levels and boundaries of xi and eta
+    float crho[8], brho[8];                   // levels and boundaries of the triplet norm
+    float dir[kOctMaxDir * kOctMaxDir][4];
+};
+
+struct OctArgs {
+    Geometry g;           // kb = b (the codec's bits), vb; kcode_off = 0
+    int key_row;          // bytes of one key row (4-byte multiple)
+    const OctTables* tab;
+    uint32_t sign_bits[kHeadDim / 32];
+    uint8_t* pool;
+    int32_t* status;
+    // encode
+    const void* K;
+    const void* V;
+    int dtype;
+    int64_t num_tokens;
+    const int64_t* slot_mapping;
+    // decode
+    const void* q;
+    int batch, hq, group;
+    const int32_t* block_table;
+    int max_blocks;
+    const int32_t* lens;
+    float sm_scale_log2;
+    float* out;
+    float* partials;      // [batch, hkv, splits, group, 4 + d]
+    int pages_per_split, num_splits;
+};
+constexpr int kOctWarps = 8;
+
+int launch_oct_encode(const OctArgs& a, int num_sms, void* stream);
+int launch_oct_decode(const OctArgs& a, void* stream);
+int oct_decode_smem_bytes(const OctArgs& a);
+
 // Launchers (return a cudaError_t as int).  The per-key-width ones are
 // explicitly instantiated, one key width per translation unit.
 int launch_encode(const EncodeArgs& a, int num_sms, void* stream);
@@ -122,6 +167,10 @@ struct tq_cache {
     double* S_host;   // m x d
     float* S_dev;     // m x d, library-owned device memory
     tq::CodeTables* tab_dev;  // library-owned device memory
+    int octopus;              // 1: OCTOPUS triplet keys (bits in g.kb)
+    int oct_key_row;
+    tq::OctTables* oct_dev;   // library-owned device memory (OCTOPUS)
+    tq::OctTables oct_host;
     int device;
     int num_sms;
 };

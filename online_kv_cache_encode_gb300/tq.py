@@ -42,6 +42,9 @@ SIGNATURES = {
     "tq_decode_attention_append": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _F, _P, _P, _SZ, _P, _P]),
     "tq_decode_attention_ring_append": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _I, _F, _P, _P, _SZ, _P,
                                              _P]),
+    "tq_cache_create_octopus": (_I, [_P, ctypes.c_int64, _I, _I, _I, _I, _I, ctypes.c_uint64, ctypes.POINTER(_P)]),
+    "tq_octopus_page_bytes": (ctypes.c_int64, [_I, _I, _I, _I]),
+    "tq_octopus_codebook": (_I, [_I, _I, _I, _P]),
     "tq_status_string": (ctypes.c_char_p, [_I]),
     "tq_last_error": (ctypes.c_char_p, []),
 }
@@ -279,3 +282,33 @@ class Cache:
                                                  block_table.shape[1], _ptr(lens), float(sm_scale), _ptr(out),
                                                  _ptr(status), _stream()))
         return out
+
+
+class OctopusCache(Cache):
+    """A cache whose keys use the OCTOPUS triplet codec (bits 2..4 per
+    coordinate on average: (bits + 1)-bit direction codes, (bits - 1)-bit norm
+    codes per triplet); values keep min-max codes.  encode / decode as Cache."""
+
+    def __init__(self, num_blocks: int, num_kv_heads: int, bits: int = 4, value_bits: int = 4, seed: int = 0,
+                 block_size: int = 16, d: int = 128, pool: torch.Tensor | None = None, device="cuda"):
+        self.num_blocks, self.hkv, self.kb, self.vb = num_blocks, num_kv_heads, bits, value_bits
+        self.m, self.seed, self.bs, self.d = 0, seed, block_size, d
+        self.page_bytes = int(lib().tq_octopus_page_bytes(d, bits, value_bits, block_size))
+        if self.page_bytes < 0:
+            raise TQError(TQ_ERR_INVALID_ARG, "invalid geometry")
+        nbytes = self.page_bytes * num_kv_heads * num_blocks
+        if pool is None:
+            pool = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        assert pool.dtype == torch.uint8 and pool.numel() >= nbytes and pool.is_contiguous()
+        self.pool = pool
+        self._h = ctypes.c_void_p()
+        _check(lib().tq_cache_create_octopus(_ptr(pool), num_blocks, block_size, num_kv_heads, d, bits, value_bits,
+                                             seed, ctypes.byref(self._h)))
+        self._ws = None
+
+
+def octopus_codebook(d: int, bits: int, kind: int) -> np.ndarray:
+    """The library's host-computed OCTOPUS levels (kind 0: xi / eta, kind 1: triplet norm)."""
+    out = np.empty(1 << bits, dtype=np.float64)
+    _check(lib().tq_octopus_codebook(d, bits, kind, out.ctypes.data_as(ctypes.c_void_p)))
+    return out

@@ -397,3 +397,116 @@ def run_ring_stream(w, oracle, tq, window: int, t0s, steps: int, checks) -> list
                                      out_gpu=out_go, out_oracle=out_o, rel_err_own_cache=rel_err(out_a, out_o),
                                      same_as_plain_decode=bool(np.array_equal(out_a, out_p)))))
     return results
+
+
+def run_octopus_case(w, oracle, tq, q_step: int = 0) -> dict:
+    """OCTOPUS keys (w.key_bits is the codec's b), min-max values: encode the
+    workload on both sides and compare the pages; decode one step with the GPU
+    reading the oracle's cache and compare with the oracle's decode.
+
+    A key triplet's codes may differ only where the decision is within 1e-5 of
+    a tie in the oracle's own arithmetic: the GPU's direction pair scores
+    within 1e-5 of the oracle's pair (<n, n^>), or xi, eta or rho lies within
+    1e-5 of a boundary of its codebook.  Such triplets stay under the (a)
+    budget, 1e-5 of all triplets scaled by the direction width factor."""
+    import torch
+
+    dev = torch.device("cuda")
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    bt = W.block_table(w)
+    nb = w.num_blocks()
+    K, V = _inputs(w)
+    slots = [W.slots(w, bt, b, 0, w.lens[b]) for b in range(w.batch)]
+    oc = oracle.OctCache(w.d, w.key_bits, w.value_bits, w.block_size, w.hkv, nb, w.seed)
+    pool_o = oc.new_pool()
+    st_o = 0
+    for b in range(w.batch):
+        st_o |= oc.encode(K[b], V[b], slots[b], pool_o)
+    gc = tq.OctopusCache(nb, w.hkv, w.key_bits, w.value_bits, w.seed)
+    assert gc.page_bytes == oc.page_bytes
+    status = tq.new_status()
+    for b in range(w.batch):
+        if w.lens[b]:
+            gc.encode(torch.from_numpy(K[b]).to(dev, tdt).contiguous(), torch.from_numpy(V[b]).to(dev, tdt).contiguous(),
+                      torch.from_numpy(slots[b]).to(dev), status)
+    torch.cuda.synchronize()
+    pool_g = gc.pool.cpu().numpy()
+    st_g = int(status.item())
+    # ---- keys ----
+    kin = np.concatenate(K).reshape(-1, w.hkv, w.d).astype(np.float64)
+    vin = np.concatenate(V).reshape(-1, w.hkv, w.d).astype(np.float64)
+    all_slots = np.concatenate(slots)
+    mism = far = 0
+    vmis = vfar = 0
+    ulp = {"gamma": 0, "scale": 0, "zero": 0}
+    n_tri = 0
+    for i, sl in enumerate(all_slots):
+        blk, off = int(sl) // w.block_size, int(sl) % w.block_size
+        for h in range(w.hkv):
+            uo = oc.unpack_slot(pool_o, blk, h, off)
+            ug = oc.unpack_slot(pool_g, blk, h, off)
+            n_tri += oc.ntri
+            for f in ulp:
+                a16 = np.array([uo[f]], dtype=np.float16).view(np.int16).astype(np.int64)[0]
+                b16 = np.array([ug[f]], dtype=np.float16).view(np.int16).astype(np.int64)[0]
+                ulp[f] = max(ulp[f], int(abs(_ordered(np.array([a16 & 0xFFFF], dtype=np.uint16))[0] -
+                                             _ordered(np.array([b16 & 0xFFFF], dtype=np.uint16))[0])))
+            bad = np.nonzero((uo["ixi"] != ug["ixi"]) | (uo["ieta"] != ug["ieta"]) | (uo["irho"] != ug["irho"]))[0]
+            if len(bad):
+                k = kin[i, h]
+                u = oracle.rotate(oc.s, k / np.linalg.norm(k))
+                u = np.concatenate([u, np.zeros(3 * oc.ntri - w.d)])
+                for j in bad:
+                    mism += 1
+                    t = u[3 * j: 3 * j + 3]
+                    rho = np.linalg.norm(t)
+                    n = t / rho if rho > 0 else np.array([0.0, 0.0, 1.0])
+                    xi, eta = oracle.oct_map(n)
+                    near = False
+                    if uo["irho"][j] != ug["irho"][j]:
+                        near = np.min(np.abs(oc.Trho - rho)) <= BOUNDARY_TOL
+                    else:
+                        near = True
+                    if (uo["ixi"][j], uo["ieta"][j]) != (ug["ixi"][j], ug["ieta"][j]):
+                        so = n @ oracle.oct_inverse(oc.Cxi[uo["ixi"][j]], oc.Cxi[uo["ieta"][j]])
+                        sg = n @ oracle.oct_inverse(oc.Cxi[ug["ixi"][j]], oc.Cxi[ug["ieta"][j]])
+                        tie = abs(so - sg) <= BOUNDARY_TOL
+                        edge = min(np.min(np.abs(oc.Txi - xi)), np.min(np.abs(oc.Txi - eta))) <= BOUNDARY_TOL
+                        near = near and (tie or edge)
+                    far += 0 if near else 1
+            vb_ = np.nonzero(uo["vq"] != ug["vq"])[0]
+            if len(vb_):
+                vr = oracle.rotate(oc.s, vin[i, h])
+                sc = (vr.max() - vr.min()) / ((1 << w.value_bits) - 1)
+                for j in vb_:
+                    vmis += 1
+                    x = (vr[j] - vr.min()) / sc
+                    if abs((x - math.floor(x)) - 0.5) > value_boundary_tol(w.value_bits) or abs(int(uo["vq"][j]) - int(ug["vq"][j])) > 1:
+                        vfar += 1
+    enc = dict(triplet_mismatch=mism, triplet_mismatch_far=far, val_mismatch=vmis, val_mismatch_far=vfar,
+               triplets=n_tri, coords=len(all_slots) * w.hkv * w.d,
+               budget=MISMATCH_FRACTION * (n_tri * width_factor(w.key_bits + 1) + len(all_slots) * w.hkv * w.d *
+                                           width_factor(w.value_bits)),
+               status_oracle=st_o, status_gpu=st_g, **{f + "_max_ulp": v for f, v in ulp.items()})
+    # ---- decode on identical caches ----
+    q = W.queries(w, q_step)
+    lens = np.array(w.lens, dtype=np.int32)
+    smv = W.sm_scale(w)
+    out_o, dst_o = oc.decode(pool_o, q.astype(np.float64), bt, lens, smv)
+    go = tq.OctopusCache(nb, w.hkv, w.key_bits, w.value_bits, w.seed, pool=torch.from_numpy(pool_o).to(dev))
+    dstat = tq.new_status()
+    out_g = go.decode(torch.from_numpy(q).to(dev, tdt).contiguous(), torch.from_numpy(bt).to(dev),
+                      torch.from_numpy(lens).to(dev), smv, status=dstat).cpu().numpy().astype(np.float64)
+    dec = dict(rel_err=rel_err(out_g, out_o), status_gpu=int(dstat.item()), status_oracle=dst_o,
+               out_gpu=out_g, out_oracle=out_o)
+    return dict(enc=enc, dec=dec, w=w)
+
+
+def assert_octopus_parity(res: dict):
+    e = res["enc"]
+    assert e["status_gpu"] == e["status_oracle"], e
+    assert e["triplet_mismatch_far"] == 0 and e["val_mismatch_far"] == 0, e
+    assert e["triplet_mismatch"] + e["val_mismatch"] <= e["budget"], e
+    for f in ("gamma", "scale", "zero"):
+        assert e[f + "_max_ulp"] <= 1, (f, e)
+    assert_decode_parity(res)

@@ -104,3 +104,15 @@ def test_binding_refuses_without_library(tq, monkeypatch):
     monkeypatch.setattr(tq, "LIB_PATH", "/nonexistent/libtq.so")
     with pytest.raises(RuntimeError, match="missing"):
         tq.lib()
+
+
+def test_octopus_codebooks_match_the_oracle(tq, oracle):
+    """The library computes its OCTOPUS codebooks on the host by a different
+    method (cumulative Simpson tables) than the oracle (Gauss-Legendre cells);
+    both must reach the same Lloyd-Max levels."""
+    for kind, bits in ((0, 3), (0, 5), (1, 1), (1, 3)):
+        lib = tq.octopus_codebook(128, bits, kind)
+        ref = oracle.oct_codebook(kind, 128, bits)[0]
+        assert abs(lib - ref).max() < 1e-9, (kind, bits)
+    assert tq.lib().tq_octopus_page_bytes(128, 4, 4, 16) == 16 * 72 + 16 * 64 + 96
+    assert tq.lib().tq_octopus_page_bytes(128, 5, 4, 16) == -1
