@@ -309,6 +309,33 @@ TQ_API tq_status tq_decode_attention_ring_append(const tq_cache* cache, const vo
                                                  float sm_scale, float* out, void* workspace,
                                                  size_t workspace_bytes, int32_t* dev_status, void* stream);
 
+/* ---------------------------------------------------------------------- */
+/* Chunked prefill attention                                               */
+/* ---------------------------------------------------------------------- */
+
+/* Workspace bytes tq_prefill_attention needs (zero-filled once before first
+ * use, like a decode workspace). */
+TQ_API size_t tq_prefill_workspace_bytes(const tq_cache* cache, int num_positions, int num_q_heads,
+                                         int max_blocks_per_seq);
+
+/* Attention for a chunk of num_positions consecutive query positions of one
+ * sequence, first_position .. first_position + num_positions - 1, over the
+ * compressed cache, causally: the query at position p attends over the
+ * sequence's tokens 0 .. p.  The chunk's own keys and values must already be
+ * in the cache (tq_encode_kv first), which is the order of the deep dive's
+ * attention forward: the new keys and values update the compressed cache,
+ * then attention reads it [TurboQuant deep dive -- attention forward with
+ * kv_cache.update; llama.cpp results: prefill speed on a par with Q8_0].
+ * q: device [num_positions, num_q_heads, d]; block_table: device int32, the
+ * sequence's one row of max_blocks_per_seq blocks; out: device fp32
+ * [num_positions, num_q_heads, d].  Each position is one row of the decode
+ * kernel (all rows read the same block-table row), so this call reads the
+ * cached pages once per position. */
+TQ_API tq_status tq_prefill_attention(const tq_cache* cache, const void* q, tq_dtype dtype, int num_positions,
+                                      int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                                      int first_position, float sm_scale, float* out, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream);
+
 /* Bytes of the fixed decode workspace built into the library (see below). */
 #define TQ_NOALLOC_WORKSPACE_BYTES (4u << 20)
 

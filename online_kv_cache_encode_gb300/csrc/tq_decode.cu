@@ -20,6 +20,18 @@ int decode_smem_bytes(const Geometry& g) {
     }
 }
 
+// lens[i] = first + i + 1: the causal lengths of a prefill chunk's positions
+__global__ void fill_positions_kernel(int32_t* lens, int n, int first) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) lens[i] = first + i + 1;
+}
+
+int launch_fill_positions(int32_t* lens, int n, int first, void* stream) {
+    if (n <= 0) return 0;
+    fill_positions_kernel<<<(n + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(lens, n, first);
+    return (int)cudaGetLastError();
+}
+
 int launch_decode(const DecodeArgs& a, void* stream) {
     switch (a.g.kb) {
         case 1: return launch_decode_kb<1>(a, stream);

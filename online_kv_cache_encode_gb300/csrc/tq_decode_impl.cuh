@@ -692,7 +692,7 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     // warp's page l of the current batch of 32 (bid_cur) and of the next batch
     // (bid_nxt).
     int len = __ldg(a.lens + b);
-    const int32_t* btw = a.block_table + (int64_t)b * a.max_blocks + p0 + warp;
+    const int32_t* btw = a.block_table + (int64_t)b * a.bt_stride + p0 + warp;
     const int reach = min(a.pages_per_split, a.max_blocks - p0) - warp;  // pages of the split at or after this warp's first
     int bid_cur = (NW * lane < reach) ? __ldg(btw + NW * lane) : -1;
     int bid_nxt = (NW * (32 + lane) < reach) ? __ldg(btw + NW * (32 + lane)) : -1;
@@ -759,7 +759,7 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                     const int64_t e = ((int64_t)b * g.hkv + h) * D + 4 * lane;
                     raw4(a.knew, a.kv_dtype, e, kraw);
                     raw4(a.vnew, a.kv_dtype, e, vraw);
-                    blknew = __ldg(a.block_table + (int64_t)b * a.max_blocks + p0 + pi);
+                    blknew = __ldg(a.block_table + (int64_t)b * a.bt_stride + p0 + pi);
                 }
             }
         }

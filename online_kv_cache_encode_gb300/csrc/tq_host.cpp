@@ -716,7 +716,8 @@ static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype,
                                const int32_t* block_table, int max_blocks_per_seq, const int32_t* lens,
                                float sm_scale, float* out, void* workspace, size_t workspace_bytes,
                                int32_t* dev_status, void* stream, const void* knew, const void* vnew,
-                               tq_dtype kv_dtype, int window) {
+                               tq_dtype kv_dtype, int window, int64_t bt_stride = -1) {
+    if (bt_stride < 0) bt_stride = max_blocks_per_seq;
     if (!c) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
     if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0)
         return fail(TQ_ERR_INVALID_ARG, "bad batch / num_q_heads / max_blocks_per_seq");
@@ -755,6 +756,7 @@ static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype,
         o.group = group;
         o.block_table = block_table;
         o.max_blocks = max_blocks_per_seq;
+        o.bt_stride = bt_stride;
         o.lens = lens;
         o.sm_scale_log2 = sm_scale * 1.4426950408889634f;
         o.out = out;
@@ -776,6 +778,7 @@ static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype,
     a.group = group;
     a.block_table = block_table;
     a.max_blocks = max_blocks_per_seq;
+    a.bt_stride = bt_stride;
     a.lens = lens;
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.out = out;
@@ -833,6 +836,38 @@ TQ_API tq_status tq_decode_attention_append(const tq_cache* c, const void* k_new
                                             int32_t* dev_status, void* stream) {
     return append_common(c, k_new, v_new, kv_dtype, q, dtype, batch, num_q_heads, block_table, max_blocks_per_seq,
                          lens, 0, sm_scale, out, workspace, workspace_bytes, dev_status, stream);
+}
+
+TQ_API size_t tq_prefill_workspace_bytes(const tq_cache* c, int num_positions, int num_q_heads,
+                                         int max_blocks_per_seq) {
+    const size_t w = tq_decode_workspace_bytes(c, num_positions, num_q_heads, max_blocks_per_seq);
+    if (w == 0) return 0;
+    return w + align_up((size_t)num_positions * sizeof(int32_t), 256);
+}
+
+TQ_API tq_status tq_prefill_attention(const tq_cache* c, const void* q, tq_dtype dtype, int num_positions,
+                                      int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                                      int first_position, float sm_scale, float* out, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (!c) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
+    if (num_positions < 0 || first_position < 0) return fail(TQ_ERR_INVALID_ARG, "negative positions");
+    if (num_positions == 0) return TQ_OK;
+    if (max_blocks_per_seq <= 0 ||
+        (int64_t)first_position + num_positions > (int64_t)max_blocks_per_seq * c->g.bs)
+        return fail(TQ_ERR_INVALID_ARG, "the block table holds fewer slots than the chunk's last position");
+    const size_t need = tq_prefill_workspace_bytes(c, num_positions, num_q_heads, max_blocks_per_seq);
+    if (need == 0) return fail(TQ_ERR_INVALID_ARG, "bad num_q_heads / max_blocks_per_seq");
+    if (!workspace) return fail(TQ_ERR_INVALID_ARG, "workspace is NULL");
+    if (workspace_bytes < need) {
+        set_error("workspace has %zu bytes, needs %zu", workspace_bytes, need);
+        return TQ_ERR_WORKSPACE;
+    }
+    const size_t dec = tq_decode_workspace_bytes(c, num_positions, num_q_heads, max_blocks_per_seq);
+    int32_t* lens = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + dec);
+    int e = launch_fill_positions(lens, num_positions, first_position, stream);
+    if (e != 0) return cuda_fail((cudaError_t)e, "prefill lengths");
+    return decode_common(c, q, dtype, num_positions, num_q_heads, block_table, max_blocks_per_seq, lens, sm_scale,
+                         out, workspace, dec, dev_status, stream, nullptr, nullptr, TQ_BF16, 0, 0);
 }
 
 TQ_API tq_status tq_decode_attention_ring_append(const tq_cache* c, const void* k_new, const void* v_new,

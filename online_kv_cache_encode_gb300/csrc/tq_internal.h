@@ -72,6 +72,7 @@ struct DecodeArgs {
     int batch, hq, group;
     const int32_t* block_table;
     int max_blocks;
+    int64_t bt_stride;    // elements between sequences' block-table rows (0: all share row 0)
     const int32_t* lens;
     float sm_scale_log2;  // sm_scale * log2(e)
     float* out;
@@ -124,6 +125,7 @@ struct OctArgs {
     int batch, hq, group;
     const int32_t* block_table;
     int max_blocks;
+    int64_t bt_stride;    // elements between sequences' block-table rows (0: all share row 0)
     const int32_t* lens;
     float sm_scale_log2;
     float* out;
@@ -141,6 +143,7 @@ int oct_decode_smem_bytes(const OctArgs& a);
 int launch_encode(const EncodeArgs& a, int num_sms, void* stream);
 int launch_decode(const DecodeArgs& a, void* stream);
 int decode_smem_bytes(const Geometry& g);
+int launch_fill_positions(int32_t* lens, int n, int first, void* stream);
 template <int KB>
 int launch_encode_kb(const EncodeArgs& a, int num_sms, void* stream);
 template <int KB>

@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kOctWarps * 32) oct_decode_kernel(const OctArg
     const int tt = lane >> 1, half = lane & 1;            // scores: token tt, triplet half
     const int i0 = half ? 22 : 0, i1 = half ? kOctTri : 22;
     for (int pi = p0 + warp; pi < pend; pi += kOctWarps) {
-        const int blk = __ldg(a.block_table + (int64_t)b * a.max_blocks + pi);
+        const int blk = __ldg(a.block_table + (int64_t)b * a.bt_stride + pi);
         if (blk < 0 || blk >= g.num_blocks) {
             if (lane == 0) flag(a.status, TQ_FLAG_BAD_SLOT);
             continue;

@@ -45,6 +45,8 @@ SIGNATURES = {
     "tq_cache_create_octopus": (_I, [_P, ctypes.c_int64, _I, _I, _I, _I, _I, ctypes.c_uint64, ctypes.POINTER(_P)]),
     "tq_octopus_page_bytes": (ctypes.c_int64, [_I, _I, _I, _I]),
     "tq_octopus_codebook": (_I, [_I, _I, _I, _P]),
+    "tq_prefill_workspace_bytes": (_SZ, [_P, _I, _I, _I]),
+    "tq_prefill_attention": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _F, _P, _P, _SZ, _P, _P]),
     "tq_status_string": (ctypes.c_char_p, [_I]),
     "tq_last_error": (ctypes.c_char_p, []),
 }
@@ -262,6 +264,28 @@ class Cache:
                                                          _ptr(lens), int(window), float(sm_scale), _ptr(out),
                                                          _ptr(workspace), workspace.numel(), _ptr(status),
                                                          _stream()))
+        return out
+
+    def prefill(self, q: torch.Tensor, block_row: torch.Tensor, first_position: int, sm_scale: float | None = None,
+                out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                status: torch.Tensor | None = None) -> torch.Tensor:
+        """Causal attention of the query positions first_position .. first_position + C - 1
+        (q: [C, Hq, d]) of one sequence over its cached tokens (the chunk's own
+        keys and values already encoded); block_row: int32 [max_blocks]."""
+        assert q.is_cuda and q.dim() == 3 and q.shape[2] == self.d and q.is_contiguous()
+        assert block_row.dtype == torch.int32 and block_row.dim() == 1 and block_row.is_contiguous()
+        C, hq, _ = q.shape
+        mb = block_row.shape[0]
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.d)
+        if out is None:
+            out = torch.empty((C, hq, self.d), dtype=torch.float32, device=q.device)
+        if workspace is None:
+            n = int(lib().tq_prefill_workspace_bytes(self._h, C, hq, mb))
+            workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+        _check(lib().tq_prefill_attention(self._h, _ptr(q), _dtype_code(q), C, hq, _ptr(block_row), mb,
+                                          int(first_position), float(sm_scale), _ptr(out), _ptr(workspace),
+                                          workspace.numel(), _ptr(status), _stream()))
         return out
 
     def decode_noalloc(self, q: torch.Tensor, block_table: torch.Tensor, lens: torch.Tensor,
