@@ -200,8 +200,13 @@ __global__ void __launch_bounds__(kOctWarps * 32) oct_encode_kernel(const OctArg
 // table, the norm levels, the rotated queries and one page per warp.
 // ---------------------------------------------------------------------------
 struct OctSmem {
-    int dir, crho, q, pages, total;
+    int dir, crho, q, pages, u, total;
 };
+constexpr int kOctHalf = kBlockSize / 2;  // tokens whose directions are rebuilt at a time
+// a rebuilt direction row keeps each 32-dim part 4 floats apart from the next,
+// so that the four parts read at once fall in different banks
+constexpr int kOctURow = 4 * 36;
+__host__ __device__ constexpr int oct_upos(int c) { return c + 4 * (c >> 5); }
 // After the page loop the whole area holds the warps' partials for the in-CTA
 // merge: [kOctWarps][8 queries][4 + d] floats.
 constexpr int kOctMergeBytes = kOctWarps * 8 * (4 + kHeadDim) * 4;
@@ -212,12 +217,13 @@ __host__ __device__ inline OctSmem oct_smem(int nxi, int page_bytes) {
     L.crho = off; off += 8 * 4;
     L.q = off; off += 8 * (kHeadDim + 4) * 4;
     L.pages = off; off += kOctWarps * ((page_bytes + 15) / 16 * 16);
+    L.u = off; off += kOctWarps * kOctHalf * kOctURow * 4;
     L.total = off > kOctMergeBytes ? off : kOctMergeBytes;
     return L;
 }
 
 template <int B, int VB>
-__global__ void __launch_bounds__(kOctWarps * 32) oct_decode_kernel(const OctArgs a) {
+__global__ void __launch_bounds__(kOctWarps * 32, 2) oct_decode_kernel(const OctArgs a) {
     constexpr int NXI = 1 << (B + 1), FB = 3 * B + 1, D = kHeadDim, QS = D + 4;
     constexpr int VROW = D * VB / 8;
     extern __shared__ __align__(16) uint8_t sm[];
@@ -260,15 +266,20 @@ __global__ void __launch_bounds__(kOctWarps * 32) oct_decode_kernel(const OctArg
     int pend = (len + kBlockSize - 1) / kBlockSize;
     if (pend > p0 + a.pages_per_split) pend = p0 + a.pages_per_split;
 
-    float m[8], l[8], acc[8][4];
+    // Scores: lane (query g = lane / 4, part = lane % 4) keeps dims 32 part ..
+    // 32 part + 31 of its rotated query in registers and dots them with the
+    // page's rebuilt rotated key directions; a query's 4 lanes then sum their
+    // parts.  Softmax state per query lives in its lanes.  Values: lane l
+    // accumulates dims 4l .. 4l+3 of every query.
+    const int gq = lane >> 2, part = lane & 3;
+    float qreg[32];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        m[q] = kOctMinus;
-        l[q] = 0.f;
-        acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-    }
-    const int tt = lane >> 1, half = lane & 1;            // scores: token tt, triplet half
-    const int i0 = half ? 22 : 0, i1 = half ? kOctTri : 22;
+    for (int c = 0; c < 32; ++c) qreg[c] = (gq < G) ? s_q[gq * QS + 32 * part + c] : 0.f;
+    float* s_u = reinterpret_cast<float*>(sm + L.u) + warp * kOctHalf * kOctURow;
+    float m_g = kOctMinus, l_g = 0.f;
+    float acc[8][4];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
     for (int pi = p0 + warp; pi < pend; pi += kOctWarps) {
         const int blk = __ldg(a.block_table + (int64_t)b * a.bt_stride + pi);
         if (blk < 0 || blk >= g.num_blocks) {
@@ -278,42 +289,67 @@ __global__ void __launch_bounds__(kOctWarps * 32) oct_decode_kernel(const OctArg
         const uint4* src = reinterpret_cast<const uint4*>(a.pool + ((int64_t)blk * g.hkv + h) * g.page_bytes);
         for (int k = lane; k < (int)(g.page_bytes / 16); k += 32) reinterpret_cast<uint4*>(s_page)[k] = __ldg(src + k);
         __syncwarp();
-        // ---- scores: lanes 2t, 2t+1 share token t's triplets ----
-        const uint32_t* row = reinterpret_cast<const uint32_t*>(s_page + tt * a.key_row);
-        float sc[8];
+        float sc[kBlockSize];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) sc[q] = 0.f;
-        for (int i = i0; i < i1; ++i) {
-            const uint32_t f = oct_bits(row, i * FB, FB);
-            const int ia = f & (NXI - 1), ie = (f >> (B + 1)) & (NXI - 1), ir = f >> (2 * (B + 1));
-            const float4 d4 = s_dir[ia * NXI + ie];
-            const float r = s_crho[ir];
-            const float e0 = r * d4.x, e1 = r * d4.y, e2 = r * d4.z;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                if (q < G) {
-                    const float* qv = s_q + q * QS + 3 * i;
-                    sc[q] = fmaf(e0, qv[0], fmaf(e1, qv[1], fmaf(e2, qv[2], sc[q])));
-                }
+        for (int hf = 0; hf < 2; ++hf) {
+            // rebuild u^ = rho^ n^ of tokens 8 hf .. 8 hf + 7 (all 43 triplets)
+            for (int j = lane; j < kOctHalf * kOctTri; j += 32) {
+                const int t = j / kOctTri, i = j - t * kOctTri;
+                const uint32_t* row = reinterpret_cast<const uint32_t*>(s_page + (kOctHalf * hf + t) * a.key_row);
+                const uint32_t f = oct_bits(row, i * FB, FB);
+                const int ia = f & (NXI - 1), ie = (f >> (B + 1)) & (NXI - 1), ir = f >> (2 * (B + 1));
+                const float4 d4 = s_dir[ia * NXI + ie];
+                const float r = s_crho[ir];
+                float* u = s_u + t * kOctURow;
+                u[oct_upos(3 * i)] = r * d4.x;
+                u[oct_upos(3 * i + 1)] = r * d4.y;
+                if (3 * i + 2 < D) u[oct_upos(3 * i + 2)] = r * d4.z;
             }
+            __syncwarp();
+#pragma unroll
+            for (int t = 0; t < kOctHalf; ++t) {
+                const float4* u4 = reinterpret_cast<const float4*>(s_u + t * kOctURow + 36 * part);
+                float x = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float4 v = u4[c];
+                    x = fmaf(v.x, qreg[4 * c], fmaf(v.y, qreg[4 * c + 1], fmaf(v.z, qreg[4 * c + 2], fmaf(v.w, qreg[4 * c + 3], x))));
+                }
+                x += __shfl_xor_sync(0xffffffffu, x, 1);
+                x += __shfl_xor_sync(0xffffffffu, x, 2);
+                sc[kOctHalf * hf + t] = x;
+            }
+            __syncwarp();  // s_u is rebuilt for the second half
         }
-        const float gam = __half2float(*reinterpret_cast<const __half*>(s_page + g.gam_off + 2 * tt));
-        const bool valid = pi * kBlockSize + tt < len;
-        float p[8];
+        // ---- online softmax, query gq's state in its four lanes ----
+        float mx = kOctMinus;
+#pragma unroll
+        for (int t = 0; t < kBlockSize; ++t) {
+            const float gam = __half2float(*reinterpret_cast<const __half*>(s_page + g.gam_off + 2 * t));
+            const bool valid = pi * kBlockSize + t < len;
+            sc[t] = valid ? sc[t] * gam : -INFINITY;
+            mx = fmaxf(mx, sc[t]);
+        }
+        float fct = 1.f;
+        if (mx > m_g) {
+            fct = exp2f(m_g - mx);
+            l_g *= fct;
+            m_g = mx;
+        }
+        // weights to shared memory (over the rebuilt directions, no longer
+        // needed): p[t][query]; a query's part-0 lane writes them
+#pragma unroll
+        for (int t = 0; t < kBlockSize; ++t) {
+            sc[t] = exp2f(sc[t] - m_g);  // -inf gives 0
+            l_g += sc[t];
+            if (part == 0) s_u[t * 8 + gq] = sc[t];
+        }
+        __syncwarp();
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             if (q >= G) continue;
-            float s = sc[q] + __shfl_xor_sync(0xffffffffu, sc[q], 1);
-            s = valid ? s * gam : -INFINITY;
-            const float mx = warp_max(s);
-            if (mx > m[q]) {
-                const float fct = exp2f(m[q] - mx);
-                l[q] *= fct;
-                acc[q][0] *= fct; acc[q][1] *= fct; acc[q][2] *= fct; acc[q][3] *= fct;
-                m[q] = mx;
-            }
-            p[q] = valid ? exp2f(s - m[q]) : 0.f;
-            l[q] += warp_sum(half ? 0.f : p[q]);
+            const float f = __shfl_sync(0xffffffffu, fct, 4 * q);
+            acc[q][0] *= f; acc[q][1] *= f; acc[q][2] *= f; acc[q][3] *= f;
         }
         // ---- values: lane holds dims 4 lane .. 4 lane + 3 ----
         for (int t = 0; t < kBlockSize; ++t) {
@@ -327,12 +363,18 @@ __global__ void __launch_bounds__(kOctWarps * 32) oct_decode_kernel(const OctArg
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 if (q >= G) continue;
-                const float pt = __shfl_sync(0xffffffffu, p[q], 2 * t);
+                const float pt = s_u[t * 8 + q];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) acc[q][k] = fmaf(pt, vv[k], acc[q][k]);
             }
         }
         __syncwarp();  // the page buffer is refilled next
+    }
+    float m[8], l[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        m[q] = __shfl_sync(0xffffffffu, m_g, 4 * q);
+        l[q] = __shfl_sync(0xffffffffu, l_g, 4 * q);
     }
     // ---- merge the warps in shared memory; warp q writes the CTA's partial
     // for query q: (max, sum, 2 pad, acc[128]) ----
