@@ -24,8 +24,12 @@
 namespace tq {
 
 constexpr int kEncWarps = 8;
-constexpr int kSPad = kHeadDim + 1;          // padded row stride of S in shared memory
-constexpr int kRPad = kHeadDim + 8;          // padded per-item residual buffer (QJL)
+// S in shared memory: each row's 16-coordinate segments start 20 floats apart,
+// so that the 8 lanes of an item read 16-byte pieces of a row from 8
+// different groups of banks
+constexpr int kSSeg = 20;
+constexpr int kSRow = 8 * kSSeg;
+__host__ __device__ constexpr int s_pos(int c) { return kSSeg * (c >> 4) + (c & 15); }
 
 // E consecutive elements starting at element index i (i a multiple of E).
 template <int E>
@@ -134,7 +138,7 @@ __device__ __forceinline__ void store_lane_codes(uint8_t* row, int s, const uint
 }
 
 template <int KB, int VB, int M, int GRP>
-__global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncodeArgs a) {
+__global__ void __launch_bounds__(kEncWarps * 32, M > 0 ? 2 : 3) encode_kernel(const EncodeArgs a) {
     constexpr int E = kHeadDim / GRP;   // coordinates per lane
     constexpr int IPW = 32 / GRP;       // items per warp
     extern __shared__ float smem[];
@@ -145,16 +149,19 @@ __global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncodeA
     constexpr int NB = (1 << KB) - 1;
     constexpr int VMAX = (1 << VB) - 1;
     constexpr int HALF = 1 << (KB - 1);
-    float* Ss = smem;                                                  // [M][kSPad]
+    float* Ss = smem;                                                  // [M][kSRow]
     // key widths above 4 bits: the positive boundaries (times sqrt(d)) for the binary search
     __shared__ float bsd_s[KB > 4 ? (1 << (KB - 1)) : 1];
-    float* rbuf = smem + M * kSPad + (warp * IPW + grp) * kRPad;  // this item's residual (QJL)
     // launched as a programmatic dependent: wait for the previous grid before
     // touching global memory, and let the next one start launching
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if constexpr (M > 0) {
-        for (int i = threadIdx.x; i < M * D; i += blockDim.x) Ss[(i / D) * kSPad + (i % D)] = a.S[i];
+        const float4* S4 = reinterpret_cast<const float4*>(a.S);  // four coordinates of one segment at a time
+        for (int i = threadIdx.x; i < M * D / 4; i += blockDim.x) {
+            const int row = (4 * i) / D, c = (4 * i) % D;
+            *reinterpret_cast<float4*>(Ss + row * kSRow + s_pos(c)) = __ldg(S4 + i);
+        }
         __syncthreads();
     }
     if constexpr (KB > 4) {
@@ -247,42 +254,6 @@ __global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncodeA
             store_lane_codes<KB, E>(page + g.kcode_off + off * (D * KB / 8), s, w, store);
         }
 
-        float rho = 0.f;
-        if constexpr (M > 0) {
-            float rr = 0.f;
-#pragma unroll
-            for (int i = 0; i < E; ++i) {
-                rbuf[E * s + i] = r[i];
-                rr = fmaf(r[i], r[i], rr);
-            }
-            rho = sqrtf(group_sum<GRP>(rr));
-            __syncwarp();
-            // lane s computes rows i = s + GRP j of S r (S rows padded to 129
-            // floats: the lanes of a group read different banks); row i is bit
-            // i & 31 of word i >> 5, which is (GRP j) >> 5 since s < GRP
-            uint32_t bits[M / 32] = {};
-#pragma unroll
-            for (int j = 0; j < M / GRP; ++j) {
-                const float* srow = Ss + (s + GRP * j) * kSPad;
-                float dot = 0.f;
-#pragma unroll 8
-                for (int c = 0; c < D; ++c) dot = fmaf(srow[c], rbuf[c], dot);
-                if (dot >= 0.f) bits[(GRP * j) >> 5] |= 1u << (s + ((GRP * j) & 31));
-            }
-#pragma unroll
-            for (int w = 0; w < M / 32; ++w)
-#pragma unroll
-                for (int m = 1; m < GRP; m <<= 1) bits[w] |= __shfl_xor_sync(0xffffffffu, bits[w], m);
-            __syncwarp();
-            if (store && s < M / 32) {
-                uint32_t* sig = reinterpret_cast<uint32_t*>(page + g.sig_off + off * (M / 8));
-                uint32_t wv = bits[0];
-#pragma unroll
-                for (int w = 1; w < M / 32; ++w) wv = (s == w) ? bits[w] : wv;
-                sig[s] = (gamma > 0.f) ? wv : 0xffffffffu;
-            }
-        }
-
         // ---- value ----
 #pragma unroll
         for (int i = 0; i < E; ++i)
@@ -307,6 +278,63 @@ __global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncodeA
             store_lane_codes<VB, E>(page + g.vcode_off + off * (D * VB / 8), s, w, store);
         }
 
+        float rho = 0.f;
+        if constexpr (M > 0) {
+            float rr = 0.f;
+#pragma unroll
+            for (int i = 0; i < E; ++i) rr = fmaf(r[i], r[i], rr);
+            rho = sqrtf(group_sum<GRP>(rr));
+            // S r, CH rows at a time: every lane forms the partial dot products
+            // of the CH rows over its own coordinates E s .. E s + E - 1, then
+            // the item's lanes sum them, each lane ending with CH / GRP rows
+            // (rows (CH/GRP) s .. of the chunk) whose sign bits it sets
+            // (bit i of sigma: (S r)_i >= 0); the words are OR-ed over the group.
+            constexpr int CH = (GRP == 8) ? 16 : 32;
+            constexpr int RPL = CH / GRP;
+            uint32_t wb[M / 32];
+#pragma unroll
+            for (int w = 0; w < M / 32; ++w) wb[w] = 0u;
+#pragma unroll
+            for (int ch = 0; ch < M / CH; ++ch) {
+                float pr[CH];
+#pragma unroll
+                for (int k = 0; k < CH; ++k) {
+                    const float* srow = Ss + (ch * CH + k) * kSRow + s_pos(E * s);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int v4 = 0; v4 < E / 4; ++v4) {
+                        const float4 sv = *reinterpret_cast<const float4*>(srow + 4 * v4);
+                        acc = fmaf(sv.x, r[4 * v4], fmaf(sv.y, r[4 * v4 + 1], fmaf(sv.z, r[4 * v4 + 2], fmaf(sv.w, r[4 * v4 + 3], acc))));
+                    }
+                    pr[k] = acc;
+                }
+#pragma unroll
+                for (int m = GRP / 2, half = CH / 2; m >= 1; m >>= 1, half >>= 1) {
+                    const bool up = (s & m) != 0;
+#pragma unroll
+                    for (int k = 0; k < half; ++k) {
+                        const float keep = up ? pr[k + half] : pr[k];
+                        const float give = up ? pr[k] : pr[k + half];
+                        pr[k] = keep + __shfl_xor_sync(0xffffffffu, give, m);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < RPL; ++k)
+                    if (pr[k] >= 0.f) wb[(ch * CH) >> 5] |= 1u << (((ch * CH) & 31) + RPL * s + k);
+            }
+            uint32_t wstore = 0u;
+#pragma unroll
+            for (int w = 0; w < M / 32; ++w) {
+#pragma unroll
+                for (int m = 1; m < GRP; m <<= 1) wb[w] |= __shfl_xor_sync(0xffffffffu, wb[w], m);
+                if (s == w) wstore = wb[w];
+            }
+            if (store && s < M / 32) {
+                uint32_t* sig = reinterpret_cast<uint32_t*>(page + g.sig_off + off * (M / 8));
+                sig[s] = (gamma > 0.f) ? wstore : 0xffffffffu;
+            }
+        }
+
         if (store && s == 0) {
             const uint16_t hg = f16_bits(gamma), hs = f16_bits(scale), hz = f16_bits(mn);
             reinterpret_cast<uint16_t*>(page + g.gam_off)[off] = hg;
@@ -328,7 +356,7 @@ __global__ void __launch_bounds__(kEncWarps * 32, 3) encode_kernel(const EncodeA
 template <int KB, int VB, int M, int GRP>
 static int launch_encode_g(const EncodeArgs& a, int64_t items, int num_sms, cudaStream_t s) {
     constexpr int IPW = 32 / GRP;
-    const size_t smem = (size_t)(M * kSPad + (M > 0 ? kEncWarps * IPW * kRPad : 0)) * sizeof(float);
+    const size_t smem = (size_t)(M * kSRow) * sizeof(float);
     auto kern = encode_kernel<KB, VB, M, GRP>;
     if (smem > 48 * 1024) {
         static int done[64] = {};
