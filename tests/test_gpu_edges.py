@@ -1,0 +1,110 @@
+"""Edge cases of the later features: odd query-group sizes on both codecs,
+OCTOPUS edge inputs (zero key, skipped and bad slots, non-finite input,
+empty sequences), a one-page sliding window, and argument checks of prefill."""
+import os
+
+import numpy as np
+import pytest
+
+from online_kv_cache_encode_gb300 import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tq(oracle):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from online_kv_cache_encode_gb300 import build
+    build.build()
+    from online_kv_cache_encode_gb300 import tq as T
+    oracle.set_threads(os.cpu_count() or 1)
+    return T
+
+
+@pytest.mark.parametrize("G", [3, 5, 7])
+def test_odd_group_sizes(tq, oracle, G):
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(700, 33, 1), hkv=2, hq=2 * G)
+    res = parity.run_case(w, oracle, tq)
+    parity.assert_encode_parity(res)
+    parity.assert_decode_parity(res)
+    parity.assert_octopus_parity(parity.run_octopus_case(w, oracle, tq))
+
+
+def test_octopus_edge_inputs(tq, oracle):
+    import torch
+    dev = "cuda"
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(40, 0, 20), hkv=1, hq=4)
+    nb = w.num_blocks()
+    bt = W.block_table(w)
+    gc = tq.OctopusCache(nb, 1, 3, 4, 0)
+    oc = oracle.OctCache(128, 3, 4, 16, 1, nb, 0)
+    pool_o = oc.new_pool()
+    K = W.kv_tokens(w, 0, 0, 0, 40)
+    V = W.kv_tokens(w, 1, 0, 0, 40)
+    K[3] = 0.0                                 # a zero key: every triplet rho = 0, n = (0, 0, 1)
+    slots = W.slots(w, bt, 0, 0, 40)
+    slots[5] = -1                              # a skipped token
+    st = tq.new_status()
+    gc.encode(torch.from_numpy(K).to(dev, torch.bfloat16), torch.from_numpy(V).to(dev, torch.bfloat16),
+              torch.from_numpy(slots).to(dev), st)
+    assert oc.encode(K, V, slots, pool_o) == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    pg = gc.pool.cpu().numpy()
+    z_g = oc.unpack_slot(pg, int(slots[3]) // 16, 0, int(slots[3]) % 16)
+    z_o = oc.unpack_slot(pool_o, int(slots[3]) // 16, 0, int(slots[3]) % 16)
+    for f in ("ixi", "ieta", "irho"):
+        assert np.array_equal(z_g[f], z_o[f]), f
+    assert z_g["gamma"] == 0.0
+    skipped = oc.unpack_slot(pg, int(W.slots(w, bt, 0, 5, 6)[0]) // 16, 0, 5)
+    assert skipped["gamma"] == 0.0 and not skipped["ixi"].any()
+    bad = torch.tensor([nb * 16 + 3], dtype=torch.int64, device=dev)
+    gc.encode(torch.ones(1, 1, 128, device=dev), torch.ones(1, 1, 128, device=dev), bad, st)
+    torch.cuda.synchronize()
+    assert st.item() & tq.FLAG_BAD_SLOT
+    st.zero_()
+    Kn = torch.ones(1, 1, 128, device=dev)
+    Kn[0, 0, 7] = float("inf")
+    gc.encode(Kn, torch.ones(1, 1, 128, device=dev), torch.tensor([int(slots[0])], device=dev), st)
+    torch.cuda.synchronize()
+    assert st.item() & tq.FLAG_NONFINITE
+    # decode on the oracle's cache: the empty sequence gives zeros
+    q = torch.from_numpy(W.queries(w, 0)).to(dev, torch.bfloat16)
+    go = tq.OctopusCache(nb, 1, 3, 4, 0, pool=torch.from_numpy(pool_o).to(dev))
+    st.zero_()
+    out = go.decode(q, torch.from_numpy(bt).to(dev), torch.tensor(w.lens, dtype=torch.int32, device=dev),
+                    status=st).cpu().numpy()
+    ref, _ = oc.decode(pool_o, q.float().cpu().numpy().astype(np.float64), bt, np.array(w.lens), W.sm_scale(w))
+    assert st.item() == 0
+    assert np.all(out[1] == 0)
+    assert parity.rel_err(out[[0, 2]], ref[[0, 2]]) <= parity.DECODE_RTOL
+
+
+def test_ring_one_page_window(tq, oracle):
+    """A ring of 16 slots (one block), overwritten every 16 steps."""
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(16, 16), hkv=2, hq=16)
+    results = parity.run_ring_stream(w, oracle, tq, 16, (3, 16), 40, {0, 12, 13, 29, 39})
+    for r in results:
+        parity.assert_encode_parity(r)
+        assert r["dec"]["rel_err"] <= parity.DECODE_RTOL
+        assert r["dec"]["same_as_plain_decode"]
+
+
+def test_prefill_and_ring_argument_checks(tq):
+    import torch
+    c = tq.Cache(4, 2)
+    q = torch.zeros((8, 16, 128), dtype=torch.bfloat16, device="cuda")
+    row = torch.arange(4, dtype=torch.int32, device="cuda")
+    with pytest.raises(tq.TQError) as e:
+        c.prefill(q, row, 60)                  # positions 60 .. 67 do not fit 4 blocks
+    assert e.value.status == tq.TQ_ERR_INVALID_ARG
+    z = torch.zeros((1, 2, 128), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    lens = torch.ones(1, dtype=torch.int32, device="cuda")
+    for window in (0, 24, 80):                 # not a positive multiple of 16, or past the table
+        with pytest.raises(tq.TQError) as e:
+            c.decode_append(z, z, q[:1], bt, lens, window=window)
+        assert e.value.status == tq.TQ_ERR_INVALID_ARG
