@@ -180,11 +180,11 @@ TQ_API void tq_cache_free(tq_cache* cache);
  * n^_i the unit direction of the stored level pair; values and the inverse
  * rotation as for the main codec.
  * tq_encode_kv, tq_decode_attention and tq_decode_workspace_bytes accept such
- * a cache (its decode runs on CUDA cores, one partial per warp merged by a
- * second kernel); the one-launch append entry points return
- * TQ_ERR_UNSUPPORTED.  Supported: d = 128, block_size = 16, bits 2..4,
- * value_bits 1..8.  The library allocates its codebooks and direction table
- * in device memory. */
+ * a cache (its decode runs on CUDA cores: the warps' partials are merged
+ * inside each CTA, the CTAs' by a second kernel); the one-launch append
+ * entry points return TQ_ERR_UNSUPPORTED.  Supported: d = 128, block_size =
+ * 16, bits 2..4, value_bits 1..8.  The library allocates its codebooks and
+ * direction table in device memory. */
 TQ_API tq_status tq_cache_create_octopus(void* pool, int64_t num_blocks, int block_size, int num_kv_heads,
                                          int d, int bits, int value_bits, uint64_t seed, tq_cache** out);
 

@@ -12,7 +12,8 @@ Data recipe (numpy PCG64, data seed 1234, independent of the method seed):
     channels {7, 33, 90, 121} and gives values none);
   - "per-token lognormal(0, 0.25)": one factor exp(N(0, 0.25^2)) per token
     position, shared by all heads of that token, drawn separately for K and V;
-  - bf16 workloads round the float32 values to bfloat16 (nearest, ties to even);
+  - bf16 and f16 workloads round the float32 values to that type (nearest,
+    ties to even);
   - queries are N(0, 1) in the workload dtype;
   - block tables hand each sequence blocks from a seeded random permutation of
     the pool (the tiny workload uses blocks in order).
@@ -40,7 +41,7 @@ class Workload:
     qjl_m: int
     block_size: int
     lens: tuple          # tokens per sequence before the decode steps
-    dtype: str           # "f32" or "bf16"
+    dtype: str           # "f32", "bf16" or "f16"
     seed: int            # method seed (rotation signs, QJL matrix)
     prefill_chunk: int   # tokens per encode call during prefill
     decode_steps: int    # decode steps after prefill, each appending `append` tokens per sequence
@@ -148,9 +149,17 @@ def kv_tokens(w: Workload, tensor: int, seq: int, t0: int, t1: int) -> np.ndarra
             x *= np.exp(rng.normal(0.0, 0.25, size=(CHUNK, 1, 1))).astype(np.float32)
         lo, hi = max(t0, c * CHUNK), min(t1, (c + 1) * CHUNK)
         out[lo - t0:hi - t0] = x[lo - c * CHUNK:hi - c * CHUNK]
+    return to_dtype(w, out)
+
+
+def to_dtype(w: Workload, x: np.ndarray) -> np.ndarray:
+    """The float32 values a workload of dtype w.dtype carries (bf16 or fp16
+    rounded to nearest even, f32 unchanged)."""
     if w.dtype == "bf16":
-        out = bf16_round(out)
-    return out
+        return bf16_round(x)
+    if w.dtype == "f16":
+        return x.astype(np.float16).astype(np.float32)
+    return x
 
 
 def kv_step(w: Workload, tensor: int, t0: int, t1: int) -> np.ndarray:
@@ -162,7 +171,7 @@ def queries(w: Workload, step: int) -> np.ndarray:
     """Decode query of step `step` for every sequence: float32 [batch, hq, d]."""
     rng = _gen(w.wid, 2, step)
     q = rng.standard_normal((w.batch, w.hq, w.d), dtype=np.float32)
-    return bf16_round(q) if w.dtype == "bf16" else q
+    return to_dtype(w, q)
 
 
 def block_table(w: Workload) -> np.ndarray:

@@ -102,7 +102,7 @@ def run_case(w, oracle, tq, q_step: int = 0, decode_gpu_pool: bool = True, decod
     import torch
 
     dev = torch.device("cuda")
-    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    tdt = {"f32": torch.float32, "f16": torch.float16}.get(w.dtype, torch.bfloat16)
     bt = W.block_table(w)
     nb = w.num_blocks()
     K, V = _inputs(w)
@@ -235,7 +235,7 @@ def run_append_case(w, oracle, tq, q_step: int = 0) -> dict:
     import torch
 
     dev = torch.device("cuda")
-    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    tdt = {"f32": torch.float32, "f16": torch.float16}.get(w.dtype, torch.bfloat16)
     bt = W.block_table(w)
     nb = w.num_blocks()
     K, V = _inputs(w)
@@ -328,7 +328,7 @@ def run_ring_stream(w, oracle, tq, window: int, t0s, steps: int, checks) -> list
     import torch
 
     dev = torch.device("cuda")
-    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    tdt = {"f32": torch.float32, "f16": torch.float16}.get(w.dtype, torch.bfloat16)
     bt = W.block_table(w)
     nb = w.num_blocks()
     B = w.batch
@@ -412,7 +412,7 @@ def run_octopus_case(w, oracle, tq, q_step: int = 0) -> dict:
     import torch
 
     dev = torch.device("cuda")
-    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    tdt = {"f32": torch.float32, "f16": torch.float16}.get(w.dtype, torch.bfloat16)
     bt = W.block_table(w)
     nb = w.num_blocks()
     K, V = _inputs(w)
