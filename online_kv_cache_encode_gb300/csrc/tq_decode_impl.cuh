@@ -1022,13 +1022,22 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             const float gr = lds_h2f(pg + F::gam + 2 * tr), gr8 = lds_h2f(pg + F::gam + 2 * (tr + 8));
             float s0 = t0 * gr, s1 = t1 * gr, s2 = t2 * gr8, s3 = t3 * gr8;
             const int tok = (p0 + warp + NW * j) * kBlockSize;
-            if (!pok || tok + kBlockSize > len) {  // the sequence's last page or a skipped one (warp-uniform)
-                if (!(pok && tok + tr < len)) s0 = s1 = -INFINITY;
-                if (!(pok && tok + tr + 8 < len)) s2 = s3 = -INFINITY;
+            // the sequence's last page or a skipped one (warp-uniform): rows past
+            // the end get no weight, and the scale and zero of their slots (never
+            // written: any bytes, NaN included) are replaced by 0
+            const bool tail = !pok || tok + kBlockSize > len;
+            const bool v0 = pok && tok + tr < len, v8 = pok && tok + tr + 8 < len;
+            if (tail) {
+                if (!v0) s0 = s1 = -INFINITY;
+                if (!v8) s2 = s3 = -INFINITY;
             }
 
             // ---------- online softmax; the max moves only when a score beats it by kLazy ----------
-            const float sr = lds_h2f(pg + F::scl + 2 * tr), sr8 = lds_h2f(pg + F::scl + 2 * (tr + 8));
+            float sr = lds_h2f(pg + F::scl + 2 * tr), sr8 = lds_h2f(pg + F::scl + 2 * (tr + 8));
+            if (tail) {
+                sr = v0 ? sr : 0.f;
+                sr8 = v8 ? sr8 : 0.f;
+            }
             float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
             constexpr float kWScale = (float)(1 << value_wshift<VB>());
             const bool exact = fmaxf(sr, sr8) > kBigScale / kWScale;
@@ -1050,7 +1059,11 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 m1 = n1;
             }
             const float p0v = ex2(s0 - m0), p1v = ex2(s1 - m1), p2v = ex2(s2 - m0), p3v = ex2(s3 - m1);
-            const float zr = lds_h2f(pg + F::zer + 2 * tr), zr8 = lds_h2f(pg + F::zer + 2 * (tr + 8));
+            float zr = lds_h2f(pg + F::zer + 2 * tr), zr8 = lds_h2f(pg + F::zer + 2 * (tr + 8));
+            if (tail) {
+                zr = v0 ? zr : 0.f;
+                zr8 = v8 ? zr8 : 0.f;
+            }
             l0 += p0v + p2v;
             l1 += p1v + p3v;
 

@@ -657,21 +657,7 @@ TQ_API tq_status tq_encode_kv(const tq_cache* c, const void* K, const void* V, t
 // splits (8 pages or more each) and four times the count that fills the SMs.
 static void decode_split_plan(const tq_cache* c, int batch, int max_blocks, int* splits, int* pps) {
     const int64_t units = (int64_t)batch * c->g.hkv;
-    if (c->octopus) {
-        // the OCTOPUS decode keeps ~35 KB of shared memory per CTA, so several
-        // CTAs share an SM: aim at four per SM to hide the page loads, with at
-        // least four pages per split
-        const int64_t sms = c->num_sms > 0 ? c->num_sms : 1;
-        int64_t s = (4 * sms + units - 1) / units;
-        const int64_t cap = (max_blocks + 3) / 4;
-        if (s > cap) s = cap;
-        if (s < 1) s = 1;
-        int p = (int)((max_blocks + s - 1) / s);
-        *pps = p;
-        *splits = (max_blocks + p - 1) / p;
-        return;
-    }
-    const int nw = (c->g.m || c->octopus) ? 8 : 12;
+    const int nw = c->g.m ? 8 : 12;  // warps per CTA (the OCTOPUS decode has 12 too)
     const int64_t sms = c->num_sms > 0 ? c->num_sms : 1;
     int64_t lim = 4 * ((sms + units - 1) / units);
     const int64_t cap = (max_blocks + 7) / 8;

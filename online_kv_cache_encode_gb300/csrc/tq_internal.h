@@ -136,7 +136,6 @@ constexpr int kOctWarps = 8;
 
 int launch_oct_encode(const OctArgs& a, int num_sms, void* stream);
 int launch_oct_decode(const OctArgs& a, void* stream);
-int oct_decode_smem_bytes(const OctArgs& a);
 
 // Launchers (return a cudaError_t as int).  The per-key-width ones are
 // explicitly instantiated, one key width per translation unit.

@@ -12,14 +12,17 @@
 //  Parametrization ..." -- key contribution "Octahedral triplet direction
 //  quantizer with norm marginals", methodology steps 1-7, bit split (b+1, b-1)]
 //
-// Decode never builds K^: for token t the logit is gamma_t times the sum over
-// triplets of rho^_i <q_rot[3i..3i+2], n^_i>, with n^ from a table of the
-// level pairs' unit directions (methodology step 7); values accumulate in the
-// rotated frame and one inverse rotation is applied per output.  Each CTA
-// warp keeps an online softmax over its pages and writes its partial; a
-// second kernel merges the partials of a sequence.
+// Decode never builds K^ in global memory: for token t the logit is gamma_t
+// times the sum over triplets of rho^_i <q_rot[3i..3i+2], n^_i>, with n^ from
+// a table of the level pairs' unit directions (methodology step 7).  Each
+// warp rebuilds rho^ n^ of one page in shared memory and scores it on the
+// tensor cores; values accumulate in the rotated frame and one inverse
+// rotation is applied per output.  The warps of a CTA merge in shared memory
+// and write one partial per query; a second kernel merges the partials of a
+// sequence.
 #include <cuda_runtime.h>
 
+#include "tq_decode_impl.cuh"  // the main codec's MMA, value-code and page-ring helpers
 #include "tq_device.cuh"
 
 namespace tq {
@@ -30,15 +33,6 @@ constexpr float kOctMinus = -1.0e30f;
 
 __device__ __forceinline__ uint32_t oct_signs(const uint32_t (&sb)[kHeadDim / 32], int lane) {
     return (sb[lane >> 3] >> (4 * (lane & 7))) & 0xFu;
-}
-
-// bits [pos, pos + n) of a little-endian word array, 1 <= n <= 32; the next
-// word is read only when the field reaches into it
-__device__ __forceinline__ uint32_t oct_bits(const uint32_t* w, int pos, int n) {
-    const int wi = pos >> 5, sh = pos & 31;
-    uint32_t x = w[wi] >> sh;
-    if (sh + n > 32) x |= w[wi + 1] << (32 - sh);
-    return (n == 32) ? x : (x & ((1u << n) - 1u));
 }
 
 // ---------------------------------------------------------------------------
@@ -195,213 +189,417 @@ __global__ void __launch_bounds__(kOctWarps * 32) oct_encode_kernel(const OctArg
 }
 
 // ---------------------------------------------------------------------------
-// decode: grid (split, KV head, sequence), kOctWarps warps; warp w takes pages
-// p0 + w, p0 + w + kOctWarps, ... of the split.  Shared memory: the direction
-// table, the norm levels, the rotated queries and one page per warp.
+// decode: grid (split, KV head, sequence), kOctDecWarps warps, one CTA per SM.
+// Warp w takes pages p0 + w, p0 + w + NW, ... of the split and streams them
+// into its own ring slots with bulk async copies completing on mbarriers.  Per
+// page the warp
+//  - rebuilds the rotated unit keys rho^ n^ of its 16 tokens into shared
+//    memory (fp32, times kOctUScale), one triplet per lane at a time; the
+//    levels come from registers by shuffles and the direction is decoded
+//    from them (a random lookup in a shared-memory direction table cost
+//    several bank wavefronts per warp and made the rebuild
+//    shared-memory-bound);
+//  - scores them against the group's queries on the tensor cores
+//    (mma.sync m16n8k16, tokens as rows, queries as the n8 side): the keys
+//    and the queries are each split into fp16 hi + lo, and the three products
+//    hi.hi + hi.lo + lo.hi are accumulated in fp32;
+//  - keeps the online softmax and accumulates the min-max values exactly as
+//    the main codec's decode does (value codes as exact fp16 subnormals, the
+//    zero-point term and the weight rounding kept in fp32).
+// The warps merge in shared memory and each CTA writes one partial per query;
+// oct_combine_kernel merges the splits and rotates back.
 // ---------------------------------------------------------------------------
-struct OctSmem {
-    int dir, crho, q, pages, u, total;
+constexpr int kOctDecWarps = 12;
+constexpr int kOctMaxSlots = 3;                 // ring slots per warp (fewer if the pages are large)
+constexpr int kOctUStride = kHeadDim + 8;       // floats per rebuilt row: consecutive rows 8 banks apart
+constexpr float kOctUScale = 64.f;              // |rho^ n^| <= 1: rebuilt keys are taken times 64
+
+// Page of an OCTOPUS cache: 16 key rows of KR bytes, then the value rows,
+// gamma, scale and zero, padded to 16 bytes.
+template <int B, int VB>
+struct OctPage {
+    static constexpr int KR = 4 * ((kOctTri * (3 * B + 1) + 31) / 32);
+    static constexpr int vcode = kBlockSize * KR;
+    static constexpr int gam = vcode + kBlockSize * kHeadDim * VB / 8;
+    static constexpr int scl = gam + 2 * kBlockSize;
+    static constexpr int zer = scl + 2 * kBlockSize;
+    static constexpr int bytes = (zer + 2 * kBlockSize + 15) / 16 * 16;
 };
-constexpr int kOctHalf = kBlockSize / 2;  // tokens whose directions are rebuilt at a time
-// a rebuilt direction row keeps each 32-dim part 4 floats apart from the next,
-// so that the four parts read at once fall in different banks
-constexpr int kOctURow = 4 * 36;
-__host__ __device__ constexpr int oct_upos(int c) { return c + 4 * (c >> 5); }
-// After the page loop the whole area holds the warps' partials for the in-CTA
-// merge: [kOctWarps][8 queries][4 + d] floats.
-constexpr int kOctMergeBytes = kOctWarps * 8 * (4 + kHeadDim) * 4;
-__host__ __device__ inline OctSmem oct_smem(int nxi, int page_bytes) {
+
+// Shared memory of the decode kernel (byte offsets).  After the page loop the
+// rebuilt-key area holds the warps' states for the in-CTA merge:
+// [NW][8 queries][4 + d] floats (max, sum, zero term, pad, acc).
+struct OctSmem {
+    int q, qsc, bars, ok, u, pages, slot, spw, total;
+};
+template <int B, int VB>
+__host__ __device__ constexpr OctSmem oct_dec_smem() {
     OctSmem L{};
     int off = 0;
-    L.dir = off; off += nxi * nxi * 16;
-    L.crho = off; off += 8 * 4;
     L.q = off; off += 8 * (kHeadDim + 4) * 4;
-    L.pages = off; off += kOctWarps * ((page_bytes + 15) / 16 * 16);
-    L.u = off; off += kOctWarps * kOctHalf * kOctURow * 4;
-    L.total = off > kOctMergeBytes ? off : kOctMergeBytes;
+    L.qsc = off; off += 8 * 4;
+    L.bars = off; off += kOctDecWarps * kOctMaxSlots * 8;
+    L.ok = off; off += kOctDecWarps * kOctMaxSlots * 4;
+    off = (off + 15) / 16 * 16;
+    L.u = off; off += kOctDecWarps * kBlockSize * kOctUStride * 4;
+    L.slot = OctPage<B, VB>::bytes;
+    L.pages = off;
+    int spw = kOctMaxSlots;
+    while (spw > 1 && off + kOctDecWarps * spw * L.slot > kSmemLimit) --spw;
+    L.spw = spw;
+    off += kOctDecWarps * spw * L.slot;
+    L.total = off;
     return L;
+}
+static_assert(kOctDecWarps * 8 * (4 + kHeadDim) * 4 <= kOctDecWarps * kBlockSize * kOctUStride * 4,
+              "the merge states must fit over the rebuilt keys");
+
+// fp16 hi + lo of a pair of floats: hi = rn(x), lo = rn(x - hi)
+__device__ __forceinline__ void split_h2(float2 x, uint32_t& hi, uint32_t& lo) {
+    hi = pack_h2(x.x, x.y);
+    const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    lo = pack_h2(x.x - h.x, x.y - h.y);
 }
 
 template <int B, int VB>
-__global__ void __launch_bounds__(kOctWarps * 32, 2) oct_decode_kernel(const OctArgs a) {
-    constexpr int NXI = 1 << (B + 1), FB = 3 * B + 1, D = kHeadDim, QS = D + 4;
-    constexpr int VROW = D * VB / 8;
-    extern __shared__ __align__(16) uint8_t sm[];
+__global__ void __launch_bounds__(kOctDecWarps * 32, 1) oct_decode_kernel(const OctArgs a) {
+    using P = OctPage<B, VB>;
+    constexpr OctSmem LY = oct_dec_smem<B, VB>();
+    constexpr int NW = kOctDecWarps, SPW = LY.spw;
+    constexpr int NXI = 1 << (B + 1), FB = 3 * B + 1, D = kHeadDim, QS = D + 4, US = kOctUStride;
+    constexpr uint32_t kFMask = (1u << FB) - 1u;
+    static_assert((kBlockSize - 1) * P::KR + ((kOctTri - 1) * FB / 32) * 4 + 8 <= P::bytes,
+                  "the two words of every key field lie inside the page");
+    static_assert(LY.total <= kSmemLimit, "OCTOPUS decode does not fit in shared memory");
+    extern __shared__ __align__(128) uint8_t sm[];
     const Geometry& g = a.g;
-    const OctSmem L = oct_smem(NXI, (int)g.page_bytes);
-    float4* s_dir = reinterpret_cast<float4*>(sm + L.dir);
-    float* s_crho = reinterpret_cast<float*>(sm + L.crho);
-    float* s_q = reinterpret_cast<float*>(sm + L.q);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = a.group;
-    uint8_t* s_page = sm + L.pages + warp * (int)((g.page_bytes + 15) / 16 * 16);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    for (int i = threadIdx.x; i < NXI * NXI; i += blockDim.x) {
-        const float* d4 = a.tab->dir[(i / NXI) * kOctMaxDir + i % NXI];
-        s_dir[i] = make_float4(d4[0], d4[1], d4[2], 0.f);
-    }
-    if (threadIdx.x < 8) s_crho[threadIdx.x] = a.tab->crho[threadIdx.x];
-    if (warp < G) {
-        // rotated query, times sm_scale log2(e); coordinate 128 (the padded
-        // triplet's third) is zero
-        float x[4];
-        load4(a.q, a.dtype, ((int64_t)b * a.hq + (int64_t)h * G + warp) * D + 4 * lane, x);
-        apply_signs(x, oct_signs(a.sign_bits, lane));
-        fwht128(x, lane);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s_q[warp * QS + 4 * lane + i] = x[i] * 0.08838834764831845f * a.sm_scale_log2;
-        if (lane < 4) s_q[warp * QS + D + lane] = 0.f;
-    }
-    __syncthreads();
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t bar_w = sbase + LY.bars + 8 * warp * kOctMaxSlots;
+    const uint32_t ring_w = sbase + LY.pages + warp * SPW * LY.slot;
+    int* slot_ok = reinterpret_cast<int*>(sm + LY.ok) + warp * kOctMaxSlots;
+    float* s_q = reinterpret_cast<float*>(sm + LY.q);
+    float* s_qsc = reinterpret_cast<float*>(sm + LY.qsc);
+    float* s_u = reinterpret_cast<float*>(sm + LY.u) + warp * kBlockSize * US;
 
+    if (lane == 0) {
+        for (int k = 0; k < SPW; ++k) mbar_init(bar_w + 8 * k, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    // ---- length, this warp's block ids (lane l: the warp's page l of the
+    // current batch of 32, and of the next batch) ----
     int len = __ldg(a.lens + b);
+    if (len < 0) len = 0;
     if (len > a.max_blocks * kBlockSize) {
-        if (threadIdx.x == 0) flag(a.status, TQ_FLAG_BAD_SLOT);
+        if (tid == 0) flag(a.status, TQ_FLAG_BAD_SLOT);
         len = a.max_blocks * kBlockSize;
     }
-    if (len < 0) len = 0;
     const int p0 = split * a.pages_per_split;
-    int pend = (len + kBlockSize - 1) / kBlockSize;
-    if (pend > p0 + a.pages_per_split) pend = p0 + a.pages_per_split;
+    int npages = (len + kBlockSize - 1) / kBlockSize - p0;
+    if (npages > a.pages_per_split) npages = a.pages_per_split;
+    if (npages < 0) npages = 0;
+    const int nmine = npages > warp ? (npages - warp + NW - 1) / NW : 0;
+    const int32_t* btw = a.block_table + (int64_t)b * a.bt_stride + p0 + warp;
+    const int reach = min(a.pages_per_split, a.max_blocks - p0) - warp;
+    int bid_cur = (NW * lane < reach) ? __ldg(btw + NW * lane) : -1;
+    int bid_nxt = (NW * (32 + lane) < reach) ? __ldg(btw + NW * (32 + lane)) : -1;
 
-    // Scores: lane (query g = lane / 4, part = lane % 4) keeps dims 32 part ..
-    // 32 part + 31 of its rotated query in registers and dots them with the
-    // page's rebuilt rotated key directions; a query's 4 lanes then sum their
-    // parts.  Softmax state per query lives in its lanes.  Values: lane l
-    // accumulates dims 4l .. 4l+3 of every query.
-    const int gq = lane >> 2, part = lane & 3;
-    float qreg[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) qreg[c] = (gq < G) ? s_q[gq * QS + 32 * part + c] : 0.f;
-    float* s_u = reinterpret_cast<float*>(sm + L.u) + warp * kOctHalf * kOctURow;
-    float m_g = kOctMinus, l_g = 0.f;
-    float acc[8][4];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-    for (int pi = p0 + warp; pi < pend; pi += kOctWarps) {
-        const int blk = __ldg(a.block_table + (int64_t)b * a.bt_stride + pi);
-        if (blk < 0 || blk >= g.num_blocks) {
-            if (lane == 0) flag(a.status, TQ_FLAG_BAD_SLOT);
-            continue;
+    // Start a page copy into ring slot `slot`; a bad block id arrives on the
+    // barrier without data and the page is skipped.
+    auto issue = [&](int slot, int blk) {
+        const bool ok = blk >= 0 && blk < g.num_blocks;
+        const uint32_t bar = bar_w + 8 * slot;
+        slot_ok[slot] = ok;
+        if (ok) {
+            mbar_arrive_tx(bar, (uint32_t)P::bytes);
+            bulk_g2s(ring_w + slot * LY.slot, a.pool + ((int64_t)blk * g.hkv + h) * P::bytes, (uint32_t)P::bytes, bar);
+        } else {
+            flag(a.status, TQ_FLAG_BAD_SLOT);
+            mbar_arrive(bar);
         }
-        const uint4* src = reinterpret_cast<const uint4*>(a.pool + ((int64_t)blk * g.hkv + h) * g.page_bytes);
-        for (int k = lane; k < (int)(g.page_bytes / 16); k += 32) reinterpret_cast<uint4*>(s_page)[k] = __ldg(src + k);
-        __syncwarp();
-        float sc[kBlockSize];
+    };
+    __syncwarp();
+    if (lane < SPW && lane < nmine) issue(lane, bid_cur);
+
+    // ---- levels (lane l holds xi / eta level l and norm level l mod 8), and
+    // the rotated queries times sm_scale log2(e) / qscale ----
+    const float cx_l = a.tab->cxi[lane & (NXI - 1)];
+    const float cr_l = a.tab->crho[lane & ((1 << (B - 1)) - 1)] * kOctUScale;
+    if (warp < 8) {
+        // qscale: a power of two putting max |x| / qscale in (256, 512]
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (warp < G) {
+            load4(a.q, a.dtype, ((int64_t)b * a.hq + (int64_t)h * G + warp) * D + 4 * lane, x);
+            apply_signs(x, oct_signs(a.sign_bits, lane));
+            fwht128(x, lane);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            // rebuild u^ = rho^ n^ of tokens 8 hf .. 8 hf + 7 (all 43 triplets)
-            for (int j = lane; j < kOctHalf * kOctTri; j += 32) {
-                const int t = j / kOctTri, i = j - t * kOctTri;
-                const uint32_t* row = reinterpret_cast<const uint32_t*>(s_page + (kOctHalf * hf + t) * a.key_row);
-                const uint32_t f = oct_bits(row, i * FB, FB);
-                const int ia = f & (NXI - 1), ie = (f >> (B + 1)) & (NXI - 1), ir = f >> (2 * (B + 1));
-                const float4 d4 = s_dir[ia * NXI + ie];
-                const float r = s_crho[ir];
-                float* u = s_u + t * kOctURow;
-                u[oct_upos(3 * i)] = r * d4.x;
-                u[oct_upos(3 * i + 1)] = r * d4.y;
-                if (3 * i + 2 < D) u[oct_upos(3 * i + 2)] = r * d4.z;
-            }
-            __syncwarp();
-#pragma unroll
-            for (int t = 0; t < kOctHalf; ++t) {
-                const float4* u4 = reinterpret_cast<const float4*>(s_u + t * kOctURow + 36 * part);
-                float x = 0.f;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float4 v = u4[c];
-                    x = fmaf(v.x, qreg[4 * c], fmaf(v.y, qreg[4 * c + 1], fmaf(v.z, qreg[4 * c + 2], fmaf(v.w, qreg[4 * c + 3], x))));
-                }
-                x += __shfl_xor_sync(0xffffffffu, x, 1);
-                x += __shfl_xor_sync(0xffffffffu, x, 2);
-                sc[kOctHalf * hf + t] = x;
-            }
-            __syncwarp();  // s_u is rebuilt for the second half
+            for (int i = 0; i < 4; ++i) x[i] *= 0.08838834764831845f * a.sm_scale_log2;
         }
-        // ---- online softmax, query gq's state in its four lanes ----
-        float mx = kOctMinus;
+        const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+        const float scl = (mx > 0.f) ? exp2f(ceilf(log2f(mx / 512.f))) : 1.f;
+        const float inv = 1.f / scl;
 #pragma unroll
-        for (int t = 0; t < kBlockSize; ++t) {
-            const float gam = __half2float(*reinterpret_cast<const __half*>(s_page + g.gam_off + 2 * t));
-            const bool valid = pi * kBlockSize + t < len;
-            sc[t] = valid ? sc[t] * gam : -INFINITY;
-            mx = fmaxf(mx, sc[t]);
-        }
-        float fct = 1.f;
-        if (mx > m_g) {
-            fct = exp2f(m_g - mx);
-            l_g *= fct;
-            m_g = mx;
-        }
-        // weights to shared memory (over the rebuilt directions, no longer
-        // needed): p[t][query]; a query's part-0 lane writes them
-#pragma unroll
-        for (int t = 0; t < kBlockSize; ++t) {
-            sc[t] = exp2f(sc[t] - m_g);  // -inf gives 0
-            l_g += sc[t];
-            if (part == 0) s_u[t * 8 + gq] = sc[t];
-        }
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (q >= G) continue;
-            const float f = __shfl_sync(0xffffffffu, fct, 4 * q);
-            acc[q][0] *= f; acc[q][1] *= f; acc[q][2] *= f; acc[q][3] *= f;
-        }
-        // ---- values: lane holds dims 4 lane .. 4 lane + 3 ----
-        for (int t = 0; t < kBlockSize; ++t) {
-            const uint32_t* vr = reinterpret_cast<const uint32_t*>(s_page + g.vcode_off + t * VROW);
-            const uint32_t cw = oct_bits(vr, 4 * lane * VB, 4 * VB);
-            const float scl = __half2float(*reinterpret_cast<const __half*>(s_page + g.scl_off + 2 * t));
-            const float zer = __half2float(*reinterpret_cast<const __half*>(s_page + g.zer_off + 2 * t));
-            float vv[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) vv[k] = fmaf(scl, (float)((cw >> (VB * k)) & ((1u << VB) - 1u)), zer);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                if (q >= G) continue;
-                const float pt = s_u[t * 8 + q];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) acc[q][k] = fmaf(pt, vv[k], acc[q][k]);
-            }
-        }
-        __syncwarp();  // the page buffer is refilled next
-    }
-    float m[8], l[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        m[q] = __shfl_sync(0xffffffffu, m_g, 4 * q);
-        l[q] = __shfl_sync(0xffffffffu, l_g, 4 * q);
-    }
-    // ---- merge the warps in shared memory; warp q writes the CTA's partial
-    // for query q: (max, sum, 2 pad, acc[128]) ----
-    __syncthreads();  // every warp is past its pages: the area is free
-    float* wst = reinterpret_cast<float*>(sm);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        if (q >= G) continue;
-        float* pq = wst + (warp * 8 + q) * (4 + D);
-        if (lane == 0) {
-            pq[0] = m[q];
-            pq[1] = l[q];
-        }
-        *reinterpret_cast<float4*>(pq + 4 + 4 * lane) = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
+        for (int i = 0; i < 4; ++i) s_q[warp * QS + 4 * lane + i] = x[i] * inv;
+        if (lane == 0) s_qsc[warp] = scl / kOctUScale;
     }
     __syncthreads();
+
+    // lane (r, qd): r = token row / query of the B operand, qd = quad index
+    const int r = lane >> 2, qd = lane & 3;
+    uint32_t QH[8][2], QL[8][2];  // query r, dims 16 ks + 2 qd + {0, 1} and + {8, 9}, fp16 hi + lo
+    {
+        const float* qr = s_q + r * QS + 2 * qd;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            split_h2(*reinterpret_cast<const float2*>(qr + 16 * ks), QH[ks][0], QL[ks][0]);
+            split_h2(*reinterpret_cast<const float2*>(qr + 16 * ks + 8), QH[ks][1], QL[ks][1]);
+        }
+    }
+    const float qs0 = s_qsc[2 * qd], qs1 = s_qsc[2 * qd + 1];
+    // Score row r holds token tr = r ^ ((r >> 1) & 1) (and row r + 8 token
+    // tr + 8), so that the value loads (tokens of rows 2qd, 2qd+1) alternate
+    // between the two halves of the bank space.
+    const int tr = r ^ ((r >> 1) & 1);
+    const int ta = (2 * qd) ^ (qd & 1), tb = (2 * qd + 1) ^ (qd & 1);
+    const float* ua = s_u + tr * US + 2 * qd;  // A rows: token tr, then tr + 8
+    const float* ub = ua + 8 * US;
+
+    float m0 = kMinusBig, m1 = kMinusBig, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+    bool timed_out = false;
+    int slot = 0;
+    uint32_t phase = 0;
+    int issued = min(SPW, nmine);
+    int jfail = nmine;
+    for (int j = 0; j < nmine; ++j) {
+        if (!mbar_wait(bar_w + 8 * slot, phase)) {
+            timed_out = true;
+            jfail = j;
+            break;
+        }
+        const uint32_t pg = ring_w + slot * LY.slot;
+        const bool pok = slot_ok[slot] != 0;
+
+        // ---------- rebuild u^ = rho^ n^ (times kOctUScale) of the 16 tokens ----------
+        // Triplet i = lane of every token (its field sits at the same bits of
+        // every key row), then the 11 x 16 triplets 32..42 spread over the lanes.
+        // A field is cut from two consecutive words of its row; the second may
+        // lie past the row but always inside the page.
+        {
+            // rho^ n^ of field f: the octahedron point (xi, eta, 1 - |xi| - |eta|),
+            // folded into the lower half-space when that is negative, normalised
+            // (the direction of the level pair, as the library's table has it)
+            auto rebuild = [&](uint32_t f, float& x, float& y, float& z) {
+                const float xi = __shfl_sync(0xffffffffu, cx_l, (int)(f & (NXI - 1)));
+                const float eta = __shfl_sync(0xffffffffu, cx_l, (int)((f >> (B + 1)) & (NXI - 1)));
+                const float rr = __shfl_sync(0xffffffffu, cr_l, (int)(f >> (2 * (B + 1))));
+                z = 1.f - fabsf(xi) - fabsf(eta);
+                const bool fold = z < 0.f;
+                x = fold ? copysignf(1.f - fabsf(eta), xi) : xi;
+                y = fold ? copysignf(1.f - fabsf(xi), eta) : eta;
+                const float sc = rr * rsqrtf(fmaf(x, x, fmaf(y, y, z * z)));
+                x *= sc;
+                y *= sc;
+                z *= sc;
+            };
+            const uint32_t kw = pg + ((lane * FB) >> 5) * 4;
+            const int ksh = (lane * FB) & 31;
+#pragma unroll 8
+            for (int t = 0; t < kBlockSize; ++t) {
+                const uint32_t f = __funnelshift_r(lds32(kw + t * P::KR), lds32(kw + t * P::KR + 4), ksh) & kFMask;
+                float x, y, z;
+                rebuild(f, x, y, z);
+                float* u = s_u + t * US + 3 * lane;
+                u[0] = x;
+                u[1] = y;
+                u[2] = z;
+            }
+            constexpr int kRest = kBlockSize * (kOctTri - 32);
+#pragma unroll
+            for (int n = 0; n < (kRest + 31) / 32; ++n) {
+                const int k = lane + 32 * n;
+                const bool act = k < kRest;  // every lane takes part in the shuffles
+                const int t = act ? k / (kOctTri - 32) : 0, i = act ? 32 + k - (kOctTri - 32) * t : 32;
+                const uint32_t w = pg + t * P::KR + ((i * FB) >> 5) * 4;
+                const uint32_t f = __funnelshift_r(lds32(w), lds32(w + 4), (i * FB) & 31) & kFMask;
+                float x, y, z;
+                rebuild(f, x, y, z);
+                if (act) {
+                    float* u = s_u + t * US + 3 * i;
+                    u[0] = x;
+                    u[1] = y;
+                    if (i < kOctTri - 1) u[2] = z;
+                }
+            }
+        }
+        __syncwarp();
+
+        // ---------- scores: 3 products per k-step on four accumulator chains ----------
+        float I0[4], I1[4], J0[4], J1[4];  // hi.hi (even / odd k-steps), hi.lo + lo.hi (even / odd)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t h0, h1, h2, h3, o0, o1, o2, o3;
+            split_h2(*reinterpret_cast<const float2*>(ua + 16 * ks), h0, o0);
+            split_h2(*reinterpret_cast<const float2*>(ub + 16 * ks), h1, o1);
+            split_h2(*reinterpret_cast<const float2*>(ua + 16 * ks + 8), h2, o2);
+            split_h2(*reinterpret_cast<const float2*>(ub + 16 * ks + 8), h3, o3);
+            float* I = (ks & 1) ? I1 : I0;
+            float* J = (ks & 1) ? J1 : J0;
+            if (ks < 2) {
+                mma16816_c(I, h0, h1, h2, h3, QH[ks][0], QH[ks][1], 0.f, 0.f, 0.f, 0.f);
+                mma16816_c(J, h0, h1, h2, h3, QL[ks][0], QL[ks][1], 0.f, 0.f, 0.f, 0.f);
+            } else {
+                mma16816(I, h0, h1, h2, h3, QH[ks][0], QH[ks][1]);
+                mma16816(J, h0, h1, h2, h3, QL[ks][0], QL[ks][1]);
+            }
+            mma16816(J, o0, o1, o2, o3, QH[ks][0], QH[ks][1]);
+        }
+        const float gr = lds_h2f(pg + P::gam + 2 * tr), gr8 = lds_h2f(pg + P::gam + 2 * (tr + 8));
+        float s0 = ((I0[0] + I1[0]) + (J0[0] + J1[0])) * qs0 * gr, s1 = ((I0[1] + I1[1]) + (J0[1] + J1[1])) * qs1 * gr;
+        float s2 = ((I0[2] + I1[2]) + (J0[2] + J1[2])) * qs0 * gr8, s3 = ((I0[3] + I1[3]) + (J0[3] + J1[3])) * qs1 * gr8;
+        float sr, sr8, zr, zr8;
+        const int tok = (p0 + warp + NW * j) * kBlockSize;
+        if (pok && tok + kBlockSize <= len) {
+            sr = lds_h2f(pg + P::scl + 2 * tr);
+            sr8 = lds_h2f(pg + P::scl + 2 * (tr + 8));
+            zr = lds_h2f(pg + P::zer + 2 * tr);
+            zr8 = lds_h2f(pg + P::zer + 2 * (tr + 8));
+        } else {
+            // the sequence's last page or a skipped one (warp-uniform): rows
+            // past the end get no weight, and their slots' bytes are not read
+            const bool v0 = pok && tok + tr < len, v8 = pok && tok + tr + 8 < len;
+            if (!v0) s0 = s1 = -INFINITY;
+            if (!v8) s2 = s3 = -INFINITY;
+            sr = v0 ? lds_h2f(pg + P::scl + 2 * tr) : 0.f;
+            zr = v0 ? lds_h2f(pg + P::zer + 2 * tr) : 0.f;
+            sr8 = v8 ? lds_h2f(pg + P::scl + 2 * (tr + 8)) : 0.f;
+            zr8 = v8 ? lds_h2f(pg + P::zer + 2 * (tr + 8)) : 0.f;
+        }
+
+        // ---------- online softmax; the max moves only when a score beats it by kLazy ----------
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+        constexpr float kWScale = (float)(1 << value_wshift<VB>());
+        const bool exact = fmaxf(sr, sr8) > kBigScale / kWScale;
+        if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy || (exact && (mx0 > m0 || mx1 > m1)))) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float f0 = ex2(m0 - n0), f1 = ex2(m1 - n1);
+            l0 *= f0; z0 *= f0; l1 *= f1; z1 *= f1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                acc[i][0] *= f0; acc[i][2] *= f0;
+                acc[i][1] *= f1; acc[i][3] *= f1;
+            }
+            m0 = n0;
+            m1 = n1;
+        }
+        const float p0v = ex2(s0 - m0), p1v = ex2(s1 - m1), p2v = ex2(s2 - m0), p3v = ex2(s3 - m1);
+        l0 += p0v + p2v;
+        l1 += p1v + p3v;
+
+        // ---------- values: O^T += Vcode^T . (p scale)^T, the main codec's arithmetic ----------
+        {
+            const float srw = sr * kWScale, sr8w = sr8 * kWScale;
+            const float w0 = p0v * srw, w1 = p1v * srw, w2 = p2v * sr8w, w3 = p3v * sr8w;
+            const uint32_t h01 = pack_h2(w0, w1), h23 = pack_h2(w2, w3);
+            const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+            const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+            constexpr float kMid = 0.5f * (float)((1 << VB) - 1) / kWScale;
+            z0 = fmaf(p0v, zr, fmaf(p2v, zr8, fmaf(kMid, (w0 - r01.x) + (w2 - r23.x), z0)));
+            z1 = fmaf(p1v, zr, fmaf(p3v, zr8, fmaf(kMid, (w1 - r01.y) + (w3 - r23.y), z1)));
+            const uint32_t bh0 = movtrans(h01);
+            const uint32_t bh1 = movtrans(h23);
+            uint32_t Pab[16], Pcd[16];
+            value_codes<VB>(pg + P::vcode, r, ta, tb, Pab);
+            value_codes<VB>(pg + P::vcode, r, ta + 8, tb + 8, Pcd);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)  // rows: dim 16r + 2mt (row r), 16r + 2mt + 1 (row r + 8)
+                mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bh0, bh1);
+        }
+
+        __syncwarp();  // every lane is done with the slot and with u^: refill the slot
+        const int jn = j + SPW;
+        if (jn < nmine) {
+            if ((jn & 31) == 0) {  // next batch of block ids; prefetch the one after it
+                bid_cur = bid_nxt;
+                const int k = NW * (jn + 32 + lane);
+                bid_nxt = (k < reach) ? __ldg(btw + k) : -1;
+            }
+            if (lane == (jn & 31)) issue(slot, bid_cur);
+            ++issued;
+        }
+        if (++slot == SPW) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+    if (timed_out) {
+        // copies this warp started must land before its shared memory goes away
+        const long long t0 = clock64();
+        for (int jj = jfail; jj < issued; ++jj) {
+            const uint32_t bar = bar_w + 8 * (jj % SPW);
+            while (!mbar_try(bar, (uint32_t)((jj / SPW) & 1)) && clock64() - t0 < kWaitCycles) {
+            }
+        }
+    }
+
+    // ---- reduce l, z over the 8 token rows; warp states over the rebuilt keys ----
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        z0 += __shfl_xor_sync(0xffffffffu, z0, o);
+        z1 += __shfl_xor_sync(0xffffffffu, z1, o);
+    }
+    __syncthreads();  // every warp is past its pages: the rebuilt-key area is free
+    float* wst = reinterpret_cast<float*>(sm + LY.u);  // [NW][8][4 + D]
+    {
+        float* pa = wst + (warp * 8 + 2 * qd) * (4 + D);
+        float* pb = pa + (4 + D);
+        if (r == 0) {
+            pa[0] = m0; pa[1] = l0; pa[2] = z0;
+            pb[0] = m1; pb[1] = l1; pb[2] = z1;
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            // undo the fp16-subnormal scaling of the value codes of dims d, d + 1
+            const float e0 = (float)(1u << (value_exp<VB>(2 * mt) - value_wshift<VB>()));
+            const float e1 = (float)(1u << (value_exp<VB>(2 * mt + 1) - value_wshift<VB>()));
+            const int d = 16 * r + 2 * mt;
+            *reinterpret_cast<float2*>(pa + 4 + d) = make_float2(acc[mt][0] * e0, acc[mt][2] * e1);
+            *reinterpret_cast<float2*>(pb + 4 + d) = make_float2(acc[mt][1] * e0, acc[mt][3] * e1);
+        }
+    }
+    timed_out = __syncthreads_or(timed_out);
+    if (timed_out) {
+        if (tid == 0) flag(a.status, TQ_FLAG_TIMEOUT);
+        return;
+    }
     if (warp < G) {
+        // query q = warp: this CTA's partial (max, sum, acc with the zero term folded in)
         const int q = warp;
-        float M = kOctMinus;
+        float M = kMinusBig;
 #pragma unroll
-        for (int w = 0; w < kOctWarps; ++w) M = fmaxf(M, wst[(w * 8 + q) * (4 + D)]);
-        float Ls = 0.f, x[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, wst[(w * 8 + q) * (4 + D)]);
+        float Ls = 0.f, Z = 0.f, x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < kOctWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             const float* pq = wst + (w * 8 + q) * (4 + D);
             const float f = exp2f(pq[0] - M);
             Ls = fmaf(f, pq[1], Ls);
+            Z = fmaf(f, pq[2], Z);
             const float4 v = *reinterpret_cast<const float4*>(pq + 4 + 4 * lane);
             x[0] = fmaf(f, v.x, x[0]); x[1] = fmaf(f, v.y, x[1]); x[2] = fmaf(f, v.z, x[2]); x[3] = fmaf(f, v.w, x[3]);
         }
@@ -410,7 +608,7 @@ __global__ void __launch_bounds__(kOctWarps * 32, 2) oct_decode_kernel(const Oct
             part[0] = M;
             part[1] = Ls;
         }
-        *reinterpret_cast<float4*>(part + 4 + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(part + 4 + 4 * lane) = make_float4(x[0] + Z, x[1] + Z, x[2] + Z, x[3] + Z);
     }
 }
 
@@ -486,13 +684,18 @@ int launch_oct_encode_t(const OctArgs& a, int num_sms, cudaStream_t s) {
 
 template <int B, int VB>
 int launch_oct_decode_t(const OctArgs& a, cudaStream_t s) {
-    const int smem = oct_smem(1 << (B + 1), (int)a.g.page_bytes).total;
+    using P = OctPage<B, VB>;
+    const Geometry& g = a.g;
+    if (g.page_bytes != P::bytes || g.kcode_off != 0 || g.vcode_off != P::vcode || g.gam_off != P::gam ||
+        g.scl_off != P::scl || g.zer_off != P::zer || a.key_row != P::KR || g.bs != kBlockSize || g.d != kHeadDim)
+        return (int)cudaErrorInvalidValue;  // the cache's geometry is not the format this kernel was built for
+    constexpr int smem = oct_dec_smem<B, VB>().total;
     auto kern = oct_decode_kernel<B, VB>;
     static int done[64] = {};
     cudaError_t e = ensure_smem_limit(kern, smem, done);
     if (e != cudaSuccess) return (int)e;
     e = launch_programmatic(kern, dim3((unsigned)a.num_splits, (unsigned)a.g.hkv, (unsigned)a.batch),
-                            dim3(kOctWarps * 32), (size_t)smem, s, a);
+                            dim3(kOctDecWarps * 32), (size_t)smem, s, a);
     if (e != cudaSuccess) return (int)e;
     const int64_t rows = (int64_t)a.batch * a.hq;
     return (int)launch_programmatic(oct_combine_kernel, dim3((unsigned)rows), dim3(256), 0, s, a);
@@ -548,10 +751,6 @@ int launch_oct_decode(const OctArgs& a, void* stream) {
         case 4: return oct_decode_b<4>(a, s);
         default: return (int)cudaErrorInvalidValue;
     }
-}
-
-int oct_decode_smem_bytes(const OctArgs& a) {
-    return oct_smem(1 << (a.g.kb + 1), (int)a.g.page_bytes).total;
 }
 
 }  // namespace tq

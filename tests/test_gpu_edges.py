@@ -1,6 +1,7 @@
 """Edge cases of the later features: odd query-group sizes on both codecs,
 OCTOPUS edge inputs (zero key, skipped and bad slots, non-finite input,
-empty sequences), a one-page sliding window, and argument checks of prefill."""
+empty sequences), slots that were never written, a one-page sliding window,
+and argument checks of prefill."""
 import os
 
 import numpy as np
@@ -81,6 +82,34 @@ def test_octopus_edge_inputs(tq, oracle):
     assert st.item() == 0
     assert np.all(out[1] == 0)
     assert parity.rel_err(out[[0, 2]], ref[[0, 2]]) <= parity.DECODE_RTOL
+
+
+@pytest.mark.parametrize("codec", ["main", "octopus"])
+def test_unwritten_slots_are_not_read(tq, codec):
+    """The slots past a sequence's end in its last page hold whatever the pool
+    held (here 0xFF bytes: fp16 NaN for every gamma, scale and zero); the
+    output must not depend on them."""
+    import torch
+    dev = "cuda"
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(21, 300, 5), hkv=2, hq=16)
+    nb = w.num_blocks()
+    bt = torch.from_numpy(W.block_table(w)).to(dev)
+    lens = torch.tensor(w.lens, dtype=torch.int32, device=dev)
+    q = torch.from_numpy(W.queries(w, 0)).to(dev, torch.bfloat16)
+    outs = []
+    for fill in (0x00, 0xFF):
+        c = tq.OctopusCache(nb, 2, 4, 4, 0) if codec == "octopus" else tq.Cache(nb, 2)
+        c.pool.fill_(fill)
+        for b in range(w.batch):
+            K = torch.from_numpy(W.kv_tokens(w, 0, b, 0, w.lens[b])).to(dev, torch.bfloat16)
+            V = torch.from_numpy(W.kv_tokens(w, 1, b, 0, w.lens[b])).to(dev, torch.bfloat16)
+            c.encode(K, V, torch.from_numpy(W.slots(w, W.block_table(w), b, 0, w.lens[b])).to(dev))
+        st = tq.new_status()
+        outs.append(c.decode(q, bt, lens, status=st).cpu().numpy())
+        torch.cuda.synchronize()
+        assert st.item() == 0
+    assert np.isfinite(outs[1]).all()
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_ring_one_page_window(tq, oracle):
