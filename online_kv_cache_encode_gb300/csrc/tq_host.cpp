@@ -651,13 +651,13 @@ TQ_API tq_status tq_encode_kv(const tq_cache* c, const void* K, const void* V, t
 // Splits per (sequence, KV head).  The decode kernel keeps one CTA per SM, so
 // a launch runs in waves of num_sms CTAs.  The split count minimises a simple
 // time model: waves x (page rounds of one CTA x 1.2 us + 6 us), a page round
-// being one page per warp (12 warps, 8 with QJL).  The constants are the
-// measured per-page and fixed (prologue, merge) costs on the 32K GQA
-// workload: 9 rounds in ~10.9 us plus ~6 us.  At most ceil(max_blocks / 8)
+// being one page per warp (12 warps, 8 with QJL, 16 for OCTOPUS keys).  The
+// constants are the measured per-page and fixed (prologue, merge) costs on
+// the 32K GQA workload: 9 rounds in ~10.9 us plus ~6 us.  At most ceil(max_blocks / 8)
 // splits (8 pages or more each) and four times the count that fills the SMs.
 static void decode_split_plan(const tq_cache* c, int batch, int max_blocks, int* splits, int* pps) {
     const int64_t units = (int64_t)batch * c->g.hkv;
-    const int nw = c->g.m ? 8 : 12;  // warps per CTA (the OCTOPUS decode has 12 too)
+    const int nw = c->octopus ? 16 : c->g.m ? 8 : 12;  // warps per CTA
     const int64_t sms = c->num_sms > 0 ? c->num_sms : 1;
     int64_t lim = 4 * ((sms + units - 1) / units);
     const int64_t cap = (max_blocks + 7) / 8;

@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kOctWarps * 32) oct_encode_kernel(const OctArg
 // The warps merge in shared memory and each CTA writes one partial per query;
 // oct_combine_kernel merges the splits and rotates back.
 // ---------------------------------------------------------------------------
-constexpr int kOctDecWarps = 12;
+constexpr int kOctDecWarps = 16;  // 12 warps: 8 % slower (dependency stalls in the key rebuild)
 constexpr int kOctMaxSlots = 3;                 // ring slots per warp (fewer if the pages are large)
 constexpr int kOctUStride = kHeadDim + 8;       // floats per rebuilt row: consecutive rows 8 banks apart
 constexpr float kOctUScale = 64.f;              // |rho^ n^| <= 1: rebuilt keys are taken times 64
@@ -230,7 +230,7 @@ struct OctPage {
 // rebuilt-key area holds the warps' states for the in-CTA merge:
 // [NW][8 queries][4 + d] floats (max, sum, zero term, pad, acc).
 struct OctSmem {
-    int q, qsc, bars, ok, u, pages, slot, spw, total;
+    int q, qsc, qf, bars, ok, u, pages, slot, spw, total;
 };
 template <int B, int VB>
 __host__ __device__ constexpr OctSmem oct_dec_smem() {
@@ -238,6 +238,7 @@ __host__ __device__ constexpr OctSmem oct_dec_smem() {
     int off = 0;
     L.q = off; off += 8 * (kHeadDim + 4) * 4;
     L.qsc = off; off += 8 * 4;
+    L.qf = off; off += 8 * 32 * 16;
     L.bars = off; off += kOctDecWarps * kOctMaxSlots * 8;
     L.ok = off; off += kOctDecWarps * kOctMaxSlots * 4;
     off = (off + 15) / 16 * 16;
@@ -349,17 +350,22 @@ __global__ void __launch_bounds__(kOctDecWarps * 32, 1) oct_decode_kernel(const 
     }
     __syncthreads();
 
+    // The B fragments of the queries, the same for every warp, once per CTA in
+    // shared memory: entry (ks, lane) holds, for query lane / 4, dims
+    // 16 ks + 2 (lane % 4) + {0, 1} and + {8, 9} in fp16 hi, then lo (read
+    // back per k-step, which leaves the registers to the key rebuild).
+    const uint32_t qf = sbase + LY.qf;
+    if (tid < 8 * 32) {
+        const int ks = tid >> 5, ln = tid & 31;
+        const float* qr = s_q + (ln >> 2) * QS + 16 * ks + 2 * (ln & 3);
+        uint32_t h0, h1, o0, o1;
+        split_h2(*reinterpret_cast<const float2*>(qr), h0, o0);
+        split_h2(*reinterpret_cast<const float2*>(qr + 8), h1, o1);
+        *reinterpret_cast<uint4*>(sm + LY.qf + 16 * tid) = make_uint4(h0, h1, o0, o1);
+    }
+    __syncthreads();
     // lane (r, qd): r = token row / query of the B operand, qd = quad index
     const int r = lane >> 2, qd = lane & 3;
-    uint32_t QH[8][2], QL[8][2];  // query r, dims 16 ks + 2 qd + {0, 1} and + {8, 9}, fp16 hi + lo
-    {
-        const float* qr = s_q + r * QS + 2 * qd;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            split_h2(*reinterpret_cast<const float2*>(qr + 16 * ks), QH[ks][0], QL[ks][0]);
-            split_h2(*reinterpret_cast<const float2*>(qr + 16 * ks + 8), QH[ks][1], QL[ks][1]);
-        }
-    }
     const float qs0 = s_qsc[2 * qd], qs1 = s_qsc[2 * qd + 1];
     // Score row r holds token tr = r ^ ((r >> 1) & 1) (and row r + 8 token
     // tr + 8), so that the value loads (tokens of rows 2qd, 2qd+1) alternate
@@ -412,7 +418,7 @@ __global__ void __launch_bounds__(kOctDecWarps * 32, 1) oct_decode_kernel(const 
             };
             const uint32_t kw = pg + ((lane * FB) >> 5) * 4;
             const int ksh = (lane * FB) & 31;
-#pragma unroll 8
+#pragma unroll
             for (int t = 0; t < kBlockSize; ++t) {
                 const uint32_t f = __funnelshift_r(lds32(kw + t * P::KR), lds32(kw + t * P::KR + 4), ksh) & kFMask;
                 float x, y, z;
@@ -446,6 +452,7 @@ __global__ void __launch_bounds__(kOctDecWarps * 32, 1) oct_decode_kernel(const 
         float I0[4], I1[4], J0[4], J1[4];  // hi.hi (even / odd k-steps), hi.lo + lo.hi (even / odd)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
+            const uint4 Q = lds128(qf + 16 * (32 * ks + lane));  // hi (x, y), lo (z, w)
             uint32_t h0, h1, h2, h3, o0, o1, o2, o3;
             split_h2(*reinterpret_cast<const float2*>(ua + 16 * ks), h0, o0);
             split_h2(*reinterpret_cast<const float2*>(ub + 16 * ks), h1, o1);
@@ -454,13 +461,13 @@ __global__ void __launch_bounds__(kOctDecWarps * 32, 1) oct_decode_kernel(const 
             float* I = (ks & 1) ? I1 : I0;
             float* J = (ks & 1) ? J1 : J0;
             if (ks < 2) {
-                mma16816_c(I, h0, h1, h2, h3, QH[ks][0], QH[ks][1], 0.f, 0.f, 0.f, 0.f);
-                mma16816_c(J, h0, h1, h2, h3, QL[ks][0], QL[ks][1], 0.f, 0.f, 0.f, 0.f);
+                mma16816_c(I, h0, h1, h2, h3, Q.x, Q.y, 0.f, 0.f, 0.f, 0.f);
+                mma16816_c(J, h0, h1, h2, h3, Q.z, Q.w, 0.f, 0.f, 0.f, 0.f);
             } else {
-                mma16816(I, h0, h1, h2, h3, QH[ks][0], QH[ks][1]);
-                mma16816(J, h0, h1, h2, h3, QL[ks][0], QL[ks][1]);
+                mma16816(I, h0, h1, h2, h3, Q.x, Q.y);
+                mma16816(J, h0, h1, h2, h3, Q.z, Q.w);
             }
-            mma16816(J, o0, o1, o2, o3, QH[ks][0], QH[ks][1]);
+            mma16816(J, o0, o1, o2, o3, Q.x, Q.y);
         }
         const float gr = lds_h2f(pg + P::gam + 2 * tr), gr8 = lds_h2f(pg + P::gam + 2 * (tr + 8));
         float s0 = ((I0[0] + I1[0]) + (J0[0] + J1[0])) * qs0 * gr, s1 = ((I0[1] + I1[1]) + (J0[1] + J1[1])) * qs1 * gr;
