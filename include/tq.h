@@ -180,8 +180,9 @@ TQ_API void tq_cache_free(tq_cache* cache);
  * n^_i the unit direction of the stored level pair; values and the inverse
  * rotation as for the main codec.
  * tq_encode_kv, tq_decode_attention and tq_decode_workspace_bytes accept such
- * a cache (its decode runs on CUDA cores: the warps' partials are merged
- * inside each CTA, the CTAs' by a second kernel); the one-launch append
+ * a cache (its decode rebuilds each page's unit keys in shared memory and
+ * scores them on the tensor cores; the warps' partials are merged inside each
+ * CTA, the CTAs' by a second kernel); the one-launch append
  * entry points return TQ_ERR_UNSUPPORTED.  Supported: d = 128, block_size =
  * 16, bits 2..4, value_bits 1..8.  The library allocates its codebooks and
  * direction table in device memory. */

@@ -1,4 +1,4 @@
-// OCTOPUS triplet key codec: encode and decode attention on CUDA cores.
+// OCTOPUS triplet key codec: encode, and decode attention on the tensor cores.
 //
 // Keys: gamma = ||k||, u = R k / gamma with the same rotation as the main
 // codec; u is cut into 43 triplets (the last padded with a zero), each stored
