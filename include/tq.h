@@ -367,6 +367,21 @@ TQ_API tq_status tq_decode_attention_noalloc(const tq_cache* cache, const void* 
                                              int max_blocks_per_seq, const int32_t* lens, float sm_scale,
                                              float* out, int32_t* dev_status, void* stream);
 
+/* Whether code on the current device can read and write the memory at p:
+ * memory of this device, managed memory, or page-locked host memory mapped
+ * into the device's address space at the same address (under unified
+ * addressing, what cudaHostAlloc and cudaMallocHost return).  Sets
+ * *accessible to 1 or 0; memory the runtime does not know (pageable host
+ * memory) gives 0.  The decode entry points read q, k_new and v_new and write
+ * out in place wherever they are, so these may be page-locked host buffers
+ * that this function accepts: the kernel then moves the step's inputs and its
+ * result over the host link (NVLink-C2C on Grace systems) itself, with no
+ * copy launches.  Every CTA of a split reads the query itself, so this is
+ * slower than staging: a 32K-token GQA decode step (64 query / 8 KV heads)
+ * took 55.3 us per step on a GB300 this way, 31.4 us with one copy each way.
+ * Returns TQ_ERR_INVALID_ARG for a NULL `accessible`. */
+TQ_API tq_status tq_device_accessible(const void* p, int* accessible);
+
 /* Text for a status code, and the detail of the last failure on this thread. */
 TQ_API const char* tq_status_string(tq_status s);
 TQ_API const char* tq_last_error(void);

@@ -309,6 +309,26 @@ using namespace tq;
 
 extern "C" {
 
+TQ_API tq_status tq_device_accessible(const void* p, int* accessible) {
+    if (!accessible) return fail(TQ_ERR_INVALID_ARG, "accessible is NULL");
+    *accessible = 0;
+    if (!p) return TQ_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaPointerAttributes at{};
+    e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();  // memory the runtime does not know: not accessible
+        return TQ_OK;
+    }
+    if ((at.type == cudaMemoryTypeDevice && at.device == dev) || at.type == cudaMemoryTypeManaged)
+        *accessible = 1;
+    else if (at.type == cudaMemoryTypeHost && at.devicePointer == p)
+        *accessible = 1;
+    return TQ_OK;
+}
+
 TQ_API const char* tq_status_string(tq_status s) {
     switch (s) {
         case TQ_OK: return "ok";

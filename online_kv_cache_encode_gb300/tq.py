@@ -47,6 +47,7 @@ SIGNATURES = {
     "tq_octopus_codebook": (_I, [_I, _I, _I, _P]),
     "tq_prefill_workspace_bytes": (_SZ, [_P, _I, _I, _I]),
     "tq_prefill_attention": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _F, _P, _P, _SZ, _P, _P]),
+    "tq_device_accessible": (_I, [_P, ctypes.POINTER(_I)]),
     "tq_status_string": (ctypes.c_char_p, [_I]),
     "tq_last_error": (ctypes.c_char_p, []),
 }
@@ -99,6 +100,19 @@ def _stream() -> int:
 def _ptr(t):
     # a plain int: the c_void_p argtypes convert it
     return None if t is None else t.data_ptr()
+
+
+def device_accessible(t: torch.Tensor) -> bool:
+    """Whether the decode kernels can read / write tensor t in place: a CUDA
+    tensor, or a pinned host tensor mapped into the device's address space
+    (the kernel then reaches it over the host link, with no copy launch)."""
+    if t.is_cuda:
+        return True
+    if not t.is_pinned():
+        return False
+    a = ctypes.c_int(0)
+    _check(lib().tq_device_accessible(_ptr(t), ctypes.byref(a)))
+    return a.value == 1
 
 
 def ring_slots(block_row, positions, window: int, block_size: int = 16):
@@ -206,8 +220,9 @@ class Cache:
     def decode(self, q: torch.Tensor, block_table: torch.Tensor, lens: torch.Tensor,
                sm_scale: float | None = None, out: torch.Tensor | None = None,
                workspace: torch.Tensor | None = None, status: torch.Tensor | None = None) -> torch.Tensor:
-        """q: [B, Hq, d]; block_table: int32 [B, max_blocks]; lens: int32 [B] -> out fp32 [B, Hq, d]."""
-        assert q.is_cuda and q.dim() == 3 and q.shape[2] == self.d and q.is_contiguous()
+        """q: [B, Hq, d]; block_table: int32 [B, max_blocks]; lens: int32 [B] -> out fp32 [B, Hq, d].
+        q and out may be pinned host tensors (see device_accessible)."""
+        assert device_accessible(q) and q.dim() == 3 and q.shape[2] == self.d and q.is_contiguous()
         B, hq, _ = q.shape
         assert block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.shape[0] == B
         assert block_table.is_contiguous() and lens.dtype == torch.int32 and lens.numel() == B
@@ -215,7 +230,8 @@ class Cache:
         if sm_scale is None:
             sm_scale = 1.0 / math.sqrt(self.d)
         if out is None:
-            out = torch.empty((B, hq, self.d), dtype=torch.float32, device=q.device)
+            out = torch.empty((B, hq, self.d), dtype=torch.float32, device=self.pool.device)
+        assert device_accessible(out)
         if workspace is None:
             key = (B, hq, mb)
             if self._ws is None or self._ws[0] != key:
@@ -235,10 +251,11 @@ class Cache:
         With `window`, each sequence's blocks form a ring of `window` slots: the
         token goes to slot (lens[b] - 1) % window and the query attends over the
         min(lens[b], window) tokens the ring holds."""
-        assert k_new.is_cuda and k_new.shape == v_new.shape and k_new.dtype == v_new.dtype
+        assert device_accessible(k_new) and device_accessible(v_new)
+        assert k_new.shape == v_new.shape and k_new.dtype == v_new.dtype
         assert k_new.dim() == 3 and k_new.shape[1] == self.hkv and k_new.shape[2] == self.d
         assert k_new.is_contiguous() and v_new.is_contiguous()
-        assert q.is_cuda and q.dim() == 3 and q.shape[2] == self.d and q.is_contiguous()
+        assert device_accessible(q) and q.dim() == 3 and q.shape[2] == self.d and q.is_contiguous()
         B, hq, _ = q.shape
         assert k_new.shape[0] == B
         assert block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.shape[0] == B
@@ -247,7 +264,8 @@ class Cache:
         if sm_scale is None:
             sm_scale = 1.0 / math.sqrt(self.d)
         if out is None:
-            out = torch.empty((B, hq, self.d), dtype=torch.float32, device=q.device)
+            out = torch.empty((B, hq, self.d), dtype=torch.float32, device=self.pool.device)
+        assert device_accessible(out)
         if workspace is None:
             key = (B, hq, mb)
             if self._ws is None or self._ws[0] != key:

@@ -1,7 +1,7 @@
 """Edge cases of the later features: odd query-group sizes on both codecs,
 OCTOPUS edge inputs (zero key, skipped and bad slots, non-finite input,
-empty sequences), slots that were never written, a one-page sliding window,
-and argument checks of prefill."""
+empty sequences), slots that were never written, decode steps on page-locked
+host buffers, a one-page sliding window, and argument checks of prefill."""
 import os
 
 import numpy as np
@@ -110,6 +110,49 @@ def test_unwritten_slots_are_not_read(tq, codec):
         assert st.item() == 0
     assert np.isfinite(outs[1]).all()
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_decode_step_on_host_buffers(tq):
+    """Where the kernel can reach page-locked host memory in place, a decode
+    step whose k_new, v_new, q and out live there gives the cache bytes and the
+    output of the same step on device buffers, bit for bit."""
+    import torch
+    dev = "cuda"
+    probe = torch.empty(1).pin_memory()
+    if not tq.device_accessible(probe):
+        pytest.skip("page-locked host memory is not mapped into the device's address space here")
+    assert not tq.device_accessible(torch.empty(1))  # pageable host memory never is
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(300, 17, 1), hkv=2, hq=16)
+    nb = w.num_blocks()
+    bt_np = W.block_table(w)
+    bt = torch.from_numpy(bt_np).to(dev)
+    lens = torch.tensor(w.lens, dtype=torch.int32, device=dev)
+    q = torch.from_numpy(W.queries(w, 0)).to(torch.bfloat16)
+    kn = torch.from_numpy(np.stack([W.kv_tokens(w, 0, b, w.lens[b] - 1, w.lens[b])[0] for b in range(w.batch)]))
+    vn = torch.from_numpy(np.stack([W.kv_tokens(w, 1, b, w.lens[b] - 1, w.lens[b])[0] for b in range(w.batch)]))
+    kn, vn = kn.to(torch.bfloat16), vn.to(torch.bfloat16)
+    res = []
+    for host in (False, True):
+        c = tq.Cache(nb, 2)
+        for b in range(w.batch):
+            n = w.lens[b] - 1
+            if n:
+                K = torch.from_numpy(W.kv_tokens(w, 0, b, 0, n)).to(dev, torch.bfloat16)
+                V = torch.from_numpy(W.kv_tokens(w, 1, b, 0, n)).to(dev, torch.bfloat16)
+                c.encode(K, V, torch.from_numpy(W.slots(w, bt_np, b, 0, n)).to(dev))
+        if host:
+            args = [t.pin_memory() for t in (kn, vn, q)]
+            out = torch.empty(w.batch, w.hq, 128).pin_memory()
+        else:
+            args = [t.to(dev) for t in (kn, vn, q)]
+            out = torch.empty(w.batch, w.hq, 128, device=dev)
+        st = tq.new_status()
+        c.decode_append(*args, bt, lens, out=out, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        res.append((out.cpu().clone(), c.pool.cpu().clone()))
+    assert torch.equal(res[0][0], res[1][0])
+    assert torch.equal(res[0][1], res[1][1])
 
 
 def test_ring_one_page_window(tq, oracle):
