@@ -211,6 +211,18 @@ def run_ours(args, rank, world, local):
     copies = [base] + [tq.Cache(nb, hkv, w.key_bits, w.value_bits, w.qjl_m, w.seed,
                                 pool=base.pool.clone()) for _ in range(N_COPIES - 1)]
     q_w = torch.from_numpy(W.queries(w, 0)).to(dev, torch.bfloat16)
+    if args.profile_octopus:
+        # an OCTOPUS 4/4 cache of the same context, then six decode launches
+        # (ncu -k regex:oct_decode -s 1 -c 1)
+        oc = tq.OctopusCache(nb, hkv, 4, 4, w.seed)
+        oc.encode(K, V, slots, status)
+        ows = oc.new_workspace(1, hq, bt.shape[1])
+        oout = torch.empty((1, hq, d), dtype=torch.float32, device=dev)
+        for _ in range(6):
+            oc.decode(q_w, bt, lens, out=oout, workspace=ows, status=status)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "gqa32k OCTOPUS 4/4 decode", "device_status": int(status.item())}), flush=True)
+        return
     widths = [] if args.profile or args.no_widths else width_sweep(tq, w, K, V, slots, bt, q_w, measured_peaks()[0])
     ring = {} if args.profile or args.no_widths else ring_stream(tq, dev, measured_peaks()[0])
     octopus = [] if args.profile or args.no_widths else octopus_sweep(tq, w, K, V, slots, bt, q_w, measured_peaks()[0])
@@ -709,6 +721,8 @@ def main():
     ap.add_argument("--no-widths", action="store_true", help="skip the other-widths measurements")
     ap.add_argument("--profile", action="store_true",
                     help="only build the caches and launch the decode kernel 6 times (for ncu)")
+    ap.add_argument("--profile-octopus", action="store_true",
+                    help="only build an OCTOPUS 4/4 cache and launch its decode 6 times (for ncu)")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
