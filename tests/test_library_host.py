@@ -95,6 +95,11 @@ def test_argument_checks_need_no_gpu(tq):
     assert L.tq_codebook_init(7, 4, ctypes.byref(h)) == tq.TQ_ERR_INVALID_ARG
     assert L.tq_codebook_init(128, 9, ctypes.byref(h)) == tq.TQ_ERR_INVALID_ARG
     assert L.tq_method_constants(0, 0, 0, None, None) == tq.TQ_ERR_INVALID_ARG
+    assert L.tq_device_accessible(fake, None) == tq.TQ_ERR_INVALID_ARG
+    acc = ctypes.c_int(7)
+    assert L.tq_device_accessible(None, ctypes.byref(acc)) == tq.TQ_OK and acc.value == 0  # NULL: never
+    import torch
+    assert not tq.device_accessible(torch.empty(4))  # pageable host memory: no runtime call needed
     assert b"invalid" in L.tq_status_string(tq.TQ_ERR_INVALID_ARG)
     assert L.tq_last_error()  # the last failure left a message
 
