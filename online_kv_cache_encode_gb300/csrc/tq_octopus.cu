@@ -13,10 +13,11 @@
 //  quantizer with norm marginals", methodology steps 1-7, bit split (b+1, b-1)]
 //
 // Decode never builds K^ in global memory: for token t the logit is gamma_t
-// times the sum over triplets of rho^_i <q_rot[3i..3i+2], n^_i>, with n^ from
-// a table of the level pairs' unit directions (methodology step 7).  Each
-// warp rebuilds rho^ n^ of one page in shared memory and scores it on the
-// tensor cores; values accumulate in the rotated frame and one inverse
+// times the sum over triplets of rho^_i <q_rot[3i..3i+2], n^_i>, with n^ the
+// unit direction of the stored level pair (methodology step 7; the encode
+// scores candidates against a table of them, the decode derives each from
+// its two levels).  Each warp rebuilds rho^ n^ of one page in shared memory
+// and scores it on the tensor cores; values accumulate in the rotated frame and one inverse
 // rotation is applied per output.  The warps of a CTA merge in shared memory
 // and write one partial per query; a second kernel merges the partials of a
 // sequence.
