@@ -26,7 +26,9 @@
  * Conventions
  *  - Every data pointer passed to an encode/decode call is a DEVICE pointer
  *    owned by the caller; the library never frees or reallocates it.  Host
- *    pointers are marked "host".
+ *    pointers are marked "host".  The one exception: q, k_new, v_new and out
+ *    of the decode calls may also be page-locked host memory that the device
+ *    reaches in place (tq_device_accessible).
  *  - Calls are asynchronous on the given CUDA stream (`stream` is a
  *    cudaStream_t; NULL is the legacy default stream).  Errors that the host
  *    can see are returned at once as a tq_status and nothing is launched.
@@ -255,9 +257,11 @@ TQ_API size_t tq_decode_workspace_bytes(const tq_cache* cache, int batch, int nu
  * and token t in block block_table[b * max_blocks_per_seq + t / block_size],
  * slot t % block_size.  Logits and values are formed in the rotated frame;
  * keys are never reconstructed; one inverse rotation is applied per output.
- * q: device [batch, num_q_heads, d] of `dtype`.  block_table: device int32.
- * lens: device int32 [batch]; a zero length yields a zero output row.
- * out: device fp32 [batch, num_q_heads, d].  sm_scale: normally 1/sqrt(d).
+ * q: device [batch, num_q_heads, d] of `dtype`, 4-element aligned.
+ * block_table: device int32.  lens: device int32 [batch]; a zero length
+ * yields a zero output row.  out: device fp32 [batch, num_q_heads, d],
+ * 16-byte aligned.  q and out may instead be page-locked host memory that
+ * tq_device_accessible accepts.  sm_scale: normally 1/sqrt(d).
  * workspace: device, at least tq_decode_workspace_bytes(...) bytes.
  * num_q_heads must be a multiple of num_kv_heads with a group size <= 8.
  * A block id outside the pool sets TQ_FLAG_BAD_SLOT and its page is skipped. */
