@@ -242,9 +242,9 @@ TQ_API tq_status tq_encode_kv(const tq_cache* cache, const void* K, const void* 
 /* Workspace bytes tq_decode_attention needs for this batch shape (split-K
  * partials plus one counter per sequence and KV head).  The workspace must
  * be zero-filled once before its first use; each call leaves its counters at
- * zero again on completion, so a workspace can be reused by later calls on
- * the same stream without clearing.  Two calls in flight at once must not
- * share a workspace. */
+ * zero again on completion, also a call that reported TQ_FLAG_TIMEOUT, so a
+ * workspace can be reused by later calls on the same stream without
+ * clearing.  Two calls in flight at once must not share a workspace. */
 TQ_API size_t tq_decode_workspace_bytes(const tq_cache* cache, int batch, int num_q_heads,
                                         int max_blocks_per_seq);
 
@@ -359,10 +359,14 @@ TQ_API tq_status tq_prefill_attention(const tq_cache* cache, const void* q, tq_d
  * Arguments are those of tq_decode_attention minus the workspace.  Returns
  * TQ_ERR_WORKSPACE, launching nothing, when the batch shape would need more
  * than TQ_NOALLOC_WORKSPACE_BYTES (tq_decode_workspace_bytes tells).
- * Uses the current CUDA device, which must be the cache's.  The first call on
- * a device looks up the scratch area's device address; make that first call
- * before any stream capture.  Each call clears the area's split counters on
- * `stream` and calls no cudaMalloc, cudaFree or other allocating routine.
+ * Uses the current CUDA device, which must be the cache's.  A call outside
+ * stream capture looks up the scratch area's device address on that device
+ * (a host-side query, so a device reset between calls does no harm); a call
+ * while `stream` is capturing reuses the address the last uncaptured call on
+ * the device found, and fails with TQ_ERR_INVALID_ARG if there was none: make
+ * the first call before any capture.  For a main-codec cache each call clears
+ * the area's split counters on `stream`; no call runs cudaMalloc, cudaFree or
+ * any other allocating routine.
  * All calls on a device share the one area and it keeps the last call's
  * contents: two calls whose work overlaps on the GPU (different streams, or
  * host threads without ordering) race and corrupt each other's results. */
@@ -380,11 +384,24 @@ TQ_API tq_status tq_decode_attention_noalloc(const tq_cache* cache, const void* 
  * out in place wherever they are, so these may be page-locked host buffers
  * that this function accepts: the kernel then moves the step's inputs and its
  * result over the host link (NVLink-C2C on Grace systems) itself, with no
- * copy launches.  Every CTA of a split reads the query itself, so this is
- * slower than staging: a 32K-token GQA decode step (64 query / 8 KV heads)
- * took 55.3 us per step on a GB300 this way, 31.4 us with one copy each way.
- * Returns TQ_ERR_INVALID_ARG for a NULL `accessible`. */
+ * copy launches.  Every CTA of a split reads the query itself over the link,
+ * so for long contexts (many splits) this is slower than staging the inputs
+ * with one copy each way.  Returns TQ_ERR_INVALID_ARG for a NULL
+ * `accessible`. */
 TQ_API tq_status tq_device_accessible(const void* p, int* accessible);
+
+/* Test hook for the device-side timeout path.  (The source pages have no
+ * counterpart: it exists so that a test can make a bounded wait run out
+ * without faulting or hanging anything.)  With cycles > 0, every decode
+ * launched afterwards in this process makes warp 0 of each CTA with an odd
+ * split index wait about `cycles` SM cycles on a shared-memory barrier that
+ * nothing arrives on.  That wait gives up and the CTA takes the same path as
+ * any timed-out wait: it waits (bounded) for its page copies in flight, sets
+ * TQ_FLAG_TIMEOUT, contributes an empty partial to its sequence's split merge
+ * and still takes part in it, so the call returns, its output is incomplete,
+ * and its workspace is fit for the next call.  cycles <= 0 turns the hook
+ * off (the default).  A process-wide host setting; not for production use. */
+TQ_API void tq_test_stall_waits(int64_t cycles);
 
 /* Text for a status code, and the detail of the last failure on this thread. */
 TQ_API const char* tq_status_string(tq_status s);

@@ -73,8 +73,12 @@ void* g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  Host code only
 // holds a stand-in for the array's name; the real address comes from the
-// runtime, looked up once per device with that device current.
-tq_status noalloc_workspace(void** out) {
+// runtime, with that device current.  Outside stream capture the lookup (a
+// host-side query) is made on every call, so a context that was reset and
+// re-created since the last call gets its own address; while `stream` is
+// capturing, the address found by the last uncaptured call on this device is
+// used, and there must have been one.
+tq_status noalloc_workspace(cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -85,17 +89,30 @@ tq_status noalloc_workspace(void** out) {
         tq::set_error("device ordinal %d is beyond the %d devices this entry point tracks", dev, kMaxDevices);
         return TQ_ERR_UNSUPPORTED;
     }
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_workspace);
-        if (e != cudaSuccess || !p) {
-            tq::set_error("cudaGetSymbolAddress of the fixed decode workspace: %s", cudaGetErrorString(e));
-            return TQ_ERR_CUDA;
-        }
-        g_noalloc_ptr[dev] = p;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) {
+        tq::set_error("cudaStreamIsCapturing: %s", cudaGetErrorString(e));
+        return TQ_ERR_CUDA;
     }
-    *out = g_noalloc_ptr[dev];
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (cap != cudaStreamCaptureStatusNone) {
+        if (!g_noalloc_ptr[dev]) {
+            tq::set_error("the stream is capturing and this device's fixed decode workspace has not been looked up "
+                          "yet: make one call outside capture first");
+            return TQ_ERR_INVALID_ARG;
+        }
+        *out = g_noalloc_ptr[dev];
+        return TQ_OK;
+    }
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_workspace);
+    if (e != cudaSuccess || !p) {
+        tq::set_error("cudaGetSymbolAddress of the fixed decode workspace: %s", cudaGetErrorString(e));
+        return TQ_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+    *out = p;
     return TQ_OK;
 }
 
@@ -122,17 +139,21 @@ extern "C" TQ_API tq_status tq_decode_attention_noalloc(const tq_cache* cache, c
         return TQ_ERR_WORKSPACE;
     }
     void* ws = nullptr;
-    tq_status st = noalloc_workspace(&ws);
+    tq_status st = noalloc_workspace(reinterpret_cast<cudaStream_t>(stream), &ws);
     if (st != TQ_OK) return st;
-    // The split counters sit at the end of the workspace and must start at
-    // zero; the array keeps whatever the previous call left, so clear them.
-    const size_t counters = (size_t)batch * cache->g.hkv * sizeof(unsigned);
-    const size_t counters_region = (counters + 255) / 256 * 256;
-    cudaError_t e = cudaMemsetAsync(static_cast<unsigned char*>(ws) + (need - counters_region), 0, counters,
-                                    reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        tq::set_error("clearing the fixed workspace counters: %s", cudaGetErrorString(e));
-        return TQ_ERR_CUDA;
+    // The main codec's split counters sit at the end of its workspace and must
+    // start at zero; the array keeps whatever the previous call left (another
+    // shape, another cache), so clear them.  OCTOPUS caches have no counters:
+    // their splits are merged by a second kernel.
+    if (!cache->octopus) {
+        const size_t counters = (size_t)batch * cache->g.hkv * sizeof(unsigned);
+        const size_t counters_region = (counters + 255) / 256 * 256;
+        cudaError_t e = cudaMemsetAsync(static_cast<unsigned char*>(ws) + (need - counters_region), 0, counters,
+                                        reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) {
+            tq::set_error("clearing the fixed workspace counters: %s", cudaGetErrorString(e));
+            return TQ_ERR_CUDA;
+        }
     }
     return tq_decode_attention(cache, q, dtype, batch, num_q_heads, block_table, max_blocks_per_seq, lens, sm_scale,
                                out, ws, need, dev_status, stream);

@@ -6,13 +6,20 @@
 //    slots with 1-D bulk async copies (cp.async.bulk) completing on mbarriers.
 //  - Per page, for the G <= 8 query heads of the group (queries as the n8 side
 //    of mma.sync, tokens as rows):
-//      scores  the key centroid is split as C[c] = alpha (c - mid) + rem[c].
-//              The integer code c, masked in place inside a 16-bit lane, is the
-//              exact fp16 subnormal c * 2^-e; it multiplies alpha*q_rot split
-//              into fp16 hi + lo parts that carry the matching 2^(e-24), so all
-//              products share one scale (m16n8k16, fp32 accumulate).  rem[c]
-//              comes in fp16 from a lane-private shared-memory table and
-//              multiplies q_rot (m16n8k16).
+//      scores  the key centroid is split into an exactly representable part
+//              and a small remainder, each multiplied on mma.sync m16n8k16 with
+//              fp32 accumulation:
+//              - 4-bit keys: C[c] = delta N[c] + rem2[c] with N[c] an integer of
+//                magnitude <= 2047 (exact in fp16) and |rem2[c]| <= delta / 2;
+//                both come, for the two codes of a code byte, from one 8-byte
+//                load of a lane-private shared-memory table; N multiplies
+//                delta*q_rot split into fp16 hi + lo, rem2 multiplies q_rot.
+//              - other widths: C[c] = alpha (c - mid) + rem[c].  The integer
+//                code c, masked in place inside a 16-bit lane, is the exact fp16
+//                subnormal c * 2^-e; it multiplies alpha*q_rot split into fp16
+//                hi + lo parts that carry the matching 2^(e-24), so all
+//                products share one scale.  rem[c] comes in fp16 from the
+//                lane-private table and multiplies q_rot.
 //              logit = gamma_t * sm_scale * (sum_j C[c_j] q_rot[j]) [+ QJL term]
 //      softmax running max / sum per query in the exp2 domain; the max is
 //              raised (and the state rescaled) only when a score beats it by
@@ -46,8 +53,9 @@ constexpr int kSmemLimit = 227 * 1024;         // opt-in dynamic shared memory p
 constexpr long long kWaitCycles = 3000000000ll;  // bound on any wait: ~1.5 s at 2 GHz
 constexpr float kMinusBig = -1.0e30f;          // running max before any token (finite: no inf - inf)
 // stage of the appended token in shared memory: key row, value row (up to 128 B
-// each), gamma / scale / zero, and the barrier that hands it to the page's owner
-constexpr int kStageValue = 128, kStageMeta = 256, kStageBar = 272, kStageBytes = 288;
+// each), gamma / scale / zero, the barrier that hands it to the page's owner, and
+// a barrier nothing arrives on (the wait-timeout test hook waits on it)
+constexpr int kStageValue = 128, kStageMeta = 256, kStageBar = 272, kStageNever = 280, kStageBytes = 288;
 // The running max is raised only when a score beats it by more than kLazy (log2
 // units), so weights stay below 2^kLazy (any reference max gives the same
 // softmax).  A page whose value scale exceeds kBigScale takes the exact max, so
@@ -84,14 +92,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Wait for the phase of the given parity.  Spins on try_wait and looks at the
 // SM cycle counter only every 256 tries; gives up after kWaitCycles (about a
 // second or two at GB300 clocks).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, long long limit) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
         for (int i = 0; i < 256; ++i)
             if (mbar_try(bar, parity)) return true;
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitCycles);
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile(
@@ -598,7 +609,9 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = a.group;
 
-    // The layout assumes dynamic shared memory starts below kMaxSmemBase.
+    // The layout assumes dynamic shared memory starts below kMaxSmemBase.  The
+    // start address is the same for every CTA of the launch, so either all of
+    // them return here (no split counter is touched) or none does.
     const uint32_t sbase = smem_u32(sm);
     if (sbase > (uint32_t)kMaxSmemBase) {
         grid_dependency_wait();
@@ -620,7 +633,10 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     const uint32_t stage_bar = sbase + LY.stage + kStageBar;
     if (lane == 0) {
         for (int k = 0; k < SPW; ++k) mbar_init(bar_w + 8 * k, 1);
-        if (warp == 0) mbar_init(stage_bar, 1);
+        if (warp == 0) {
+            mbar_init(stage_bar, 1);
+            mbar_init(sbase + LY.stage + kStageNever, 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     uint16_t* rem = reinterpret_cast<uint16_t*>(sm + LY.rem);
@@ -928,7 +944,15 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
         uint32_t phase = 0;
         int issued = min(SPW, nmine);   // pages of this warp whose copies were started
         int jfail = nmine;              // first page whose wait gave up
-        for (int j = 0; j < nmine; ++j) {
+        if (a.stall_cycles > 0 && (split & 1) && warp == 0) {
+            // test hook: a bounded wait on a barrier that nothing arrives on runs
+            // out, and the warp takes the timeout path below before its first page
+            if (!mbar_wait_for(sbase + LY.stage + kStageNever, 0, a.stall_cycles)) {
+                timed_out = true;
+                jfail = 0;
+            }
+        }
+        for (int j = 0; j < (timed_out ? 0 : nmine); ++j) {
             if (!mbar_wait(bar_w + 8 * slot, phase)) {
                 timed_out = true;
                 jfail = j;
@@ -1151,18 +1175,19 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 make_float2(acc[mt][1] * e0, acc[mt][3] * e1);
         }
     }
+    // A CTA with a wait that gave up flags it and contributes an empty partial
+    // (max -inf, sum 0, acc 0), but still takes part in the split merge below:
+    // every CTA bumps the counter, so the last one still merges and resets it,
+    // and the workspace stays usable for the next call.
     timed_out = __syncthreads_or(timed_out);  // (B)
-    if (timed_out) {
-        if (tid == 0) flag(a.status, TQ_FLAG_TIMEOUT);
-        return;
-    }
+    if (timed_out && tid == 0) flag(a.status, TQ_FLAG_TIMEOUT);
 
     // ---- merge the warps: thread (query warp, lane) owns dims 4 lane .. 4 lane + 3 ----
     const float* wst = reinterpret_cast<const float*>(sm + lut_off);
     const float* wacc = reinterpret_cast<const float*>(sm + lut_off + 2048);
     const int qg = warp;  // query of this warp (warps 0..7)
     float Mx = kMinusBig, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-    if (warp < 8) {
+    if (warp < 8 && !timed_out) {
         for (int w = 0; w < NW; ++w) Mx = fmaxf(Mx, wst[(w * 8 + qg) * 3]);
         float Z = 0.f;
         const int dsw = (4 * lane) ^ (4 * (qg >> 1));

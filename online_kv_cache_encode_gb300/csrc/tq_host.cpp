@@ -3,6 +3,7 @@
 // that launch the kernels.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -33,6 +34,11 @@ static tq_status cuda_fail(cudaError_t e, const char* what) {
     set_error("%s: %s", what, cudaGetErrorString(e));
     return TQ_ERR_CUDA;
 }
+
+// Wait-timeout test hook (tq_test_stall_waits): SM cycles the stalled warps
+// wait, 0 when off.  Read once per decode launch.
+static std::atomic<long long> g_stall_cycles{0};
+long long test_stall_cycles() { return g_stall_cycles.load(std::memory_order_relaxed); }
 
 // ---------------------------------------------------------------------------
 // Counter-based SplitMix64 stream: output i of stream (seed, tag) is the
@@ -341,6 +347,10 @@ TQ_API const char* tq_status_string(tq_status s) {
 }
 
 TQ_API const char* tq_last_error(void) { return g_last_error; }
+
+TQ_API void tq_test_stall_waits(int64_t cycles) {
+    g_stall_cycles.store(cycles > 0 ? (long long)cycles : 0, std::memory_order_relaxed);
+}
 
 TQ_API tq_status tq_codebook_init(int d, int bits, tq_codebook** out) {
     if (!out) return fail(TQ_ERR_INVALID_ARG, "out is NULL");
@@ -769,6 +779,7 @@ static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype,
         o.partials = (float*)workspace;
         o.pages_per_split = pps;
         o.num_splits = splits;
+        o.stall_cycles = test_stall_cycles();
         int e = launch_oct_decode(o, stream);
         if (e != 0) return cuda_fail((cudaError_t)e, "OCTOPUS decode launch");
         return TQ_OK;
@@ -800,6 +811,7 @@ static tq_status decode_common(const tq_cache* c, const void* q, tq_dtype dtype,
     a.vnew = vnew;
     a.kv_dtype = (int)kv_dtype;
     a.window = window;
+    a.stall_cycles = test_stall_cycles();
     int e = launch_decode(a, stream);
     if (e != 0) return cuda_fail((cudaError_t)e, "decode launch");
     return TQ_OK;

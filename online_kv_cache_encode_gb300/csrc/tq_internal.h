@@ -90,6 +90,9 @@ struct DecodeArgs {
     // ring of `window` slots per sequence (0: no ring): the appended token goes
     // to slot (lens[b] - 1) mod window, attention runs over min(lens[b], window) slots
     int window;
+    // test hook (0: off): warp 0 of every odd split waits this many SM cycles on
+    // a barrier nothing arrives on, so that the timeout path runs
+    long long stall_cycles;
 };
 
 // ---------------------------------------------------------------------------
@@ -131,6 +134,7 @@ struct OctArgs {
     float* out;
     float* partials;      // [batch, hkv, splits, group, 4 + d]
     int pages_per_split, num_splits;
+    long long stall_cycles;  // test hook, as in DecodeArgs
 };
 constexpr int kOctWarps = 8;
 
@@ -151,6 +155,7 @@ template <int KB>
 int decode_smem_kb(const Geometry& g);
 
 void set_error(const char* fmt, ...);
+long long test_stall_cycles();  // the wait-timeout test hook's current setting (0: off)
 
 }  // namespace tq
 

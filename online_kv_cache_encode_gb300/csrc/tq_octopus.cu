@@ -231,7 +231,7 @@ struct OctPage {
 // rebuilt-key area holds the warps' states for the in-CTA merge:
 // [NW][8 queries][4 + d] floats (max, sum, zero term, pad, acc).
 struct OctSmem {
-    int q, qsc, qf, bars, ok, u, pages, slot, spw, total;
+    int q, qsc, qf, bars, never, ok, u, pages, slot, spw, total;
 };
 template <int B, int VB>
 __host__ __device__ constexpr OctSmem oct_dec_smem() {
@@ -241,6 +241,7 @@ __host__ __device__ constexpr OctSmem oct_dec_smem() {
     L.qsc = off; off += 8 * 4;
     L.qf = off; off += 8 * 32 * 16;
     L.bars = off; off += kOctDecWarps * kOctMaxSlots * 8;
+    L.never = off; off += 8;  // a barrier nothing arrives on (the wait-timeout test hook)
     L.ok = off; off += kOctDecWarps * kOctMaxSlots * 4;
     off = (off + 15) / 16 * 16;
     L.u = off; off += kOctDecWarps * kBlockSize * kOctUStride * 4;
@@ -288,6 +289,7 @@ __global__ void __launch_bounds__(kOctDecWarps * 32, 1) oct_decode_kernel(const 
 
     if (lane == 0) {
         for (int k = 0; k < SPW; ++k) mbar_init(bar_w + 8 * k, 1);
+        if (warp == 0) mbar_init(sbase + LY.never, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     grid_dependency_wait();
@@ -386,7 +388,15 @@ __global__ void __launch_bounds__(kOctDecWarps * 32, 1) oct_decode_kernel(const 
     uint32_t phase = 0;
     int issued = min(SPW, nmine);
     int jfail = nmine;
-    for (int j = 0; j < nmine; ++j) {
+    if (a.stall_cycles > 0 && (split & 1) && warp == 0) {
+        // test hook: a bounded wait on a barrier that nothing arrives on runs
+        // out, and the warp takes the timeout path below before its first page
+        if (!mbar_wait_for(sbase + LY.never, 0, a.stall_cycles)) {
+            timed_out = true;
+            jfail = 0;
+        }
+    }
+    for (int j = 0; j < (timed_out ? 0 : nmine); ++j) {
         if (!mbar_wait(bar_w + 8 * slot, phase)) {
             timed_out = true;
             jfail = j;
@@ -590,14 +600,22 @@ __global__ void __launch_bounds__(kOctDecWarps * 32, 1) oct_decode_kernel(const 
             *reinterpret_cast<float2*>(pb + 4 + d) = make_float2(acc[mt][1] * e0, acc[mt][3] * e1);
         }
     }
+    // A CTA with a wait that gave up flags it and writes an empty partial (max
+    // -inf, sum 0, acc 0), so the combine kernel never reads a stale one.
     timed_out = __syncthreads_or(timed_out);
-    if (timed_out) {
-        if (tid == 0) flag(a.status, TQ_FLAG_TIMEOUT);
-        return;
-    }
+    if (timed_out && tid == 0) flag(a.status, TQ_FLAG_TIMEOUT);
     if (warp < G) {
         // query q = warp: this CTA's partial (max, sum, acc with the zero term folded in)
         const int q = warp;
+        float* part = a.partials + ((((int64_t)b * g.hkv + h) * a.num_splits + split) * G + q) * (4 + D);
+        if (timed_out) {
+            if (lane == 0) {
+                part[0] = kMinusBig;
+                part[1] = 0.f;
+            }
+            *reinterpret_cast<float4*>(part + 4 + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+            return;
+        }
         float M = kMinusBig;
 #pragma unroll
         for (int w = 0; w < NW; ++w) M = fmaxf(M, wst[(w * 8 + q) * (4 + D)]);
@@ -611,7 +629,6 @@ __global__ void __launch_bounds__(kOctDecWarps * 32, 1) oct_decode_kernel(const 
             const float4 v = *reinterpret_cast<const float4*>(pq + 4 + 4 * lane);
             x[0] = fmaf(f, v.x, x[0]); x[1] = fmaf(f, v.y, x[1]); x[2] = fmaf(f, v.z, x[2]); x[3] = fmaf(f, v.w, x[3]);
         }
-        float* part = a.partials + ((((int64_t)b * g.hkv + h) * a.num_splits + split) * G + q) * (4 + D);
         if (lane == 0) {
             part[0] = M;
             part[1] = Ls;

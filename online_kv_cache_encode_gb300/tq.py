@@ -48,6 +48,7 @@ SIGNATURES = {
     "tq_prefill_workspace_bytes": (_SZ, [_P, _I, _I, _I]),
     "tq_prefill_attention": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _F, _P, _P, _SZ, _P, _P]),
     "tq_device_accessible": (_I, [_P, ctypes.POINTER(_I)]),
+    "tq_test_stall_waits": (None, [_I64]),
     "tq_status_string": (ctypes.c_char_p, [_I]),
     "tq_last_error": (ctypes.c_char_p, []),
 }
@@ -113,6 +114,13 @@ def device_accessible(t: torch.Tensor) -> bool:
     a = ctypes.c_int(0)
     _check(lib().tq_device_accessible(_ptr(t), ctypes.byref(a)))
     return a.value == 1
+
+
+def set_test_stall(cycles: int) -> None:
+    """Test hook of the device-side timeout path (tq_test_stall_waits): with
+    cycles > 0 every later decode launch lets warp 0 of each odd split give up
+    a bounded wait; 0 turns it off."""
+    lib().tq_test_stall_waits(int(cycles))
 
 
 def ring_slots(block_row, positions, window: int, block_size: int = 16):
