@@ -149,3 +149,83 @@ def test_octopus_encode_unpack_and_decode_invariants(oracle):
     out, st = c.decode(pool, q, bt, np.array([T]), 0.1)
     for h in range(hkv):
         np.testing.assert_allclose(out[0, 2 * h + 1], vhat[:, h].mean(axis=0), rtol=0, atol=1e-12)
+
+
+def _rotated_frame_decode(oracle, c, pool, q, bt, lens, sm_scale, swap=False):
+    """A second route to the OCTOPUS decode, independent of the oracle's decode
+    loop: fields read by the numpy page reader, the unit keys rebuilt by
+    OctCache.direction (pinned by the distortion test), logits in the rotated
+    frame, gamma_t sm_scale <R q, u^_t>, values accumulated in the rotated
+    frame, then one inverse rotation per output ["OCTOPUS ..." -- step 7:
+    attention from the codes without materialising K^].  swap=True exchanges
+    xi and eta: a planted mistake the comparison must catch."""
+    from tests import parity
+    B, hq, d = q.shape
+    G = hq // c.hkv
+    out = np.zeros_like(q)
+    for b in range(B):
+        n = int(lens[b])
+        if n == 0:
+            continue
+        t = np.arange(n)
+        slots = bt[b, t // c.bs].astype(np.int64) * c.bs + t % c.bs
+        for h in range(c.hkv):
+            f = parity.unpack_octopus(pool, d, c.b, c.vb, c.bs, c.hkv, c.page_bytes, slots, np.full(n, h))
+            a_, e_ = (f["ieta"], f["ixi"]) if swap else (f["ixi"], f["ieta"])
+            U = np.stack([c.direction(a_[i], e_[i], f["irho"][i]) for i in range(n)])
+            Vr = f["scale"][:, None] * f["vq"] + f["zero"][:, None]
+            for g in range(G):
+                qh = h * G + g
+                logit = sm_scale * f["gamma"] * (U @ oracle.rotate(c.s, q[b, qh]))
+                p = np.exp(logit - logit.max())
+                out[b, qh] = oracle.rotate_inverse(c.s, (p @ Vr) / p.sum())
+    return out
+
+
+@pytest.mark.parametrize("b,G", [(2, 1), (3, 4), (4, 2)])
+def test_decode_matches_rotated_frame_route(oracle, b, G):
+    """The oracle's OCTOPUS decode (keys rebuilt, rotated back, plain softmax)
+    against the rotated-frame route above on random distinct keys, ragged
+    lengths and a permuted block table: agreement to 1e-12, while the same
+    route with xi and eta swapped is far off."""
+    d, hkv, vb, bs = 128, 2, 4, 16
+    lens = np.array([37, 70])
+    nbk = 5
+    c = oracle.OctCache(d, b, vb, bs, hkv, 2 * nbk, 11)
+    rng = np.random.default_rng(20 + b)
+    bt = rng.permutation(2 * nbk).reshape(2, nbk).astype(np.int32)
+    pool = c.new_pool()
+    for s in range(2):
+        K = rng.standard_normal((lens[s], hkv, d))
+        K[:, :, rng.choice(d, 4, replace=False)] *= 20.0
+        V = rng.standard_normal((lens[s], hkv, d))
+        t = np.arange(lens[s])
+        assert c.encode(K, V, bt[s, t // bs].astype(np.int64) * bs + t % bs, pool) == 0
+    q = rng.standard_normal((2, hkv * G, d)) * 3.0
+    sm = 1.0 / math.sqrt(d)
+    out, st = c.decode(pool, q, bt, lens, sm)
+    assert st == 0
+    ref = _rotated_frame_decode(oracle, c, pool, q, bt, lens, sm)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+    bad = _rotated_frame_decode(oracle, c, pool, q, bt, lens, sm, swap=True)
+    assert np.abs(bad - ref).max() > 1e-3 * np.abs(ref).max()
+
+
+def test_numpy_page_reader_matches_encoder_codes(oracle):
+    """The numpy reader gives back the codes and fp16 fields the oracle's key
+    and value encoders produce for each slot."""
+    from tests import parity
+    d, b, vb, bs, hkv = 128, 3, 3, 16, 1
+    c = oracle.OctCache(d, b, vb, bs, hkv, 2, 5)
+    rng = np.random.default_rng(4)
+    K = rng.standard_normal((20, hkv, d))
+    V = rng.standard_normal((20, hkv, d))
+    pool = c.new_pool()
+    slots = np.arange(20) + 5
+    assert c.encode(K, V, slots, pool) == 0
+    f = parity.unpack_octopus(pool, d, b, vb, bs, hkv, c.page_bytes, slots, np.zeros(20, dtype=np.int64))
+    for t in range(20):
+        g, a, e, r = c.encode_key_vector(K[t, 0])
+        assert np.array_equal(f["ixi"][t], a) and np.array_equal(f["ieta"][t], e) and np.array_equal(f["irho"][t], r)
+        assert f["gamma"][t] == float(np.float16(g))
+        assert np.array_equal(f["vq"][t], c.unpack_slot(pool, int(slots[t]) // bs, 0, int(slots[t]) % bs)["vq"])
