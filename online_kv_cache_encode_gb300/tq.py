@@ -49,6 +49,7 @@ SIGNATURES = {
     "tq_prefill_attention": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _F, _P, _P, _SZ, _P, _P]),
     "tq_device_accessible": (_I, [_P, ctypes.POINTER(_I)]),
     "tq_test_stall_waits": (None, [_I64]),
+    "tq_selftest_tcgen05": (_I, [_P, _P, _P, _P, _P]),
     "tq_status_string": (ctypes.c_char_p, [_I]),
     "tq_last_error": (ctypes.c_char_p, []),
 }
@@ -121,6 +122,15 @@ def set_test_stall(cycles: int) -> None:
     cycles > 0 every later decode launch lets warp 0 of each odd split give up
     a bounded wait; 0 turns it off."""
     lib().tq_test_stall_waits(int(cycles))
+
+
+def selftest_tcgen05(A: torch.Tensor, B: torch.Tensor, status: torch.Tensor | None = None) -> torch.Tensor:
+    """tq_selftest_tcgen05: A [128, 256] and B [256, 16] fp16 (CUDA) -> out [3, 128, 16] fp32."""
+    assert A.is_cuda and A.dtype == torch.float16 and A.shape == (128, 256) and A.is_contiguous()
+    assert B.is_cuda and B.dtype == torch.float16 and B.shape == (256, 16) and B.is_contiguous()
+    out = torch.full((3, 128, 16), float("nan"), dtype=torch.float32, device=A.device)
+    _check(lib().tq_selftest_tcgen05(_ptr(A), _ptr(B), _ptr(out), _ptr(status), _stream()))
+    return out
 
 
 def ring_slots(block_row, positions, window: int, block_size: int = 16):
