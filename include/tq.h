@@ -408,10 +408,11 @@ TQ_API void tq_test_stall_waits(int64_t cycles);
  * use of tensor memory and the asynchronous MMA).  One CTA computes
  * D = A . B with A [128 x 256] and B [256 x 16] fp16 (device, row-major,
  * 16-byte aligned) and fp32 accumulation, and writes out (device fp32,
- * 3 x 128 x 16): [0] A staged in tensor memory, B in shared memory, D read
+ * 4 x 128 x 16): [0] A staged in tensor memory, B in shared memory, D read
  * back one row per thread; [1] the same D read back in the 16-lane fragment
  * layout and stored by that layout's documented positions; [2] A and B both
- * from shared memory.  All three equal A . B up to fp32 summation order.
+ * from shared memory; [3] A written to tensor memory with the 16-lane
+ * fragment store.  All four equal A . B up to fp32 summation order.
  * A bounded wait that gives up sets TQ_FLAG_TIMEOUT in *dev_status. */
 TQ_API tq_status tq_selftest_tcgen05(const void* A, const void* B, float* out, int32_t* dev_status, void* stream);
 

@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include "tq_device.cuh"
+#include "tq_tcgen05.cuh"
 
 namespace tq {
 
@@ -589,6 +590,258 @@ __device__ __forceinline__ void patch_page(uint8_t* pg, int off, const uint8_t* 
 }
 
 // ---------------------------------------------------------------------------
+// One page's online softmax and PV contraction for lane (r, qd) of a warp:
+// t0..t3 are the lane's logits in log2 units before the key norm (rows r and
+// r + 8, i.e. slots tr and tr + 8; queries 2qd and 2qd + 1), tok the sequence
+// position of the page's first slot.  Values: O^T[128 x 8 q] += Vcode^T[128 x 16
+// tok] . (p * scale)^T[16 tok x 8 q] on mma.sync m16n8k16 (lane (r, qd) holds
+// dims 16r..16r+15 of the tokens of rows 2qd, 2qd+1, 2qd+8, 2qd+9).
+// ---------------------------------------------------------------------------
+template <int KB, int VB, int M>
+__device__ __forceinline__ void softmax_pv_page(uint32_t pg, bool pok, int tok, int len, float t0, float t1, float t2,
+                                                float t3, int r, int tr, int ta, int tb, float& m0, float& m1,
+                                                float& l0, float& l1, float& z0, float& z1, float (&acc)[8][4]) {
+    using F = PageFmt<KB, VB, M>;
+    const float gr = lds_h2f(pg + F::gam + 2 * tr), gr8 = lds_h2f(pg + F::gam + 2 * (tr + 8));
+    float s0 = t0 * gr, s1 = t1 * gr, s2 = t2 * gr8, s3 = t3 * gr8;
+    // the sequence's last page or a skipped one (warp-uniform): rows past
+    // the end get no weight, and the scale and zero of their slots (never
+    // written: any bytes, NaN included) are replaced by 0
+    const bool tail = !pok || tok + kBlockSize > len;
+    const bool v0 = pok && tok + tr < len, v8 = pok && tok + tr + 8 < len;
+    if (tail) {
+        if (!v0) s0 = s1 = -INFINITY;
+        if (!v8) s2 = s3 = -INFINITY;
+    }
+
+    // ---------- online softmax; the max moves only when a score beats it by kLazy ----------
+    float sr = lds_h2f(pg + F::scl + 2 * tr), sr8 = lds_h2f(pg + F::scl + 2 * (tr + 8));
+    if (tail) {
+        sr = v0 ? sr : 0.f;
+        sr8 = v8 ? sr8 : 0.f;
+    }
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+    constexpr float kWScale = (float)(1 << value_wshift<VB>());
+    const bool exact = fmaxf(sr, sr8) > kBigScale / kWScale;
+    if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy || (exact && (mx0 > m0 || mx1 > m1)))) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float f0 = ex2(m0 - n0), f1 = ex2(m1 - n1);
+        l0 *= f0; z0 *= f0; l1 *= f1; z1 *= f1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            acc[i][0] *= f0; acc[i][2] *= f0;
+            acc[i][1] *= f1; acc[i][3] *= f1;
+        }
+        m0 = n0;
+        m1 = n1;
+    }
+    const float p0v = ex2(s0 - m0), p1v = ex2(s1 - m1), p2v = ex2(s2 - m0), p3v = ex2(s3 - m1);
+    float zr = lds_h2f(pg + F::zer + 2 * tr), zr8 = lds_h2f(pg + F::zer + 2 * (tr + 8));
+    if (tail) {
+        zr = v0 ? zr : 0.f;
+        zr8 = v8 ? zr8 : 0.f;
+    }
+    l0 += p0v + p2v;
+    l1 += p1v + p3v;
+
+    // ---------- values: lane (r, qd) holds dims 16r..16r+15 of the tokens of rows 2qd, 2qd+1, 2qd+8, 2qd+9 ----------
+    // The weights w = p * scale (p <= 2^kLazy) go in as single fp16 w'.  The
+    // codes are not centred, so the rounding w - w' is also added back times
+    // the mid code through the fp32 zero-point sum; what is left is
+    // (w - w') (c - mid), a few 1e-4 of the output at most.
+    {
+        const float srw = sr * kWScale, sr8w = sr8 * kWScale;
+        const float w0 = p0v * srw, w1 = p1v * srw, w2 = p2v * sr8w, w3 = p3v * sr8w;
+        const uint32_t h01 = pack_h2(w0, w1), h23 = pack_h2(w2, w3);
+        const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+        const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+        constexpr float kMid = 0.5f * (float)((1 << VB) - 1) / kWScale;
+        z0 = fmaf(p0v, zr, fmaf(p2v, zr8, fmaf(kMid, (w0 - r01.x) + (w2 - r23.x), z0)));
+        z1 = fmaf(p1v, zr, fmaf(p3v, zr8, fmaf(kMid, (w1 - r01.y) + (w3 - r23.y), z1)));
+        const uint32_t bh0 = movtrans(h01);
+        const uint32_t bh1 = movtrans(h23);
+        uint32_t Pab[16], Pcd[16];
+        value_codes<VB>(pg + F::vcode, r, ta, tb, Pab);
+        value_codes<VB>(pg + F::vcode, r, ta + 8, tb + 8, Pcd);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)  // rows: dim 16r + 2mt (row r), 16r + 2mt + 1 (row r + 8)
+            mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bh0, bh1);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue shared by the decode kernels: reduce each warp's softmax state over
+// its token rows, merge the NW warps in shared memory (over the remainder
+// table, free by then), rotate back, and either write the output (one split)
+// or publish this split's partial and let the last CTA of the (sequence, KV
+// head) merge the splits.  A CTA whose wait gave up contributes an empty
+// partial.  With TMEM_COLS > 0 the CTA's tensor memory is released once every
+// warp is past its pages.
+// ---------------------------------------------------------------------------
+template <int NW, int VB, int TMEM_COLS>
+__device__ __forceinline__ void decode_epilogue(const DecodeArgs& a, uint8_t* sm, int lut_off, bool timed_out,
+                                                int split, int h, int b, float m0, float m1, float l0, float l1,
+                                                float z0, float z1, float (&acc)[8][4], uint32_t tmem) {
+    constexpr int D = kHeadDim;
+    const Geometry& g = a.g;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = lane >> 2, qd = lane & 3;
+    const int G = a.group;
+    // ---- reduce l, z over the 8 token rows, publish warp state ----
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        z0 += __shfl_xor_sync(0xffffffffu, z0, o);
+        z1 += __shfl_xor_sync(0xffffffffu, z1, o);
+    }
+    if constexpr (TMEM_COLS > 0) tc::fence_before_sync();
+    __syncthreads();  // (A) every warp is past its pages: the remainder table is free
+    if constexpr (TMEM_COLS > 0) {
+        // every tensor-core operation of the CTA is complete: release tensor memory
+        if (warp == 0) {
+            tc::fence_after_sync();
+            tc::tmem_dealloc<TMEM_COLS>(tmem);
+        }
+    }
+    // warp states [NW][8][3] and accumulators [NW][8][128] over the table; a
+    // query's dims are stored XOR-swizzled by 4 * (query / 2) so that both
+    // these stores and the merge's 16-byte loads stay clear of bank conflicts
+    float* wst_w = reinterpret_cast<float*>(sm + lut_off);
+    float* wacc_w = reinterpret_cast<float*>(sm + lut_off + 2048);
+    if (r == 0) {
+        wst_w[(warp * 8 + 2 * qd) * 3 + 0] = m0;
+        wst_w[(warp * 8 + 2 * qd) * 3 + 1] = l0;
+        wst_w[(warp * 8 + 2 * qd) * 3 + 2] = z0;
+        wst_w[(warp * 8 + 2 * qd + 1) * 3 + 0] = m1;
+        wst_w[(warp * 8 + 2 * qd + 1) * 3 + 1] = l1;
+        wst_w[(warp * 8 + 2 * qd + 1) * 3 + 2] = z1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        // undo the fp16-subnormal scaling of the value codes of dims d, d + 1
+        const float e0 = (float)(1u << (value_exp<VB>(2 * mt) - value_wshift<VB>()));
+        const float e1 = (float)(1u << (value_exp<VB>(2 * mt + 1) - value_wshift<VB>()));
+        const int d = (16 * r + 2 * mt) ^ (4 * qd);
+        *reinterpret_cast<float2*>(wacc_w + (warp * 8 + 2 * qd) * D + d) = make_float2(acc[mt][0] * e0, acc[mt][2] * e1);
+        *reinterpret_cast<float2*>(wacc_w + (warp * 8 + 2 * qd + 1) * D + d) =
+            make_float2(acc[mt][1] * e0, acc[mt][3] * e1);
+    }
+    // A CTA with a wait that gave up flags it and contributes an empty partial
+    // (max -inf, sum 0, acc 0), but still takes part in the split merge below:
+    // every CTA bumps the counter, so the last one still merges and resets it,
+    // and the workspace stays usable for the next call.
+    timed_out = __syncthreads_or(timed_out);  // (B)
+    if (timed_out && tid == 0) flag(a.status, TQ_FLAG_TIMEOUT);
+
+    // ---- merge the warps: thread (query warp, lane) owns dims 4 lane .. 4 lane + 3 ----
+    const float* wst = reinterpret_cast<const float*>(sm + lut_off);
+    const float* wacc = reinterpret_cast<const float*>(sm + lut_off + 2048);
+    const int qg = warp;  // query of this warp (warps 0..7)
+    float Mx = kMinusBig, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
+    if (warp < 8 && !timed_out) {
+        for (int w = 0; w < NW; ++w) Mx = fmaxf(Mx, wst[(w * 8 + qg) * 3]);
+        float Z = 0.f;
+        const int dsw = (4 * lane) ^ (4 * (qg >> 1));
+        for (int w = 0; w < NW; ++w) {
+            const float f = exp2f(wst[(w * 8 + qg) * 3] - Mx);
+            L = fmaf(f, wst[(w * 8 + qg) * 3 + 1], L);
+            Z = fmaf(f, wst[(w * 8 + qg) * 3 + 2], Z);
+            const float4 v = *reinterpret_cast<const float4*>(wacc + (w * 8 + qg) * D + dsw);
+            O[0] = fmaf(f, v.x, O[0]); O[1] = fmaf(f, v.y, O[1]);
+            O[2] = fmaf(f, v.z, O[2]); O[3] = fmaf(f, v.w, O[3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) O[i] += Z;
+    }
+
+    // Rotate this CTA's unnormalised accumulator back now, R^T O = s (.) H O / sqrt(d):
+    // R^T is linear, so the split merge below is then a plain weighted sum.
+    if (warp < G) {
+        fwht128(O, lane);
+        const uint32_t sg = lane_signs(a.c, lane);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            O[i] *= 0.08838834764831845f;
+            if ((sg >> i) & 1u) O[i] = -O[i];
+        }
+    }
+    float* o = a.out + ((int64_t)b * a.hq + (int64_t)h * G + qg) * D;
+    if (a.num_splits == 1) {
+        if (warp < G) {
+            const float inv = (L > 0.f) ? 1.f / L : 0.f;
+            *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
+        }
+        return;
+    }
+
+    // publish this split's partial (max, sum, rotated acc with the zero term folded in)
+    const int64_t unit = (int64_t)b * g.hkv + h;
+    float* part = a.partials + ((unit * a.num_splits + split) * G) * kPartStride;
+    if (warp < G) {
+        float* pp = part + qg * kPartStride;
+        if (lane == 0) { pp[0] = Mx; pp[1] = L; }
+        *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(O[0], O[1], O[2], O[3]);
+    }
+    // The CTA barrier orders every thread's partial writes before thread 0's
+    // gpu-scope release (cumulativity); the acquire side pairs with the other
+    // CTAs' releases before the last one reads their partials.
+    __syncthreads();
+    __shared__ int s_last;
+    if (tid == 0) {
+        unsigned old;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + unit) : "memory");
+        s_last = (old == (unsigned)a.num_splits - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    if (warp < G) {
+        // Lane k loads (max, sum) of split s0 + k and every lane its 4 dims of all
+        // kChunk splits, all before any use: one L2 round trip per chunk.
+        constexpr int kChunk = 20;
+        const float* base = a.partials + (unit * a.num_splits * G + qg) * kPartStride;
+        const int ns = a.num_splits;
+        float runM = kMinusBig, runL = 0.f;
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s0 = 0; s0 < ns; s0 += kChunk) {
+            const int n = min(kChunk, ns - s0);
+            float ms = kMinusBig, ls = 0.f;
+            if (lane < n) {
+                ms = __ldcg(base + (int64_t)(s0 + lane) * G * kPartStride);
+                ls = __ldcg(base + (int64_t)(s0 + lane) * G * kPartStride + 1);
+            }
+            float4 v[kChunk];
+#pragma unroll
+            for (int k = 0; k < kChunk; ++k)
+                v[k] = (k < n) ? __ldcg(reinterpret_cast<const float4*>(base + (int64_t)(s0 + k) * G * kPartStride + 4 + 4 * lane))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float cm = fmaxf(runM, warp_max(ms));
+            const float fr = exp2f(runM - cm);
+            const float f = exp2f(ms - cm);
+            runL = fmaf(runL, fr, warp_sum(f * ls));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc4[i] *= fr;
+#pragma unroll
+            for (int k = 0; k < kChunk; ++k) {
+                const float fk = __shfl_sync(0xffffffffu, f, k);
+                acc4[0] = fmaf(fk, v[k].x, acc4[0]); acc4[1] = fmaf(fk, v[k].y, acc4[1]);
+                acc4[2] = fmaf(fk, v[k].z, acc4[2]); acc4[3] = fmaf(fk, v[k].w, acc4[3]);
+            }
+            runM = cm;
+        }
+        const float inv = (runL > 0.f) ? 1.f / runL : 0.f;
+        *reinterpret_cast<float4*>(o + 4 * lane) =
+            make_float4(acc4[0] * inv, acc4[1] * inv, acc4[2] * inv, acc4[3] * inv);
+    }
+    if (tid == 0) a.counters[unit] = 0u;
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 template <int KB, int VB, int M>
@@ -788,6 +1041,10 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     if (lane < kFirst && lane < nmine) issue(lane, bid_cur);
 
     bool timed_out = false;
+    float m0 = kMinusBig, m1 = kMinusBig, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     {
         // q_rot = R q for query (warp) of this group; its per-query constants:
         //   qoff   = sm_scale log2(e) alpha mid sum(q_rot)
@@ -935,10 +1192,6 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
         const int ta = (2 * qd) ^ (qd & 1), tb = (2 * qd + 1) ^ (qd & 1);  // tokens of rows 2qd, 2qd+1
         const int koff = F::kcode + tr * KROW + qd * 4 * KB;  // this lane's key chunk in a page
 
-        float m0 = kMinusBig, m1 = kMinusBig, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
-        float acc[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
         int slot = 0;
         uint32_t phase = 0;
@@ -1043,77 +1296,8 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
                 t0 = fmaf(rr, sQ[0], t0); t1 = fmaf(rr, sQ[1], t1);
                 t2 = fmaf(rr8, sQ[2], t2); t3 = fmaf(rr8, sQ[3], t3);
             }
-            const float gr = lds_h2f(pg + F::gam + 2 * tr), gr8 = lds_h2f(pg + F::gam + 2 * (tr + 8));
-            float s0 = t0 * gr, s1 = t1 * gr, s2 = t2 * gr8, s3 = t3 * gr8;
-            const int tok = (p0 + warp + NW * j) * kBlockSize;
-            // the sequence's last page or a skipped one (warp-uniform): rows past
-            // the end get no weight, and the scale and zero of their slots (never
-            // written: any bytes, NaN included) are replaced by 0
-            const bool tail = !pok || tok + kBlockSize > len;
-            const bool v0 = pok && tok + tr < len, v8 = pok && tok + tr + 8 < len;
-            if (tail) {
-                if (!v0) s0 = s1 = -INFINITY;
-                if (!v8) s2 = s3 = -INFINITY;
-            }
-
-            // ---------- online softmax; the max moves only when a score beats it by kLazy ----------
-            float sr = lds_h2f(pg + F::scl + 2 * tr), sr8 = lds_h2f(pg + F::scl + 2 * (tr + 8));
-            if (tail) {
-                sr = v0 ? sr : 0.f;
-                sr8 = v8 ? sr8 : 0.f;
-            }
-            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-            constexpr float kWScale = (float)(1 << value_wshift<VB>());
-            const bool exact = fmaxf(sr, sr8) > kBigScale / kWScale;
-            if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy || (exact && (mx0 > m0 || mx1 > m1)))) {
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-                }
-                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-                const float f0 = ex2(m0 - n0), f1 = ex2(m1 - n1);
-                l0 *= f0; z0 *= f0; l1 *= f1; z1 *= f1;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    acc[i][0] *= f0; acc[i][2] *= f0;
-                    acc[i][1] *= f1; acc[i][3] *= f1;
-                }
-                m0 = n0;
-                m1 = n1;
-            }
-            const float p0v = ex2(s0 - m0), p1v = ex2(s1 - m1), p2v = ex2(s2 - m0), p3v = ex2(s3 - m1);
-            float zr = lds_h2f(pg + F::zer + 2 * tr), zr8 = lds_h2f(pg + F::zer + 2 * (tr + 8));
-            if (tail) {
-                zr = v0 ? zr : 0.f;
-                zr8 = v8 ? zr8 : 0.f;
-            }
-            l0 += p0v + p2v;
-            l1 += p1v + p3v;
-
-            // ---------- values: lane (r, qd) holds dims 16r..16r+15 of the tokens of rows 2qd, 2qd+1, 2qd+8, 2qd+9 ----------
-            // The weights w = p * scale (p <= 2^kLazy) go in as single fp16 w'.  The
-            // codes are not centred, so the rounding w - w' is also added back times
-            // the mid code through the fp32 zero-point sum; what is left is
-            // (w - w') (c - mid), a few 1e-4 of the output at most.
-            {
-                const float srw = sr * kWScale, sr8w = sr8 * kWScale;
-                const float w0 = p0v * srw, w1 = p1v * srw, w2 = p2v * sr8w, w3 = p3v * sr8w;
-                const uint32_t h01 = pack_h2(w0, w1), h23 = pack_h2(w2, w3);
-                const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-                const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-                constexpr float kMid = 0.5f * (float)((1 << VB) - 1) / kWScale;
-                z0 = fmaf(p0v, zr, fmaf(p2v, zr8, fmaf(kMid, (w0 - r01.x) + (w2 - r23.x), z0)));
-                z1 = fmaf(p1v, zr, fmaf(p3v, zr8, fmaf(kMid, (w1 - r01.y) + (w3 - r23.y), z1)));
-                const uint32_t bh0 = movtrans(h01);
-                const uint32_t bh1 = movtrans(h23);
-                uint32_t Pab[16], Pcd[16];
-                value_codes<VB>(pg + F::vcode, r, ta, tb, Pab);
-                value_codes<VB>(pg + F::vcode, r, ta + 8, tb + 8, Pcd);
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt)  // rows: dim 16r + 2mt (row r), 16r + 2mt + 1 (row r + 8)
-                    mma16816(acc[mt], Pab[2 * mt], Pab[2 * mt + 1], Pcd[2 * mt], Pcd[2 * mt + 1], bh0, bh1);
-            }
+            softmax_pv_page<KB, VB, M>(pg, pok, (p0 + warp + NW * j) * kBlockSize, len, t0, t1, t2, t3, r, tr, ta, tb,
+                                       m0, m1, l0, l1, z0, z1, acc);
 
             __syncwarp();  // every lane has read the slot: refill it with the page SPW ahead
             const int jn = j + SPW;
@@ -1142,146 +1326,8 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
             }
         }
 
-        // ---- reduce l, z over the 8 token rows, publish warp state ----
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-            z0 += __shfl_xor_sync(0xffffffffu, z0, o);
-            z1 += __shfl_xor_sync(0xffffffffu, z1, o);
-        }
-        __syncthreads();  // (A) every warp is past its pages: the remainder table is free
-        // warp states [NW][8][3] and accumulators [NW][8][128] over the table; a
-        // query's dims are stored XOR-swizzled by 4 * (query / 2) so that both
-        // these stores and the merge's 16-byte loads stay clear of bank conflicts
-        float* wst = reinterpret_cast<float*>(sm + lut_off);
-        float* wacc = reinterpret_cast<float*>(sm + lut_off + 2048);
-        if (r == 0) {
-            wst[(warp * 8 + 2 * qd) * 3 + 0] = m0;
-            wst[(warp * 8 + 2 * qd) * 3 + 1] = l0;
-            wst[(warp * 8 + 2 * qd) * 3 + 2] = z0;
-            wst[(warp * 8 + 2 * qd + 1) * 3 + 0] = m1;
-            wst[(warp * 8 + 2 * qd + 1) * 3 + 1] = l1;
-            wst[(warp * 8 + 2 * qd + 1) * 3 + 2] = z1;
-        }
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            // undo the fp16-subnormal scaling of the value codes of dims d, d + 1
-            const float e0 = (float)(1u << (value_exp<VB>(2 * mt) - value_wshift<VB>()));
-            const float e1 = (float)(1u << (value_exp<VB>(2 * mt + 1) - value_wshift<VB>()));
-            const int d = (16 * r + 2 * mt) ^ (4 * qd);
-            *reinterpret_cast<float2*>(wacc + (warp * 8 + 2 * qd) * D + d) = make_float2(acc[mt][0] * e0, acc[mt][2] * e1);
-            *reinterpret_cast<float2*>(wacc + (warp * 8 + 2 * qd + 1) * D + d) =
-                make_float2(acc[mt][1] * e0, acc[mt][3] * e1);
-        }
     }
-    // A CTA with a wait that gave up flags it and contributes an empty partial
-    // (max -inf, sum 0, acc 0), but still takes part in the split merge below:
-    // every CTA bumps the counter, so the last one still merges and resets it,
-    // and the workspace stays usable for the next call.
-    timed_out = __syncthreads_or(timed_out);  // (B)
-    if (timed_out && tid == 0) flag(a.status, TQ_FLAG_TIMEOUT);
-
-    // ---- merge the warps: thread (query warp, lane) owns dims 4 lane .. 4 lane + 3 ----
-    const float* wst = reinterpret_cast<const float*>(sm + lut_off);
-    const float* wacc = reinterpret_cast<const float*>(sm + lut_off + 2048);
-    const int qg = warp;  // query of this warp (warps 0..7)
-    float Mx = kMinusBig, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-    if (warp < 8 && !timed_out) {
-        for (int w = 0; w < NW; ++w) Mx = fmaxf(Mx, wst[(w * 8 + qg) * 3]);
-        float Z = 0.f;
-        const int dsw = (4 * lane) ^ (4 * (qg >> 1));
-        for (int w = 0; w < NW; ++w) {
-            const float f = exp2f(wst[(w * 8 + qg) * 3] - Mx);
-            L = fmaf(f, wst[(w * 8 + qg) * 3 + 1], L);
-            Z = fmaf(f, wst[(w * 8 + qg) * 3 + 2], Z);
-            const float4 v = *reinterpret_cast<const float4*>(wacc + (w * 8 + qg) * D + dsw);
-            O[0] = fmaf(f, v.x, O[0]); O[1] = fmaf(f, v.y, O[1]);
-            O[2] = fmaf(f, v.z, O[2]); O[3] = fmaf(f, v.w, O[3]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) O[i] += Z;
-    }
-
-    // Rotate this CTA's unnormalised accumulator back now, R^T O = s (.) H O / sqrt(d):
-    // R^T is linear, so the split merge below is then a plain weighted sum.
-    if (warp < G) {
-        fwht128(O, lane);
-        const uint32_t sg = lane_signs(a.c, lane);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            O[i] *= 0.08838834764831845f;
-            if ((sg >> i) & 1u) O[i] = -O[i];
-        }
-    }
-    float* o = a.out + ((int64_t)b * a.hq + (int64_t)h * G + qg) * D;
-    if (a.num_splits == 1) {
-        if (warp < G) {
-            const float inv = (L > 0.f) ? 1.f / L : 0.f;
-            *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-        }
-        return;
-    }
-
-    // publish this split's partial (max, sum, rotated acc with the zero term folded in)
-    const int64_t unit = (int64_t)b * g.hkv + h;
-    float* part = a.partials + ((unit * a.num_splits + split) * G) * kPartStride;
-    if (warp < G) {
-        float* pp = part + qg * kPartStride;
-        if (lane == 0) { pp[0] = Mx; pp[1] = L; }
-        *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(O[0], O[1], O[2], O[3]);
-    }
-    // The CTA barrier orders every thread's partial writes before thread 0's
-    // gpu-scope release (cumulativity); the acquire side pairs with the other
-    // CTAs' releases before the last one reads their partials.
-    __syncthreads();
-    __shared__ int s_last;
-    if (tid == 0) {
-        unsigned old;
-        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + unit) : "memory");
-        s_last = (old == (unsigned)a.num_splits - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    if (warp < G) {
-        // Lane k loads (max, sum) of split s0 + k and every lane its 4 dims of all
-        // kChunk splits, all before any use: one L2 round trip per chunk.
-        constexpr int kChunk = 20;
-        const float* base = a.partials + (unit * a.num_splits * G + qg) * kPartStride;
-        const int ns = a.num_splits;
-        float runM = kMinusBig, runL = 0.f;
-        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s0 = 0; s0 < ns; s0 += kChunk) {
-            const int n = min(kChunk, ns - s0);
-            float ms = kMinusBig, ls = 0.f;
-            if (lane < n) {
-                ms = __ldcg(base + (int64_t)(s0 + lane) * G * kPartStride);
-                ls = __ldcg(base + (int64_t)(s0 + lane) * G * kPartStride + 1);
-            }
-            float4 v[kChunk];
-#pragma unroll
-            for (int k = 0; k < kChunk; ++k)
-                v[k] = (k < n) ? __ldcg(reinterpret_cast<const float4*>(base + (int64_t)(s0 + k) * G * kPartStride + 4 + 4 * lane))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float cm = fmaxf(runM, warp_max(ms));
-            const float fr = exp2f(runM - cm);
-            const float f = exp2f(ms - cm);
-            runL = fmaf(runL, fr, warp_sum(f * ls));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc4[i] *= fr;
-#pragma unroll
-            for (int k = 0; k < kChunk; ++k) {
-                const float fk = __shfl_sync(0xffffffffu, f, k);
-                acc4[0] = fmaf(fk, v[k].x, acc4[0]); acc4[1] = fmaf(fk, v[k].y, acc4[1]);
-                acc4[2] = fmaf(fk, v[k].z, acc4[2]); acc4[3] = fmaf(fk, v[k].w, acc4[3]);
-            }
-            runM = cm;
-        }
-        const float inv = (runL > 0.f) ? 1.f / runL : 0.f;
-        *reinterpret_cast<float4*>(o + 4 * lane) =
-            make_float4(acc4[0] * inv, acc4[1] * inv, acc4[2] * inv, acc4[3] * inv);
-    }
-    if (tid == 0) a.counters[unit] = 0u;
+    decode_epilogue<NW, VB, 0>(a, sm, lut_off, timed_out, split, h, b, m0, m1, l0, l1, z0, z1, acc, 0u);
 }
 
 template <int KB, int VB, int M>
@@ -1325,11 +1371,20 @@ int decode_smem_kb(const Geometry& g) {
     }
 }
 
+// The tensor-core decode of 4-bit keys (tq_decode_tc.cuh), defined in the
+// 4-bit translation unit.
+int launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
+
 // All value widths (and the QJL sketch, for widths 2 .. 4) of one key width.
+// 4-bit keys without the QJL sketch and with values of 1..4 bits take the
+// decode whose score contraction runs on the tcgen05 tensor cores.
 template <int KB>
 int launch_decode_kb(const DecodeArgs& a, void* stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int vb = a.g.vb, m = a.g.m;
+    if constexpr (KB == 4) {
+        if (m == 0 && vb >= 1 && vb <= 4) return launch_decode_tc(a, s);
+    }
     if constexpr (KB >= 2 && KB <= 4) {
         if (m) {
             if (vb == 2) return launch_decode_t<KB, 2, 128>(a, s);

@@ -1,11 +1,14 @@
 // Self-test of the tensor-core building blocks the decode kernels use (see
 // tq_tcgen05.cuh): one CTA computes D = A . B for A 128 x 256 and B 256 x 16
-// (fp16, fp32 accumulate) three ways and writes all three results:
+// (fp16, fp32 accumulate) in several ways and writes every result:
 //   out[0]     A from tensor memory, B from shared memory; D read back with
 //              the 32-lanes x 32-bit load (thread = row);
 //   out[1]     the same D read back with the 16-lanes x 256-bit load, each value
 //              stored where that load's documented fragment layout puts it;
-//   out[2]     A and B both from shared memory.
+//   out[2]     A and B both from shared memory;
+//   out[3]     A written to tensor memory with the 16-lanes x 256-bit store
+//              (each value placed where that store's documented fragment
+//              layout puts it), B from shared memory.
 // A test compares each with A . B computed on the host.
 #include <cuda_runtime.h>
 
@@ -38,7 +41,7 @@ __global__ void __launch_bounds__(128, 1) tc_selftest_kernel(const uint16_t* A, 
         mbar_init(bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) tc::tmem_alloc<256>(smem_u32(taddr_s));
+    if (warp == 0) tc::tmem_alloc<512>(smem_u32(taddr_s));
     for (int i = tid; i < kSelfN * kSelfK; i += 128) {  // B[k][n] as the N x K operand
         const int k = i / kSelfN, n = i % kSelfN;
         *reinterpret_cast<uint16_t*>(sm + kmajor_off(n, k)) = B[i];
@@ -68,7 +71,30 @@ __global__ void __launch_bounds__(128, 1) tc_selftest_kernel(const uint16_t* A, 
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    constexpr uint32_t kD = 128, kD2 = 144;  // TMEM columns of the two results
+    // the same A again at columns 160.., through the 16-lane stores: thread i of
+    // the warp holds rows 16 e + i/4 and 16 e + i/4 + 8 of its lane block, column
+    // pairs 8k + 2 (i%4), 8k + 2 (i%4) + 1 of each 8-column block k
+    constexpr uint32_t kA2 = 160;
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t r[32];
+            const int row0 = warp * 32 + 16 * e + lane / 4;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = row0 + 8 * (q >> 1), col = 64 * half + 8 * k + 2 * (lane % 4) + (q & 1);
+                    r[4 * k + q] = (uint32_t)A[row * kSelfK + 2 * col] | ((uint32_t)A[row * kSelfK + 2 * col + 1] << 16);
+                }
+            tc::st_16x256b_x8(tbase + ((uint32_t)(warp * 32 + 16 * e) << 16) + kA2 + 64 * half, r);
+        }
+    tc::wait_st();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    constexpr uint32_t kD = 128, kD2 = 144, kD3 = 288;  // TMEM columns of the three results
     if (tid == 0) {
         constexpr uint32_t idesc = tc::idesc_f16_f32(kSelfM, kSelfN);
 #pragma unroll 1
@@ -76,6 +102,7 @@ __global__ void __launch_bounds__(128, 1) tc_selftest_kernel(const uint16_t* A, 
             const uint64_t bd = tc::smem_desc(sB + 256 * s, kLbo, kSbo);
             tc::mma_f16_ts(tbase + kD, tbase + 8 * s, bd, idesc, s > 0);
             tc::mma_f16_ss(tbase + kD2, tc::smem_desc(sA + 256 * s, kLbo, kSbo), bd, idesc, s > 0);
+            tc::mma_f16_ts(tbase + kD3, tbase + kA2 + 8 * s, bd, idesc, s > 0);
         }
         tc::commit(bar);
     }
@@ -92,6 +119,10 @@ __global__ void __launch_bounds__(128, 1) tc_selftest_kernel(const uint16_t* A, 
         tc::wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) out[2 * kSelfM * kSelfN + tid * 16 + j] = __uint_as_float(r[j]);
+        tc::ld_32x32b_x16(mylanes + kD3, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) out[3 * kSelfM * kSelfN + tid * 16 + j] = __uint_as_float(r[j]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t f[8];
@@ -113,7 +144,7 @@ __global__ void __launch_bounds__(128, 1) tc_selftest_kernel(const uint16_t* A, 
     __syncthreads();
     if (warp == 0) {
         tc::fence_after_sync();
-        tc::tmem_dealloc<256>(tbase);
+        tc::tmem_dealloc<512>(tbase);
     }
 }
 

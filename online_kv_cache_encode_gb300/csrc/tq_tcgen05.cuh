@@ -91,6 +91,20 @@ __device__ __forceinline__ void ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) 
                  : "memory");
 }
 
+// 16 lanes x 256 bits, eight times along the columns: thread i writes, for the
+// lanes base + i/4 (r[4k], r[4k + 1]) and base + i/4 + 8 (r[4k + 2], r[4k + 3]),
+// columns 8k + 2 (i%4) and 8k + 2 (i%4) + 1, k = 0..7 -- the layout of ld_16x256b.
+__device__ __forceinline__ void st_16x256b_x8(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 // D[tmem] (+)= A[tmem] . B[smem descriptor]; accumulate when `acc` is nonzero.
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                            uint32_t acc) {

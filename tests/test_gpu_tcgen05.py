@@ -22,5 +22,6 @@ def test_tcgen05_building_blocks():
     out = tq.selftest_tcgen05(A.cuda(), B.cuda(), st).cpu().numpy().astype(np.float64)
     torch.cuda.synchronize()
     assert st.item() == 0
-    for i, what in enumerate(["A in tensor memory", "fragment-layout read back", "A in shared memory"]):
+    for i, what in enumerate(["A in tensor memory", "fragment-layout read back", "A in shared memory",
+                              "A through the fragment-layout store"]):
         np.testing.assert_allclose(out[i], ref, rtol=1e-5, atol=1e-4, err_msg=what)
