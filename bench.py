@@ -86,7 +86,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("tq_decode_impl.cuh", "tq_device.cuh", "tq_internal.h"):
+    for f in ("tq_decode_tc.cuh", "tq_tcgen05.cuh", "tq_decode_impl.cuh", "tq_device.cuh", "tq_internal.h"):
         with open(os.path.join(ROOT, "online_kv_cache_encode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -228,6 +228,7 @@ def run_ours(args, rank, world, local):
     ring = {} if args.profile or args.no_widths else ring_stream(tq, dev, measured_peaks()[0])
     octopus = [] if args.profile or args.no_widths else octopus_sweep(tq, w, K, V, slots, bt, q_w, measured_peaks()[0])
     prefill = {} if args.profile or args.no_widths else prefill_chunk(tq, w, base, bt)
+    configs = {} if args.profile or args.no_widths else config_rows(tq, dev, measured_peaks()[0])
     del K, V
 
     # ---- per-step inputs: the new token (position T-1) and the query ----
@@ -239,7 +240,7 @@ def run_ours(args, rank, world, local):
     wss = [c.new_workspace(1, hq, bt.shape[1]) for c in copies]
 
     if args.profile:
-        # three warm-up decode launches, then three to capture (ncu -k regex:decode_kernel -s 3 -c 3)
+        # three warm-up decode launches, then three to capture (ncu -k regex:decode_tc_kernel -s 3 -c 3)
         for i in range(6):
             copies[i % N_COPIES].decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
         torch.cuda.synchronize()
@@ -367,7 +368,8 @@ def run_ours(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "operands": "4-bit codes as exact fp16 integers, fp16 hi+lo split queries/probabilities, fp32 accumulate",
+        "operands": "scores: two-level fp16 centroid operand in tensor memory x fp16 hi+lo queries (tcgen05, fp32 "
+                    "accumulate); values: codes as exact fp16 subnormals x fp16 weights (mma.sync, fp32 accumulate)",
         "data": "synthetic (seeded N(0,1) bf16 K/V with 4 x20 outlier channels per KV head and per-token lognormal(0,0.25); N(0,1) bf16 q)",
         "config": {
             "workload": "gqa32k: 64 query / 8 KV heads, head_dim 128, 32768-token context, batch 1, "
@@ -381,7 +383,7 @@ def run_ours(args, rank, world, local):
         },
         "pct_of_hbm_peak": round(100 * value / peak, 2),
         "roofline": {
-            "kernel": "decode_kernel<4,4,0>",
+            "kernel": "decode_tc_kernel<4>",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -413,6 +415,7 @@ def run_ours(args, rank, world, local):
         "ring": ring,
         "octopus": octopus,
         "prefill": prefill,
+        "configs": configs,
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "device_status": st,
@@ -635,6 +638,171 @@ def ring_stream(tq, dev, peak):
             "launches_per_step": layers, "us_per_step": round(best * 1e3, 2),
             "bytes_per_step": step_bytes, "GBps": round(gbps, 1), "frac": round(gbps / peak, 4),
             "copies": nsets}
+
+
+def device_kv(dev, T, hkv, d, seed, dtype=None):
+    """Synthetic K or V [T, hkv, d] made on the device with the workloads' recipe
+    (N(0,1), 4 channels per KV head scaled x20, one lognormal(0, 0.25) factor per
+    token), for throughput rows whose full-size inputs would take long to draw
+    on the host; the parity tests use the host generator."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(seed)
+    x = torch.randn((T, hkv, d), generator=g, device=dev)
+    ch = torch.stack([torch.randperm(d, generator=g, device=dev)[:4] for _ in range(hkv)])
+    scale = torch.ones((hkv, d), device=dev)
+    scale.scatter_(1, ch, 20.0)
+    x = x * scale[None] * torch.exp(0.25 * torch.randn((T, 1, 1), generator=g, device=dev))
+    return x.to(dtype or torch.bfloat16)
+
+
+def _time_graph(fn, reps, warm=3, rounds=3):
+    """Best per-call milliseconds of fn(i) captured reps times in one CUDA graph."""
+    import torch
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 1e9
+    for _ in range(rounds):
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) / reps)
+    del g
+    return best
+
+
+def config_rows(tq, dev, peak):
+    """Throughput of every workload at its stated size: encode Mtokens/s (one
+    token = one position of one sequence, all its KV heads) and the decode step
+    in GB/s of compressed cache read and as a fraction of HBM.  Caches that fit
+    in L2 are rotated among copies until the working set exceeds 512 MB."""
+    import torch
+    rows = {}
+
+    def rotated(make, nbytes):
+        n = max(1, -(-512_000_000 // max(nbytes, 1)))
+        return [make(i) for i in range(n)], n
+
+    # --- tiny: 1 KV head, 1024 fp32 tokens, 4/4 ---
+    w = W.WORKLOADS["tiny"]
+    T = w.lens[0]
+    K = torch.from_numpy(W.kv_tokens(w, 0, 0, 0, T)).to(dev)
+    V = torch.from_numpy(W.kv_tokens(w, 1, 0, 0, T)).to(dev)
+    bt = torch.from_numpy(W.block_table(w)).to(dev)
+    sl = torch.from_numpy(W.slots(w, W.block_table(w), 0, 0, T)).to(dev)
+    base = tq.Cache(w.num_blocks(), 1, 4, 4, 0, w.seed)
+    enc_ms = _time_graph(lambda i: base.encode(K, V, sl), 20)
+    nbytes = T * w.bytes_per_token_head()
+    caches, n = rotated(lambda i: base if i == 0 else tq.Cache(w.num_blocks(), 1, 4, 4, 0, w.seed,
+                                                              pool=base.pool.clone()), nbytes)
+    q = torch.from_numpy(W.queries(w, 0)).to(dev)
+    lens = torch.tensor([T], dtype=torch.int32, device=dev)
+    out = torch.empty((1, 1, w.d), dtype=torch.float32, device=dev)
+    wss = [c.new_workspace(1, 1, bt.shape[1]) for c in caches]
+    dec_ms = _time_graph(lambda i: caches[i % n].decode(q, bt, lens, out=out, workspace=wss[i % n]), max(20, n))
+    rows["tiny"] = {"encode_Mtok_s": round(T / (enc_ms * 1e-3) / 1e6, 2), "encode_us": round(enc_ms * 1e3, 2),
+                    "decode_us": round(dec_ms * 1e3, 2), "decode_GBps": round(nbytes / (dec_ms * 1e-3) / 1e9, 1),
+                    "decode_frac": round(nbytes / (dec_ms * 1e-3) / 1e9 / peak, 4), "decode_copies": n,
+                    "note": "137 KB of cache per step: latency-bound by size"}
+    del caches, wss, base
+    # --- swa8x4096: 8 layers (as 8 sequences) x 20 heads, window 4096, 4/4 ---
+    w = W.WORKLOADS["swa8x4096"]
+    T, B = w.lens[0], w.batch
+    btn = W.block_table(w)
+    bt = torch.from_numpy(btn).to(dev)
+    K = torch.cat([torch.from_numpy(W.kv_tokens(w, 0, b, 0, T)) for b in range(B)]).to(dev, torch.bfloat16)
+    V = torch.cat([torch.from_numpy(W.kv_tokens(w, 1, b, 0, T)) for b in range(B)]).to(dev, torch.bfloat16)
+    sl = torch.from_numpy(np.concatenate([W.slots(w, btn, b, 0, T) for b in range(B)])).to(dev)
+    base = tq.Cache(w.num_blocks(), w.hkv, 4, 4, 0, w.seed)
+    enc_ms = _time_graph(lambda i: base.encode(K, V, sl), 10)
+    nbytes = B * T * w.hkv * w.bytes_per_token_head()
+    caches, n = rotated(lambda i: base if i == 0 else tq.Cache(w.num_blocks(), w.hkv, 4, 4, 0, w.seed,
+                                                              pool=base.pool.clone()), nbytes)
+    q = torch.from_numpy(W.queries(w, 0)).to(dev, torch.bfloat16)
+    lens = torch.tensor(w.lens, dtype=torch.int32, device=dev)
+    out = torch.empty((B, w.hq, w.d), dtype=torch.float32, device=dev)
+    wss = [c.new_workspace(B, w.hq, bt.shape[1]) for c in caches]
+    dec_ms = _time_graph(lambda i: caches[i % n].decode(q, bt, lens, out=out, workspace=wss[i % n]), max(20, n))
+    rows["swa8x4096"] = {"encode_Mtok_s": round(B * T / (enc_ms * 1e-3) / 1e6, 2), "encode_us": round(enc_ms * 1e3, 2),
+                         "decode_us": round(dec_ms * 1e3, 2),
+                         "decode_GBps": round(nbytes / (dec_ms * 1e-3) / 1e9, 1),
+                         "decode_frac": round(nbytes / (dec_ms * 1e-3) / 1e9 / peak, 4), "decode_copies": n,
+                         "step": "the 8 layers' windows in one decode launch (batch 8)"}
+    del caches, wss, base, K, V
+    torch.cuda.empty_cache()
+    # --- long128k3: 4 x 131072 tokens, 3/3; prefill in 4096-token chunks, then the append + attend step ---
+    w = W.WORKLOADS["long128k3"]
+    T, B, C = w.lens[0], w.batch, w.prefill_chunk
+    btn = W.block_table(w)
+    bt = torch.from_numpy(btn).to(dev)
+    cache = tq.Cache(w.num_blocks(), w.hkv, 3, 3, 0, w.seed)
+    chunks = [(device_kv(dev, C, w.hkv, w.d, 10 + k), device_kv(dev, C, w.hkv, w.d, 20 + k)) for k in range(4)]
+    slot_chunks = [torch.from_numpy(W.slots(w, btn, b, t0, t0 + C)).to(dev) for b in range(B) for t0 in range(0, T, C)]
+    nch = len(slot_chunks)
+    enc_ms = _time_graph(lambda i: cache.encode(chunks[i % 4][0], chunks[i % 4][1], slot_chunks[i % nch]), nch)
+    kn = device_kv(dev, B, w.hkv, w.d, 30)
+    vn = device_kv(dev, B, w.hkv, w.d, 31)
+    q = device_kv(dev, B, w.hq, w.d, 32)
+    lens = torch.full((B,), T + 1, dtype=torch.int32, device=dev)
+    out = torch.empty((B, w.hq, w.d), dtype=torch.float32, device=dev)
+    ws = cache.new_workspace(B, w.hq, bt.shape[1])
+    nbytes = B * (T + 1) * w.hkv * w.bytes_per_token_head()
+    step_ms = _time_graph(lambda i: cache.decode_append(kn, vn, q, bt, lens, out=out, workspace=ws), 20)
+    dec_ms = _time_graph(lambda i: cache.decode(q, bt, lens, out=out, workspace=ws), 20)
+    rows["long128k3"] = {"prefill_encode_Mtok_s": round(C / (enc_ms * 1e-3) / 1e6, 2),
+                         "prefill_chunk_us": round(enc_ms * 1e3, 2),
+                         "step_us": round(step_ms * 1e3, 2), "step_GBps": round(nbytes / (step_ms * 1e-3) / 1e9, 1),
+                         "step_frac": round(nbytes / (step_ms * 1e-3) / 1e9 / peak, 4),
+                         "decode_us": round(dec_ms * 1e3, 2),
+                         "decode_GBps": round(nbytes / (dec_ms * 1e-3) / 1e9, 1),
+                         "decode_frac": round(nbytes / (dec_ms * 1e-3) / 1e9 / peak, 4),
+                         "cache_MB": round(nbytes / 1e6, 1),
+                         "step": "append 1 token per sequence + attend 64 query heads over 131073 tokens, one launch",
+                         "data": "K/V/q drawn on the device with the workloads' recipe"}
+    del cache, chunks, slot_chunks, ws
+    torch.cuda.empty_cache()
+    # --- qjl64: 64 sequences of U[1K, 16K] tokens, 2-bit keys + QJL (m = 128), 2-bit values ---
+    w = W.WORKLOADS["qjl64"]
+    B = w.batch
+    btn = W.block_table(w)
+    bt = torch.from_numpy(btn).to(dev)
+    cache = tq.Cache(w.num_blocks(), w.hkv, 2, 2, 128, w.seed)
+    tot = sum(w.lens)
+    Kall = device_kv(dev, tot, w.hkv, w.d, 40)
+    Vall = device_kv(dev, tot, w.hkv, w.d, 41)
+    sl = torch.from_numpy(np.concatenate([W.slots(w, btn, b, 0, w.lens[b]) for b in range(B)])).to(dev)
+    enc_ms = _time_graph(lambda i: cache.encode(Kall, Vall, sl), 5)
+    kn = device_kv(dev, B, w.hkv, w.d, 42)
+    vn = device_kv(dev, B, w.hkv, w.d, 43)
+    q = device_kv(dev, B, w.hq, w.d, 44)
+    lens_np = np.array(w.lens, dtype=np.int64) + 1
+    lens = torch.from_numpy(lens_np.astype(np.int32)).to(dev)
+    out = torch.empty((B, w.hq, w.d), dtype=torch.float32, device=dev)
+    ws = cache.new_workspace(B, w.hq, bt.shape[1])
+    nbytes = int(lens_np.sum()) * w.hkv * w.bytes_per_token_head()
+
+    step_ms = _time_graph(lambda i: cache.decode_append(kn, vn, q, bt, lens, out=out, workspace=ws), 20)
+    dec_ms = _time_graph(lambda i: cache.decode(q, bt, lens, out=out, workspace=ws), 20)
+    rows["qjl64"] = {"prefill_encode_Mtok_s": round(tot / (enc_ms * 1e-3) / 1e6, 2),
+                     "step_us": round(step_ms * 1e3, 2), "step_GBps": round(nbytes / (step_ms * 1e-3) / 1e9, 1),
+                     "step_frac": round(nbytes / (step_ms * 1e-3) / 1e9 / peak, 4),
+                     "decode_us": round(dec_ms * 1e3, 2),
+                     "decode_GBps": round(nbytes / (dec_ms * 1e-3) / 1e9, 1),
+                     "decode_frac": round(nbytes / (dec_ms * 1e-3) / 1e9 / peak, 4),
+                     "cache_MB": round(nbytes / 1e6, 1), "launches_per_step": 1,
+                     "step": "append 1 token per sequence (codes, QJL sign row) + attend 32 query heads, one launch",
+                     "data": "K/V/q drawn on the device with the workloads' recipe"}
+    del cache, Kall, Vall, ws
+    torch.cuda.empty_cache()
+    return rows
 
 
 # --------------------------------------------------------------------------- oracle (CPU)

@@ -281,8 +281,10 @@ TQ_API tq_status tq_decode_attention(const tq_cache* cache, const void* q, tq_dt
  * of the pages' decode step -- the new key/value enters the compressed cache,
  * then the query reads it ["TurboQuant: KV Cache Vector Quantization" -- three
  * steps; Bit-Axon -- KV cache memory model] -- without a separate encode
- * launch between the two.  Caches with a QJL sketch (qjl_m > 0) return
- * TQ_ERR_UNSUPPORTED: use tq_encode_kv, then tq_decode_attention. */
+ * launch between the two.  With a QJL sketch (qjl_m > 0) the appended token's
+ * residual norm and sign row are computed in the same launch, with the same
+ * arithmetic as tq_encode_kv ["OCTOPUS ..." -- methodology step 8].  OCTOPUS
+ * caches return TQ_ERR_UNSUPPORTED. */
 TQ_API tq_status tq_decode_attention_append(const tq_cache* cache, const void* k_new, const void* v_new,
                                             tq_dtype kv_dtype, const void* q, tq_dtype dtype, int batch,
                                             int num_q_heads, const int32_t* block_table,

@@ -54,9 +54,11 @@ constexpr int kSmemLimit = 227 * 1024;         // opt-in dynamic shared memory p
 constexpr long long kWaitCycles = 3000000000ll;  // bound on any wait: ~1.5 s at 2 GHz
 constexpr float kMinusBig = -1.0e30f;          // running max before any token (finite: no inf - inf)
 // stage of the appended token in shared memory: key row, value row (up to 128 B
-// each), gamma / scale / zero, the barrier that hands it to the page's owner, and
-// a barrier nothing arrives on (the wait-timeout test hook waits on it)
-constexpr int kStageValue = 128, kStageMeta = 256, kStageBar = 272, kStageNever = 280, kStageBytes = 288;
+// each), gamma / scale / zero / rho, the barrier that hands it to the page's
+// owner, a barrier nothing arrives on (the wait-timeout test hook waits on it),
+// and the QJL sign row (m / 8 = 16 bytes)
+constexpr int kStageValue = 128, kStageMeta = 256, kStageBar = 272, kStageNever = 280, kStageSig = 288,
+              kStageBytes = 304;
 // The running max is raised only when a score beats it by more than kLazy (log2
 // units), so weights stay below 2^kLazy (any reference max gives the same
 // softmax).  A page whose value scale exceeds kBigScale takes the exact max, so
@@ -502,6 +504,14 @@ __device__ __forceinline__ void cvt4(const uint32_t r[4], int dtype, float x[4])
     }
 }
 
+// Warp sum in the order the encode kernel's one-warp layout uses (strides 1, 2,
+// .. 16), so that the appended token's bytes equal what tq_encode_kv writes.
+__device__ __forceinline__ float warp_sum_up(float v) {
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
 // kraw, vraw: raw4 bits of this lane's coordinates 4 lane .. 4 lane + 3 of the new token
 template <int KB, int VB, int M>
 __device__ void append_token(const DecodeArgs& a, uint8_t* page, int off, uint8_t* stage, int lane,
@@ -520,17 +530,27 @@ __device__ void append_token(const DecodeArgs& a, uint8_t* page, int off, uint8_
     }
     const bool finite = (warp_sum(z) == 0.f);
     if (!finite && lane == 0) flag(a.status, TQ_FLAG_NONFINITE);
-    const float gamma = sqrtf(warp_sum(ss));
+    const float gamma = sqrtf(warp_sum_up(ss));
     const uint32_t sg = lane_signs(a.c, lane);
     apply_signs(k, sg);
     fwht128(k, lane);
     uint32_t kp = 0;
+    float rsd[4] = {0.f, 0.f, 0.f, 0.f};  // QJL: residual r = u_rot - C[code] in the unit frame
     if constexpr (KB <= 4) {
         const KeyThresholds<KB> kt(a.c, gamma);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int c = (gamma > 0.f) ? kt.code(k[i]) : HALF - 1;
             kp |= (uint32_t)c << (KB * i);
+            if constexpr (M > 0) {
+                if (gamma > 0.f) {
+                    const float u = (k[i] * 0.08838834764831845f) / gamma;
+                    float cv = 0.f;
+#pragma unroll
+                    for (int bb = 0; bb < (1 << KB); ++bb) cv = (c == bb) ? a.c.centroid[bb] : cv;
+                    rsd[i] = u - cv;
+                }
+            }
         }
     } else {
 #pragma unroll
@@ -558,6 +578,50 @@ __device__ void append_token(const DecodeArgs& a, uint8_t* page, int off, uint8_
     }
     store_row_both<KB>(page + F::kcode + off * (D * KB / 8), stage, kp, lane);
     store_row_both<VB>(page + F::vcode + off * (D * VB / 8), stage + kStageValue, vp, lane);
+    uint16_t hr = 0;
+    if constexpr (M > 0) {
+        // rho = ||r||; sigma_i = [(S r)_i >= 0] with the encode kernel's arithmetic
+        // (one warp, four coordinates per lane): per chunk of 32 rows every lane
+        // forms the partial dot products over its coordinates, a butterfly sums
+        // them so that lane l ends with row 32 ch + l, and the bits are OR-ed
+        // into words.  ["OCTOPUS ..." -- contribution "Optional 1-bit QJL
+        // residual"; methodology step 8]
+        float rr = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rr = fmaf(rsd[i], rsd[i], rr);
+        const float rho = sqrtf(warp_sum_up(rr));
+        hr = f16_bits(rho);
+        const float4* S4 = reinterpret_cast<const float4*>(a.S) + lane;  // row i: S4[32 i]
+        uint32_t wb[M / 32];
+#pragma unroll
+        for (int ch = 0; ch < M / 32; ++ch) {
+            float pr[32];
+#pragma unroll
+            for (int kk = 0; kk < 32; ++kk) {
+                const float4 sv = __ldg(S4 + (ch * 32 + kk) * 32);
+                pr[kk] = fmaf(sv.x, rsd[0], fmaf(sv.y, rsd[1], fmaf(sv.z, rsd[2], fmaf(sv.w, rsd[3], 0.f))));
+            }
+#pragma unroll
+            for (int m = 16, half = 16; m >= 1; m >>= 1, half >>= 1) {
+                const bool up = (lane & m) != 0;
+#pragma unroll
+                for (int kk = 0; kk < half; ++kk) {
+                    const float keep = up ? pr[kk + half] : pr[kk];
+                    const float give = up ? pr[kk] : pr[kk + half];
+                    pr[kk] = keep + __shfl_xor_sync(0xffffffffu, give, m);
+                }
+            }
+            wb[ch] = __ballot_sync(0xffffffffu, pr[0] >= 0.f);
+        }
+        if (lane < M / 32) {
+            uint32_t word = wb[0];
+#pragma unroll
+            for (int ch = 1; ch < M / 32; ++ch) word = (lane == ch) ? wb[ch] : word;
+            if (!(gamma > 0.f)) word = 0xffffffffu;
+            reinterpret_cast<uint32_t*>(page + F::sig + off * (M / 8))[lane] = word;
+            reinterpret_cast<uint32_t*>(stage + kStageSig)[lane] = word;
+        }
+    }
     if (lane == 0) {
         const uint16_t hg = f16_bits(gamma), hs = f16_bits(scale), hz = f16_bits(mn);
         reinterpret_cast<uint16_t*>(page + F::gam)[off] = hg;
@@ -565,7 +629,12 @@ __device__ void append_token(const DecodeArgs& a, uint8_t* page, int off, uint8_
         reinterpret_cast<uint16_t*>(page + F::zer)[off] = hz;
         uint16_t* sm3 = reinterpret_cast<uint16_t*>(stage + kStageMeta);
         sm3[0] = hg; sm3[1] = hs; sm3[2] = hz;
-        const bool ovf = ((hg & 0x7FFF) == 0x7C00) || ((hs & 0x7FFF) == 0x7C00) || ((hz & 0x7FFF) == 0x7C00);
+        bool ovf = ((hg & 0x7FFF) == 0x7C00) || ((hs & 0x7FFF) == 0x7C00) || ((hz & 0x7FFF) == 0x7C00);
+        if constexpr (M > 0) {
+            reinterpret_cast<uint16_t*>(page + F::rho)[off] = hr;
+            sm3[3] = hr;
+            ovf = ovf || ((hr & 0x7FFF) == 0x7C00);
+        }
         if (ovf && finite) flag(a.status, TQ_FLAG_OVERFLOW);
     }
     __syncwarp();
@@ -585,6 +654,12 @@ __device__ __forceinline__ void patch_page(uint8_t* pg, int off, const uint8_t* 
         reinterpret_cast<uint16_t*>(pg + F::gam)[off] = sm3[0];
         reinterpret_cast<uint16_t*>(pg + F::scl)[off] = sm3[1];
         reinterpret_cast<uint16_t*>(pg + F::zer)[off] = sm3[2];
+        if constexpr (M > 0) reinterpret_cast<uint16_t*>(pg + F::rho)[off] = sm3[3];
+    }
+    if constexpr (M > 0) {
+        if (lane < M / 32)
+            reinterpret_cast<uint32_t*>(pg + F::sig + off * (M / 8))[lane] =
+                reinterpret_cast<const uint32_t*>(stage + kStageSig)[lane];
     }
     __syncwarp();
 }
@@ -1016,7 +1091,7 @@ __global__ void __launch_bounds__(decode_warps<M>() * 32, 1) decode_kernel(const
     int blknew = -1;
     const int offnew = pos_new & (kBlockSize - 1);
     uint32_t kraw[4] = {0u, 0u, 0u, 0u}, vraw[4] = {0u, 0u, 0u, 0u};
-    if constexpr (M == 0) {
+    {
         if (a.knew != nullptr && len > 0) {
             const int pi = pos_new / kBlockSize - p0;
             if (pi >= 0 && pi < npages) {

@@ -838,9 +838,6 @@ static tq_status append_common(const tq_cache* c, const void* k_new, const void*
     if (c->octopus)
         return fail(TQ_ERR_UNSUPPORTED, "appending inside decode is not built for OCTOPUS caches; "
                                         "use tq_encode_kv then tq_decode_attention");
-    if (c->g.m > 0)
-        return fail(TQ_ERR_UNSUPPORTED, "appending inside decode is built for caches without QJL; "
-                                        "use tq_encode_kv then tq_decode_attention");
     if (batch > 0 && (!k_new || !v_new)) return fail(TQ_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
     if (kv_dtype != TQ_F32 && kv_dtype != TQ_BF16 && kv_dtype != TQ_F16) return fail(TQ_ERR_INVALID_ARG, "bad kv dtype");
     if ((reinterpret_cast<uintptr_t>(k_new) % 16) || (reinterpret_cast<uintptr_t>(v_new) % 16))

@@ -42,13 +42,10 @@ def test_append_gqa32k_full_size(tq, oracle):
     _check(parity.run_append_case(W.WORKLOADS["gqa32k"], oracle, tq))
 
 
-def test_append_refuses_qjl(tq):
-    import torch
-    c = tq.Cache(8, 2, 2, 2, 128)
-    z = torch.zeros((1, 2, 128), dtype=torch.bfloat16, device="cuda")
-    q = torch.zeros((1, 8, 128), dtype=torch.bfloat16, device="cuda")
-    bt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
-    lens = torch.ones(1, dtype=torch.int32, device="cuda")
-    with pytest.raises(tq.TQError) as e:
-        c.decode_append(z, z, q, bt, lens)
-    assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+@pytest.mark.parametrize("kb,vb", [(2, 2), (3, 4), (4, 3)])
+def test_append_qjl(tq, oracle, kb, vb):
+    """Caches with the QJL sketch (m = 128): the appended token's sign row and
+    residual norm are the bytes tq_encode_kv writes, and the step matches the
+    oracle and the plain decode."""
+    w = W.scaled(W.WORKLOADS["qjl64"], lens=(3000, 1201, 16, 1), hkv=2, hq=8, key_bits=kb, value_bits=vb)
+    _check(parity.run_append_case(w, oracle, tq))

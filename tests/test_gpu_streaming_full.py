@@ -38,7 +38,7 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 UNITS = 8          # (sequence, KV head) units the oracle follows in full
-APPEND_QJL = False  # whether the one-launch append step takes caches with the QJL sketch
+APPEND_QJL = True   # whether the one-launch append step takes caches with the QJL sketch
 EXTRA_CHECKS = 2   # seeded checked steps besides the first, middle and last
 
 
