@@ -86,7 +86,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("tq_decode_tc.cuh", "tq_tcgen05.cuh", "tq_decode_impl.cuh", "tq_device.cuh", "tq_internal.h"):
+    for f in ("tq_decode_impl.cuh", "tq_device.cuh", "tq_internal.h"):
         with open(os.path.join(ROOT, "online_kv_cache_encode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -240,7 +240,7 @@ def run_ours(args, rank, world, local):
     wss = [c.new_workspace(1, hq, bt.shape[1]) for c in copies]
 
     if args.profile:
-        # three warm-up decode launches, then three to capture (ncu -k regex:decode_tc_kernel -s 3 -c 3)
+        # three warm-up decode launches, then three to capture (ncu -k regex:decode_kernel -s 3 -c 3)
         for i in range(6):
             copies[i % N_COPIES].decode(q, bt, lens, out=out, workspace=wss[i % N_COPIES], status=status)
         torch.cuda.synchronize()
@@ -368,8 +368,8 @@ def run_ours(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "operands": "scores: two-level fp16 centroid operand in tensor memory x fp16 hi+lo queries (tcgen05, fp32 "
-                    "accumulate); values: codes as exact fp16 subnormals x fp16 weights (mma.sync, fp32 accumulate)",
+        "operands": "4-bit key centroids as two-level fp16 (integer part + remainder) x fp16 hi+lo queries; value "
+                    "codes as exact fp16 subnormals x fp16 weights; mma.sync, fp32 accumulate",
         "data": "synthetic (seeded N(0,1) bf16 K/V with 4 x20 outlier channels per KV head and per-token lognormal(0,0.25); N(0,1) bf16 q)",
         "config": {
             "workload": "gqa32k: 64 query / 8 KV heads, head_dim 128, 32768-token context, batch 1, "
@@ -383,7 +383,7 @@ def run_ours(args, rank, world, local):
         },
         "pct_of_hbm_peak": round(100 * value / peak, 2),
         "roofline": {
-            "kernel": "decode_tc_kernel<4>",
+            "kernel": "decode_kernel<4,4,0>",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

@@ -1446,20 +1446,11 @@ int decode_smem_kb(const Geometry& g) {
     }
 }
 
-// The tensor-core decode of 4-bit keys (tq_decode_tc.cuh), defined in the
-// 4-bit translation unit.
-int launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
-
 // All value widths (and the QJL sketch, for widths 2 .. 4) of one key width.
-// 4-bit keys without the QJL sketch and with values of 1..4 bits take the
-// decode whose score contraction runs on the tcgen05 tensor cores.
 template <int KB>
 int launch_decode_kb(const DecodeArgs& a, void* stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int vb = a.g.vb, m = a.g.m;
-    if constexpr (KB == 4) {
-        if (m == 0 && vb >= 1 && vb <= 4) return launch_decode_tc(a, s);
-    }
     if constexpr (KB >= 2 && KB <= 4) {
         if (m) {
             if (vb == 2) return launch_decode_t<KB, 2, 128>(a, s);

@@ -477,7 +477,6 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
             if (nq < -2047.0) nq = -2047.0;
             c->c.cint_f16[i] = half_bits_from_double(nq);
             c->c.crem_f16[i] = half_bits_from_double(cb->centroid[i] - (double)fd * nq);
-            c->c.cremd_f16[i] = half_bits_from_double((cb->centroid[i] - (double)fd * nq) / (double)fd);
         }
     }
     tq_codebook_free(cb);
@@ -688,9 +687,7 @@ TQ_API tq_status tq_encode_kv(const tq_cache* c, const void* K, const void* V, t
 // splits (8 pages or more each) and four times the count that fills the SMs.
 static void decode_split_plan(const tq_cache* c, int batch, int max_blocks, int* splits, int* pps) {
     const int64_t units = (int64_t)batch * c->g.hkv;
-    // warps per CTA (the tensor-core decode of 4-bit keys runs eight)
-    const bool tc4 = !c->octopus && c->g.kb == 4 && c->g.m == 0 && c->g.vb <= 4;
-    const int nw = c->octopus ? 16 : (c->g.m || tc4) ? 8 : 12;
+    const int nw = c->octopus ? 16 : c->g.m ? 8 : 12;  // warps per CTA
     const int64_t sms = c->num_sms > 0 ? c->num_sms : 1;
     int64_t lim = 4 * ((sms + units - 1) / units);
     const int64_t cap = (max_blocks + 7) / 8;

@@ -38,7 +38,6 @@ struct Consts {
     float delta;
     uint16_t cint_f16[kMaxCodebook];   // N[c] in binary16
     uint16_t crem_f16[kMaxCodebook];   // rem2[c] in binary16
-    uint16_t cremd_f16[kMaxCodebook];  // rem2[c] / delta in binary16 (|.| <= 1/2; tensor-memory operand)
     uint32_t sign_bits[kHeadDim / 32];  // bit j set when s_j = -1
 };
 
