@@ -410,11 +410,14 @@ TQ_API void tq_test_stall_waits(int64_t cycles);
  * use of tensor memory and the asynchronous MMA).  One CTA computes
  * D = A . B with A [128 x 256] and B [256 x 16] fp16 (device, row-major,
  * 16-byte aligned) and fp32 accumulation, and writes out (device fp32,
- * 4 x 128 x 16): [0] A staged in tensor memory, B in shared memory, D read
+ * 6 x 128 x 16): [0] A staged in tensor memory, B in shared memory, D read
  * back one row per thread; [1] the same D read back in the 16-lane fragment
  * layout and stored by that layout's documented positions; [2] A and B both
  * from shared memory; [3] A written to tensor memory with the 16-lane
- * fragment store.  All four equal A . B up to fp32 summation order.
+ * fragment store; [4] and [5] B in the MN-major layout under the two
+ * readings of the descriptor's byte offsets.  [0]..[3] equal A . B up to
+ * fp32 summation order, and so does the one of [4], [5] whose reading the
+ * hardware uses.
  * A bounded wait that gives up sets TQ_FLAG_TIMEOUT in *dev_status. */
 TQ_API tq_status tq_selftest_tcgen05(const void* A, const void* B, float* out, int32_t* dev_status, void* stream);
 

@@ -8,7 +8,12 @@
 //   out[2]     A and B both from shared memory;
 //   out[3]     A written to tensor memory with the 16-lanes x 256-bit store
 //              (each value placed where that store's documented fragment
-//              layout puts it), B from shared memory.
+//              layout puts it), B from shared memory;
+//   out[4], out[5]  A from tensor memory, B in the MN-major layout (element
+//              (k, n) at (n / 8) 4096 + (k / 8) 128 + (k % 8) 16 + (n % 8) 2),
+//              with the descriptor's leading / stride byte offsets read as
+//              (K step, N step) = (128, 4096) and as (4096, 128); either reading
+//              stays inside the 8 KB operand.
 // A test compares each with A . B computed on the host.
 #include <cuda_runtime.h>
 
@@ -21,7 +26,7 @@ namespace {
 constexpr int kSelfM = 128, kSelfK = 256, kSelfN = 16;
 constexpr int kSelfB = kSelfN * kSelfK * 2;        // B in shared memory: 8 KB
 constexpr int kSelfA = kSelfM * kSelfK * 2;        // A in shared memory: 64 KB
-constexpr int kSelfSmem = kSelfB + kSelfA + 16;   // + barrier + TMEM address
+constexpr int kSelfSmem = kSelfB + kSelfA + 16 + kSelfB;   // + barrier + TMEM address + MN-major B
 constexpr uint32_t kLbo = 128;                     // core matrices along K are adjacent
 constexpr uint32_t kSbo = kSelfK / 8 * 128;        // the next 8 rows: 32 core matrices on
 
@@ -49,6 +54,11 @@ __global__ void __launch_bounds__(128, 1) tc_selftest_kernel(const uint16_t* A, 
     for (int i = tid; i < kSelfM * kSelfK; i += 128) {
         const int m = i / kSelfK, k = i % kSelfK;
         *reinterpret_cast<uint16_t*>(sm + kSelfB + kmajor_off(m, k)) = A[i];
+    }
+    uint8_t* bmn = sm + kSelfB + kSelfA + 16;  // B again, MN-major
+    for (int i = tid; i < kSelfN * kSelfK; i += 128) {
+        const int k = i / kSelfN, n = i % kSelfN;
+        *reinterpret_cast<uint16_t*>(bmn + (n / 8) * 4096 + (k / 8) * 128 + (k % 8) * 16 + (n % 8) * 2) = B[i];
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
     tc::fence_before_sync();
@@ -94,15 +104,19 @@ __global__ void __launch_bounds__(128, 1) tc_selftest_kernel(const uint16_t* A, 
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    constexpr uint32_t kD = 128, kD2 = 144, kD3 = 288;  // TMEM columns of the three results
+    constexpr uint32_t kD = 128, kD2 = 144, kD3 = 288, kD4 = 304, kD5 = 320;  // TMEM columns of the results
     if (tid == 0) {
         constexpr uint32_t idesc = tc::idesc_f16_f32(kSelfM, kSelfN);
+        constexpr uint32_t idesc_mn = tc::idesc_f16_f32_bmn(kSelfM, kSelfN);
+        const uint32_t sBmn = sbase + kSelfB + kSelfA + 16;
 #pragma unroll 1
         for (int s = 0; s < kSelfK / 16; ++s) {
             const uint64_t bd = tc::smem_desc(sB + 256 * s, kLbo, kSbo);
             tc::mma_f16_ts(tbase + kD, tbase + 8 * s, bd, idesc, s > 0);
             tc::mma_f16_ss(tbase + kD2, tc::smem_desc(sA + 256 * s, kLbo, kSbo), bd, idesc, s > 0);
             tc::mma_f16_ts(tbase + kD3, tbase + kA2 + 8 * s, bd, idesc, s > 0);
+            tc::mma_f16_ts(tbase + kD4, tbase + 8 * s, tc::smem_desc(sBmn + 256 * s, 128, 4096), idesc_mn, s > 0);
+            tc::mma_f16_ts(tbase + kD5, tbase + 8 * s, tc::smem_desc(sBmn + 256 * s, 4096, 128), idesc_mn, s > 0);
         }
         tc::commit(bar);
     }
@@ -123,6 +137,14 @@ __global__ void __launch_bounds__(128, 1) tc_selftest_kernel(const uint16_t* A, 
         tc::wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) out[3 * kSelfM * kSelfN + tid * 16 + j] = __uint_as_float(r[j]);
+        tc::ld_32x32b_x16(mylanes + kD4, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) out[4 * kSelfM * kSelfN + tid * 16 + j] = __uint_as_float(r[j]);
+        tc::ld_32x32b_x16(mylanes + kD5, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) out[5 * kSelfM * kSelfN + tid * 16 + j] = __uint_as_float(r[j]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t f[8];

@@ -24,6 +24,8 @@ namespace tc {
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same with B in the MN-major layout (transpose-B bit 16).
+__host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int M, int N) { return idesc_f16_f32(M, N) | (1u << 16); }
 
 // Shared-memory matrix descriptor, no swizzle: start address, leading-dimension
 // byte offset (between core matrices adjacent along K), stride-dimension byte

@@ -125,10 +125,10 @@ def set_test_stall(cycles: int) -> None:
 
 
 def selftest_tcgen05(A: torch.Tensor, B: torch.Tensor, status: torch.Tensor | None = None) -> torch.Tensor:
-    """tq_selftest_tcgen05: A [128, 256] and B [256, 16] fp16 (CUDA) -> out [4, 128, 16] fp32."""
+    """tq_selftest_tcgen05: A [128, 256] and B [256, 16] fp16 (CUDA) -> out [6, 128, 16] fp32."""
     assert A.is_cuda and A.dtype == torch.float16 and A.shape == (128, 256) and A.is_contiguous()
     assert B.is_cuda and B.dtype == torch.float16 and B.shape == (256, 16) and B.is_contiguous()
-    out = torch.full((4, 128, 16), float("nan"), dtype=torch.float32, device=A.device)
+    out = torch.full((6, 128, 16), float("nan"), dtype=torch.float32, device=A.device)
     _check(lib().tq_selftest_tcgen05(_ptr(A), _ptr(B), _ptr(out), _ptr(status), _stream()))
     return out
 
