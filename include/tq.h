@@ -335,9 +335,12 @@ TQ_API size_t tq_prefill_workspace_bytes(const tq_cache* cache, int num_position
  * kv_cache.update; llama.cpp results: prefill speed on a par with Q8_0].
  * q: device [num_positions, num_q_heads, d]; block_table: device int32, the
  * sequence's one row of max_blocks_per_seq blocks; out: device fp32
- * [num_positions, num_q_heads, d].  Each position is one row of the decode
- * kernel (all rows read the same block-table row), so this call reads the
- * cached pages once per position. */
+ * [num_positions, num_q_heads, d].  For 4-bit keys without the QJL sketch and
+ * value codes of 1..4 bits the scores and values are dense tcgen05 tensor-core
+ * contractions: each page is unpacked once for all num_positions x group
+ * query rows of its KV head (128 rows at a time), and a second launch merges
+ * the token splits.  Other caches run each position as one row of the decode
+ * kernel, which reads the cached pages once per position. */
 TQ_API tq_status tq_prefill_attention(const tq_cache* cache, const void* q, tq_dtype dtype, int num_positions,
                                       int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
                                       int first_position, float sm_scale, float* out, void* workspace,

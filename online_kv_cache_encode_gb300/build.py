@@ -20,7 +20,8 @@ LIB = os.path.join(HERE, "libtq.so")
 # (source, extra flags, object name); the kernels of each key width 1 .. 8 are
 # one compilation of tq_inst.cu, so the widths build in parallel
 SOURCES = [("tq_host.cpp", [], "tq_host.o"), ("tq_encode.cu", [], "tq_encode.o"), ("tq_decode.cu", [], "tq_decode.o"),
-           ("tq_octopus.cu", [], "tq_octopus.o"), ("tq_selftest.cu", [], "tq_selftest.o")]
+           ("tq_octopus.cu", [], "tq_octopus.o"), ("tq_selftest.cu", [], "tq_selftest.o"),
+           ("tq_prefill_tc.cu", [], "tq_prefill_tc.o")]
 SOURCES += [("tq_inst.cu", [f"-DTQ_KB={kb}"], f"tq_inst_k{kb}.o") for kb in range(1, 9)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

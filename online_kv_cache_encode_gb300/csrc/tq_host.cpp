@@ -477,6 +477,7 @@ TQ_API tq_status tq_cache_create(void* pool, int64_t num_blocks, int block_size,
             if (nq < -2047.0) nq = -2047.0;
             c->c.cint_f16[i] = half_bits_from_double(nq);
             c->c.crem_f16[i] = half_bits_from_double(cb->centroid[i] - (double)fd * nq);
+            c->c.cremd_f16[i] = half_bits_from_double((cb->centroid[i] - (double)fd * nq) / (double)fd);
         }
     }
     tq_codebook_free(cb);
@@ -853,8 +854,29 @@ TQ_API tq_status tq_decode_attention_append(const tq_cache* c, const void* k_new
                          lens, 0, sm_scale, out, workspace, workspace_bytes, dev_status, stream);
 }
 
+// Splits of the tensor-core prefill: the (KV head, 128-row block) units spread
+// over the SMs, at most one split per 128-token tile of the block table.
+static int prefill_tc_splits(const tq_cache* c, int num_positions, int num_q_heads, int max_blocks) {
+    const int64_t rows = (int64_t)num_positions * (num_q_heads / c->g.hkv);
+    const int64_t nrb = (rows + prefill_tc_rows_per_block() - 1) / prefill_tc_rows_per_block();
+    const int64_t units = (int64_t)c->g.hkv * nrb;
+    const int64_t sms = c->num_sms > 0 ? c->num_sms : 1;
+    int64_t s = sms / units;
+    const int64_t tiles = ((int64_t)max_blocks * c->g.bs + prefill_tc_tile_tokens() - 1) / prefill_tc_tile_tokens();
+    if (s > tiles) s = tiles;
+    if (s < 1) s = 1;
+    return (int)s;
+}
+
+static bool prefill_on_tc(const tq_cache* c) { return !c->octopus && prefill_tc_supported(c->g); }
+
 TQ_API size_t tq_prefill_workspace_bytes(const tq_cache* c, int num_positions, int num_q_heads,
                                          int max_blocks_per_seq) {
+    if (!c || num_positions <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_q_heads % c->g.hkv) return 0;
+    if (prefill_on_tc(c)) {
+        const int splits = prefill_tc_splits(c, num_positions, num_q_heads, max_blocks_per_seq);
+        return align_up(prefill_tc_partials_bytes(c->g, num_positions, num_q_heads, splits), 256);
+    }
     const size_t w = tq_decode_workspace_bytes(c, num_positions, num_q_heads, max_blocks_per_seq);
     if (w == 0) return 0;
     return w + align_up((size_t)num_positions * sizeof(int32_t), 256);
@@ -876,6 +898,42 @@ TQ_API tq_status tq_prefill_attention(const tq_cache* c, const void* q, tq_dtype
     if (workspace_bytes < need) {
         set_error("workspace has %zu bytes, needs %zu", workspace_bytes, need);
         return TQ_ERR_WORKSPACE;
+    }
+    if (prefill_on_tc(c)) {
+        if (num_q_heads % c->g.hkv) return fail(TQ_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+        const int group = num_q_heads / c->g.hkv;
+        if (group > 8) return fail(TQ_ERR_UNSUPPORTED, "query group larger than 8");
+        if (!q || !block_table || !out) return fail(TQ_ERR_INVALID_ARG, "q, block_table and out must be non-NULL");
+        if (dtype != TQ_F32 && dtype != TQ_BF16 && dtype != TQ_F16) return fail(TQ_ERR_INVALID_ARG, "bad dtype");
+        if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale)) return fail(TQ_ERR_INVALID_ARG, "sm_scale must be positive");
+        const int64_t elem = dtype == TQ_F32 ? 4 : 2;
+        if ((reinterpret_cast<uintptr_t>(q) % (4 * elem)) || (reinterpret_cast<uintptr_t>(out) % 16) ||
+            (reinterpret_cast<uintptr_t>(workspace) % 256))
+            return fail(TQ_ERR_INVALID_ARG, "q must be aligned to 4 elements, out to 16 bytes, workspace to 256");
+        PrefillArgs p{};
+        p.g = c->g;
+        p.c = c->c;
+        p.pool = (const uint8_t*)c->pool;
+        p.q = q;
+        p.dtype = (int)dtype;
+        p.C = num_positions;
+        p.hq = num_q_heads;
+        p.group = group;
+        p.block_row = block_table;
+        p.max_blocks = max_blocks_per_seq;
+        p.first = first_position;
+        p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+        p.out = out;
+        p.partials = (float*)workspace;
+        p.nrb = (num_positions * group + prefill_tc_rows_per_block() - 1) / prefill_tc_rows_per_block();
+        p.splits = prefill_tc_splits(c, num_positions, num_q_heads, max_blocks_per_seq);
+        const int ntile = (first_position + num_positions + prefill_tc_tile_tokens() - 1) / prefill_tc_tile_tokens();
+        p.tiles_per_split = (ntile + p.splits - 1) / p.splits;
+        p.status = dev_status;
+        p.stall_cycles = test_stall_cycles();
+        int e = launch_prefill_tc(p, stream);
+        if (e != 0) return cuda_fail((cudaError_t)e, "prefill launch");
+        return TQ_OK;
     }
     const size_t dec = tq_decode_workspace_bytes(c, num_positions, num_q_heads, max_blocks_per_seq);
     int32_t* lens = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + dec);

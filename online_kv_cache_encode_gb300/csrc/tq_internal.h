@@ -38,6 +38,7 @@ struct Consts {
     float delta;
     uint16_t cint_f16[kMaxCodebook];   // N[c] in binary16
     uint16_t crem_f16[kMaxCodebook];   // rem2[c] in binary16
+    uint16_t cremd_f16[kMaxCodebook];  // rem2[c] / delta in binary16 (|.| <= 1/2), for the prefill
     uint32_t sign_bits[kHeadDim / 32];  // bit j set when s_j = -1
 };
 
@@ -94,6 +95,30 @@ struct DecodeArgs {
     // a barrier nothing arrives on, so that the timeout path runs
     long long stall_cycles;
 };
+
+// Chunked prefill on the tensor cores (4-bit keys, no QJL, values of 1..4 bits).
+struct PrefillArgs {
+    Geometry g;
+    Consts c;
+    const uint8_t* pool;
+    const void* q;        // [C, hq, d]
+    int dtype;
+    int C, hq, group;
+    const int32_t* block_row;
+    int max_blocks;
+    int first;            // position of the chunk's first query
+    float sm_scale_log2;
+    float* out;           // [C, hq, d] fp32
+    float* partials;      // [hkv, nrb, splits, 128 rows, 4 + d]
+    int nrb, splits, tiles_per_split;
+    int32_t* status;
+    long long stall_cycles;  // test hook, as in DecodeArgs
+};
+bool prefill_tc_supported(const Geometry& g);
+size_t prefill_tc_partials_bytes(const Geometry& g, int C, int hq, int splits);
+int prefill_tc_rows_per_block();
+int prefill_tc_tile_tokens();
+int launch_prefill_tc(const PrefillArgs& a, void* stream);
 
 // ---------------------------------------------------------------------------
 // OCTOPUS triplet key codec (second codec of a cache; values keep min-max codes)

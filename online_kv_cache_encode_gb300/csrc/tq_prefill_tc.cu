@@ -1,0 +1,599 @@
+// Chunked-prefill attention on the tcgen05 tensor cores: C consecutive query
+// positions of one sequence attend causally over its compressed cache, for
+// 4-bit keys without the QJL sketch and value codes of 1..4 bits.
+//
+// A chunk gives every KV head C x G query rows; they are far more than the
+// decode's 8, so scores and values are dense contractions and each page is
+// unpacked once for all of them.  Grid (split, row block, KV head): a CTA
+// takes 128 query rows (row r = position index * G + query in group) and the
+// 128-token tiles of its split of the token range (tiles past the block's last
+// position are skipped).  Its warps:
+//   warps 0-3  softmax: thread = query row = tensor-memory lane.  Before the
+//              tiles it rotates its query (q_rot = R q, in registers) and
+//              stores x = sm_scale log2(e) delta q_rot / qscale in fp16 hi and
+//              lo parts as the tensor-memory A operand.  Per tile it reads the
+//              row's 128 scores, applies the key norms, the causal mask and a
+//              lazy running max (raised only when a score beats it by more
+//              than 8 in log2 units), and writes the weights p * scale in fp16
+//              hi and lo parts to tensor memory as the A operand of PV.
+//   warps 4-7  producers: thread = token of the tile.  They unpack the key
+//              codes through a 256-entry table into the two-level centroid
+//              operand C[c] / delta = N[c] + rem2[c] / delta (N an integer of
+//              magnitude <= 2047, |rem2 / delta| <= 1/2, both exact enough in
+//              fp16), the value codes into exact fp16 subnormals, and the
+//              norms, scales and zero points into shared memory.
+//   lane 0 of warp 0 also loads the pages (bulk async copies into a two-tile
+//              ring) and issues the MMAs: scores S [128 rows x 128 tokens] =
+//              q_hi . N + q_lo . N + q_hi . rem2/delta (24 kind::f16 MMAs,
+//              K = 16), and O [128 rows x 128 dims] += w_hi . V + w_lo . V (16
+//              MMAs) in fp32 tensor memory, each group committed to an
+//              mbarrier.  Right after the softmax of tile u it issues PV of
+//              tile u, starts the copies of tile u + 2 and the scores of tile
+//              u + 1, which the producers have prepared meanwhile.
+// Logits and values stay in the rotated frame; keys are never reconstructed
+// ["OCTOPUS ..." -- TL;DR / step 7; deep dive -- [RHT effect]].  Each split
+// writes its rows' partial (max, sum, unnormalised rotated accumulator with
+// the zero-point term) and a second kernel merges the splits and applies the
+// one inverse rotation R^T = diag(s) H / sqrt(d) per output.  The chunk's own
+// keys and values are in the cache before attention reads it [TurboQuant deep
+// dive -- attention forward with kv_cache.update].
+#include <cuda_runtime.h>
+
+#include "tq_decode_impl.cuh"
+#include "tq_tcgen05.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kPfRows = 128;                    // query rows per CTA (tensor-memory lanes)
+constexpr int kPfTile = 128;                    // tokens per tile
+constexpr int kPfPages = kPfTile / kBlockSize;  // pages per tile
+constexpr int kPfWarps = 8;
+constexpr int kPfThreads = kPfWarps * 32;
+constexpr int kPartRow = 4 + kHeadDim;          // partial record: max, sum, 2 pad, acc[128]
+// tensor-memory columns: query operand (hi 0..63, lo 64..127), scores, weights
+// (hi 256..319, lo 320..383), output accumulator
+constexpr uint32_t kTq = 0, kTs = 128, kTp = 256, kTo = 384;
+constexpr int kTmemCols = 512;
+// key operand [N = 128 tokens x K = 128 dims], K-major core matrices
+constexpr uint32_t kKLbo = 128, kKSbo = 2048;
+// value operand [K = 128 tokens x N = 128 dims], MN-major core matrices (8
+// tokens x 8 dims, dims contiguous): 8-token groups 128 bytes apart, 8-dim
+// groups 2048 apart.  The descriptor's leading byte offset is the step along K
+// and its stride byte offset the step along N, as in the K-major layout (the
+// self-test checks this reading).
+constexpr uint32_t kVLbo = 128, kVSbo = 2048;
+// barriers: page slots [2][8], then key operand full, value operand full,
+// scores full, weights full, output updated, query operand stored, and one
+// that nothing arrives on (the wait-timeout test hook waits on it)
+constexpr int kBarBk = 2 * kPfPages, kBarBv = kBarBk + 1, kBarS = kBarBk + 2, kBarP = kBarBk + 3,
+              kBarO = kBarBk + 4, kBarQ = kBarBk + 5, kBarNever = kBarBk + 6, kNumBars = kBarBk + 7;
+// The PV weights go in as w = p * scale * 2^-8 (p <= 2^8 under the lazy max),
+// so that their fp16 hi part never overflows; the output takes 2^(24 + 8) back
+// (2^24 from the value codes held as fp16 subnormals).
+constexpr float kWShift = 0.00390625f, kOutScale = 4294967296.f;
+
+template <int VB>
+struct PfLayout {
+    static constexpr int bn = 0;                        // key operand, integer parts
+    static constexpr int br = bn + kPfTile * kHeadDim * 2;   // key operand, remainders / delta
+    static constexpr int bv = br + kPfTile * kHeadDim * 2;   // value operand
+    static constexpr int ring = bv + kPfTile * kHeadDim * 2;
+    static constexpr int stride = PageFmt<4, VB, 0>::stride;
+    // per token of a tile, two tiles deep (by tile parity): gamma, scale, zero
+    // and the mask (0, or -inf for a token that is not there)
+    static constexpr int gam = ring + 2 * kPfPages * stride;
+    static constexpr int scl = gam + 2 * kPfTile * 4;
+    static constexpr int zer = scl + 2 * kPfTile * 4;
+    static constexpr int msk = zer + 2 * kPfTile * 4;
+    static constexpr int lut = msk + 2 * kPfTile * 4;   // 256 entries x (N pair, rem2/delta pair)
+    static constexpr int bars = lut + 256 * 8;
+    static constexpr int ok = bars + 8 * kNumBars;      // page copy issued and its block id valid [2][8]
+    static constexpr int taddr = ok + 4 * 2 * kPfPages;
+    static constexpr int total = taddr + 16;
+};
+
+// element (token t, dims 8 dg .. 8 dg + 7) chunk of the key operand
+__device__ __forceinline__ uint32_t key_chunk(int t, int dg) {
+    return (uint32_t)((t >> 3) * kKSbo + dg * kKLbo + (t & 7) * 16);
+}
+// element (token t, dims 8 dg .. 8 dg + 7) chunk of the value operand
+__device__ __forceinline__ uint32_t val_chunk(int t, int dg) {
+    return (uint32_t)(dg * kVSbo + (t >> 3) * kVLbo + (t & 7) * 16);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Bounded wait that gives up at once after an earlier one of this thread gave up.
+__device__ __forceinline__ void pf_wait(uint32_t bar, uint32_t parity, bool& bad) {
+    if (!bad && !mbar_wait(bar, parity)) bad = true;
+}
+
+template <int VB>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const PrefillArgs a) {
+    using F = PageFmt<4, VB, 0>;
+    using L = PfLayout<VB>;
+    constexpr int D = kHeadDim;
+    static_assert(L::total <= kSmemLimit, "prefill does not fit in shared memory");
+    extern __shared__ __align__(128) uint8_t sm[];
+    const Geometry& g = a.g;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int split = blockIdx.x, rb = blockIdx.y, h = blockIdx.z;
+    const int G = a.group;
+    const int R = a.C * G;                            // query rows of this KV head
+    const int r0 = rb * kPfRows;                      // first row of the block
+    const int rows = min(kPfRows, R - r0);
+    const int p_hi = a.first + (r0 + rows - 1) / G;   // last position of the block
+    const int nt_rb = p_hi / kPfTile + 1;             // tiles the block needs
+    const int t_first = split * a.tiles_per_split;
+    const int U = min(a.tiles_per_split, nt_rb - t_first);  // this CTA's tiles
+    float* part = a.partials + (((int64_t)h * a.nrb + rb) * a.splits + split) * kPfRows * kPartRow;
+
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (U <= 0) {
+        // no tile of this split reaches the block's positions: empty partials
+        for (int i = tid; i < kPfRows; i += kPfThreads) {
+            part[i * kPartRow] = kMinusBig;
+            part[i * kPartRow + 1] = 0.f;
+        }
+        for (int i = tid; i < kPfRows * D; i += kPfThreads) part[(i / D) * kPartRow + 4 + (i % D)] = 0.f;
+        return;
+    }
+
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t bar0 = sbase + L::bars;
+    auto bar = [&](int i) { return bar0 + 8 * i; };
+    int* page_ok = reinterpret_cast<int*>(sm + L::ok);
+    float* gam_s = reinterpret_cast<float*>(sm + L::gam);
+    float* scl_s = reinterpret_cast<float*>(sm + L::scl);
+    float* zer_s = reinterpret_cast<float*>(sm + L::zer);
+    float* msk_s = reinterpret_cast<float*>(sm + L::msk);
+    if (tid == 0) {
+        for (int i = 0; i < 2 * kPfPages; ++i) mbar_init(bar(i), 1);
+        mbar_init(bar(kBarBk), 4);
+        mbar_init(bar(kBarBv), 4);
+        mbar_init(bar(kBarS), 1);
+        mbar_init(bar(kBarP), 4);
+        mbar_init(bar(kBarO), 1);
+        mbar_init(bar(kBarQ), 4);
+        mbar_init(bar(kBarNever), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tc::tmem_alloc<kTmemCols>(sbase + L::taddr);
+    {
+        // byte e (codes e & 15, e >> 4) -> (N[e & 15], N[e >> 4]), (rem2/delta[e & 15], rem2/delta[e >> 4])
+        uint32_t* lut = reinterpret_cast<uint32_t*>(sm + L::lut);
+        for (int e = tid; e < 256; e += kPfThreads) {
+            lut[2 * e] = (uint32_t)a.c.cint_f16[e & 15] | ((uint32_t)a.c.cint_f16[e >> 4] << 16);
+            lut[2 * e + 1] = (uint32_t)a.c.cremd_f16[e & 15] | ((uint32_t)a.c.cremd_f16[e >> 4] << 16);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + L::taddr);
+    bool bad = false;  // a bounded wait of this thread gave up
+    bool stalled = false;
+    if (a.stall_cycles > 0 && (split & 1)) {
+        // test hook: every thread of the CTA waits on a barrier that nothing
+        // arrives on; the wait runs out and the CTA skips its tiles
+        stalled = !mbar_wait_for(bar(kBarNever), 0, a.stall_cycles);
+    }
+
+    // ---- loader / MMA issuer (lane 0 of warp 0) ----
+    const int npg = (p_hi + kBlockSize) / kBlockSize;  // pages the block needs
+    auto load_tile = [&](int u) {
+        const int half = u & 1;
+        for (int j = 0; j < kPfPages; ++j) {
+            const int pgi = (t_first + u) * kPfPages + j;
+            const uint32_t b = bar(half * kPfPages + j);
+            if (pgi < npg) {
+                const int blk = __ldg(a.block_row + pgi);
+                if (blk >= 0 && blk < g.num_blocks) {
+                    page_ok[half * kPfPages + j] = 1;
+                    mbar_arrive_tx(b, (uint32_t)F::bytes);
+                    bulk_g2s(sbase + L::ring + (half * kPfPages + j) * L::stride,
+                             a.pool + ((int64_t)blk * g.hkv + h) * F::bytes, (uint32_t)F::bytes, b);
+                } else {
+                    flag(a.status, TQ_FLAG_BAD_SLOT);
+                    page_ok[half * kPfPages + j] = 0;
+                    mbar_arrive(b);
+                }
+            } else {
+                page_ok[half * kPfPages + j] = -1;  // past the block's last position: not loaded
+                mbar_arrive(b);
+            }
+        }
+    };
+    constexpr uint32_t idesc_s = tc::idesc_f16_f32(kPfRows, kPfTile);
+    constexpr uint32_t idesc_v = tc::idesc_f16_f32_bmn(kPfRows, kHeadDim);
+    // scores of tile u: needs its key operand (and the previous tile's scores read)
+    auto issue_scores = [&](int u) {
+        pf_wait(bar(kBarBk), u & 1, bad);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            tc::mma_f16_ts(tmem + kTs, tmem + kTq + 8 * s, tc::smem_desc(sbase + L::bn + 256 * s, kKLbo, kKSbo),
+                           idesc_s, s > 0 ? 1u : 0u);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            tc::mma_f16_ts(tmem + kTs, tmem + kTq + 64 + 8 * s, tc::smem_desc(sbase + L::bn + 256 * s, kKLbo, kKSbo),
+                           idesc_s, 1u);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            tc::mma_f16_ts(tmem + kTs, tmem + kTq + 8 * s, tc::smem_desc(sbase + L::br + 256 * s, kKLbo, kKSbo),
+                           idesc_s, 1u);
+        tc::commit(bar(kBarS));
+    };
+    // values of tile u: needs its value operand and all weights
+    auto issue_values = [&](int u) {
+        pf_wait(bar(kBarBv), u & 1, bad);
+        pf_wait(bar(kBarP), u & 1, bad);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            tc::mma_f16_ts(tmem + kTo, tmem + kTp + 8 * s, tc::smem_desc(sbase + L::bv + 256 * s, kVLbo, kVSbo),
+                           idesc_v, (u > 0 || s > 0) ? 1u : 0u);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            tc::mma_f16_ts(tmem + kTo, tmem + kTp + 64 + 8 * s, tc::smem_desc(sbase + L::bv + 256 * s, kVLbo, kVSbo),
+                           idesc_v, 1u);
+        tc::commit(bar(kBarO));
+    };
+    const bool issuer = warp == 0 && lane == 0;
+    if (issuer && !stalled) {
+        load_tile(0);
+        if (U > 1) load_tile(1);
+    }
+
+    if (stalled) {
+        for (int i = tid; i < kPfRows; i += kPfThreads) {
+            part[i * kPartRow] = kMinusBig;
+            part[i * kPartRow + 1] = 0.f;
+        }
+        for (int i = tid; i < kPfRows * D; i += kPfThreads) part[(i / D) * kPartRow + 4 + (i % D)] = 0.f;
+        bad = true;
+    } else if (warp >= 4) {
+        // ================= producers: thread = token of the tile =================
+        const int t = tid - 128;          // token of the tile
+        const int j = t >> 4, slot = t & 15;
+        const uint32_t* lut = reinterpret_cast<const uint32_t*>(sm + L::lut);
+        for (int u = 0; u < U; ++u) {
+            const int half = u & 1;
+            pf_wait(bar(half * kPfPages + j), (u >> 1) & 1, bad);
+            const int pok = page_ok[half * kPfPages + j];
+            const int tok = (t_first + u) * kPfTile + t;
+            const bool valid = pok == 1 && tok <= p_hi && !bad;
+            const uint32_t pg = sbase + L::ring + (half * kPfPages + j) * L::stride;
+            // ---- keys: the previous tile's scores MMA has read the operand ----
+            if (u > 0) pf_wait(bar(kBarS), (u - 1) & 1, bad);
+            {
+                uint32_t w[16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 v4 = valid ? lds128(pg + F::kcode + slot * 64 + 16 * c) : make_uint4(0, 0, 0, 0);
+                    w[4 * c] = v4.x; w[4 * c + 1] = v4.y; w[4 * c + 2] = v4.z; w[4 * c + 3] = v4.w;
+                }
+#pragma unroll
+                for (int dg = 0; dg < 16; ++dg) {
+                    // dims 8 dg .. 8 dg + 7 = code bytes 4 dg .. 4 dg + 3 = word dg
+                    uint32_t nn[4], rr[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t e = (w[dg] >> (8 * k)) & 0xFFu;
+                        const uint2 v = valid ? *reinterpret_cast<const uint2*>(lut + 2 * e) : make_uint2(0u, 0u);
+                        nn[k] = v.x;
+                        rr[k] = v.y;
+                    }
+                    sts128(sbase + L::bn + key_chunk(t, dg), nn[0], nn[1], nn[2], nn[3]);
+                    sts128(sbase + L::br + key_chunk(t, dg), rr[0], rr[1], rr[2], rr[3]);
+                }
+                float gm = 0.f;
+                if (valid) gm = lds_h2f(pg + F::gam + 2 * slot);
+                gam_s[half * kPfTile + t] = gm;
+                msk_s[half * kPfTile + t] = valid ? 0.f : -INFINITY;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarBk));
+            // ---- values: the previous tile's PV MMA has read the operand ----
+            if (u > 0) pf_wait(bar(kBarO), (u - 1) & 1, bad);
+            {
+                constexpr int VROW = D * VB / 8;
+                uint32_t w[VB * 4];
+#pragma unroll
+                for (int c = 0; c < VB; ++c) {
+                    const uint4 v4 = valid ? lds128(pg + F::vcode + slot * VROW + 16 * c) : make_uint4(0, 0, 0, 0);
+                    w[4 * c] = v4.x; w[4 * c + 1] = v4.y; w[4 * c + 2] = v4.z; w[4 * c + 3] = v4.w;
+                }
+#pragma unroll
+                for (int dg = 0; dg < 16; ++dg) {
+                    uint32_t pr[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        // codes of dims 8 dg + 2k, 8 dg + 2k + 1 as fp16 subnormals c * 2^-24
+                        const uint32_t c0 = bits_at<VB * 4>(w, VB * (8 * dg + 2 * k), VB);
+                        const uint32_t c1 = bits_at<VB * 4>(w, VB * (8 * dg + 2 * k + 1), VB);
+                        pr[k] = c0 | (c1 << 16);
+                    }
+                    sts128(sbase + L::bv + val_chunk(t, dg), pr[0], pr[1], pr[2], pr[3]);
+                }
+                float sc = 0.f, zr = 0.f;
+                if (valid) {
+                    sc = lds_h2f(pg + F::scl + 2 * slot);
+                    zr = lds_h2f(pg + F::zer + 2 * slot);
+                }
+                scl_s[half * kPfTile + t] = sc * kWShift;
+                zer_s[half * kPfTile + t] = zr;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarBv));
+        }
+    } else {
+        // ================= softmax: thread = query row =================
+        const int r = tid;
+        const int rg = r0 + r;
+        const bool row_ok = r < rows;
+        const int pos = row_ok ? a.first + rg / G : -1;  // the row's position (-1: padding row)
+        const uint32_t tl = (uint32_t)(warp * 32) << 16;
+        const float ksc = a.sm_scale_log2;
+        float qs = 1.f;
+        {
+            // q_rot = R q for this row, in registers; x = ksc delta q_rot / qscale to tensor memory
+            float x[D];
+            if (row_ok) {
+                const int64_t qrow = ((int64_t)(rg / G) * a.hq + (int64_t)h * G + rg % G) * D;
+#pragma unroll
+                for (int i = 0; i < D; i += 4) load4(a.q, a.dtype, qrow + i, x + i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < D; ++i) x[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < D; ++i)
+                if ((a.c.sign_bits[i >> 5] >> (i & 31)) & 1u) x[i] = -x[i];
+#pragma unroll
+            for (int hh = 1; hh < D; hh <<= 1)
+#pragma unroll
+                for (int i = 0; i < D; ++i)
+                    if ((i & hh) == 0) {
+                        const float p = x[i], q2 = x[i + hh];
+                        x[i] = p + q2;
+                        x[i + hh] = p - q2;
+                    }
+            float mx = 0.f;
+#pragma unroll
+            for (int i = 0; i < D; ++i) {
+                x[i] *= 0.08838834764831845f;
+                mx = fmaxf(mx, fabsf(x[i]));
+            }
+            const float big = fabsf(a.c.delta) * ksc * mx;
+            qs = (big > 0.f) ? exp2f(ceilf(log2f(big / 512.f))) : 1.f;
+            const float e = ksc * a.c.delta / qs;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float x0 = e * x[64 * c + 2 * k], x1 = e * x[64 * c + 2 * k + 1];
+                    hi[k] = pack_h2(x0, x1);
+                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
+                    lo[k] = pack_h2(x0 - hf.x, x1 - hf.y);
+                }
+                tc::st_32x32b_x32(tmem + tl + kTq + 32 * c, hi);
+                tc::st_32x32b_x32(tmem + tl + kTq + 64 + 32 * c, lo);
+            }
+            tc::wait_st();
+        }
+        // the query operand of this warp's 32 rows is in tensor memory
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQ));
+        if (issuer) {
+            pf_wait(bar(kBarQ), 0, bad);
+            issue_scores(0);
+        }
+        __syncwarp();
+
+        float m = kMinusBig, l = 0.f, z = 0.f;
+        for (int u = 0; u < U; ++u) {
+            const int base = (t_first + u) * kPfTile;
+            // scores of tile u, then its per-token norms, masks, scales and zero
+            // points: the producers write them all before arriving on the value
+            // barrier (whose next phase needs this warpgroup's weights, so a wait
+            // on it never falls a whole phase behind)
+            pf_wait(bar(kBarS), u & 1, bad);
+            pf_wait(bar(kBarBv), u & 1, bad);
+            tc::fence_after_sync();
+            float s[kPfTile];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tc::ld_32x32b_x32(tmem + tl + kTs + 32 * c, v);
+                tc::wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) s[32 * c + k] = __uint_as_float(v[k]);
+            }
+            // logit (log2 units) = S * qscale * gamma; tokens that are not there
+            // and, causally, tokens after the row's position get -inf
+            float mt = kMinusBig;
+            const int kmax = pos - base;  // the last token of the tile the row sees
+            const float4* g4 = reinterpret_cast<const float4*>(gam_s + (u & 1) * kPfTile);
+            const float4* m4 = reinterpret_cast<const float4*>(msk_s + (u & 1) * kPfTile);
+#pragma unroll
+            for (int k4 = 0; k4 < kPfTile / 4; ++k4) {
+                const float4 gg = g4[k4], mm = m4[k4];
+                const float gv[4] = {gg.x, gg.y, gg.z, gg.w}, mv[4] = {mm.x, mm.y, mm.z, mm.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int k = 4 * k4 + i;
+                    const float v = fmaf(s[k] * qs, gv[i], mv[i]);
+                    s[k] = (k <= kmax) ? v : -INFINITY;
+                    mt = fmaxf(mt, s[k]);
+                }
+            }
+            // the weights' region and the output accumulator are free again
+            if (u > 0) pf_wait(bar(kBarO), (u - 1) & 1, bad);
+            tc::fence_after_sync();
+            if (mt > m + kLazy) {
+                const float f = ex2(m - mt);
+                l *= f;
+                z *= f;
+                if (u > 0) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[32];
+                        tc::ld_32x32b_x32(tmem + tl + kTo + 32 * c, v);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
+                        tc::st_32x32b_x32(tmem + tl + kTo + 32 * c, v);
+                    }
+                }
+                m = mt;
+            }
+            const float2* z2 = reinterpret_cast<const float2*>(zer_s + (u & 1) * kPfTile);
+            const float2* c2 = reinterpret_cast<const float2*>(scl_s + (u & 1) * kPfTile);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int t0 = 32 * c + 2 * k, t1 = t0 + 1;
+                    const float p0 = ex2(s[t0] - m), p1 = ex2(s[t1] - m);
+                    const float2 zz = z2[16 * c + k], cc = c2[16 * c + k];
+                    l += p0 + p1;
+                    z = fmaf(p0, zz.x, fmaf(p1, zz.y, z));
+                    const float w0 = p0 * cc.x, w1 = p1 * cc.y;
+                    hi[k] = pack_h2(w0, w1);
+                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
+                    lo[k] = pack_h2(w0 - hf.x, w1 - hf.y);
+                }
+                tc::st_32x32b_x16(tmem + tl + kTp + 16 * c, hi);
+                tc::st_32x32b_x16(tmem + tl + kTp + 64 + 16 * c, lo);
+            }
+            tc::wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarP));
+            if (issuer) {
+                issue_values(u);
+                // the ring half of tile u is free: its values are unpacked
+                if (u + 2 < U) load_tile(u + 2);
+                if (u + 1 < U) issue_scores(u + 1);
+            }
+            __syncwarp();
+        }
+        // ---- this split's partial for the row: max, sum, rotated accumulator + zero term ----
+        pf_wait(bar(kBarO), (U - 1) & 1, bad);
+        tc::fence_after_sync();
+        float* pr = part + r * kPartRow;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tc::ld_32x32b_x32(tmem + tl + kTo + 32 * c, v);
+            tc::wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4*>(pr + 4 + 32 * c + k) =
+                    make_float4(fmaf(__uint_as_float(v[k]), kOutScale, z), fmaf(__uint_as_float(v[k + 1]), kOutScale, z),
+                                fmaf(__uint_as_float(v[k + 2]), kOutScale, z), fmaf(__uint_as_float(v[k + 3]), kOutScale, z));
+        }
+        pr[0] = m;
+        pr[1] = l;
+    }
+    // every tensor-core operation of the CTA is complete (the softmax warps
+    // waited for the last PV commit): release tensor memory
+    bad = __syncthreads_or(bad);
+    if (bad && tid == 0) flag(a.status, TQ_FLAG_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc<kTmemCols>(tmem);
+    }
+}
+
+// One warp per output row (position, query head): merge the splits' partials
+// of its row and rotate back, out = R^T (acc / sum) = diag(s) H (acc / sum) / sqrt(d).
+__global__ void __launch_bounds__(128) prefill_merge_kernel(const PrefillArgs a) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);  // i * hq + query head
+    if (row >= (int64_t)a.C * a.hq) return;
+    const int i = (int)(row / a.hq), qh = (int)(row % a.hq);
+    const int G = a.group, h = qh / G, g = qh % G;
+    const int rg = i * G + g, rb = rg / kPfRows, r = rg % kPfRows;
+    const float* base = a.partials + (((int64_t)h * a.nrb + rb) * a.splits) * kPfRows * kPartRow + r * kPartRow;
+    const int64_t sstride = (int64_t)kPfRows * kPartRow;
+    float M = kMinusBig;
+    for (int s = 0; s < a.splits; ++s) M = fmaxf(M, base[s * sstride]);
+    float Ls = 0.f, x[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < a.splits; ++s) {
+        const float* p = base + s * sstride;
+        const float f = exp2f(p[0] - M);
+        Ls = fmaf(f, p[1], Ls);
+        const float4 v = *reinterpret_cast<const float4*>(p + 4 + 4 * lane);
+        x[0] = fmaf(f, v.x, x[0]); x[1] = fmaf(f, v.y, x[1]); x[2] = fmaf(f, v.z, x[2]); x[3] = fmaf(f, v.w, x[3]);
+    }
+    const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k] *= inv;
+    fwht128(x, lane);
+    const uint32_t sg = (a.c.sign_bits[lane >> 3] >> (4 * (lane & 7))) & 0xFu;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        x[k] *= 0.08838834764831845f;
+        if ((sg >> k) & 1u) x[k] = -x[k];
+    }
+    *reinterpret_cast<float4*>(a.out + row * kHeadDim + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
+}
+
+template <int VB>
+int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t s) {
+    using F = PageFmt<4, VB, 0>;
+    const Geometry& g = a.g;
+    if (g.page_bytes != F::bytes || g.vcode_off != F::vcode || g.gam_off != F::gam || g.scl_off != F::scl ||
+        g.zer_off != F::zer || g.bs != kBlockSize || g.d != kHeadDim || g.m != 0 || g.kb != 4)
+        return (int)cudaErrorInvalidValue;
+    auto kern = prefill_tc_kernel<VB>;
+    static int done[64] = {};
+    cudaError_t e = ensure_smem_limit(kern, PfLayout<VB>::total, done);
+    if (e != cudaSuccess) return (int)e;
+    e = launch_programmatic(kern, dim3((unsigned)a.splits, (unsigned)a.nrb, (unsigned)g.hkv), dim3(kPfThreads),
+                            (size_t)PfLayout<VB>::total, s, a);
+    if (e != cudaSuccess) return (int)e;
+    const int64_t rows = (int64_t)a.C * a.hq;
+    return (int)launch_programmatic(prefill_merge_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, s, a);
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const Geometry& g) { return g.kb == 4 && g.m == 0 && g.vb >= 1 && g.vb <= 4; }
+
+size_t prefill_tc_partials_bytes(const Geometry& g, int C, int hq, int splits) {
+    const int G = hq / g.hkv;
+    const int64_t nrb = ((int64_t)C * G + kPfRows - 1) / kPfRows;
+    return (size_t)g.hkv * nrb * splits * kPfRows * kPartRow * sizeof(float);
+}
+
+int prefill_tc_rows_per_block() { return kPfRows; }
+int prefill_tc_tile_tokens() { return kPfTile; }
+
+int launch_prefill_tc(const PrefillArgs& a, void* stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (a.g.vb) {
+        case 1: return launch_prefill_tc_t<1>(a, s);
+        case 2: return launch_prefill_tc_t<2>(a, s);
+        case 3: return launch_prefill_tc_t<3>(a, s);
+        case 4: return launch_prefill_tc_t<4>(a, s);
+        default: return (int)cudaErrorNotSupported;
+    }
+}
+
+}  // namespace tq

@@ -11,9 +11,10 @@
 //              layout puts it), B from shared memory;
 //   out[4], out[5]  A from tensor memory, B in the MN-major layout (element
 //              (k, n) at (n / 8) 4096 + (k / 8) 128 + (k % 8) 16 + (n % 8) 2),
-//              with the descriptor's leading / stride byte offsets read as
-//              (K step, N step) = (128, 4096) and as (4096, 128); either reading
-//              stays inside the 8 KB operand.
+//              with the descriptor's leading / stride byte offsets set to
+//              (128, 4096) and to (4096, 128); either setting stays inside the
+//              8 KB operand, and only the first (leading = step along K) is the
+//              hardware's reading.
 // A test compares each with A . B computed on the host.
 #include <cuda_runtime.h>
 

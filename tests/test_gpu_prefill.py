@@ -24,10 +24,11 @@ def tq(oracle):
     return T
 
 
-def _prefill_case(tq, oracle, first, C, kb=4, vb=4, G=8, octopus=False):
+def _prefill_case(tq, oracle, first, C, kb=4, vb=4, G=8, octopus=False, dtype="bf16", bad_block=None):
     import torch
 
-    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(first + C,), hkv=2, hq=2 * G, key_bits=kb, value_bits=vb)
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(first + C,), hkv=2, hq=2 * G, key_bits=kb, value_bits=vb,
+                 dtype=dtype)
     bt = W.block_table(w)
     nb = w.num_blocks()
     K = W.kv_tokens(w, 0, 0, 0, first + C)
@@ -39,19 +40,24 @@ def _prefill_case(tq, oracle, first, C, kb=4, vb=4, G=8, octopus=False):
         oc = oracle.Cache(w.d, kb, vb, 0, w.block_size, w.hkv, nb, w.seed)
     pool = oc.new_pool()
     assert oc.encode(K, V, sl, pool) == 0
-    q = W.bf16_round(np.random.default_rng(first * 7 + C).standard_normal((C, w.hq, w.d)).astype(np.float32))
+    q = W.to_dtype(w, np.random.default_rng(first * 7 + C).standard_normal((C, w.hq, w.d)).astype(np.float32))
     sm = W.sm_scale(w)
     lens = np.arange(first + 1, first + C + 1, dtype=np.int32)
+    if bad_block is not None:
+        bt = bt.copy()
+        bt[0, bad_block] = nb + 3   # a block id past the pool: that page is skipped and flagged
     out_o, st = oc.decode(pool, q.astype(np.float64), np.repeat(bt, C, axis=0), lens, sm)
-    assert st == 0
+    assert st == (0 if bad_block is None else oracle.FLAG_BAD_SLOT)
     dev = torch.device("cuda")
     pt = torch.from_numpy(pool).to(dev)
     gc = (tq.OctopusCache(nb, w.hkv, kb, vb, w.seed, pool=pt) if octopus
           else tq.Cache(nb, w.hkv, kb, vb, 0, w.seed, pool=pt))
     status = tq.new_status()
-    out = gc.prefill(torch.from_numpy(q).to(dev, torch.bfloat16), torch.from_numpy(bt[0]).to(dev), first, sm,
+    tdt = {"f32": torch.float32, "f16": torch.float16}.get(dtype, torch.bfloat16)
+    out = gc.prefill(torch.from_numpy(q).to(dev, tdt), torch.from_numpy(bt[0]).to(dev), first, sm,
                      status=status).cpu().numpy().astype(np.float64)
-    assert int(status.item()) == 0
+    assert int(status.item()) == (0 if bad_block is None else tq.FLAG_BAD_SLOT)
+    assert np.all(np.isfinite(out))
     return parity.rel_err(out, out_o)
 
 
@@ -66,3 +72,18 @@ def test_prefill_three_bit_and_single_query_group(tq, oracle):
 
 def test_prefill_octopus_cache(tq, oracle):
     assert _prefill_case(tq, oracle, 500, 24, kb=4, vb=4, octopus=True) <= parity.DECODE_RTOL
+
+
+@pytest.mark.parametrize("G,vb,C", [(1, 4, 70), (4, 2, 33), (8, 3, 200), (2, 1, 5)])
+def test_prefill_tensor_core_shapes(tq, oracle, G, vb, C):
+    """4-bit keys (the tensor-core prefill): query groups 1..8, value widths 1..4,
+    chunks whose rows fill several 128-row blocks or only part of one."""
+    assert _prefill_case(tq, oracle, 900, C, vb=vb, G=G) <= parity.DECODE_RTOL
+
+
+def test_prefill_fp32_queries_and_start_of_sequence(tq, oracle):
+    assert _prefill_case(tq, oracle, 0, 130, dtype="f32") <= parity.DECODE_RTOL
+
+
+def test_prefill_bad_block_is_skipped_and_flagged(tq, oracle):
+    assert _prefill_case(tq, oracle, 600, 40, bad_block=7) <= parity.DECODE_RTOL

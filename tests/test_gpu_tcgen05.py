@@ -26,8 +26,9 @@ def test_tcgen05_building_blocks():
                               "A through the fragment-layout store"]):
         np.testing.assert_allclose(out[i], ref, rtol=1e-5, atol=1e-4, err_msg=what)
     # B in the MN-major layout: the descriptor reading the prefill kernel uses
-    # (leading byte offset = step between 8-element groups along N, stride byte
-    # offset = step between 8-row groups along K) must match
+    # (leading byte offset = step between 8-row groups along K, stride byte
+    # offset = step between 8-element groups along N, the roles they have in
+    # the K-major layout) must match, and the other must not
     match = [bool(np.allclose(out[i], ref, rtol=1e-5, atol=1e-4)) for i in (4, 5)]
     print("MN-major B, readings (K step, N step) = (128, 4096) / (4096, 128):", match)
-    assert match[1], match
+    assert match == [True, False], match

@@ -125,3 +125,29 @@ def test_timeout_octopus(tq):
     torch.cuda.synchronize()
     assert st.item() == 0
     assert torch.equal(again, ref)
+
+
+def test_timeout_prefill(tq):
+    """The tensor-core prefill: CTAs of odd splits give up a bounded wait and
+    contribute empty partials; the call is flagged and the next one is exact."""
+    import torch
+    dev = "cuda"
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(3000,), hkv=2, hq=16)
+    cache, _, bt, _ = _filled(tq, tq.Cache, w)
+    q = torch.from_numpy(W.bf16_round(np.random.default_rng(3).standard_normal((64, 16, 128)).astype(np.float32)))
+    q = q.to(dev, torch.bfloat16)
+    row = bt[0].contiguous()
+    ref = cache.prefill(q, row, 3000 - 64).clone()
+    st = tq.new_status()
+    tq.set_test_stall(STALL_CYCLES)
+    try:
+        cache.prefill(q, row, 3000 - 64, status=st)
+        torch.cuda.synchronize()
+    finally:
+        tq.set_test_stall(0)
+    assert st.item() & tq.FLAG_TIMEOUT
+    st.zero_()
+    again = cache.prefill(q, row, 3000 - 64, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(again, ref)
