@@ -439,8 +439,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             // the weights' region and the output accumulator are free again
             if (u > 0) pf_wait(bar(kBarO), (u - 1) & 1, bad);
             tc::fence_after_sync();
-            if (mt > m + kLazy) {
-                const float f = ex2(m - mt);
+            // The tensor-memory loads and stores are warp-wide (.sync.aligned), so
+            // the rescale is decided for the whole warp: a row that keeps its max
+            // takes the factor 1.
+            if (__any_sync(0xffffffffu, mt > m + kLazy)) {
+                const float mn = (mt > m + kLazy) ? mt : m;
+                const float f = ex2(m - mn);
                 l *= f;
                 z *= f;
                 if (u > 0) {
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                         tc::st_32x32b_x32(tmem + tl + kTo + 32 * c, v);
                     }
                 }
-                m = mt;
+                m = mn;
             }
             const float2* z2 = reinterpret_cast<const float2*>(zer_s + (u & 1) * kPfTile);
             const float2* c2 = reinterpret_cast<const float2*>(scl_s + (u & 1) * kPfTile);
