@@ -14,8 +14,9 @@
 //              lo parts as the tensor-memory A operand.  Per tile it reads the
 //              row's 128 scores, applies the key norms, the causal mask and a
 //              lazy running max (raised only when a score beats it by more
-//              than 8 in log2 units), and writes the weights p * scale in fp16
-//              hi and lo parts to tensor memory as the A operand of PV.
+//              than 8 in log2 units, so p <= 2^8; a tile with a value scale
+//              above 255 takes the exact max), and writes the weights p * scale
+//              in fp16 hi and lo parts to tensor memory as the A operand of PV.
 //   warps 4-7  producers: thread = token of the tile.  They unpack the key
 //              codes through a 256-entry table into the two-level centroid
 //              operand C[c] / delta = N[c] + rem2[c] / delta (N an integer of
@@ -68,10 +69,8 @@ constexpr uint32_t kVLbo = 128, kVSbo = 2048;
 // that nothing arrives on (the wait-timeout test hook waits on it)
 constexpr int kBarBk = 2 * kPfPages, kBarBv = kBarBk + 1, kBarS = kBarBk + 2, kBarP = kBarBk + 3,
               kBarO = kBarBk + 4, kBarQ = kBarBk + 5, kBarNever = kBarBk + 6, kNumBars = kBarBk + 7;
-// The PV weights go in as w = p * scale * 2^-8 (p <= 2^8 under the lazy max),
-// so that their fp16 hi part never overflows; the output takes 2^(24 + 8) back
-// (2^24 from the value codes held as fp16 subnormals).
-constexpr float kWShift = 0.00390625f, kOutScale = 4294967296.f;
+// The output takes 2^24 back: the value codes are held as fp16 subnormals.
+constexpr float kOutScale = 16777216.f;
 
 template <int VB>
 struct PfLayout {
@@ -86,7 +85,8 @@ struct PfLayout {
     static constexpr int scl = gam + 2 * kPfTile * 4;
     static constexpr int zer = scl + 2 * kPfTile * 4;
     static constexpr int msk = zer + 2 * kPfTile * 4;
-    static constexpr int lut = msk + 2 * kPfTile * 4;   // 256 entries x (N pair, rem2/delta pair)
+    static constexpr int big = msk + 2 * kPfTile * 4;   // per tile parity and producer warp: a scale > kBigScale
+    static constexpr int lut = big + 2 * 4 * 4;         // 256 entries x (N pair, rem2/delta pair)
     static constexpr int bars = lut + 256 * 8;
     static constexpr int ok = bars + 8 * kNumBars;      // page copy issued and its block id valid [2][8]
     static constexpr int taddr = ok + 4 * 2 * kPfPages;
@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
     float* scl_s = reinterpret_cast<float*>(sm + L::scl);
     float* zer_s = reinterpret_cast<float*>(sm + L::zer);
     float* msk_s = reinterpret_cast<float*>(sm + L::msk);
+    int* big_s = reinterpret_cast<int*>(sm + L::big);
     if (tid == 0) {
         for (int i = 0; i < 2 * kPfPages; ++i) mbar_init(bar(i), 1);
         mbar_init(bar(kBarBk), 4);
@@ -326,8 +327,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                     sc = lds_h2f(pg + F::scl + 2 * slot);
                     zr = lds_h2f(pg + F::zer + 2 * slot);
                 }
-                scl_s[half * kPfTile + t] = sc * kWShift;
+                scl_s[half * kPfTile + t] = sc;
                 zer_s[half * kPfTile + t] = zr;
+                // a scale above kBigScale makes this tile take the exact max, so
+                // that p * scale (p <= 1 then) stays inside the fp16 range
+                const bool bg = __any_sync(0xffffffffu, sc > kBigScale);
+                if (lane == 0) big_s[half * 4 + (warp - 4)] = bg ? 1 : 0;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
@@ -442,8 +447,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             // The tensor-memory loads and stores are warp-wide (.sync.aligned), so
             // the rescale is decided for the whole warp: a row that keeps its max
             // takes the factor 1.
-            if (__any_sync(0xffffffffu, mt > m + kLazy)) {
-                const float mn = (mt > m + kLazy) ? mt : m;
+            const int4 bg4 = *reinterpret_cast<const int4*>(big_s + 4 * (u & 1));
+            const bool exact = (bg4.x | bg4.y | bg4.z | bg4.w) != 0;
+            const bool raise = mt > m + kLazy || (exact && mt > m);
+            if (__any_sync(0xffffffffu, raise)) {
+                const float mn = raise ? mt : m;
                 const float f = ex2(m - mn);
                 l *= f;
                 z *= f;
