@@ -224,6 +224,21 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         print(json.dumps({"profile": "gqa32k OCTOPUS 4/4 decode", "device_status": int(status.item())}), flush=True)
         return
+    if args.profile_prefill:
+        # the 64-position chunked prefill at the end of the context, four launches
+        # (ncu -k regex:prefill_tc_kernel -s 1 -c 1)
+        C = 64
+        qp = torch.from_numpy(W.bf16_round(np.random.default_rng(5).standard_normal((C, hq, d)).astype(np.float32)))
+        qp = qp.to(dev, torch.bfloat16)
+        row = bt[0].contiguous()
+        pout = torch.empty((C, hq, d), dtype=torch.float32, device=dev)
+        nbytes = int(tq.lib().tq_prefill_workspace_bytes(base._h, C, hq, row.shape[0]))
+        pws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        for _ in range(4):
+            base.prefill(qp, row, T - C, out=pout, workspace=pws, status=status)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "gqa32k 64-position prefill", "device_status": int(status.item())}), flush=True)
+        return
     widths = [] if args.profile or args.no_widths else width_sweep(tq, w, K, V, slots, bt, q_w, measured_peaks()[0])
     ring = {} if args.profile or args.no_widths else ring_stream(tq, dev, measured_peaks()[0])
     octopus = [] if args.profile or args.no_widths else octopus_sweep(tq, w, K, V, slots, bt, q_w, measured_peaks()[0])
@@ -568,9 +583,12 @@ def prefill_chunk(tq, w, base, bt, C=64):
         best = min(best, e0.elapsed_time(e1) / reps)
     del g, caches, wss
     torch.cuda.empty_cache()
+    flops = 2 * 2 * C * hq * T * d  # scores and PV, 2 FLOP per multiply-add (causal: < 0.2 % fewer)
     return {"workload": f"gqa32k: the last {C} positions of the 32768-token sequence, causal, 4/4",
             "us_per_chunk": round(best * 1e3, 2), "positions_per_s": round(C / (best * 1e-3), 1),
-            "note": "one decode row per position: the cache is read once per position (L2 serves the repeats)"}
+            "tflops": round(flops / (best * 1e-3) / 1e12, 1),
+            "kernel": "prefill_tc_kernel (tcgen05: 128 query rows per CTA, each page unpacked once per row block) "
+                      "+ prefill_merge_kernel"}
 
 
 def ring_stream(tq, dev, peak):
@@ -891,6 +909,8 @@ def main():
     ap.add_argument("--no-widths", action="store_true", help="skip the other-widths measurements")
     ap.add_argument("--profile", action="store_true",
                     help="only build the caches and launch the decode kernel 6 times (for ncu)")
+    ap.add_argument("--profile-prefill", action="store_true",
+                    help="only build the cache and launch the 64-position chunked prefill 4 times (for ncu)")
     ap.add_argument("--profile-octopus", action="store_true",
                     help="only build an OCTOPUS 4/4 cache and launch its decode 6 times (for ncu)")
     args = ap.parse_args()
