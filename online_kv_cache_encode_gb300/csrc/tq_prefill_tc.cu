@@ -23,14 +23,19 @@
 //              magnitude <= 2047, |rem2 / delta| <= 1/2, both exact enough in
 //              fp16), the value codes into exact fp16 subnormals, and the
 //              norms, scales and zero points into shared memory.
-//   lane 0 of warp 0 also loads the pages (bulk async copies into a two-tile
+//   warp 8     lane 0 loads the pages (bulk async copies into a four-tile
 //              ring) and issues the MMAs: scores S [128 rows x 128 tokens] =
 //              q_hi . N + q_lo . N + q_hi . rem2/delta (24 kind::f16 MMAs,
 //              K = 16), and O [128 rows x 128 dims] += w_hi . V + w_lo . V (16
 //              MMAs) in fp32 tensor memory, each group committed to an
 //              mbarrier.  Right after the softmax of tile u it issues PV of
-//              tile u, starts the copies of tile u + 2 and the scores of tile
-//              u + 1, which the producers have prepared meanwhile.
+//              tile u, starts the copies of tile u + 4 and the scores of tile
+//              u + 2.
+// Scores and weights of a tile share tensor-memory columns (the weights
+// overwrite the scores the softmax has read), two tiles deep, and the value
+// operand is double-buffered: the scores of tile u + 1 run on the tensor cores
+// while the softmax works on tile u, and the values of tile u + 1 are unpacked
+// before PV of tile u has read its operand.
 // Logits and values stay in the rotated frame; keys are never reconstructed
 // ["OCTOPUS ..." -- TL;DR / step 7; deep dive -- [RHT effect]].  Each split
 // writes its rows' partial (max, sum, unnormalised rotated accumulator with
@@ -49,13 +54,16 @@ namespace {
 constexpr int kPfRows = 128;                    // query rows per CTA (tensor-memory lanes)
 constexpr int kPfTile = 128;                    // tokens per tile
 constexpr int kPfPages = kPfTile / kBlockSize;  // pages per tile
-constexpr int kPfWarps = 8;
+constexpr int kPfWarps = 9;                     // softmax 0-3, producers 4-7, issuer 8
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPartRow = 4 + kHeadDim;          // partial record: max, sum, 2 pad, acc[128]
-// tensor-memory columns: query operand (hi 0..63, lo 64..127), scores, weights
-// (hi 256..319, lo 320..383), output accumulator
-constexpr uint32_t kTq = 0, kTs = 128, kTp = 256, kTo = 384;
+// tensor-memory columns: query operand (hi 0..63, lo 64..127); scores of tile
+// u at kTs + 128 (u & 1), overwritten first by its logits and then by its
+// weights (for the 16 tokens of K-step s: hi parts at +16 s .. +16 s + 7, lo
+// parts at +16 s + 8 .. +16 s + 15); output accumulator
+constexpr uint32_t kTq = 0, kTs = 128, kTo = 384;
 constexpr int kTmemCols = 512;
+constexpr int kRing = 4;                        // tiles of pages in flight
 // key operand [N = 128 tokens x K = 128 dims], K-major core matrices
 constexpr uint32_t kKLbo = 128, kKSbo = 2048;
 // value operand [K = 128 tokens x N = 128 dims], MN-major core matrices (8
@@ -64,11 +72,12 @@ constexpr uint32_t kKLbo = 128, kKSbo = 2048;
 // and its stride byte offset the step along N, as in the K-major layout (the
 // self-test checks this reading).
 constexpr uint32_t kVLbo = 128, kVSbo = 2048;
-// barriers: page slots [2][8], then key operand full, value operand full,
-// scores full, weights full, output updated, query operand stored, and one
-// that nothing arrives on (the wait-timeout test hook waits on it)
-constexpr int kBarBk = 2 * kPfPages, kBarBv = kBarBk + 1, kBarS = kBarBk + 2, kBarP = kBarBk + 3,
-              kBarO = kBarBk + 4, kBarQ = kBarBk + 5, kBarNever = kBarBk + 6, kNumBars = kBarBk + 7;
+// barriers: page slots [kRing][8], then key operand full, value operand full
+// [2], scores full [2], weights full [2], values multiplied [2] (all four by
+// tile parity), query operand stored, and one that nothing arrives on (the
+// wait-timeout test hook waits on it)
+constexpr int kBarBk = kRing * kPfPages, kBarBv = kBarBk + 1, kBarS = kBarBv + 2, kBarP = kBarS + 2,
+              kBarO = kBarP + 2, kBarQ = kBarO + 2, kBarNever = kBarQ + 1, kNumBars = kBarNever + 1;
 // The output takes 2^24 back: the value codes are held as fp16 subnormals.
 constexpr float kOutScale = 16777216.f;
 
@@ -76,20 +85,22 @@ template <int VB>
 struct PfLayout {
     static constexpr int bn = 0;                        // key operand, integer parts
     static constexpr int br = bn + kPfTile * kHeadDim * 2;   // key operand, remainders / delta
-    static constexpr int bv = br + kPfTile * kHeadDim * 2;   // value operand
-    static constexpr int ring = bv + kPfTile * kHeadDim * 2;
+    static constexpr int bv = br + kPfTile * kHeadDim * 2;   // value operand [2] (by tile parity)
+    static constexpr int bv_size = kPfTile * kHeadDim * 2;
+    static constexpr int ring = bv + 2 * bv_size;
     static constexpr int stride = PageFmt<4, VB, 0>::stride;
-    // per token of a tile, two tiles deep (by tile parity): gamma, scale, zero
-    // and the mask (0, or -inf for a token that is not there)
-    static constexpr int gam = ring + 2 * kPfPages * stride;
-    static constexpr int scl = gam + 2 * kPfTile * 4;
+    // per token of a tile: gamma and the mask (0, or -inf for a token that is
+    // not there) four tiles deep (by u & 3: the scores of tile u + 1 may finish
+    // while the softmax still reads tile u - 1's), scale and zero two deep
+    static constexpr int gam = ring + kRing * kPfPages * stride;
+    static constexpr int msk = gam + 4 * kPfTile * 4;
+    static constexpr int scl = msk + 4 * kPfTile * 4;
     static constexpr int zer = scl + 2 * kPfTile * 4;
-    static constexpr int msk = zer + 2 * kPfTile * 4;
-    static constexpr int big = msk + 2 * kPfTile * 4;   // per tile parity and producer warp: a scale > kBigScale
+    static constexpr int big = zer + 2 * kPfTile * 4;   // per tile parity and producer warp: a scale > kBigScale
     static constexpr int lut = big + 2 * 4 * 4;         // 256 entries x (N pair, rem2/delta pair)
     static constexpr int bars = lut + 256 * 8;
-    static constexpr int ok = bars + 8 * kNumBars;      // page copy issued and its block id valid [2][8]
-    static constexpr int taddr = ok + 4 * 2 * kPfPages;
+    static constexpr int ok = bars + 8 * kNumBars;      // page copy issued and its block id valid [kRing][8]
+    static constexpr int taddr = ok + 4 * kRing * kPfPages;
     static constexpr int total = taddr + 16;
 };
 
@@ -153,12 +164,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
     float* msk_s = reinterpret_cast<float*>(sm + L::msk);
     int* big_s = reinterpret_cast<int*>(sm + L::big);
     if (tid == 0) {
-        for (int i = 0; i < 2 * kPfPages; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < kRing * kPfPages; ++i) mbar_init(bar(i), 1);
         mbar_init(bar(kBarBk), 4);
-        mbar_init(bar(kBarBv), 4);
-        mbar_init(bar(kBarS), 1);
-        mbar_init(bar(kBarP), 4);
-        mbar_init(bar(kBarO), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(kBarBv + b), 4);
+            mbar_init(bar(kBarS + b), 1);
+            mbar_init(bar(kBarP + b), 4);
+            mbar_init(bar(kBarO + b), 1);
+        }
         mbar_init(bar(kBarQ), 4);
         mbar_init(bar(kBarNever), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -184,71 +197,80 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         stalled = !mbar_wait_for(bar(kBarNever), 0, a.stall_cycles);
     }
 
-    // ---- loader / MMA issuer (lane 0 of warp 0) ----
+    // ---- loader / MMA issuer (lane 0 of warp 8) ----
     const int npg = (p_hi + kBlockSize) / kBlockSize;  // pages the block needs
-    auto load_tile = [&](int u) {
-        const int half = u & 1;
+    // the block ids of tile u's pages (fetched a tile ahead of their use)
+    auto fetch_ids = [&](int u, int (&blks)[kPfPages]) {
+#pragma unroll
         for (int j = 0; j < kPfPages; ++j) {
             const int pgi = (t_first + u) * kPfPages + j;
-            const uint32_t b = bar(half * kPfPages + j);
+            blks[j] = (u < U && pgi < npg) ? __ldg(a.block_row + pgi) : 0;
+        }
+    };
+    auto load_tile = [&](int u, const int (&blks)[kPfPages]) {
+        const int slot = u & (kRing - 1);
+#pragma unroll
+        for (int j = 0; j < kPfPages; ++j) {
+            const int pgi = (t_first + u) * kPfPages + j;
+            const int si = slot * kPfPages + j;
+            const uint32_t b = bar(si);
             if (pgi < npg) {
-                const int blk = __ldg(a.block_row + pgi);
+                const int blk = blks[j];
                 if (blk >= 0 && blk < g.num_blocks) {
-                    page_ok[half * kPfPages + j] = 1;
+                    page_ok[si] = 1;
                     mbar_arrive_tx(b, (uint32_t)F::bytes);
-                    bulk_g2s(sbase + L::ring + (half * kPfPages + j) * L::stride,
-                             a.pool + ((int64_t)blk * g.hkv + h) * F::bytes, (uint32_t)F::bytes, b);
+                    bulk_g2s(sbase + L::ring + si * L::stride, a.pool + ((int64_t)blk * g.hkv + h) * F::bytes,
+                             (uint32_t)F::bytes, b);
                 } else {
                     flag(a.status, TQ_FLAG_BAD_SLOT);
-                    page_ok[half * kPfPages + j] = 0;
+                    page_ok[si] = 0;
                     mbar_arrive(b);
                 }
             } else {
-                page_ok[half * kPfPages + j] = -1;  // past the block's last position: not loaded
+                page_ok[si] = -1;  // past the block's last position: not loaded
                 mbar_arrive(b);
             }
         }
     };
     constexpr uint32_t idesc_s = tc::idesc_f16_f32(kPfRows, kPfTile);
     constexpr uint32_t idesc_v = tc::idesc_f16_f32_bmn(kPfRows, kHeadDim);
-    // scores of tile u: needs its key operand (and the previous tile's scores read)
+    // scores of tile u into its columns: needs its key operand (written once
+    // the scores of tile u - 1 had read the previous one); issued after PV of
+    // tile u - 2, which read the weights these columns held
     auto issue_scores = [&](int u) {
         pf_wait(bar(kBarBk), u & 1, bad);
         tc::fence_after_sync();
+        const uint32_t ts = tmem + kTs + 128 * (u & 1);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            tc::mma_f16_ts(tmem + kTs, tmem + kTq + 8 * s, tc::smem_desc(sbase + L::bn + 256 * s, kKLbo, kKSbo),
-                           idesc_s, s > 0 ? 1u : 0u);
+            tc::mma_f16_ts(ts, tmem + kTq + 8 * s, tc::smem_desc(sbase + L::bn + 256 * s, kKLbo, kKSbo), idesc_s,
+                           s > 0 ? 1u : 0u);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            tc::mma_f16_ts(tmem + kTs, tmem + kTq + 64 + 8 * s, tc::smem_desc(sbase + L::bn + 256 * s, kKLbo, kKSbo),
-                           idesc_s, 1u);
+            tc::mma_f16_ts(ts, tmem + kTq + 64 + 8 * s, tc::smem_desc(sbase + L::bn + 256 * s, kKLbo, kKSbo), idesc_s,
+                           1u);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            tc::mma_f16_ts(tmem + kTs, tmem + kTq + 8 * s, tc::smem_desc(sbase + L::br + 256 * s, kKLbo, kKSbo),
-                           idesc_s, 1u);
-        tc::commit(bar(kBarS));
+            tc::mma_f16_ts(ts, tmem + kTq + 8 * s, tc::smem_desc(sbase + L::br + 256 * s, kKLbo, kKSbo), idesc_s, 1u);
+        tc::commit(bar(kBarS + (u & 1)));
     };
     // values of tile u: needs its value operand and all weights
     auto issue_values = [&](int u) {
-        pf_wait(bar(kBarBv), u & 1, bad);
-        pf_wait(bar(kBarP), u & 1, bad);
+        pf_wait(bar(kBarBv + (u & 1)), (u >> 1) & 1, bad);
+        pf_wait(bar(kBarP + (u & 1)), (u >> 1) & 1, bad);
         tc::fence_after_sync();
+        const uint32_t tp = tmem + kTs + 128 * (u & 1);
+        const uint32_t bv = sbase + L::bv + (u & 1) * L::bv_size;
+        // K-step s: hi parts at columns 16 s .., lo parts at 16 s + 8 ..
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            tc::mma_f16_ts(tmem + kTo, tmem + kTp + 8 * s, tc::smem_desc(sbase + L::bv + 256 * s, kVLbo, kVSbo),
-                           idesc_v, (u > 0 || s > 0) ? 1u : 0u);
+            tc::mma_f16_ts(tmem + kTo, tp + 16 * s, tc::smem_desc(bv + 256 * s, kVLbo, kVSbo), idesc_v,
+                           (u > 0 || s > 0) ? 1u : 0u);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            tc::mma_f16_ts(tmem + kTo, tmem + kTp + 64 + 8 * s, tc::smem_desc(sbase + L::bv + 256 * s, kVLbo, kVSbo),
-                           idesc_v, 1u);
-        tc::commit(bar(kBarO));
+            tc::mma_f16_ts(tmem + kTo, tp + 16 * s + 8, tc::smem_desc(bv + 256 * s, kVLbo, kVSbo), idesc_v, 1u);
+        tc::commit(bar(kBarO + (u & 1)));
     };
-    const bool issuer = warp == 0 && lane == 0;
-    if (issuer && !stalled) {
-        load_tile(0);
-        if (U > 1) load_tile(1);
-    }
 
     if (stalled) {
         for (int i = tid; i < kPfRows; i += kPfThreads) {
@@ -257,6 +279,32 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         }
         for (int i = tid; i < kPfRows * D; i += kPfThreads) part[(i / D) * kPartRow + 4 + (i % D)] = 0.f;
         bad = true;
+    } else if (warp == 8) {
+        // ================= loader and MMA issuer =================
+        // Issuing an MMA waits while the tensor pipe's queue is full, so this
+        // warp does nothing else: its waits never hold up the softmax.
+        if (lane == 0) {
+            int ids[kPfPages];
+            for (int u = 0; u < kRing && u < U; ++u) {
+                fetch_ids(u, ids);
+                load_tile(u, ids);
+            }
+            fetch_ids(kRing, ids);
+            pf_wait(bar(kBarQ), 0, bad);
+            issue_scores(0);
+            if (U > 1) issue_scores(1);
+            for (int u = 0; u < U; ++u) {
+                issue_values(u);
+                // the ring slot of tile u is free: its values are unpacked
+                if (u + kRing < U) {
+                    load_tile(u + kRing, ids);
+                    fetch_ids(u + kRing + 1, ids);
+                }
+                // into the columns whose weights PV of tile u has just been queued to read
+                if (u + 2 < U) issue_scores(u + 2);
+            }
+        }
+        __syncwarp();
     } else if (warp >= 4) {
         // ================= producers: thread = token of the tile =================
         const int t = tid - 128;          // token of the tile
@@ -264,13 +312,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         const uint32_t* lut = reinterpret_cast<const uint32_t*>(sm + L::lut);
         for (int u = 0; u < U; ++u) {
             const int half = u & 1;
-            pf_wait(bar(half * kPfPages + j), (u >> 1) & 1, bad);
-            const int pok = page_ok[half * kPfPages + j];
+            const int si = (u & (kRing - 1)) * kPfPages + j;
+            pf_wait(bar(si), (u / kRing) & 1, bad);
+            const int pok = page_ok[si];
             const int tok = (t_first + u) * kPfTile + t;
             const bool valid = pok == 1 && tok <= p_hi && !bad;
-            const uint32_t pg = sbase + L::ring + (half * kPfPages + j) * L::stride;
+            const uint32_t pg = sbase + L::ring + si * L::stride;
             // ---- keys: the previous tile's scores MMA has read the operand ----
-            if (u > 0) pf_wait(bar(kBarS), (u - 1) & 1, bad);
+            if (u > 0) pf_wait(bar(kBarS + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
             {
                 uint32_t w[16];
 #pragma unroll
@@ -294,14 +343,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                 }
                 float gm = 0.f;
                 if (valid) gm = lds_h2f(pg + F::gam + 2 * slot);
-                gam_s[half * kPfTile + t] = gm;
-                msk_s[half * kPfTile + t] = valid ? 0.f : -INFINITY;
+                gam_s[(u & 3) * kPfTile + t] = gm;
+                msk_s[(u & 3) * kPfTile + t] = valid ? 0.f : -INFINITY;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarBk));
-            // ---- values: the previous tile's PV MMA has read the operand ----
-            if (u > 0) pf_wait(bar(kBarO), (u - 1) & 1, bad);
+            // ---- values: PV of tile u - 2 has read this value buffer ----
+            if (u > 1) pf_wait(bar(kBarO + half), ((u - 2) >> 1) & 1, bad);
             {
                 constexpr int VROW = D * VB / 8;
                 uint32_t w[VB * 4];
@@ -320,7 +369,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                         const uint32_t c1 = bits_at<VB * 4>(w, VB * (8 * dg + 2 * k + 1), VB);
                         pr[k] = c0 | (c1 << 16);
                     }
-                    sts128(sbase + L::bv + val_chunk(t, dg), pr[0], pr[1], pr[2], pr[3]);
+                    sts128(sbase + L::bv + half * L::bv_size + val_chunk(t, dg), pr[0], pr[1], pr[2], pr[3]);
                 }
                 float sc = 0.f, zr = 0.f;
                 if (valid) {
@@ -336,7 +385,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarBv));
+            if (lane == 0) mbar_arrive(bar(kBarBv + half));
         }
     } else {
         // ================= softmax: thread = query row =================
@@ -398,52 +447,47 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarQ));
-        if (issuer) {
-            pf_wait(bar(kBarQ), 0, bad);
-            issue_scores(0);
-        }
-        __syncwarp();
 
         float m = kMinusBig, l = 0.f, z = 0.f;
         for (int u = 0; u < U; ++u) {
             const int base = (t_first + u) * kPfTile;
             // scores of tile u, then its per-token norms, masks, scales and zero
             // points: the producers write them all before arriving on the value
-            // barrier (whose next phase needs this warpgroup's weights, so a wait
-            // on it never falls a whole phase behind)
-            pf_wait(bar(kBarS), u & 1, bad);
-            pf_wait(bar(kBarBv), u & 1, bad);
+            // barrier of the tile's parity (whose next phase needs this
+            // warpgroup's weights, so a wait on it never falls a whole phase behind)
+            pf_wait(bar(kBarS + (u & 1)), (u >> 1) & 1, bad);
+            pf_wait(bar(kBarBv + (u & 1)), (u >> 1) & 1, bad);
             tc::fence_after_sync();
-            float s[kPfTile];
+            const uint32_t tsp = tmem + tl + kTs + 128 * (u & 1);
+            // pass 1, 32 tokens at a time: logit (log2 units) = S * qscale * gamma;
+            // tokens that are not there and, causally, tokens after the row's
+            // position get -inf; the logits go back over the scores
+            float mt = kMinusBig;
+            const int kmax = pos - base;  // the last token of the tile the row sees
+            const float4* g4 = reinterpret_cast<const float4*>(gam_s + (u & 3) * kPfTile);
+            const float4* m4 = reinterpret_cast<const float4*>(msk_s + (u & 3) * kPfTile);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
-                tc::ld_32x32b_x32(tmem + tl + kTs + 32 * c, v);
+                tc::ld_32x32b_x32(tsp + 32 * c, v);
                 tc::wait_ld();
+                tc::reg_fence(v);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) s[32 * c + k] = __uint_as_float(v[k]);
-            }
-            // logit (log2 units) = S * qscale * gamma; tokens that are not there
-            // and, causally, tokens after the row's position get -inf
-            float mt = kMinusBig;
-            const int kmax = pos - base;  // the last token of the tile the row sees
-            const float4* g4 = reinterpret_cast<const float4*>(gam_s + (u & 1) * kPfTile);
-            const float4* m4 = reinterpret_cast<const float4*>(msk_s + (u & 1) * kPfTile);
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 gg = g4[8 * c + k4], mm = m4[8 * c + k4];
+                    const float gv[4] = {gg.x, gg.y, gg.z, gg.w}, mv[4] = {mm.x, mm.y, mm.z, mm.w};
 #pragma unroll
-            for (int k4 = 0; k4 < kPfTile / 4; ++k4) {
-                const float4 gg = g4[k4], mm = m4[k4];
-                const float gv[4] = {gg.x, gg.y, gg.z, gg.w}, mv[4] = {mm.x, mm.y, mm.z, mm.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int k = 4 * k4 + i;
-                    const float v = fmaf(s[k] * qs, gv[i], mv[i]);
-                    s[k] = (k <= kmax) ? v : -INFINITY;
-                    mt = fmaxf(mt, s[k]);
+                    for (int i = 0; i < 4; ++i) {
+                        const int k = 32 * c + 4 * k4 + i;
+                        float x = fmaf(__uint_as_float(v[4 * k4 + i]) * qs, gv[i], mv[i]);
+                        x = (k <= kmax) ? x : -INFINITY;
+                        mt = fmaxf(mt, x);
+                        v[4 * k4 + i] = __float_as_uint(x);
+                    }
                 }
+                tc::st_32x32b_x32(tsp + 32 * c, v);
             }
-            // the weights' region and the output accumulator are free again
-            if (u > 0) pf_wait(bar(kBarO), (u - 1) & 1, bad);
-            tc::fence_after_sync();
+            tc::wait_st();
             // The tensor-memory loads and stores are warp-wide (.sync.aligned), so
             // the rescale is decided for the whole warp: a row that keeps its max
             // takes the factor 1.
@@ -456,6 +500,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                 l *= f;
                 z *= f;
                 if (u > 0) {
+                    // the output accumulator holds every PV up to tile u - 1
+                    pf_wait(bar(kBarO + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
+                    tc::fence_after_sync();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t v[32];
@@ -468,15 +515,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                 }
                 m = mn;
             }
+            // pass 2: the weights over the logits, 32 tokens at a time; the 16
+            // tokens of K-step s take columns 16 s .. 16 s + 7 (hi parts, pairs)
+            // and 16 s + 8 .. 16 s + 15 (lo parts), so a chunk's weights land
+            // exactly on its own logits
             const float2* z2 = reinterpret_cast<const float2*>(zer_s + (u & 1) * kPfTile);
             const float2* c2 = reinterpret_cast<const float2*>(scl_s + (u & 1) * kPfTile);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tc::ld_32x32b_x32(tsp + 32 * c, v);
+                tc::wait_ld();
+                tc::reg_fence(v);
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const int t0 = 32 * c + 2 * k, t1 = t0 + 1;
-                    const float p0 = ex2(s[t0] - m), p1 = ex2(s[t1] - m);
+                    const float p0 = ex2(__uint_as_float(v[2 * k]) - m), p1 = ex2(__uint_as_float(v[2 * k + 1]) - m);
                     const float2 zz = z2[16 * c + k], cc = c2[16 * c + k];
                     l += p0 + p1;
                     z = fmaf(p0, zz.x, fmaf(p1, zz.y, z));
@@ -485,23 +539,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                     const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
                     lo[k] = pack_h2(w0 - hf.x, w1 - hf.y);
                 }
-                tc::st_32x32b_x16(tmem + tl + kTp + 16 * c, hi);
-                tc::st_32x32b_x16(tmem + tl + kTp + 64 + 16 * c, lo);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    v[16 * (k >> 3) + (k & 7)] = hi[k];
+                    v[16 * (k >> 3) + 8 + (k & 7)] = lo[k];
+                }
+                tc::st_32x32b_x32(tsp + 32 * c, v);
             }
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarP));
-            if (issuer) {
-                issue_values(u);
-                // the ring half of tile u is free: its values are unpacked
-                if (u + 2 < U) load_tile(u + 2);
-                if (u + 1 < U) issue_scores(u + 1);
-            }
-            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarP + (u & 1)));
         }
         // ---- this split's partial for the row: max, sum, rotated accumulator + zero term ----
-        pf_wait(bar(kBarO), (U - 1) & 1, bad);
+        pf_wait(bar(kBarO + ((U - 1) & 1)), ((U - 1) >> 1) & 1, bad);
         tc::fence_after_sync();
         float* pr = part + r * kPartRow;
 #pragma unroll
