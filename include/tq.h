@@ -228,6 +228,14 @@ TQ_API tq_status tq_cache_gaussian(const tq_cache* cache, double* S);
  *   value: v_rot = R v; mn = min, mx = max over coordinates; scale =
  *          (mx - mn)/(2^vb - 1); code = clamp(round-half-even((v_rot - mn) /
  *          scale), 0, 2^vb - 1) (all 0 if scale == 0); scale, mn as fp16.
+ * Arithmetic is fp32.  Encodes of bf16 / fp16 inputs without QJL and with at
+ * least two 128-row tiles of (token, KV head) items per SM form R k and R v
+ * on the tensor cores (exact products, fp32 accumulation: the same values as
+ * the butterfly up to the order of the additions); the others use the
+ * butterfly.  An input coordinate that is inf or NaN sets TQ_FLAG_NONFINITE
+ * (on the tensor-core path, so does a finite input whose rotated coordinate
+ * exceeds the fp32 range, above about 2.6e36); a stored fp16 field that
+ * overflows sets TQ_FLAG_OVERFLOW.
  * [three steps (split/rotate/codebook); Bit-Axon -- quantization function;
  *  deep dive -- Step 1 (RHT), Step 3 (value codes); "OCTOPUS ..." -- step 8]
  * Tokens that map to the same slot race; the last writer is unspecified. */

@@ -28,9 +28,9 @@ inline cudaError_t ensure_smem_limit(Kernel kern, int bytes, int (&done)[64]) {
 // Launch with programmatic stream serialization: the kernel may start while the
 // previous kernel in the stream drains, and must execute griddepcontrol.wait
 // before it touches global memory.
-template <typename Kernel, typename Args>
+template <typename Kernel, typename... Args>
 inline cudaError_t launch_programmatic(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                                       const Args& args) {
+                                       const Args&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -41,7 +41,7 @@ inline cudaError_t launch_programmatic(Kernel kern, dim3 grid, dim3 block, size_
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args);
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 __device__ __forceinline__ void flag(int32_t* status, int bits) {

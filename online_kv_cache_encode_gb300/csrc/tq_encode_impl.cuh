@@ -376,6 +376,13 @@ __global__ void __launch_bounds__(kEncWarps * 32, M > 0 ? 2 : 3) encode_kernel(c
     }
 }
 
+}  // namespace tq
+
+// the tensor-core encode (uses key_code_bsearch above)
+#include "tq_encode_tc.cuh"
+
+namespace tq {
+
 // The grid is at most one wave: the CTAs that fit on every SM at once (from
 // the occupancy calculator, once per kernel) loop over the items.
 template <int KB, int VB, int M, int GRP>
@@ -404,6 +411,10 @@ static int launch_encode_g(const EncodeArgs& a, int64_t items, int num_sms, cuda
 template <int KB, int VB, int M>
 static int launch_encode_t(const EncodeArgs& a, int num_sms, cudaStream_t s) {
     const int64_t items = a.num_tokens * a.g.hkv;
+    if constexpr (M == 0) {
+        // bulk 16-bit encodes rotate on the tensor cores
+        if (encode_tc_eligible(a, items, num_sms)) return launch_encode_tc<KB, VB>(a, items, num_sms, s);
+    }
     // four items per warp once there are enough to give every warp slot of
     // the GPU four; one item per warp (lower latency) below that
     if (items >= (int64_t)num_sms * (M > 0 ? 2 : 8) * kEncWarps * 4)

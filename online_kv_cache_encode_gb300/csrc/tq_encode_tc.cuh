@@ -1,0 +1,355 @@
+// Bulk encode with the rotation on the tcgen05 tensor cores (16-bit inputs,
+// no QJL sketch).
+//
+// Rotating a tile of 128 (token, KV head) vectors is one dense contraction:
+// U = X H^T, X the tile [128 rows x 128 coordinates] and
+// H[n][k] = (-1)^popcount(n & k) s_k, the natural-order Walsh-Hadamard matrix
+// times the random signs.  The inputs (bf16 or fp16) and H (entries +-1) are
+// exact tensor-core operands; the products are exact and accumulate in fp32 in
+// tensor memory, so row m of U is FWHT(s (.) x_m), unnormalised, as the CUDA-core
+// encode computes it, up to the order of the fp32 additions.  H stays in shared
+// memory for the whole kernel.  The rest of the encode reads one row per
+// thread from tensor memory and needs no cross-lane traffic:
+//   key:   gamma = ||U_k|| / sqrt(d) = ||k||; code_j = #{boundaries < u_j} with
+//          u = U_k / (sqrt(d) gamma), decided as U_k against sqrt(d) t_b gamma;
+//   value: v_rot = U_v / sqrt(d); per-token min / max;
+//          code = clamp(rint((v_rot - min) / scale), 0, 2^b - 1).
+// ["TurboQuant: KV Cache Vector Quantization" -- three steps; deep dive
+//  (cell-devlog) -- Step 1 (RHT), Step 3 (value codes); Bit-Axon --
+//  quantization function; "OCTOPUS ..." -- methodology steps 1, 2]
+//
+// CTA: four warpgroups, two per tile slot.  A slot has its own input buffers
+// in shared memory (the tile's key and value rows in the K-major core-matrix
+// layout, filled by 16-byte asynchronous copies) and 256 tensor-memory columns
+// (U_k, U_v).  Each warpgroup of a slot takes one half of the columns: it sums
+// the squares and finds the minimum and maximum over its half, the two halves
+// exchange these through shared memory, and each codes its half.  A slot takes every other tile of the CTA's share: the copies of
+// its next tile run while it codes the current one, and the other slot's work
+// fills the gaps.  One CTA per SM, persistent over the tiles.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "tq_decode_impl.cuh"  // mbarrier, grid-dependency and shared-address helpers
+#include "tq_device.cuh"
+#include "tq_tcgen05.cuh"
+
+namespace tq {
+
+constexpr int kEtRows = 128;                   // rows (token, KV head) per tile
+constexpr int kEtThreads = 512;                // two slots x two column halves, one warpgroup each
+constexpr uint32_t kEtLbo = 128, kEtSbo = 2048;  // K-major core matrices: along K adjacent, 8-row groups 2 KB apart
+constexpr int kEtOp = kEtRows * kHeadDim * 2;  // one 128 x 128 16-bit operand: 32 KB
+constexpr int kEtH = 0;                        // H [n][k]
+constexpr int kEtX = kEtOp;                    // slot s: keys at kEtX + 2 s kEtOp, values kEtOp further
+constexpr int kEtXchg = kEtX + 4 * kEtOp;      // [slot][half][row] (sum of squares, min, max, finite)
+constexpr int kEtBsd = kEtXchg + 2 * 2 * kEtRows * 16;  // key widths above 4 bits: sqrt(d) t_b of the positive half
+constexpr int kEtBars = kEtBsd + 4 * (kMaxLevels / 2);
+constexpr int kEtTaddr = kEtBars + 16;
+constexpr int kEtSmem = kEtTaddr + 16;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// OR of `v` over the 256 threads of a tile slot (named barrier `id`)
+__device__ __forceinline__ bool et_any256(bool v, int id) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
+// B words at p (4-byte aligned; 8-byte when B is even, 16-byte when B % 4 == 0)
+template <int B>
+__device__ __forceinline__ void et_store_words(uint8_t* p, const uint32_t (&w)[B]) {
+    if constexpr (B % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < B / 4; ++j)
+            reinterpret_cast<uint4*>(p)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    } else if constexpr (B % 2 == 0) {
+#pragma unroll
+        for (int j = 0; j < B / 2; ++j) reinterpret_cast<uint2*>(p)[j] = make_uint2(w[2 * j], w[2 * j + 1]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < B; ++j) reinterpret_cast<uint32_t*>(p)[j] = w[j];
+    }
+}
+
+// Value codes of 32 coordinates x (rotated, unnormalised) of one row:
+// rint((x / sqrt(d) - mn) / scale), the quotient formed as a product with
+// rs = 1 / scale.  That product is within VMAX 2^-22 of the exact quotient,
+// so it rounds to the same integer unless it lies within 2^(VB - 21) of a
+// half-integer; if any of the 32 does, the row's chunk is coded again with the
+// division (rint of the correctly rounded quotient, as everywhere else).
+template <int VB>
+__device__ __forceinline__ void et_value_codes(const float (&x)[32], float mn, float scale, float rs, int (&vc)[32]) {
+    constexpr float VMAX = (float)((1 << VB) - 1);
+    constexpr float kTie = 0.5f - (float)(1 << VB) * 4.76837158203125e-7f;  // 0.5 - 2^(VB - 21)
+    const float inv_sqrt_d = 0.08838834764831845f;
+    if (!(scale > 0.f)) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) vc[j] = 0;
+        return;
+    }
+    bool near = false;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float q = (x[j] * inv_sqrt_d - mn) * rs;
+        const float r = rintf(q);
+        near = near || (fabsf(q - r) > kTie);
+        vc[j] = (int)fminf(fmaxf(r, 0.f), VMAX);
+    }
+    if (near) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) vc[j] = (int)fminf(fmaxf(rintf((x[j] * inv_sqrt_d - mn) / scale), 0.f), VMAX);
+    }
+}
+
+// This thread's row of tensor memory, 32 columns at taddr.
+__device__ __forceinline__ void et_load32(uint32_t taddr, float (&x)[32]) {
+    uint32_t r[32];
+    tc::ld_32x32b_x32(taddr, r);
+    tc::wait_ld();
+    tc::reg_fence(r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+}
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(kEtThreads, 1) encode_tc_kernel(const EncodeArgs a, int64_t items, int num_tiles) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    constexpr int D = kHeadDim;
+    constexpr int HALF = 1 << (KB - 1);
+    constexpr int VMAX = (1 << VB) - 1;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wg = tid >> 7, tw = tid & 127;
+    const Geometry& g = a.g;
+    const uint32_t sbase = smem_u32(sm);
+    float* bsd_s = reinterpret_cast<float*>(sm + kEtBsd);
+
+    grid_dependency_wait();  // the previous grid's writes (inputs, pool) are visible
+    if (tid == 0) {
+        mbar_init(sbase + kEtBars, 1);
+        mbar_init(sbase + kEtBars + 8, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tc::tmem_alloc<512>(sbase + kEtTaddr);
+    {
+        // H[n][k] = (-1)^(popcount(n & k) + [s_k = -1]) in the input type, K-major:
+        // element (n, k) at (n / 8) 2048 + (k / 8) 128 + (n % 8) 16 + (k % 8) 2
+        const uint32_t one = (a.dtype == TQ_BF16) ? 0x3F80u : 0x3C00u;
+        for (int c = tid; c < D * (D / 8); c += kEtThreads) {
+            const int n = c >> 4, k8 = c & 15;
+            uint32_t w[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint32_t hv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 8 * k8 + 2 * p + e;
+                    const uint32_t neg = ((uint32_t)__popc(n & k) + ((a.c.sign_bits[k >> 5] >> (k & 31)) & 1u)) & 1u;
+                    hv[e] = one | (neg << 15);
+                }
+                w[p] = hv[0] | (hv[1] << 16);
+            }
+            *reinterpret_cast<uint4*>(sm + kEtH + (n >> 3) * kEtSbo + k8 * kEtLbo + (n & 7) * 16) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    if constexpr (KB > 4) {
+        for (int i = tid; i < HALF - 1; i += kEtThreads) bsd_s[i] = a.tab->boundary_sd_pos[i];
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // H: generic writes -> tensor-core reads
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kEtTaddr);
+    // only now may a dependent grid start: one of its CTAs on this SM must not
+    // take the tensor-memory columns this CTA waits for
+    grid_launch_dependents();
+
+    const int slot = wg >> 1, half = wg & 1;  // tile slot; column half this warpgroup codes
+    const int ts = tid & 255;                   // thread of the slot
+    const uint32_t xk = sbase + kEtX + slot * 2 * kEtOp, xv = xk + kEtOp;
+    const uint32_t tcol = tmem + 256u * slot;                                        // U_k at +0, U_v at +128
+    const uint32_t tk = tcol + ((uint32_t)((warp & 3) * 32) << 16), tv = tk + 128;  // this warp's lanes
+    const uint32_t mbar = sbase + kEtBars + 8 * slot;
+    const uint16_t* K16 = static_cast<const uint16_t*>(a.K);
+    const uint16_t* V16 = static_cast<const uint16_t*>(a.V);
+    // the rows of `tile` into this slot's buffers: per warp instruction,
+    // lanes l and l + 8, l + 16, l + 24 take 16-byte pieces k8 .. k8 + 3 of
+    // row 8 rg + l (l < 8): 8 rows x 64 contiguous bytes from global memory,
+    // 32 different 16-byte slots of shared memory in four bank-conflict-free
+    // groups; rows past the last item are zero-filled
+    auto load = [&](int tile) {
+        const int64_t r0 = (int64_t)tile * kEtRows;
+        const int wi = ts >> 5;
+#pragma unroll 4
+        for (int i = 0; i < 8; ++i) {
+            const int wc = wi * 8 + i, rg = wc >> 2;
+            const int m = rg * 8 + (lane & 7), k8 = (wc & 3) * 4 + (lane >> 3);
+            const int64_t row = r0 + m;
+            const bool ok = row < items;
+            const int64_t e = (ok ? row : 0) * D + k8 * 8;
+            const uint32_t dst = (uint32_t)(rg * kEtSbo + k8 * kEtLbo + (lane & 7) * 16);
+            cp_async16(xk + dst, K16 + e, ok ? 16u : 0u);
+            cp_async16(xv + dst, V16 + e, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+    const uint32_t idesc = (a.dtype == TQ_BF16) ? tc::idesc_bf16_f32(kEtRows, D) : tc::idesc_f16_f32(kEtRows, D);
+    const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
+    const int hkv = g.hkv;
+    const int64_t cap = g.num_blocks * kBlockSize;
+    bool bad = false;
+    int tile = blockIdx.x + slot * gridDim.x;
+    if (tile < num_tiles) load(tile);
+    for (int i = 0; tile < num_tiles; ++i) {
+        // this slot's copies have landed, and its threads are done reading the
+        // tensor-memory columns the MMAs are about to overwrite
+        cp_async_wait_all();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc::fence_before_sync();
+        asm volatile("bar.sync %0, 256;" ::"r"(1 + slot) : "memory");
+        if (ts == 0) {
+            tc::fence_after_sync();
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s)
+                tc::mma_f16_ss(tcol, tc::smem_desc(xk + 256 * s, kEtLbo, kEtSbo),
+                               tc::smem_desc(sbase + kEtH + 256 * s, kEtLbo, kEtSbo), idesc, s > 0 ? 1u : 0u);
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s)
+                tc::mma_f16_ss(tcol + 128, tc::smem_desc(xv + 256 * s, kEtLbo, kEtSbo),
+                               tc::smem_desc(sbase + kEtH + 256 * s, kEtLbo, kEtSbo), idesc, s > 0 ? 1u : 0u);
+            tc::commit(mbar);
+        }
+        // this row's (token, KV head) item and its slot, loaded while the MMAs run
+        const int64_t it = (int64_t)tile * kEtRows + tw;
+        const bool live = it < items;
+        const uint32_t itu = (uint32_t)(live ? it : 0);  // items < 2^31
+        const uint32_t t = itu / (uint32_t)hkv;
+        const int hc = (int)(itu - t * (uint32_t)hkv);
+        const int64_t sl = live ? __ldg(a.slot_mapping + t) : -1;
+        // a wait that gives up ends the slot's loop for all its threads
+        // together (the named barriers need all 256)
+        bad = et_any256(!mbar_wait(mbar, (uint32_t)(i & 1)), 1 + slot);
+        if (bad) break;
+        tc::fence_after_sync();
+        const int next = tile + 2 * (int)gridDim.x;
+        if (next < num_tiles) load(next);  // the buffers are free: the MMAs have read them
+
+        // ---- row tw of the tile ----
+        if (half == 0 && live && sl >= cap) flag(a.status, TQ_FLAG_BAD_SLOT);
+        const bool store = live && sl >= 0 && sl < cap;
+        static_assert(kBlockSize == 16, "page index by shift");
+        const int64_t blk = store ? (sl >> 4) : 0;
+        const int off = (int)(sl & (kBlockSize - 1));
+        uint8_t* page = a.pool + (blk * hkv + hc) * g.page_bytes;
+
+        float x[32];
+        // ---- this half's sum of squares of U_k (||U_k||^2 = d ||k||^2, d = 128:
+        // an exact scaling), minimum and maximum of U_v ----
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        float lo4[4] = {3.4e38f, 3.4e38f, 3.4e38f, 3.4e38f}, hi4[4] = {-3.4e38f, -3.4e38f, -3.4e38f, -3.4e38f};
+        bool finite = true;
+#pragma unroll 1
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
+            et_load32(tk + 32 * c, x);
+            // a non-finite input coordinate makes every rotated coordinate inf
+            // or NaN (H has no zero entry), so one coordinate tells
+            finite = finite && isfinite(x[0]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s4[j & 3] = fmaf(x[j], x[j], s4[j & 3]);
+            et_load32(tv + 32 * c, x);
+            finite = finite && isfinite(x[0]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                lo4[j & 3] = fminf(lo4[j & 3], x[j]);
+                hi4[j & 3] = fmaxf(hi4[j & 3], x[j]);
+            }
+        }
+        float4* xchg = reinterpret_cast<float4*>(sm + kEtXchg) + slot * 2 * kEtRows;
+        xchg[half * kEtRows + tw] = make_float4((s4[0] + s4[1]) + (s4[2] + s4[3]),
+                                                fminf(fminf(lo4[0], lo4[1]), fminf(lo4[2], lo4[3])),
+                                                fmaxf(fmaxf(hi4[0], hi4[1]), fmaxf(hi4[2], hi4[3])), finite ? 1.f : 0.f);
+        asm volatile("bar.sync %0, 256;" ::"r"(1 + slot) : "memory");
+        // both halves combine the two records in the same order: the same gamma,
+        // min and max
+        const float4 e0 = xchg[tw], e1 = xchg[kEtRows + tw];
+        const float gamma = sqrtf((e0.x + e1.x) * (1.f / 128.f));
+        // the scaling by 1/sqrt(d) is monotone, so min and max commute with it
+        const float mn = fminf(e0.y, e1.y) * inv_sqrt_d;
+        const float mx = fmaxf(e0.z, e1.z) * inv_sqrt_d;
+        finite = e0.w != 0.f && e1.w != 0.f;
+        const float scale = (mx - mn) / (float)VMAX;
+        const float rs = 1.f / scale;
+        {
+            uint8_t* krow = page + g.kcode_off + off * (D * KB / 8);
+            uint8_t* vrow = page + g.vcode_off + off * (D * VB / 8);
+            const KeyThresholds<KB <= 4 ? KB : 1> kt(a.c, gamma);
+#pragma unroll 1
+            for (int c = 2 * half; c < 2 * half + 2; ++c) {
+                et_load32(tk + 32 * c, x);
+                int kc[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (!(gamma > 0.f)) kc[j] = HALF - 1;
+                    else if constexpr (KB <= 4) kc[j] = key_code_bsearch<KB>(kt, x[j]);
+                    else kc[j] = key_code_search<KB>(x[j], gamma, bsd_s);
+                }
+                uint32_t wk[KB];
+                pack_words<KB, 32>(kc, wk);
+                if (store) et_store_words<KB>(krow + c * 4 * KB, wk);
+                et_load32(tv + 32 * c, x);
+                int vc[32];
+                et_value_codes<VB>(x, mn, scale, rs, vc);
+                uint32_t wv[VB];
+                pack_words<VB, 32>(vc, wv);
+                if (store) et_store_words<VB>(vrow + c * 4 * VB, wv);
+            }
+        }
+        if (store && half == 0) {
+            if (!finite) flag(a.status, TQ_FLAG_NONFINITE);
+            const uint16_t hg = f16_bits(gamma), hs = f16_bits(scale), hz = f16_bits(mn);
+            reinterpret_cast<uint16_t*>(page + g.gam_off)[off] = hg;
+            reinterpret_cast<uint16_t*>(page + g.scl_off)[off] = hs;
+            reinterpret_cast<uint16_t*>(page + g.zer_off)[off] = hz;
+            const bool ovf = ((hg & 0x7FFF) == 0x7C00) || ((hs & 0x7FFF) == 0x7C00) || ((hz & 0x7FFF) == 0x7C00);
+            if (ovf && finite) flag(a.status, TQ_FLAG_OVERFLOW);
+        }
+        tile = next;
+    }
+    if (bad && ts == 0) flag(a.status, TQ_FLAG_TIMEOUT);
+    // every MMA of the CTA has completed (each warpgroup waited for its last)
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc<512>(tmem);
+    }
+}
+
+// Whether the tensor-core encode takes this call: 16-bit inputs, no QJL, and
+// enough tiles to give both tile slots of every SM one each.
+inline bool encode_tc_eligible(const EncodeArgs& a, int64_t items, int num_sms) {
+    return a.g.m == 0 && a.g.d == kHeadDim && (a.dtype == TQ_BF16 || a.dtype == TQ_F16) &&
+           items >= (int64_t)num_sms * 2 * kEtRows && items < ((int64_t)1 << 31);
+}
+
+template <int KB, int VB>
+int launch_encode_tc(const EncodeArgs& a, int64_t items, int num_sms, cudaStream_t s) {
+    auto kern = encode_tc_kernel<KB, VB>;
+    static int done[64] = {};
+    cudaError_t e = ensure_smem_limit(kern, kEtSmem, done);
+    if (e != cudaSuccess) return (int)e;
+    const int num_tiles = (int)((items + kEtRows - 1) / kEtRows);
+    const int grid = num_tiles < num_sms ? num_tiles : num_sms;
+    return (int)launch_programmatic(kern, dim3((unsigned)grid), dim3(kEtThreads), (size_t)kEtSmem, s, a, items,
+                                    num_tiles);
+}
+
+}  // namespace tq

@@ -29,6 +29,10 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
 }
 // The same with B in the MN-major layout (transpose-B bit 16).
 __host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int M, int N) { return idesc_f16_f32(M, N) | (1u << 16); }
+// kind::f16 with bf16 A and B (A/B format 1), fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return idesc_f16_f32(M, N) | (1u << 7) | (1u << 10);
+}
 
 // Shared-memory matrix descriptor, no swizzle: start address, leading-dimension
 // byte offset (between core matrices adjacent along K), stride-dimension byte
@@ -96,6 +100,15 @@ __device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
         : "r"(taddr)
         : "memory");
 }
+// After wait_ld: the registers a tensor-memory load filled are defined here,
+// so the compiler keeps every use of them after the wait (no instruction).
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8)
+        asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]),
+                     "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+
 // 16 lanes x 256 bits, twice along the columns: thread i gets, for the lanes
 // base + i/4 and base + i/4 + 8, columns 2 (i%4) and 2 (i%4) + 1 of the first
 // 8 columns (r[0..3]) and of the next 8 (r[4..7]) -- the accumulator layout of
