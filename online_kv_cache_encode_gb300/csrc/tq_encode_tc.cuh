@@ -79,44 +79,113 @@ __device__ __forceinline__ void et_store_words(uint8_t* p, const uint32_t (&w)[B
     }
 }
 
-// Value codes of 32 coordinates x (rotated, unnormalised) of one row:
+// Codes are formed in the fp32 add pipe rather than with compares, selects and
+// conversions: for |q| < 2^22, q + 1.5 2^23 rounds q to the nearest integer
+// (ties to even) and holds it in its low mantissa bits above the constant
+// 0x4B400000.  Such "biased" fields are packed by integer multiply-adds; the
+// constant's share of every word is removed once (the fields do not overlap, so
+// the sums are the ORs of the codes).
+constexpr float kEtMagic = 12582912.f;  // 1.5 * 2^23
+constexpr uint32_t kEtMagicBits = 0x4B400000u;
+
+// The constant's share of word k when 32 B-bit biased fields are packed
+// LSB-first into B words (field i at bit B i; a field that crosses a word
+// boundary continues at bit 0 of the next word).
+__host__ __device__ constexpr uint32_t et_pack_bias(int B, int k) {
+    uint32_t sum = 0;
+    for (int i = 0; i < 32; ++i) {
+        const int pos = B * i, wi = pos >> 5, sh = pos & 31;
+        if (wi == k) sum += kEtMagicBits << sh;
+        if (sh + B > 32 && wi + 1 == k) sum += kEtMagicBits >> (32 - sh);
+    }
+    return 0u - sum;
+}
+
+template <int B>
+__device__ __forceinline__ void et_pack_biased(const uint32_t (&f)[32], uint32_t (&w)[B]) {
+#pragma unroll
+    for (int k = 0; k < B; ++k) w[k] = et_pack_bias(B, k);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int pos = B * i, wi = pos >> 5, sh = pos & 31;
+        w[wi] += f[i] * (1u << sh);
+        if (sh + B > 32) w[wi + 1] += f[i] >> (32 - sh);
+    }
+}
+
+// Key codes (widths up to 4 bits) of 32 rotated coordinates x against the
+// positive thresholds scaled by F (T[b] = F sqrt(d) t_{HALF+b} gamma), with F a
+// power of two such that (|x| - thr_b) F >= 2 whenever |x| > thr_b: then
+// sat(|x| F - T[b]) is exactly [|x| > thr_b], and n = #{b : |x| > thr_b} is
+// their sum; the code is HALF + n for x > 0 and HALF - 1 - n otherwise, i.e.
+// n ^ HALF or n ^ (HALF - 1) for n < HALF.
+template <int KB>
+__device__ __forceinline__ void et_key_codes(const float (&x)[32], const float (&T)[(1 << (KB - 1)) > 1 ? (1 << (KB - 1)) - 1 : 1],
+                                             float F, uint32_t (&f)[32]) {
+    constexpr int HALF = 1 << (KB - 1);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float n = 0.f;
+        if constexpr (HALF > 1) {
+            const float X = fabsf(x[j]) * F;
+            float s[HALF - 1];
+#pragma unroll
+            for (int b = 0; b < HALF - 1; ++b) s[b] = __saturatef(X - T[b]);
+#pragma unroll
+            for (int step = 1; step < HALF - 1; step <<= 1)
+#pragma unroll
+                for (int b = 0; b + step < HALF - 1; b += 2 * step) s[b] += s[b + step];
+            n = s[0];
+        }
+        f[j] = __float_as_uint(n + kEtMagic) ^ (uint32_t)((x[j] > 0.f) ? HALF : HALF - 1);
+    }
+}
+
+// Value codes of 32 coordinates x (rotated, unnormalised) of one row, biased:
 // rint((x / sqrt(d) - mn) / scale), the quotient formed as a product with
 // rs = 1 / scale.  That product is within VMAX 2^-22 of the exact quotient,
 // so it rounds to the same integer unless it lies within 2^(VB - 21) of a
 // half-integer; if any of the 32 does, the row's chunk is coded again with the
 // division (rint of the correctly rounded quotient, as everywhere else).
 template <int VB>
-__device__ __forceinline__ void et_value_codes(const float (&x)[32], float mn, float scale, float rs, int (&vc)[32]) {
+__device__ __forceinline__ void et_value_codes(const float (&x)[32], float mn, float scale, float rs, uint32_t (&f)[32]) {
     constexpr float VMAX = (float)((1 << VB) - 1);
     constexpr float kTie = 0.5f - (float)(1 << VB) * 4.76837158203125e-7f;  // 0.5 - 2^(VB - 21)
     const float inv_sqrt_d = 0.08838834764831845f;
     if (!(scale > 0.f)) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) vc[j] = 0;
+        for (int j = 0; j < 32; ++j) f[j] = kEtMagicBits;
         return;
     }
     bool near = false;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const float q = (x[j] * inv_sqrt_d - mn) * rs;
-        const float r = rintf(q);
-        near = near || (fabsf(q - r) > kTie);
-        vc[j] = (int)fminf(fmaxf(r, 0.f), VMAX);
+        const float t = q + kEtMagic;
+        near = near || (fabsf(q - (t - kEtMagic)) > kTie);
+        f[j] = __float_as_uint(t);
     }
     if (near) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) vc[j] = (int)fminf(fmaxf(rintf((x[j] * inv_sqrt_d - mn) / scale), 0.f), VMAX);
+        for (int j = 0; j < 32; ++j)
+            f[j] = __float_as_uint(fminf(fmaxf(rintf((x[j] * inv_sqrt_d - mn) / scale), 0.f), VMAX) + kEtMagic);
     }
 }
 
-// This thread's row of tensor memory, 32 columns at taddr.
-__device__ __forceinline__ void et_load32(uint32_t taddr, float (&x)[32]) {
-    uint32_t r[32];
-    tc::ld_32x32b_x32(taddr, r);
+// This thread's row of tensor memory, 32 columns at ta and 32 at tb, with one
+// wait for both loads.
+__device__ __forceinline__ void et_load2x32(uint32_t ta, uint32_t tb, float (&xa)[32], float (&xb)[32]) {
+    uint32_t ra[32], rb[32];
+    tc::ld_32x32b_x32(ta, ra);
+    tc::ld_32x32b_x32(tb, rb);
     tc::wait_ld();
-    tc::reg_fence(r);
+    tc::reg_fence(ra);
+    tc::reg_fence(rb);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+    for (int j = 0; j < 32; ++j) {
+        xa[j] = __uint_as_float(ra[j]);
+        xb[j] = __uint_as_float(rb[j]);
+    }
 }
 
 template <int KB, int VB>
@@ -250,7 +319,7 @@ __global__ void __launch_bounds__(kEtThreads, 1) encode_tc_kernel(const EncodeAr
         const int off = (int)(sl & (kBlockSize - 1));
         uint8_t* page = a.pool + (blk * hkv + hc) * g.page_bytes;
 
-        float x[32];
+        float xk_[32], xv_[32];
         // ---- this half's sum of squares of U_k (||U_k||^2 = d ||k||^2, d = 128:
         // an exact scaling), minimum and maximum of U_v ----
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -258,18 +327,15 @@ __global__ void __launch_bounds__(kEtThreads, 1) encode_tc_kernel(const EncodeAr
         bool finite = true;
 #pragma unroll 1
         for (int c = 2 * half; c < 2 * half + 2; ++c) {
-            et_load32(tk + 32 * c, x);
+            et_load2x32(tk + 32 * c, tv + 32 * c, xk_, xv_);
             // a non-finite input coordinate makes every rotated coordinate inf
             // or NaN (H has no zero entry), so one coordinate tells
-            finite = finite && isfinite(x[0]);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) s4[j & 3] = fmaf(x[j], x[j], s4[j & 3]);
-            et_load32(tv + 32 * c, x);
-            finite = finite && isfinite(x[0]);
+            finite = finite && isfinite(xk_[0]) && isfinite(xv_[0]);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                lo4[j & 3] = fminf(lo4[j & 3], x[j]);
-                hi4[j & 3] = fmaxf(hi4[j & 3], x[j]);
+                s4[j & 3] = fmaf(xk_[j], xk_[j], s4[j & 3]);
+                lo4[j & 3] = fminf(lo4[j & 3], xv_[j]);
+                hi4[j & 3] = fmaxf(hi4[j & 3], xv_[j]);
             }
         }
         float4* xchg = reinterpret_cast<float4*>(sm + kEtXchg) + slot * 2 * kEtRows;
@@ -291,24 +357,44 @@ __global__ void __launch_bounds__(kEtThreads, 1) encode_tc_kernel(const EncodeAr
             uint8_t* krow = page + g.kcode_off + off * (D * KB / 8);
             uint8_t* vrow = page + g.vcode_off + off * (D * VB / 8);
             const KeyThresholds<KB <= 4 ? KB : 1> kt(a.c, gamma);
+            // T = F thr: F = 2^(24 - e) with 2^e <= thr_0 < 2^(e + 1), so that
+            // (|x| - thr_b) F >= 2 when |x| > thr_b (the difference of two floats
+            // at least thr_0 apart in exponent is a multiple of 2^(e - 23));
+            // |x| F stays below 2^25 / t_{HALF} (|x| <= sqrt(d) gamma)
+            constexpr int NT = (KB <= 4 && HALF > 1) ? HALF - 1 : 1;
+            float T[NT];
+            float F = 1.f;
+            const int e0 = (int)((__float_as_uint(kt.thr[0]) >> 23) & 0xFFu) - 127;
+            const bool fast = KB <= 4 && gamma > 0.f && e0 > -100 && e0 < 100;
+            if constexpr (KB <= 4 && HALF > 1) {
+                F = __uint_as_float((uint32_t)(127 + 24 - e0) << 23);
+#pragma unroll
+                for (int b = 0; b < NT; ++b) T[b] = kt.thr[b] * F;
+            }
 #pragma unroll 1
             for (int c = 2 * half; c < 2 * half + 2; ++c) {
-                et_load32(tk + 32 * c, x);
-                int kc[32];
+                et_load2x32(tk + 32 * c, tv + 32 * c, xk_, xv_);
+                uint32_t fk[32];
+                if (fast) {
+                    if constexpr (KB <= 4) et_key_codes<KB>(xk_, T, F, fk);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (!(gamma > 0.f)) kc[j] = HALF - 1;
-                    else if constexpr (KB <= 4) kc[j] = key_code_bsearch<KB>(kt, x[j]);
-                    else kc[j] = key_code_search<KB>(x[j], gamma, bsd_s);
+                    for (int j = 0; j < 32; ++j) {
+                        int code = HALF - 1;  // a zero key (gamma = 0)
+                        if (gamma > 0.f) {
+                            if constexpr (KB <= 4) code = key_code_bsearch<KB>(kt, xk_[j]);
+                            else code = key_code_search<KB>(xk_[j], gamma, bsd_s);
+                        }
+                        fk[j] = kEtMagicBits + (uint32_t)code;
+                    }
                 }
                 uint32_t wk[KB];
-                pack_words<KB, 32>(kc, wk);
+                et_pack_biased<KB>(fk, wk);
                 if (store) et_store_words<KB>(krow + c * 4 * KB, wk);
-                et_load32(tv + 32 * c, x);
-                int vc[32];
-                et_value_codes<VB>(x, mn, scale, rs, vc);
+                uint32_t fv[32];
+                et_value_codes<VB>(xv_, mn, scale, rs, fv);
                 uint32_t wv[VB];
-                pack_words<VB, 32>(vc, wv);
+                et_pack_biased<VB>(fv, wv);
                 if (store) et_store_words<VB>(vrow + c * 4 * VB, wv);
             }
         }
