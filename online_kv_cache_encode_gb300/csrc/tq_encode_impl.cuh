@@ -413,7 +413,10 @@ static int launch_encode_t(const EncodeArgs& a, int num_sms, cudaStream_t s) {
     const int64_t items = a.num_tokens * a.g.hkv;
     if constexpr (M == 0) {
         // bulk 16-bit encodes rotate on the tensor cores
-        if (encode_tc_eligible(a, items, num_sms)) return launch_encode_tc<KB, VB>(a, items, num_sms, s);
+        if (encode_tc_eligible(a, items, num_sms)) {
+            const int r = launch_encode_tc<KB, VB>(a, items, num_sms, s);
+            if (r >= 0) return r;
+        }
     }
     // four items per warp once there are enough to give every warp slot of
     // the GPU four; one item per warp (lower latency) below that

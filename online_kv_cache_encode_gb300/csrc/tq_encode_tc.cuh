@@ -20,13 +20,16 @@
 //
 // CTA: four warpgroups, two per tile slot.  A slot has its own input buffers
 // in shared memory (the tile's key and value rows in the K-major core-matrix
-// layout, filled by 16-byte asynchronous copies) and 256 tensor-memory columns
+// layout with the 128-byte swizzle, filled by TMA tile copies of 64
+// coordinates x 128 rows, two per operand) and 256 tensor-memory columns
 // (U_k, U_v).  Each warpgroup of a slot takes one half of the columns: it sums
 // the squares and finds the minimum and maximum over its half, the two halves
 // exchange these through shared memory, and each codes its half.  A slot takes every other tile of the CTA's share: the copies of
 // its next tile run while it codes the current one, and the other slot's work
 // fills the gaps.  One CTA per SM, persistent over the tiles.
 #pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "tq_decode_impl.cuh"  // mbarrier, grid-dependency and shared-address helpers
@@ -37,21 +40,29 @@ namespace tq {
 
 constexpr int kEtRows = 128;                   // rows (token, KV head) per tile
 constexpr int kEtThreads = 512;                // two slots x two column halves, one warpgroup each
-constexpr uint32_t kEtLbo = 128, kEtSbo = 2048;  // K-major core matrices: along K adjacent, 8-row groups 2 KB apart
+// H: K-major core matrices without swizzle, along K adjacent, 8-row groups
+// 2 KB apart.  The inputs: the TMA boxes' 128-byte-swizzled K-major layout
+// (row r of a box at 128 r, its 16-byte pieces permuted by r % 8; 8-row groups
+// 1 KB apart; the box of coordinates 64 .. 127 16 KB after the first).
+constexpr uint32_t kEtLbo = 128, kEtSbo = 2048;
+constexpr uint32_t kEtXSbo = 1024, kEtXBox = 16384;
 constexpr int kEtOp = kEtRows * kHeadDim * 2;  // one 128 x 128 16-bit operand: 32 KB
 constexpr int kEtH = 0;                        // H [n][k]
 constexpr int kEtX = kEtOp;                    // slot s: keys at kEtX + 2 s kEtOp, values kEtOp further
 constexpr int kEtXchg = kEtX + 4 * kEtOp;      // [slot][half][row] (sum of squares, min, max, finite)
 constexpr int kEtBsd = kEtXchg + 2 * 2 * kEtRows * 16;  // key widths above 4 bits: sqrt(d) t_b of the positive half
-constexpr int kEtBars = kEtBsd + 4 * (kMaxLevels / 2);
-constexpr int kEtTaddr = kEtBars + 16;
-constexpr int kEtSmem = kEtTaddr + 16;
+constexpr int kEtBars = kEtBsd + 4 * (kMaxLevels / 2);  // per slot: MMAs done, inputs landed
+constexpr int kEtTaddr = kEtBars + 32;
+constexpr int kEtSmem = kEtTaddr + 16 + 1024;  // + room to align the base to 1 KB (swizzle atoms)
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+// Box (x, y) of a 2-D tensor map into shared memory, completing on `bar`.
+__device__ __forceinline__ void et_tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // OR of `v` over the 256 threads of a tile slot (named barrier `id`)
 __device__ __forceinline__ bool et_any256(bool v, int id) {
     uint32_t r;
@@ -189,21 +200,24 @@ __device__ __forceinline__ void et_load2x32(uint32_t ta, uint32_t tb, float (&xa
 }
 
 template <int KB, int VB>
-__global__ void __launch_bounds__(kEtThreads, 1) encode_tc_kernel(const EncodeArgs a, int64_t items, int num_tiles) {
-    extern __shared__ __align__(128) uint8_t sm[];
+__global__ void __launch_bounds__(kEtThreads, 1)
+    encode_tc_kernel(const EncodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     int64_t items, int num_tiles) {
+    extern __shared__ __align__(1024) uint8_t sm_raw[];
     constexpr int D = kHeadDim;
     constexpr int HALF = 1 << (KB - 1);
     constexpr int VMAX = (1 << VB) - 1;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wg = tid >> 7, tw = tid & 127;
     const Geometry& g = a.g;
+    // the swizzled layout repeats every 1 KB and is anchored at 1 KB boundaries
+    uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     float* bsd_s = reinterpret_cast<float*>(sm + kEtBsd);
 
     grid_dependency_wait();  // the previous grid's writes (inputs, pool) are visible
     if (tid == 0) {
-        mbar_init(sbase + kEtBars, 1);
-        mbar_init(sbase + kEtBars + 8, 1);
+        for (int b = 0; b < 4; ++b) mbar_init(sbase + kEtBars + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tc::tmem_alloc<512>(sbase + kEtTaddr);
@@ -247,28 +261,17 @@ __global__ void __launch_bounds__(kEtThreads, 1) encode_tc_kernel(const EncodeAr
     const uint32_t tcol = tmem + 256u * slot;                                        // U_k at +0, U_v at +128
     const uint32_t tk = tcol + ((uint32_t)((warp & 3) * 32) << 16), tv = tk + 128;  // this warp's lanes
     const uint32_t mbar = sbase + kEtBars + 8 * slot;
-    const uint16_t* K16 = static_cast<const uint16_t*>(a.K);
-    const uint16_t* V16 = static_cast<const uint16_t*>(a.V);
-    // the rows of `tile` into this slot's buffers: per warp instruction,
-    // lanes l and l + 8, l + 16, l + 24 take 16-byte pieces k8 .. k8 + 3 of
-    // row 8 rg + l (l < 8): 8 rows x 64 contiguous bytes from global memory,
-    // 32 different 16-byte slots of shared memory in four bank-conflict-free
-    // groups; rows past the last item are zero-filled
+    const uint32_t full = sbase + kEtBars + 16 + 8 * slot;
+    // the rows of `tile` into this slot's buffers (thread 0 of the slot): box
+    // k8 holds coordinates 8 k8 .. 8 k8 + 7 of the 128 rows, rows past the last
+    // item zero-filled
     auto load = [&](int tile) {
-        const int64_t r0 = (int64_t)tile * kEtRows;
-        const int wi = ts >> 5;
-#pragma unroll 4
-        for (int i = 0; i < 8; ++i) {
-            const int wc = wi * 8 + i, rg = wc >> 2;
-            const int m = rg * 8 + (lane & 7), k8 = (wc & 3) * 4 + (lane >> 3);
-            const int64_t row = r0 + m;
-            const bool ok = row < items;
-            const int64_t e = (ok ? row : 0) * D + k8 * 8;
-            const uint32_t dst = (uint32_t)(rg * kEtSbo + k8 * kEtLbo + (lane & 7) * 16);
-            cp_async16(xk + dst, K16 + e, ok ? 16u : 0u);
-            cp_async16(xv + dst, V16 + e, ok ? 16u : 0u);
+        mbar_arrive_tx(full, 2u * kEtOp);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            et_tma_2d(xk + j * kEtXBox, &tmk, 64 * j, tile * kEtRows, full);
+            et_tma_2d(xv + j * kEtXBox, &tmv, 64 * j, tile * kEtRows, full);
         }
-        cp_async_commit();
     };
     const uint32_t idesc = (a.dtype == TQ_BF16) ? tc::idesc_bf16_f32(kEtRows, D) : tc::idesc_f16_f32(kEtRows, D);
     const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
@@ -276,25 +279,27 @@ __global__ void __launch_bounds__(kEtThreads, 1) encode_tc_kernel(const EncodeAr
     const int64_t cap = g.num_blocks * kBlockSize;
     bool bad = false;
     int tile = blockIdx.x + slot * gridDim.x;
-    if (tile < num_tiles) load(tile);
+    if (ts == 0 && tile < num_tiles) load(tile);
     for (int i = 0; tile < num_tiles; ++i) {
-        // this slot's copies have landed, and its threads are done reading the
-        // tensor-memory columns the MMAs are about to overwrite
-        cp_async_wait_all();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // the slot's threads are done reading the tensor-memory columns the
+        // MMAs are about to overwrite
         tc::fence_before_sync();
         asm volatile("bar.sync %0, 256;" ::"r"(1 + slot) : "memory");
         if (ts == 0) {
-            tc::fence_after_sync();
+            // the tile's rows have landed (a wait that gives up issues nothing:
+            // the MMA wait below then gives up too)
+            if (mbar_wait(full, (uint32_t)(i & 1))) {
+                tc::fence_after_sync();
 #pragma unroll
-            for (int s = 0; s < D / 16; ++s)
-                tc::mma_f16_ss(tcol, tc::smem_desc(xk + 256 * s, kEtLbo, kEtSbo),
-                               tc::smem_desc(sbase + kEtH + 256 * s, kEtLbo, kEtSbo), idesc, s > 0 ? 1u : 0u);
+                for (int s = 0; s < D / 16; ++s)
+                    tc::mma_f16_ss(tcol, tc::smem_desc_sw128(xk + (s >> 2) * kEtXBox + 32 * (s & 3), kEtXSbo),
+                                   tc::smem_desc(sbase + kEtH + 256 * s, kEtLbo, kEtSbo), idesc, s > 0 ? 1u : 0u);
 #pragma unroll
-            for (int s = 0; s < D / 16; ++s)
-                tc::mma_f16_ss(tcol + 128, tc::smem_desc(xv + 256 * s, kEtLbo, kEtSbo),
-                               tc::smem_desc(sbase + kEtH + 256 * s, kEtLbo, kEtSbo), idesc, s > 0 ? 1u : 0u);
-            tc::commit(mbar);
+                for (int s = 0; s < D / 16; ++s)
+                    tc::mma_f16_ss(tcol + 128, tc::smem_desc_sw128(xv + (s >> 2) * kEtXBox + 32 * (s & 3), kEtXSbo),
+                                   tc::smem_desc(sbase + kEtH + 256 * s, kEtLbo, kEtSbo), idesc, s > 0 ? 1u : 0u);
+                tc::commit(mbar);
+            }
         }
         // this row's (token, KV head) item and its slot, loaded while the MMAs run
         const int64_t it = (int64_t)tile * kEtRows + tw;
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(kEtThreads, 1) encode_tc_kernel(const EncodeAr
         if (bad) break;
         tc::fence_after_sync();
         const int next = tile + 2 * (int)gridDim.x;
-        if (next < num_tiles) load(next);  // the buffers are free: the MMAs have read them
+        if (ts == 0 && next < num_tiles) load(next);  // the buffers are free: the MMAs have read them
 
         // ---- row tw of the tile ----
         if (half == 0 && live && sl >= cap) flag(a.status, TQ_FLAG_BAD_SLOT);
@@ -426,16 +431,45 @@ inline bool encode_tc_eligible(const EncodeArgs& a, int64_t items, int num_sms) 
            items >= (int64_t)num_sms * 2 * kEtRows && items < ((int64_t)1 << 31);
 }
 
+// The tensor map of one input: 16-bit elements, [rows][128] row-major, boxes of
+// 64 coordinates x 128 rows landing in the 128-byte swizzle, out-of-range rows
+// read as zero.  The encoder entry
+// point comes from the driver once per process (any thread that gets there
+// first stores the same pointer).
+inline bool et_tensor_map(CUtensorMap* map, const void* base, int64_t rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kEtRows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launches the tensor-core encode; returns -1 (nothing launched) when the
+// tensor maps cannot be made, so that the caller takes the CUDA-core kernel.
 template <int KB, int VB>
 int launch_encode_tc(const EncodeArgs& a, int64_t items, int num_sms, cudaStream_t s) {
+    CUtensorMap tmk, tmv;
+    if (!et_tensor_map(&tmk, a.K, items) || !et_tensor_map(&tmv, a.V, items)) return -1;
     auto kern = encode_tc_kernel<KB, VB>;
     static int done[64] = {};
     cudaError_t e = ensure_smem_limit(kern, kEtSmem, done);
     if (e != cudaSuccess) return (int)e;
     const int num_tiles = (int)((items + kEtRows - 1) / kEtRows);
     const int grid = num_tiles < num_sms ? num_tiles : num_sms;
-    return (int)launch_programmatic(kern, dim3((unsigned)grid), dim3(kEtThreads), (size_t)kEtSmem, s, a, items,
-                                    num_tiles);
+    return (int)launch_programmatic(kern, dim3((unsigned)grid), dim3(kEtThreads), (size_t)kEtSmem, s, a, tmk, tmv,
+                                    items, num_tiles);
 }
 
 }  // namespace tq

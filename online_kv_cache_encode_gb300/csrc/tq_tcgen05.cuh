@@ -43,6 +43,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
+// The same for a K-major operand in the 128-byte swizzle (layout type 2 at bits
+// 61-63): rows of 128 bytes whose 16-byte pieces are permuted by row % 8,
+// 8-row groups `sbo` bytes apart; the leading byte offset is unused (1).  The
+// atoms sit on 1 KB boundaries, and a K-step of 16 elements inside the 128-byte
+// row advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
 // Allocate `ncols` TMEM columns (a power of two, 32 .. 512); the whole warp
 // executes it and the address lands in shared memory at `dst`.
 template <int NCOLS>
