@@ -90,6 +90,37 @@ __device__ __forceinline__ void et_store_words(uint8_t* p, const uint32_t (&w)[B
     }
 }
 
+// Two fp32 lanes in one 64-bit register and the packed add / multiply / fma of
+// sm_100 and later: one instruction for two coordinates.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // Codes are formed in the fp32 add pipe rather than with compares, selects and
 // conversions: for |q| < 2^22, q + 1.5 2^23 rounds q to the nearest integer
 // (ties to even) and holds it in its low mantissa bits above the constant
@@ -169,17 +200,24 @@ __device__ __forceinline__ void et_value_codes(const float (&x)[32], float mn, f
         return;
     }
     bool near = false;
+    const uint64_t C2 = f2_pack(inv_sqrt_d, inv_sqrt_d), NMN2 = f2_pack(-mn, -mn), RS2 = f2_pack(rs, rs),
+                   MG2 = f2_pack(kEtMagic, kEtMagic);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float q = (x[j] * inv_sqrt_d - mn) * rs;
-        const float t = q + kEtMagic;
-        near = near || (fabsf(q - (t - kEtMagic)) > kTie);
-        f[j] = __float_as_uint(t);
+    for (int j = 0; j < 32; j += 2) {
+        // q = (x / sqrt(d) - mn) / scale as fma then product, two coordinates at a time
+        const uint64_t q = f2_mul(f2_fma(f2_pack(x[j], x[j + 1]), C2, NMN2), RS2);
+        const uint64_t t = f2_add(q, MG2);
+        float e0, e1, t0, t1;
+        f2_unpack(f2_sub(q, f2_sub(t, MG2)), e0, e1);
+        f2_unpack(t, t0, t1);
+        near = near || fabsf(e0) > kTie || fabsf(e1) > kTie;
+        f[j] = __float_as_uint(t0);
+        f[j + 1] = __float_as_uint(t1);
     }
     if (near) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            f[j] = __float_as_uint(fminf(fmaxf(rintf((x[j] * inv_sqrt_d - mn) / scale), 0.f), VMAX) + kEtMagic);
+            f[j] = __float_as_uint(fminf(fmaxf(rintf(fmaf(x[j], inv_sqrt_d, -mn) / scale), 0.f), VMAX) + kEtMagic);
     }
 }
 
@@ -327,7 +365,7 @@ __global__ void __launch_bounds__(kEtThreads, 1)
         float xk_[32], xv_[32];
         // ---- this half's sum of squares of U_k (||U_k||^2 = d ||k||^2, d = 128:
         // an exact scaling), minimum and maximum of U_v ----
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t ss2[2] = {0ull, 0ull};  // four partial sums of squares, two per register
         float lo4[4] = {3.4e38f, 3.4e38f, 3.4e38f, 3.4e38f}, hi4[4] = {-3.4e38f, -3.4e38f, -3.4e38f, -3.4e38f};
         bool finite = true;
 #pragma unroll 1
@@ -338,12 +376,18 @@ __global__ void __launch_bounds__(kEtThreads, 1)
             finite = finite && isfinite(xk_[0]) && isfinite(xv_[0]);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                s4[j & 3] = fmaf(xk_[j], xk_[j], s4[j & 3]);
+                if ((j & 1) == 0) {
+                    const uint64_t p = f2_pack(xk_[j], xk_[j + 1]);
+                    ss2[(j >> 1) & 1] = f2_fma(p, p, ss2[(j >> 1) & 1]);
+                }
                 lo4[j & 3] = fminf(lo4[j & 3], xv_[j]);
                 hi4[j & 3] = fmaxf(hi4[j & 3], xv_[j]);
             }
         }
         float4* xchg = reinterpret_cast<float4*>(sm + kEtXchg) + slot * 2 * kEtRows;
+        float s4[4];
+        f2_unpack(ss2[0], s4[0], s4[1]);
+        f2_unpack(ss2[1], s4[2], s4[3]);
         xchg[half * kEtRows + tw] = make_float4((s4[0] + s4[1]) + (s4[2] + s4[3]),
                                                 fminf(fminf(lo4[0], lo4[1]), fminf(lo4[2], lo4[3])),
                                                 fmaxf(fmaxf(hi4[0], hi4[1]), fmaxf(hi4[2], hi4[3])), finite ? 1.f : 0.f);
