@@ -158,28 +158,52 @@ __device__ __forceinline__ void et_pack_biased(const uint32_t (&f)[32], uint32_t
 // Key codes (widths up to 4 bits) of 32 rotated coordinates x against the
 // positive thresholds scaled by F (T[b] = F sqrt(d) t_{HALF+b} gamma), with F a
 // power of two such that (|x| - thr_b) F >= 2 whenever |x| > thr_b: then
-// sat(|x| F - T[b]) is exactly [|x| > thr_b], and n = #{b : |x| > thr_b} is
-// their sum; the code is HALF + n for x > 0 and HALF - 1 - n otherwise, i.e.
-// n ^ HALF or n ^ (HALF - 1) for n < HALF.
+// sat(|x| F - T[b]) is exactly [|x| > thr_b].  n = #{b : |x| > thr_b} comes from
+// a binary search over the thresholds whose steps are such saturated
+// differences, the next threshold picked by the exact select
+// fma(s, A, fma(s, -B, B)) = (s ? A : B) for s in {0, 1} (two coordinates per
+// packed instruction); the code is HALF + n for x > 0 and HALF - 1 - n
+// otherwise, i.e. n ^ HALF or n ^ (HALF - 1) for n < HALF.
 template <int KB>
 __device__ __forceinline__ void et_key_codes(const float (&x)[32], const float (&T)[(1 << (KB - 1)) > 1 ? (1 << (KB - 1)) - 1 : 1],
                                              float F, uint32_t (&f)[32]) {
     constexpr int HALF = 1 << (KB - 1);
+    const uint64_t MG2 = f2_pack(kEtMagic, kEtMagic);
+    // the select constants: (A, -B, B) pairs per select of constant thresholds
+    auto c2 = [](float v) { return f2_pack(v, v); };
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        float n = 0.f;
-        if constexpr (HALF > 1) {
-            const float X = fabsf(x[j]) * F;
-            float s[HALF - 1];
-#pragma unroll
-            for (int b = 0; b < HALF - 1; ++b) s[b] = __saturatef(X - T[b]);
-#pragma unroll
-            for (int step = 1; step < HALF - 1; step <<= 1)
-#pragma unroll
-                for (int b = 0; b + step < HALF - 1; b += 2 * step) s[b] += s[b + step];
-            n = s[0];
+    for (int j = 0; j < 32; j += 2) {
+        const float X0 = fabsf(x[j]) * F, X1 = fabsf(x[j + 1]) * F;
+        uint64_t N;
+        if constexpr (HALF == 8) {
+            const float a0 = __saturatef(X0 - T[3]), a1 = __saturatef(X1 - T[3]);
+            const uint64_t S4 = f2_pack(a0, a1);
+            float tA0, tA1;
+            f2_unpack(f2_fma(S4, c2(T[5]), f2_fma(S4, c2(-T[1]), c2(T[1]))), tA0, tA1);
+            const float b0 = __saturatef(X0 - tA0), b1 = __saturatef(X1 - tA1);
+            const uint64_t S2 = f2_pack(b0, b1), NS2 = f2_pack(-b0, -b1);
+            const uint64_t U = f2_fma(S4, c2(T[6]), f2_fma(S4, c2(-T[2]), c2(T[2])));
+            const uint64_t L = f2_fma(S4, c2(T[4]), f2_fma(S4, c2(-T[0]), c2(T[0])));
+            float tB0, tB1;
+            f2_unpack(f2_fma(S2, U, f2_fma(NS2, L, L)), tB0, tB1);
+            const uint64_t S1 = f2_pack(__saturatef(X0 - tB0), __saturatef(X1 - tB1));
+            N = f2_fma(S4, c2(4.f), f2_fma(S2, c2(2.f), S1));
+        } else if constexpr (HALF == 4) {
+            const float a0 = __saturatef(X0 - T[1]), a1 = __saturatef(X1 - T[1]);
+            const uint64_t S2 = f2_pack(a0, a1);
+            float tA0, tA1;
+            f2_unpack(f2_fma(S2, c2(T[2]), f2_fma(S2, c2(-T[0]), c2(T[0]))), tA0, tA1);
+            const uint64_t S1 = f2_pack(__saturatef(X0 - tA0), __saturatef(X1 - tA1));
+            N = f2_fma(S2, c2(2.f), S1);
+        } else if constexpr (HALF == 2) {
+            N = f2_pack(__saturatef(X0 - T[0]), __saturatef(X1 - T[0]));
+        } else {
+            N = 0ull;
         }
-        f[j] = __float_as_uint(n + kEtMagic) ^ (uint32_t)((x[j] > 0.f) ? HALF : HALF - 1);
+        float n0, n1;
+        f2_unpack(f2_add(N, MG2), n0, n1);
+        f[j] = __float_as_uint(n0) ^ (uint32_t)((x[j] > 0.f) ? HALF : HALF - 1);
+        f[j + 1] = __float_as_uint(n1) ^ (uint32_t)((x[j + 1] > 0.f) ? HALF : HALF - 1);
     }
 }
 
