@@ -229,7 +229,7 @@ TQ_API tq_status tq_cache_gaussian(const tq_cache* cache, double* S);
  *          (mx - mn)/(2^vb - 1); code = clamp(round-half-even((v_rot - mn) /
  *          scale), 0, 2^vb - 1) (all 0 if scale == 0); scale, mn as fp16.
  * Arithmetic is fp32.  Encodes of bf16 / fp16 inputs without QJL and with at
- * least two 128-row tiles of (token, KV head) items per SM form R k and R v
+ * least one 128-row tile of (token, KV head) items per SM form R k and R v
  * on the tensor cores (exact products, fp32 accumulation: the same values as
  * the butterfly up to the order of the additions); the others use the
  * butterfly.  An input coordinate that is inf or NaN sets TQ_FLAG_NONFINITE

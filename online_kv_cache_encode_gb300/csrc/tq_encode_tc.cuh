@@ -90,37 +90,6 @@ __device__ __forceinline__ void et_store_words(uint8_t* p, const uint32_t (&w)[B
     }
 }
 
-// Two fp32 lanes in one 64-bit register and the packed add / multiply / fma of
-// sm_100 and later: one instruction for two coordinates.
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
 // Codes are formed in the fp32 add pipe rather than with compares, selects and
 // conversions: for |q| < 2^22, q + 1.5 2^23 rounds q to the nearest integer
 // (ties to even) and holds it in its low mantissa bits above the constant
@@ -493,10 +462,10 @@ __global__ void __launch_bounds__(kEtThreads, 1)
 }
 
 // Whether the tensor-core encode takes this call: 16-bit inputs, no QJL, and
-// enough tiles to give both tile slots of every SM one each.
+// at least one 128-row tile per SM.
 inline bool encode_tc_eligible(const EncodeArgs& a, int64_t items, int num_sms) {
     return a.g.m == 0 && a.g.d == kHeadDim && (a.dtype == TQ_BF16 || a.dtype == TQ_F16) &&
-           items >= (int64_t)num_sms * 2 * kEtRows && items < ((int64_t)1 << 31);
+           items >= (int64_t)num_sms * kEtRows && items < ((int64_t)1 << 31);
 }
 
 // The tensor map of one input: 16-bit elements, [rows][128] row-major, boxes of

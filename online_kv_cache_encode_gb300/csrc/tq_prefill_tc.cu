@@ -448,7 +448,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarQ));
 
-        float m = kMinusBig, l = 0.f, z = 0.f;
+        float m = kMinusBig;
+        uint64_t l2 = 0ull, z2acc = 0ull;  // running sum and zero-point sum, two lanes each
+        const int p_lo = a.first + r0 / G;  // the block's first position
         for (int u = 0; u < U; ++u) {
             const int base = (t_first + u) * kPfTile;
             // scores of tile u, then its per-token norms, masks, scales and zero
@@ -462,10 +464,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             // pass 1, 32 tokens at a time: logit (log2 units) = S * qscale * gamma;
             // tokens that are not there and, causally, tokens after the row's
             // position get -inf; the logits go back over the scores
-            float mt = kMinusBig;
+            float mt0 = kMinusBig, mt1 = kMinusBig;
             const int kmax = pos - base;  // the last token of the tile the row sees
-            const float4* g4 = reinterpret_cast<const float4*>(gam_s + (u & 3) * kPfTile);
-            const float4* m4 = reinterpret_cast<const float4*>(msk_s + (u & 3) * kPfTile);
+            // a tile wholly before the block's first position needs no causal mask
+            // (uniform over the CTA)
+            const bool diag = base + kPfTile - 1 > p_lo;
+            const float2* g2 = reinterpret_cast<const float2*>(gam_s + (u & 3) * kPfTile);
+            const float2* m2 = reinterpret_cast<const float2*>(msk_s + (u & 3) * kPfTile);
+            const uint64_t QS2 = f2_pack(qs, qs);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
@@ -473,21 +479,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                 tc::wait_ld();
                 tc::reg_fence(v);
 #pragma unroll
-                for (int k4 = 0; k4 < 8; ++k4) {
-                    const float4 gg = g4[8 * c + k4], mm = m4[8 * c + k4];
-                    const float gv[4] = {gg.x, gg.y, gg.z, gg.w}, mv[4] = {mm.x, mm.y, mm.z, mm.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int k = 32 * c + 4 * k4 + i;
-                        float x = fmaf(__uint_as_float(v[4 * k4 + i]) * qs, gv[i], mv[i]);
-                        x = (k <= kmax) ? x : -INFINITY;
-                        mt = fmaxf(mt, x);
-                        v[4 * k4 + i] = __float_as_uint(x);
+                for (int k2 = 0; k2 < 16; ++k2) {
+                    const float2 gg = g2[16 * c + k2], mm = m2[16 * c + k2];
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_mul(f2_pack(__uint_as_float(v[2 * k2]), __uint_as_float(v[2 * k2 + 1])), QS2),
+                                     f2_pack(gg.x, gg.y), f2_pack(mm.x, mm.y)),
+                              x0, x1);
+                    if (diag) {
+                        const int k = 32 * c + 2 * k2;
+                        x0 = (k <= kmax) ? x0 : -INFINITY;
+                        x1 = (k + 1 <= kmax) ? x1 : -INFINITY;
                     }
+                    mt0 = fmaxf(mt0, x0);
+                    mt1 = fmaxf(mt1, x1);
+                    v[2 * k2] = __float_as_uint(x0);
+                    v[2 * k2 + 1] = __float_as_uint(x1);
                 }
                 tc::st_32x32b_x32(tsp + 32 * c, v);
             }
             tc::wait_st();
+            const float mt = fmaxf(mt0, mt1);
             // The tensor-memory loads and stores are warp-wide (.sync.aligned), so
             // the rescale is decided for the whole warp: a row that keeps its max
             // takes the factor 1.
@@ -497,8 +508,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             if (__any_sync(0xffffffffu, raise)) {
                 const float mn = raise ? mt : m;
                 const float f = ex2(m - mn);
-                l *= f;
-                z *= f;
+                const uint64_t F2 = f2_pack(f, f);
+                l2 = f2_mul(l2, F2);
+                z2acc = f2_mul(z2acc, F2);
                 if (u > 0) {
                     // the output accumulator holds every PV up to tile u - 1
                     pf_wait(bar(kBarO + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
@@ -521,6 +533,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             // exactly on its own logits
             const float2* z2 = reinterpret_cast<const float2*>(zer_s + (u & 1) * kPfTile);
             const float2* c2 = reinterpret_cast<const float2*>(scl_s + (u & 1) * kPfTile);
+            const uint64_t M2 = f2_pack(m, m);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
@@ -530,14 +543,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float p0 = ex2(__uint_as_float(v[2 * k]) - m), p1 = ex2(__uint_as_float(v[2 * k + 1]) - m);
+                    float d0, d1;
+                    f2_unpack(f2_sub(f2_pack(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), M2), d0, d1);
+                    const uint64_t P2 = f2_pack(ex2(d0), ex2(d1));
                     const float2 zz = z2[16 * c + k], cc = c2[16 * c + k];
-                    l += p0 + p1;
-                    z = fmaf(p0, zz.x, fmaf(p1, zz.y, z));
-                    const float w0 = p0 * cc.x, w1 = p1 * cc.y;
+                    l2 = f2_add(l2, P2);
+                    z2acc = f2_fma(P2, f2_pack(zz.x, zz.y), z2acc);
+                    const uint64_t W2 = f2_mul(P2, f2_pack(cc.x, cc.y));
+                    float w0, w1;
+                    f2_unpack(W2, w0, w1);
                     hi[k] = pack_h2(w0, w1);
                     const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
-                    lo[k] = pack_h2(w0 - hf.x, w1 - hf.y);
+                    float lo0, lo1;
+                    f2_unpack(f2_sub(W2, f2_pack(hf.x, hf.y)), lo0, lo1);
+                    lo[k] = pack_h2(lo0, lo1);
                 }
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
@@ -552,6 +571,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             if (lane == 0) mbar_arrive(bar(kBarP + (u & 1)));
         }
         // ---- this split's partial for the row: max, sum, rotated accumulator + zero term ----
+        float l, z, l_b, z_b;
+        f2_unpack(l2, l, l_b);
+        f2_unpack(z2acc, z, z_b);
+        l += l_b;
+        z += z_b;
         pf_wait(bar(kBarO + ((U - 1) & 1)), ((U - 1) >> 1) & 1, bad);
         tc::fence_after_sync();
         float* pr = part + r * kPartRow;

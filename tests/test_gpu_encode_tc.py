@@ -1,5 +1,5 @@
 """The bulk encode on the tensor cores (16-bit inputs without the QJL sketch,
-at least two 128-row tiles per SM): parity with the oracle with a ragged last
+at least one 128-row tile per SM): parity with the oracle with a ragged last
 tile, bf16 and fp16 inputs and key / value widths 1..8; the status flags of
 its rows (non-finite input, fp16 overflow, a slot past the pool, a skipped
 slot)."""
@@ -26,12 +26,12 @@ def tq(oracle):
     return T
 
 
-def _bulk_tokens(hkv: int) -> int:
-    """Tokens whose (token, KV head) items fill two 128-row tiles per SM, plus a
-    ragged last tile."""
+def _bulk_tokens(hkv: int, tiles_per_sm: int = 2) -> int:
+    """Tokens whose (token, KV head) items fill `tiles_per_sm` 128-row tiles per
+    SM, plus a ragged last tile."""
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return (2 * sms * 128 + hkv - 1) // hkv + 37
+    return (tiles_per_sm * sms * 128 + hkv - 1) // hkv + 37
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
@@ -42,6 +42,15 @@ def test_bulk_encode_parity(tq, oracle, dtype, kb, vb):
     res = parity.run_case(w, oracle, tq, decode=False)
     assert (n * 8) % 128 != 0
     parity.assert_encode_parity(res)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_one_tile_per_sm(tq, oracle, dtype):
+    """The smallest encode the tensor cores take: one tile per SM and a few
+    more, so most CTAs code a single tile and some slots none."""
+    n = _bulk_tokens(8, tiles_per_sm=1)
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(n,), hkv=8, hq=16, dtype=dtype)
+    parity.assert_encode_parity(parity.run_case(w, oracle, tq, decode=False))
 
 
 def test_bulk_encode_two_sequences_and_decode(tq, oracle):
