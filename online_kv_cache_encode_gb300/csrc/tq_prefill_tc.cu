@@ -97,7 +97,8 @@ struct PfLayout {
     static constexpr int scl = msk + 4 * kPfTile * 4;
     static constexpr int zer = scl + 2 * kPfTile * 4;
     static constexpr int big = zer + 2 * kPfTile * 4;   // per tile parity and producer warp: a scale > kBigScale
-    static constexpr int lut = big + 2 * 4 * 4;         // 256 entries x (N pair, rem2/delta pair)
+    static constexpr int inv = big + 2 * 4 * 4;         // per tile (u & 3) and producer warp: a token not there
+    static constexpr int lut = inv + 4 * 4 * 4;         // 256 entries x (N pair, rem2/delta pair)
     static constexpr int bars = lut + 256 * 8;
     static constexpr int ok = bars + 8 * kNumBars;      // page copy issued and its block id valid [kRing][8]
     static constexpr int taddr = ok + 4 * kRing * kPfPages;
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
     float* zer_s = reinterpret_cast<float*>(sm + L::zer);
     float* msk_s = reinterpret_cast<float*>(sm + L::msk);
     int* big_s = reinterpret_cast<int*>(sm + L::big);
+    int* inv_s = reinterpret_cast<int*>(sm + L::inv);
     if (tid == 0) {
         for (int i = 0; i < kRing * kPfPages; ++i) mbar_init(bar(i), 1);
         mbar_init(bar(kBarBk), 4);
@@ -345,6 +347,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                 if (valid) gm = lds_h2f(pg + F::gam + 2 * slot);
                 gam_s[(u & 3) * kPfTile + t] = gm;
                 msk_s[(u & 3) * kPfTile + t] = valid ? 0.f : -INFINITY;
+                const bool any_inv = __any_sync(0xffffffffu, !valid);
+                if (lane == 0) inv_s[(u & 3) * 4 + (warp - 4)] = any_inv ? 1 : 0;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
@@ -472,6 +476,35 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             const float2* g2 = reinterpret_cast<const float2*>(gam_s + (u & 3) * kPfTile);
             const float2* m2 = reinterpret_cast<const float2*>(msk_s + (u & 3) * kPfTile);
             const uint64_t QS2 = f2_pack(qs, qs);
+            const int4 iv4 = *reinterpret_cast<const int4*>(inv_s + 4 * (u & 3));
+            if (!diag && (iv4.x | iv4.y | iv4.z | iv4.w) == 0) {
+                // every token of the tile is there and visible to every row: no mask
+                const float4* g4 = reinterpret_cast<const float4*>(gam_s + (u & 3) * kPfTile);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tc::ld_32x32b_x32(tsp + 32 * c, v);
+                    tc::wait_ld();
+                    tc::reg_fence(v);
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4) {
+                        const float4 gg = g4[8 * c + k4];
+                        float x[4];
+                        f2_unpack(f2_mul(f2_mul(f2_pack(__uint_as_float(v[4 * k4]), __uint_as_float(v[4 * k4 + 1])), QS2),
+                                         f2_pack(gg.x, gg.y)),
+                                  x[0], x[1]);
+                        f2_unpack(f2_mul(f2_mul(f2_pack(__uint_as_float(v[4 * k4 + 2]), __uint_as_float(v[4 * k4 + 3])),
+                                                QS2),
+                                         f2_pack(gg.z, gg.w)),
+                                  x[2], x[3]);
+                        mt0 = fmaxf(mt0, fmaxf(x[0], x[2]));
+                        mt1 = fmaxf(mt1, fmaxf(x[1], x[3]));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) v[4 * k4 + i] = __float_as_uint(x[i]);
+                    }
+                    tc::st_32x32b_x32(tsp + 32 * c, v);
+                }
+            } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
@@ -496,6 +529,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                     v[2 * k2 + 1] = __float_as_uint(x1);
                 }
                 tc::st_32x32b_x32(tsp + 32 * c, v);
+            }
             }
             tc::wait_st();
             const float mt = fmaxf(mt0, mt1);
