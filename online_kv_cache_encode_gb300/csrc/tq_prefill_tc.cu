@@ -11,12 +11,13 @@
 //   warps 0-3  softmax: thread = query row = tensor-memory lane.  Before the
 //              tiles it rotates its query (q_rot = R q, in registers) and
 //              stores x = sm_scale log2(e) delta q_rot / qscale in fp16 hi and
-//              lo parts as the tensor-memory A operand.  Per tile it reads the
-//              row's 128 scores, applies the key norms, the causal mask and a
-//              lazy running max (raised only when a score beats it by more
-//              than 8 in log2 units, so p <= 2^8; a tile with a value scale
-//              above 255 takes the exact max), and writes the weights p * scale
-//              in fp16 hi and lo parts to tensor memory as the A operand of PV.
+//              lo parts as the tensor-memory A operand.  Per tile, 32 scores at
+//              a time, it applies the key norms, the causal mask and a lazy
+//              running max (raised only when a score beats it by more than 8
+//              in log2 units, so p <= 2^8; a tile with a value scale above 255
+//              takes the exact max; a raise rescales the chunks already
+//              written), and writes the weights p * scale in fp16 hi and lo
+//              parts over the scores as the A operand of PV.
 //   warps 4-7  producers: thread = token of the tile.  They unpack the key
 //              codes through a 256-entry table into the two-level centroid
 //              operand C[c] / delta = N[c] + rem2[c] / delta (N an integer of
@@ -465,120 +466,108 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             pf_wait(bar(kBarBv + (u & 1)), (u >> 1) & 1, bad);
             tc::fence_after_sync();
             const uint32_t tsp = tmem + tl + kTs + 128 * (u & 1);
-            // pass 1, 32 tokens at a time: logit (log2 units) = S * qscale * gamma;
-            // tokens that are not there and, causally, tokens after the row's
-            // position get -inf; the logits go back over the scores
-            float mt0 = kMinusBig, mt1 = kMinusBig;
+            // One pass, 32 tokens at a time: logit (log2 units) = S * qscale *
+            // gamma (tokens that are not there and, causally, tokens after the
+            // row's position get -inf), then the weights w = 2^(logit - m) *
+            // scale over the chunk's own scores: the 16 tokens of K-step s take
+            // columns 16 s .. 16 s + 7 (hi parts, pairs) and 16 s + 8 .. 16 s + 15
+            // (lo parts).  The lazy max m is raised when a chunk's logits beat it
+            // by more than 8 (or at all, on a tile with a value scale above 255);
+            // the weights already written for the tile's earlier chunks, the
+            // output accumulator and the sums then take the factor 2^(m - m_new).
+            // The tensor-memory loads and stores are warp-wide (.sync.aligned),
+            // so a raise is decided for the whole warp: a row that keeps its max
+            // takes the factor 1.
             const int kmax = pos - base;  // the last token of the tile the row sees
             // a tile wholly before the block's first position needs no causal mask
             // (uniform over the CTA)
             const bool diag = base + kPfTile - 1 > p_lo;
+            const int4 iv4 = *reinterpret_cast<const int4*>(inv_s + 4 * (u & 3));
+            const bool plain = !diag && (iv4.x | iv4.y | iv4.z | iv4.w) == 0;
             const float2* g2 = reinterpret_cast<const float2*>(gam_s + (u & 3) * kPfTile);
             const float2* m2 = reinterpret_cast<const float2*>(msk_s + (u & 3) * kPfTile);
-            const uint64_t QS2 = f2_pack(qs, qs);
-            const int4 iv4 = *reinterpret_cast<const int4*>(inv_s + 4 * (u & 3));
-            if (!diag && (iv4.x | iv4.y | iv4.z | iv4.w) == 0) {
-                // every token of the tile is there and visible to every row: no mask
-                const float4* g4 = reinterpret_cast<const float4*>(gam_s + (u & 3) * kPfTile);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tc::ld_32x32b_x32(tsp + 32 * c, v);
-                    tc::wait_ld();
-                    tc::reg_fence(v);
-#pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4) {
-                        const float4 gg = g4[8 * c + k4];
-                        float x[4];
-                        f2_unpack(f2_mul(f2_mul(f2_pack(__uint_as_float(v[4 * k4]), __uint_as_float(v[4 * k4 + 1])), QS2),
-                                         f2_pack(gg.x, gg.y)),
-                                  x[0], x[1]);
-                        f2_unpack(f2_mul(f2_mul(f2_pack(__uint_as_float(v[4 * k4 + 2]), __uint_as_float(v[4 * k4 + 3])),
-                                                QS2),
-                                         f2_pack(gg.z, gg.w)),
-                                  x[2], x[3]);
-                        mt0 = fmaxf(mt0, fmaxf(x[0], x[2]));
-                        mt1 = fmaxf(mt1, fmaxf(x[1], x[3]));
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) v[4 * k4 + i] = __float_as_uint(x[i]);
-                    }
-                    tc::st_32x32b_x32(tsp + 32 * c, v);
-                }
-            } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tc::ld_32x32b_x32(tsp + 32 * c, v);
-                tc::wait_ld();
-                tc::reg_fence(v);
-#pragma unroll
-                for (int k2 = 0; k2 < 16; ++k2) {
-                    const float2 gg = g2[16 * c + k2], mm = m2[16 * c + k2];
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_mul(f2_pack(__uint_as_float(v[2 * k2]), __uint_as_float(v[2 * k2 + 1])), QS2),
-                                     f2_pack(gg.x, gg.y), f2_pack(mm.x, mm.y)),
-                              x0, x1);
-                    if (diag) {
-                        const int k = 32 * c + 2 * k2;
-                        x0 = (k <= kmax) ? x0 : -INFINITY;
-                        x1 = (k + 1 <= kmax) ? x1 : -INFINITY;
-                    }
-                    mt0 = fmaxf(mt0, x0);
-                    mt1 = fmaxf(mt1, x1);
-                    v[2 * k2] = __float_as_uint(x0);
-                    v[2 * k2 + 1] = __float_as_uint(x1);
-                }
-                tc::st_32x32b_x32(tsp + 32 * c, v);
-            }
-            }
-            tc::wait_st();
-            const float mt = fmaxf(mt0, mt1);
-            // The tensor-memory loads and stores are warp-wide (.sync.aligned), so
-            // the rescale is decided for the whole warp: a row that keeps its max
-            // takes the factor 1.
-            const int4 bg4 = *reinterpret_cast<const int4*>(big_s + 4 * (u & 1));
-            const bool exact = (bg4.x | bg4.y | bg4.z | bg4.w) != 0;
-            const bool raise = mt > m + kLazy || (exact && mt > m);
-            if (__any_sync(0xffffffffu, raise)) {
-                const float mn = raise ? mt : m;
-                const float f = ex2(m - mn);
-                const uint64_t F2 = f2_pack(f, f);
-                l2 = f2_mul(l2, F2);
-                z2acc = f2_mul(z2acc, F2);
-                if (u > 0) {
-                    // the output accumulator holds every PV up to tile u - 1
-                    pf_wait(bar(kBarO + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t v[32];
-                        tc::ld_32x32b_x32(tmem + tl + kTo + 32 * c, v);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
-                        tc::st_32x32b_x32(tmem + tl + kTo + 32 * c, v);
-                    }
-                }
-                m = mn;
-            }
-            // pass 2: the weights over the logits, 32 tokens at a time; the 16
-            // tokens of K-step s take columns 16 s .. 16 s + 7 (hi parts, pairs)
-            // and 16 s + 8 .. 16 s + 15 (lo parts), so a chunk's weights land
-            // exactly on its own logits
             const float2* z2 = reinterpret_cast<const float2*>(zer_s + (u & 1) * kPfTile);
             const float2* c2 = reinterpret_cast<const float2*>(scl_s + (u & 1) * kPfTile);
-            const uint64_t M2 = f2_pack(m, m);
-#pragma unroll
+            const int4 bg4 = *reinterpret_cast<const int4*>(big_s + 4 * (u & 1));
+            const bool exact = (bg4.x | bg4.y | bg4.z | bg4.w) != 0;
+            const uint64_t QS2 = f2_pack(qs, qs);
+            bool o_scaled = false;  // the output accumulator was waited for in this tile
+            // (not unrolled: nine warps in three roles share the instruction cache)
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
                 tc::ld_32x32b_x32(tsp + 32 * c, v);
                 tc::wait_ld();
                 tc::reg_fence(v);
+                float x[32];
+                float mt0 = kMinusBig, mt1 = kMinusBig;
+#pragma unroll
+                for (int k2 = 0; k2 < 16; ++k2) {
+                    const float2 gg = g2[16 * c + k2];
+                    const uint64_t s2 = f2_mul(f2_pack(__uint_as_float(v[2 * k2]), __uint_as_float(v[2 * k2 + 1])), QS2);
+                    if (plain) {
+                        f2_unpack(f2_mul(s2, f2_pack(gg.x, gg.y)), x[2 * k2], x[2 * k2 + 1]);
+                    } else {
+                        const float2 mm = m2[16 * c + k2];
+                        f2_unpack(f2_fma(s2, f2_pack(gg.x, gg.y), f2_pack(mm.x, mm.y)), x[2 * k2], x[2 * k2 + 1]);
+                        const int k = 32 * c + 2 * k2;
+                        if (k > kmax) x[2 * k2] = -INFINITY;
+                        if (k + 1 > kmax) x[2 * k2 + 1] = -INFINITY;
+                    }
+                    mt0 = fmaxf(mt0, x[2 * k2]);
+                    mt1 = fmaxf(mt1, x[2 * k2 + 1]);
+                }
+                const float mt = fmaxf(mt0, mt1);
+                const bool raise = mt > m + kLazy || (exact && mt > m);
+                if (__any_sync(0xffffffffu, raise)) {
+                    const float mn = raise ? mt : m;
+                    const float f = ex2(m - mn);
+                    const uint64_t F2 = f2_pack(f, f);
+                    l2 = f2_mul(l2, F2);
+                    z2acc = f2_mul(z2acc, F2);
+                    // the weights of this tile's earlier chunks (their stores first)
+                    if (c > 0) tc::wait_st();
+#pragma unroll 1
+                    for (int cp = 0; cp < c; ++cp) {
+                        uint32_t pw[32];
+                        tc::ld_32x32b_x32(tsp + 32 * cp, pw);
+                        tc::wait_ld();
+                        tc::reg_fence(pw);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const int ih = 16 * (k >> 3) + (k & 7), il = ih + 8;
+                            const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pw[ih]));
+                            const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&pw[il]));
+                            const float w0 = (h.x + lo.x) * f, w1 = (h.y + lo.y) * f;
+                            pw[ih] = pack_h2(w0, w1);
+                            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&pw[ih]));
+                            pw[il] = pack_h2(w0 - hf.x, w1 - hf.y);
+                        }
+                        tc::st_32x32b_x32(tsp + 32 * cp, pw);
+                    }
+                    if (u > 0) {
+                        // the output accumulator holds every PV up to tile u - 1
+                        if (!o_scaled) pf_wait(bar(kBarO + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
+                        o_scaled = true;
+                        tc::fence_after_sync();
+#pragma unroll 1
+                        for (int cc = 0; cc < 4; ++cc) {
+                            uint32_t ov[32];
+                            tc::ld_32x32b_x32(tmem + tl + kTo + 32 * cc, ov);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * f);
+                            tc::st_32x32b_x32(tmem + tl + kTo + 32 * cc, ov);
+                        }
+                    }
+                    m = mn;
+                }
+                const uint64_t M2 = f2_pack(m, m);
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     float d0, d1;
-                    f2_unpack(f2_sub(f2_pack(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), M2), d0, d1);
+                    f2_unpack(f2_sub(f2_pack(x[2 * k], x[2 * k + 1]), M2), d0, d1);
                     const uint64_t P2 = f2_pack(ex2(d0), ex2(d1));
                     const float2 zz = z2[16 * c + k], cc = c2[16 * c + k];
                     l2 = f2_add(l2, P2);
