@@ -324,25 +324,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             // ---- keys: the previous tile's scores MMA has read the operand ----
             if (u > 0) pf_wait(bar(kBarS + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
             {
-                uint32_t w[16];
-#pragma unroll
+                // 16 code bytes (32 dims) at a time; the loop is not unrolled (nine
+                // warps in three roles share the instruction cache)
+#pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     const uint4 v4 = valid ? lds128(pg + F::kcode + slot * 64 + 16 * c) : make_uint4(0, 0, 0, 0);
-                    w[4 * c] = v4.x; w[4 * c + 1] = v4.y; w[4 * c + 2] = v4.z; w[4 * c + 3] = v4.w;
-                }
+                    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-                for (int dg = 0; dg < 16; ++dg) {
-                    // dims 8 dg .. 8 dg + 7 = code bytes 4 dg .. 4 dg + 3 = word dg
-                    uint32_t nn[4], rr[4];
+                    for (int q = 0; q < 4; ++q) {
+                        // dims 8 dg .. 8 dg + 7 = code bytes 4 dg .. 4 dg + 3 = word q
+                        const int dg = 4 * c + q;
+                        uint32_t nn[4], rr[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t e = (w[dg] >> (8 * k)) & 0xFFu;
-                        const uint2 v = valid ? *reinterpret_cast<const uint2*>(lut + 2 * e) : make_uint2(0u, 0u);
-                        nn[k] = v.x;
-                        rr[k] = v.y;
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t e = (w4[q] >> (8 * k)) & 0xFFu;
+                            const uint2 v = valid ? *reinterpret_cast<const uint2*>(lut + 2 * e) : make_uint2(0u, 0u);
+                            nn[k] = v.x;
+                            rr[k] = v.y;
+                        }
+                        sts128(sbase + L::bn + key_chunk(t, dg), nn[0], nn[1], nn[2], nn[3]);
+                        sts128(sbase + L::br + key_chunk(t, dg), rr[0], rr[1], rr[2], rr[3]);
                     }
-                    sts128(sbase + L::bn + key_chunk(t, dg), nn[0], nn[1], nn[2], nn[3]);
-                    sts128(sbase + L::br + key_chunk(t, dg), rr[0], rr[1], rr[2], rr[3]);
                 }
                 float gm = 0.f;
                 if (valid) gm = lds_h2f(pg + F::gam + 2 * slot);
@@ -358,23 +360,46 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             if (u > 1) pf_wait(bar(kBarO + half), ((u - 2) >> 1) & 1, bad);
             {
                 constexpr int VROW = D * VB / 8;
-                uint32_t w[VB * 4];
+                const uint32_t bvb = sbase + L::bv + half * L::bv_size;
+                if constexpr (VB == 3) {
+                    uint32_t w[VB * 4];
 #pragma unroll
-                for (int c = 0; c < VB; ++c) {
-                    const uint4 v4 = valid ? lds128(pg + F::vcode + slot * VROW + 16 * c) : make_uint4(0, 0, 0, 0);
-                    w[4 * c] = v4.x; w[4 * c + 1] = v4.y; w[4 * c + 2] = v4.z; w[4 * c + 3] = v4.w;
-                }
-#pragma unroll
-                for (int dg = 0; dg < 16; ++dg) {
-                    uint32_t pr[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        // codes of dims 8 dg + 2k, 8 dg + 2k + 1 as fp16 subnormals c * 2^-24
-                        const uint32_t c0 = bits_at<VB * 4>(w, VB * (8 * dg + 2 * k), VB);
-                        const uint32_t c1 = bits_at<VB * 4>(w, VB * (8 * dg + 2 * k + 1), VB);
-                        pr[k] = c0 | (c1 << 16);
+                    for (int c = 0; c < VB; ++c) {
+                        const uint4 v4 = valid ? lds128(pg + F::vcode + slot * VROW + 16 * c) : make_uint4(0, 0, 0, 0);
+                        w[4 * c] = v4.x; w[4 * c + 1] = v4.y; w[4 * c + 2] = v4.z; w[4 * c + 3] = v4.w;
                     }
-                    sts128(sbase + L::bv + half * L::bv_size + val_chunk(t, dg), pr[0], pr[1], pr[2], pr[3]);
+#pragma unroll
+                    for (int dg = 0; dg < 16; ++dg) {
+                        uint32_t pr[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            // codes of dims 8 dg + 2k, 8 dg + 2k + 1 as fp16 subnormals c * 2^-24
+                            const uint32_t c0 = bits_at<VB * 4>(w, VB * (8 * dg + 2 * k), VB);
+                            const uint32_t c1 = bits_at<VB * 4>(w, VB * (8 * dg + 2 * k + 1), VB);
+                            pr[k] = c0 | (c1 << 16);
+                        }
+                        sts128(bvb + val_chunk(t, dg), pr[0], pr[1], pr[2], pr[3]);
+                    }
+                } else {
+                    // 16 code bytes at a time: 16 / VB groups of 8 dims
+                    constexpr int DGC = 16 / VB;
+#pragma unroll 1
+                    for (int c = 0; c < VB; ++c) {
+                        const uint4 v4 = valid ? lds128(pg + F::vcode + slot * VROW + 16 * c) : make_uint4(0, 0, 0, 0);
+                        const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                        for (int q = 0; q < DGC; ++q) {
+                            uint32_t pr[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                // codes of dims 8 dg + 2k, 8 dg + 2k + 1 as fp16 subnormals c * 2^-24
+                                const uint32_t c0 = bits_at<4>(w4, VB * (8 * q + 2 * k), VB);
+                                const uint32_t c1 = bits_at<4>(w4, VB * (8 * q + 2 * k + 1), VB);
+                                pr[k] = c0 | (c1 << 16);
+                            }
+                            sts128(bvb + val_chunk(t, DGC * c + q), pr[0], pr[1], pr[2], pr[3]);
+                        }
+                    }
                 }
                 float sc = 0.f, zr = 0.f;
                 if (valid) {
