@@ -246,7 +246,9 @@ __global__ void __launch_bounds__(kEtThreads, 1)
     const uint32_t sbase = smem_u32(sm);
     float* bsd_s = reinterpret_cast<float*>(sm + kEtBsd);
 
-    grid_dependency_wait();  // the previous grid's writes (inputs, pool) are visible
+    // The set-up up to the H matrix reads only kernel parameters and shared
+    // memory, so it runs before the wait for the previous grid (programmatic
+    // dependent launch) and overlaps that grid's last CTAs.
     if (tid == 0) {
         for (int b = 0; b < 4; ++b) mbar_init(sbase + kEtBars + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(kEtThreads, 1)
                 make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
+    grid_dependency_wait();  // the previous grid's writes (inputs, pool) are visible
     if constexpr (KB > 4) {
         for (int i = tid; i < HALF - 1; i += kEtThreads) bsd_s[i] = a.tab->boundary_sd_pos[i];
     }
