@@ -55,7 +55,8 @@ namespace {
 constexpr int kPfRows = 128;                    // query rows per CTA (tensor-memory lanes)
 constexpr int kPfTile = 128;                    // tokens per tile
 constexpr int kPfPages = kPfTile / kBlockSize;  // pages per tile
-constexpr int kPfWarps = 9;                     // softmax 0-3, producers 4-7, issuer 8
+constexpr int kPfWarps = 13;                    // softmax 0-7 (two per row), producers 8-11, issuer 12
+constexpr int kPfSoftmax = 256;                 // softmax threads (named barrier 1)
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPartRow = 4 + kHeadDim;          // partial record: max, sum, 2 pad, acc[128]
 // tensor-memory columns: query operand (hi 0..63, lo 64..127); scores of tile
@@ -99,7 +100,8 @@ struct PfLayout {
     static constexpr int zer = scl + 2 * kPfTile * 4;
     static constexpr int big = zer + 2 * kPfTile * 4;   // per tile parity and producer warp: a scale > kBigScale
     static constexpr int inv = big + 2 * 4 * 4;         // per tile (u & 3) and producer warp: a token not there
-    static constexpr int lut = inv + 4 * 4 * 4;         // 256 entries x (N pair, rem2/delta pair)
+    static constexpr int xch = inv + 4 * 4 * 4;         // softmax pair exchange: [2][2][128] floats x 2
+    static constexpr int lut = xch + 4 * 2 * kPfRows * 4;   // 256 entries x (N pair, rem2/delta pair)
     static constexpr int bars = lut + 256 * 8;
     static constexpr int ok = bars + 8 * kNumBars;      // page copy issued and its block id valid [kRing][8]
     static constexpr int taddr = ok + 4 * kRing * kPfPages;
@@ -172,10 +174,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(kBarBv + b), 4);
             mbar_init(bar(kBarS + b), 1);
-            mbar_init(bar(kBarP + b), 4);
+            mbar_init(bar(kBarP + b), 8);
             mbar_init(bar(kBarO + b), 1);
         }
-        mbar_init(bar(kBarQ), 4);
+        mbar_init(bar(kBarQ), 8);
         mbar_init(bar(kBarNever), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         }
         for (int i = tid; i < kPfRows * D; i += kPfThreads) part[(i / D) * kPartRow + 4 + (i % D)] = 0.f;
         bad = true;
-    } else if (warp == 8) {
+    } else if (warp == 12) {
         // ================= loader and MMA issuer =================
         // Issuing an MMA waits while the tensor pipe's queue is full, so this
         // warp does nothing else: its waits never hold up the softmax.
@@ -308,9 +310,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 8) {
         // ================= producers: thread = token of the tile =================
-        const int t = tid - 128;          // token of the tile
+        const int t = tid - 256;          // token of the tile
         const int j = t >> 4, slot = t & 15;
         const uint32_t* lut = reinterpret_cast<const uint32_t*>(sm + L::lut);
         for (int u = 0; u < U; ++u) {
@@ -323,6 +325,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             const uint32_t pg = sbase + L::ring + si * L::stride;
             // ---- keys: the previous tile's scores MMA has read the operand ----
             if (u > 0) pf_wait(bar(kBarS + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
+            // the softmax warps use the key operand's space for the query rotation
+            else pf_wait(bar(kBarQ), 0, bad);
             {
                 // 16 code bytes (32 dims) at a time; the loop is not unrolled (nine
                 // warps in three roles share the instruction cache)
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                 gam_s[(u & 3) * kPfTile + t] = gm;
                 msk_s[(u & 3) * kPfTile + t] = valid ? 0.f : -INFINITY;
                 const bool any_inv = __any_sync(0xffffffffu, !valid);
-                if (lane == 0) inv_s[(u & 3) * 4 + (warp - 4)] = any_inv ? 1 : 0;
+                if (lane == 0) inv_s[(u & 3) * 4 + (warp - 8)] = any_inv ? 1 : 0;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
@@ -411,98 +415,107 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                 // a scale above kBigScale makes this tile take the exact max, so
                 // that p * scale (p <= 1 then) stays inside the fp16 range
                 const bool bg = __any_sync(0xffffffffu, sc > kBigScale);
-                if (lane == 0) big_s[half * 4 + (warp - 4)] = bg ? 1 : 0;
+                if (lane == 0) big_s[half * 4 + (warp - 8)] = bg ? 1 : 0;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarBv + half));
         }
     } else {
-        // ================= softmax: thread = query row =================
-        const int r = tid;
+        // ================= softmax: two threads per query row =================
+        // Warps w and w + 4 share tensor-memory lanes 32 (w % 4) ..: thread
+        // (row r, half hf) works on columns 64 hf .. 64 hf + 63 of the row's
+        // scores and weights and on dims 64 hf .. 64 hf + 63 of its query and
+        // output.  The halves exchange the row's maxima and sums in shared
+        // memory (named barrier 1 over the 256 softmax threads).
+        const int r = tid & 127, hf = warp >> 2;
         const int rg = r0 + r;
         const bool row_ok = r < rows;
         const int pos = row_ok ? a.first + rg / G : -1;  // the row's position (-1: padding row)
-        const uint32_t tl = (uint32_t)(warp * 32) << 16;
+        const uint32_t tl = (uint32_t)((warp & 3) * 32) << 16;
         const float ksc = a.sm_scale_log2;
+        float* xch = reinterpret_cast<float*>(sm + L::xch);  // [4][2][128]: two rounds x halves x rows
+        auto pair_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kPfSoftmax) : "memory"); };
         float qs = 1.f;
         {
-            // q_rot = R q for this row, in registers; x = ksc delta q_rot / qscale to tensor memory
-            float x[D];
+            // q_rot = R q: the half of the row in registers (signs, butterflies of
+            // strides 1 .. 32), the last stage (stride 64) through shared memory
+            // (the key operand's space, which the producers leave alone until the
+            // query operand is stored)
+            float x[64];
             if (row_ok) {
-                const int64_t qrow = ((int64_t)(rg / G) * a.hq + (int64_t)h * G + rg % G) * D;
+                const int64_t qrow = ((int64_t)(rg / G) * a.hq + (int64_t)h * G + rg % G) * D + 64 * hf;
 #pragma unroll
-                for (int i = 0; i < D; i += 4) load4(a.q, a.dtype, qrow + i, x + i);
+                for (int i = 0; i < 64; i += 4) load4(a.q, a.dtype, qrow + i, x + i);
             } else {
 #pragma unroll
-                for (int i = 0; i < D; ++i) x[i] = 0.f;
+                for (int i = 0; i < 64; ++i) x[i] = 0.f;
             }
 #pragma unroll
-            for (int i = 0; i < D; ++i)
-                if ((a.c.sign_bits[i >> 5] >> (i & 31)) & 1u) x[i] = -x[i];
+            for (int i = 0; i < 64; ++i) {
+                const int d = 64 * hf + i;
+                if ((a.c.sign_bits[d >> 5] >> (d & 31)) & 1u) x[i] = -x[i];
+            }
 #pragma unroll
-            for (int hh = 1; hh < D; hh <<= 1)
+            for (int hh = 1; hh < 64; hh <<= 1)
 #pragma unroll
-                for (int i = 0; i < D; ++i)
+                for (int i = 0; i < 64; ++i)
                     if ((i & hh) == 0) {
                         const float p = x[i], q2 = x[i + hh];
                         x[i] = p + q2;
                         x[i + hh] = p - q2;
                     }
+            float* xs = reinterpret_cast<float*>(sm + L::bn);  // [half][64][128 rows]
+#pragma unroll
+            for (int i = 0; i < 64; ++i) xs[(hf * 64 + i) * kPfRows + r] = x[i];
+            pair_sync();
             float mx = 0.f;
 #pragma unroll
-            for (int i = 0; i < D; ++i) {
-                x[i] *= 0.08838834764831845f;
+            for (int i = 0; i < 64; ++i) {
+                const float o = xs[((1 - hf) * 64 + i) * kPfRows + r];
+                // dims i and i + 64: (first half) + (second half), (first half) - (second half)
+                x[i] = (hf == 0 ? x[i] + o : o - x[i]) * 0.08838834764831845f;
                 mx = fmaxf(mx, fabsf(x[i]));
             }
+            xch[hf * kPfRows + r] = mx;
+            pair_sync();
+            mx = fmaxf(xch[r], xch[kPfRows + r]);
             const float big = fabsf(a.c.delta) * ksc * mx;
             qs = (big > 0.f) ? exp2f(ceilf(log2f(big / 512.f))) : 1.f;
             const float e = ksc * a.c.delta / qs;
+            uint32_t hi[32], lo[32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t hi[32], lo[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float x0 = e * x[64 * c + 2 * k], x1 = e * x[64 * c + 2 * k + 1];
-                    hi[k] = pack_h2(x0, x1);
-                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
-                    lo[k] = pack_h2(x0 - hf.x, x1 - hf.y);
-                }
-                tc::st_32x32b_x32(tmem + tl + kTq + 32 * c, hi);
-                tc::st_32x32b_x32(tmem + tl + kTq + 64 + 32 * c, lo);
+            for (int k = 0; k < 32; ++k) {
+                const float x0 = e * x[2 * k], x1 = e * x[2 * k + 1];
+                hi[k] = pack_h2(x0, x1);
+                const float2 hf2 = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
+                lo[k] = pack_h2(x0 - hf2.x, x1 - hf2.y);
             }
+            tc::st_32x32b_x32(tmem + tl + kTq + 32 * hf, hi);
+            tc::st_32x32b_x32(tmem + tl + kTq + 64 + 32 * hf, lo);
             tc::wait_st();
         }
-        // the query operand of this warp's 32 rows is in tensor memory
+        // the query operand of this warp's 32 rows, half hf, is in tensor memory
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarQ));
+        if ((tid & 31) == 0) mbar_arrive(bar(kBarQ));
 
         float m = kMinusBig;
-        uint64_t l2 = 0ull, z2acc = 0ull;  // running sum and zero-point sum, two lanes each
+        uint64_t l2 = 0ull, z2acc = 0ull;  // this half's running sum and zero-point sum, two lanes each
         const int p_lo = a.first + r0 / G;  // the block's first position
         for (int u = 0; u < U; ++u) {
             const int base = (t_first + u) * kPfTile;
             // scores of tile u, then its per-token norms, masks, scales and zero
             // points: the producers write them all before arriving on the value
-            // barrier of the tile's parity (whose next phase needs this
-            // warpgroup's weights, so a wait on it never falls a whole phase behind)
+            // barrier of the tile's parity (whose next phase needs these warps'
+            // weights, so a wait on it never falls a whole phase behind)
             pf_wait(bar(kBarS + (u & 1)), (u >> 1) & 1, bad);
             pf_wait(bar(kBarBv + (u & 1)), (u >> 1) & 1, bad);
             tc::fence_after_sync();
             const uint32_t tsp = tmem + tl + kTs + 128 * (u & 1);
-            // One pass, 32 tokens at a time: logit (log2 units) = S * qscale *
-            // gamma (tokens that are not there and, causally, tokens after the
-            // row's position get -inf), then the weights w = 2^(logit - m) *
-            // scale over the chunk's own scores: the 16 tokens of K-step s take
-            // columns 16 s .. 16 s + 7 (hi parts, pairs) and 16 s + 8 .. 16 s + 15
-            // (lo parts).  The lazy max m is raised when a chunk's logits beat it
-            // by more than 8 (or at all, on a tile with a value scale above 255);
-            // the weights already written for the tile's earlier chunks, the
-            // output accumulator and the sums then take the factor 2^(m - m_new).
-            // The tensor-memory loads and stores are warp-wide (.sync.aligned),
-            // so a raise is decided for the whole warp: a row that keeps its max
-            // takes the factor 1.
+            // logit (log2 units) = S * qscale * gamma of this half's 64 tokens;
+            // tokens that are not there and, causally, tokens after the row's
+            // position get -inf
             const int kmax = pos - base;  // the last token of the tile the row sees
             // a tile wholly before the block's first position needs no causal mask
             // (uniform over the CTA)
@@ -511,112 +524,100 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             const bool plain = !diag && (iv4.x | iv4.y | iv4.z | iv4.w) == 0;
             const float2* g2 = reinterpret_cast<const float2*>(gam_s + (u & 3) * kPfTile);
             const float2* m2 = reinterpret_cast<const float2*>(msk_s + (u & 3) * kPfTile);
-            const float2* z2 = reinterpret_cast<const float2*>(zer_s + (u & 1) * kPfTile);
-            const float2* c2 = reinterpret_cast<const float2*>(scl_s + (u & 1) * kPfTile);
-            const int4 bg4 = *reinterpret_cast<const int4*>(big_s + 4 * (u & 1));
-            const bool exact = (bg4.x | bg4.y | bg4.z | bg4.w) != 0;
             const uint64_t QS2 = f2_pack(qs, qs);
-            bool o_scaled = false;  // the output accumulator was waited for in this tile
-            // (not unrolled: nine warps in three roles share the instruction cache)
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            float x[64];
+            float mt0 = kMinusBig, mt1 = kMinusBig;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int col = 64 * hf + 32 * c;
                 uint32_t v[32];
-                tc::ld_32x32b_x32(tsp + 32 * c, v);
+                tc::ld_32x32b_x32(tsp + col, v);
                 tc::wait_ld();
                 tc::reg_fence(v);
-                float x[32];
-                float mt0 = kMinusBig, mt1 = kMinusBig;
 #pragma unroll
                 for (int k2 = 0; k2 < 16; ++k2) {
-                    const float2 gg = g2[16 * c + k2];
+                    const float2 gg = g2[col / 2 + k2];
                     const uint64_t s2 = f2_mul(f2_pack(__uint_as_float(v[2 * k2]), __uint_as_float(v[2 * k2 + 1])), QS2);
+                    float* xx = x + 32 * c + 2 * k2;
                     if (plain) {
-                        f2_unpack(f2_mul(s2, f2_pack(gg.x, gg.y)), x[2 * k2], x[2 * k2 + 1]);
+                        f2_unpack(f2_mul(s2, f2_pack(gg.x, gg.y)), xx[0], xx[1]);
                     } else {
-                        const float2 mm = m2[16 * c + k2];
-                        f2_unpack(f2_fma(s2, f2_pack(gg.x, gg.y), f2_pack(mm.x, mm.y)), x[2 * k2], x[2 * k2 + 1]);
-                        const int k = 32 * c + 2 * k2;
-                        if (k > kmax) x[2 * k2] = -INFINITY;
-                        if (k + 1 > kmax) x[2 * k2 + 1] = -INFINITY;
+                        const float2 mm = m2[col / 2 + k2];
+                        f2_unpack(f2_fma(s2, f2_pack(gg.x, gg.y), f2_pack(mm.x, mm.y)), xx[0], xx[1]);
+                        const int k = col + 2 * k2;
+                        if (k > kmax) xx[0] = -INFINITY;
+                        if (k + 1 > kmax) xx[1] = -INFINITY;
                     }
-                    mt0 = fmaxf(mt0, x[2 * k2]);
-                    mt1 = fmaxf(mt1, x[2 * k2 + 1]);
+                    mt0 = fmaxf(mt0, xx[0]);
+                    mt1 = fmaxf(mt1, xx[1]);
                 }
-                const float mt = fmaxf(mt0, mt1);
-                const bool raise = mt > m + kLazy || (exact && mt > m);
-                if (__any_sync(0xffffffffu, raise)) {
-                    const float mn = raise ? mt : m;
-                    const float f = ex2(m - mn);
-                    const uint64_t F2 = f2_pack(f, f);
-                    l2 = f2_mul(l2, F2);
-                    z2acc = f2_mul(z2acc, F2);
-                    // the weights of this tile's earlier chunks (their stores first)
-                    if (c > 0) tc::wait_st();
+            }
+            // the row's tile max from both halves (exchange buffer by tile parity)
+            float* mxx = xch + 2 * kPfRows * (2 + (u & 1));
+            mxx[hf * kPfRows + r] = fmaxf(mt0, mt1);
+            pair_sync();
+            const float mt = fmaxf(mxx[r], mxx[kPfRows + r]);
+            // The tensor-memory loads and stores are warp-wide (.sync.aligned), so
+            // the rescale is decided for the whole warp (both halves decide alike):
+            // a row that keeps its max takes the factor 1.
+            const int4 bg4 = *reinterpret_cast<const int4*>(big_s + 4 * (u & 1));
+            const bool exact = (bg4.x | bg4.y | bg4.z | bg4.w) != 0;
+            const bool raise = mt > m + kLazy || (exact && mt > m);
+            if (__any_sync(0xffffffffu, raise)) {
+                const float mn = raise ? mt : m;
+                const float f = ex2(m - mn);
+                const uint64_t F2 = f2_pack(f, f);
+                l2 = f2_mul(l2, F2);
+                z2acc = f2_mul(z2acc, F2);
+                if (u > 0) {
+                    // the output accumulator holds every PV up to tile u - 1
+                    pf_wait(bar(kBarO + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
+                    tc::fence_after_sync();
 #pragma unroll 1
-                    for (int cp = 0; cp < c; ++cp) {
-                        uint32_t pw[32];
-                        tc::ld_32x32b_x32(tsp + 32 * cp, pw);
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t ov[32];
+                        tc::ld_32x32b_x32(tmem + tl + kTo + 64 * hf + 32 * c, ov);
                         tc::wait_ld();
-                        tc::reg_fence(pw);
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const int ih = 16 * (k >> 3) + (k & 7), il = ih + 8;
-                            const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pw[ih]));
-                            const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&pw[il]));
-                            const float w0 = (h.x + lo.x) * f, w1 = (h.y + lo.y) * f;
-                            pw[ih] = pack_h2(w0, w1);
-                            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&pw[ih]));
-                            pw[il] = pack_h2(w0 - hf.x, w1 - hf.y);
-                        }
-                        tc::st_32x32b_x32(tsp + 32 * cp, pw);
+                        for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * f);
+                        tc::st_32x32b_x32(tmem + tl + kTo + 64 * hf + 32 * c, ov);
                     }
-                    if (u > 0) {
-                        // the output accumulator holds every PV up to tile u - 1
-                        if (!o_scaled) pf_wait(bar(kBarO + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
-                        o_scaled = true;
-                        tc::fence_after_sync();
-#pragma unroll 1
-                        for (int cc = 0; cc < 4; ++cc) {
-                            uint32_t ov[32];
-                            tc::ld_32x32b_x32(tmem + tl + kTo + 32 * cc, ov);
-                            tc::wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * f);
-                            tc::st_32x32b_x32(tmem + tl + kTo + 32 * cc, ov);
-                        }
-                    }
-                    m = mn;
                 }
-                const uint64_t M2 = f2_pack(m, m);
-                uint32_t hi[16], lo[16];
+                m = mn;
+            }
+            // the weights over the scores: the 16 tokens of K-step s take columns
+            // 16 s .. 16 s + 7 (hi parts, pairs) and 16 s + 8 .. 16 s + 15 (lo parts)
+            const float2* z2 = reinterpret_cast<const float2*>(zer_s + (u & 1) * kPfTile);
+            const float2* c2 = reinterpret_cast<const float2*>(scl_s + (u & 1) * kPfTile);
+            const uint64_t M2 = f2_pack(m, m);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int col = 64 * hf + 32 * c;
+                uint32_t v[32];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     float d0, d1;
-                    f2_unpack(f2_sub(f2_pack(x[2 * k], x[2 * k + 1]), M2), d0, d1);
+                    f2_unpack(f2_sub(f2_pack(x[32 * c + 2 * k], x[32 * c + 2 * k + 1]), M2), d0, d1);
                     const uint64_t P2 = f2_pack(ex2(d0), ex2(d1));
-                    const float2 zz = z2[16 * c + k], cc = c2[16 * c + k];
+                    const float2 zz = z2[col / 2 + k], cc = c2[col / 2 + k];
                     l2 = f2_add(l2, P2);
                     z2acc = f2_fma(P2, f2_pack(zz.x, zz.y), z2acc);
                     const uint64_t W2 = f2_mul(P2, f2_pack(cc.x, cc.y));
                     float w0, w1;
                     f2_unpack(W2, w0, w1);
-                    hi[k] = pack_h2(w0, w1);
-                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[k]));
+                    const uint32_t hi = pack_h2(w0, w1);
+                    const float2 hf2 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
                     float lo0, lo1;
-                    f2_unpack(f2_sub(W2, f2_pack(hf.x, hf.y)), lo0, lo1);
-                    lo[k] = pack_h2(lo0, lo1);
+                    f2_unpack(f2_sub(W2, f2_pack(hf2.x, hf2.y)), lo0, lo1);
+                    v[16 * (k >> 3) + (k & 7)] = hi;
+                    v[16 * (k >> 3) + 8 + (k & 7)] = pack_h2(lo0, lo1);
                 }
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    v[16 * (k >> 3) + (k & 7)] = hi[k];
-                    v[16 * (k >> 3) + 8 + (k & 7)] = lo[k];
-                }
-                tc::st_32x32b_x32(tsp + 32 * c, v);
+                tc::st_32x32b_x32(tsp + col, v);
             }
             tc::wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarP + (u & 1)));
+            if ((tid & 31) == 0) mbar_arrive(bar(kBarP + (u & 1)));
         }
         // ---- this split's partial for the row: max, sum, rotated accumulator + zero term ----
         float l, z, l_b, z_b;
@@ -624,22 +625,29 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         f2_unpack(z2acc, z, z_b);
         l += l_b;
         z += z_b;
+        xch[hf * kPfRows + r] = l;
+        xch[2 * kPfRows + hf * kPfRows + r] = z;
+        pair_sync();
+        l = xch[r] + xch[kPfRows + r];
+        z = xch[2 * kPfRows + r] + xch[3 * kPfRows + r];
         pf_wait(bar(kBarO + ((U - 1) & 1)), ((U - 1) >> 1) & 1, bad);
         tc::fence_after_sync();
         float* pr = part + r * kPartRow;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
-            tc::ld_32x32b_x32(tmem + tl + kTo + 32 * c, v);
+            tc::ld_32x32b_x32(tmem + tl + kTo + 64 * hf + 32 * c, v);
             tc::wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; k += 4)
-                *reinterpret_cast<float4*>(pr + 4 + 32 * c + k) =
+                *reinterpret_cast<float4*>(pr + 4 + 64 * hf + 32 * c + k) =
                     make_float4(fmaf(__uint_as_float(v[k]), kOutScale, z), fmaf(__uint_as_float(v[k + 1]), kOutScale, z),
                                 fmaf(__uint_as_float(v[k + 2]), kOutScale, z), fmaf(__uint_as_float(v[k + 3]), kOutScale, z));
         }
-        pr[0] = m;
-        pr[1] = l;
+        if (hf == 0) {
+            pr[0] = m;
+            pr[1] = l;
+        }
     }
     // every tensor-core operation of the CTA is complete (the softmax warps
     // waited for the last PV commit): release tensor memory
