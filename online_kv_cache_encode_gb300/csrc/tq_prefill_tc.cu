@@ -7,24 +7,28 @@
 // unpacked once for all of them.  Grid (split, row block, KV head): a CTA
 // takes 128 query rows (row r = position index * G + query in group) and the
 // 128-token tiles of its split of the token range (tiles past the block's last
-// position are skipped).  Its warps:
-//   warps 0-3  softmax: thread = query row = tensor-memory lane.  Before the
-//              tiles it rotates its query (q_rot = R q, in registers) and
-//              stores x = sm_scale log2(e) delta q_rot / qscale in fp16 hi and
-//              lo parts as the tensor-memory A operand.  Per tile, 32 scores at
-//              a time, it applies the key norms, the causal mask and a lazy
-//              running max (raised only when a score beats it by more than 8
-//              in log2 units, so p <= 2^8; a tile with a value scale above 255
-//              takes the exact max; a raise rescales the chunks already
-//              written), and writes the weights p * scale in fp16 hi and lo
-//              parts over the scores as the A operand of PV.
-//   warps 4-7  producers: thread = token of the tile.  They unpack the key
+// position are skipped).  Its 13 warps:
+//   warps 0-7  softmax, two warps per query row: thread = (column half, query
+//              row = tensor-memory lane).  Before the tiles the pair rotates
+//              its query (q_rot = R q: each half takes 64 dimensions through
+//              the butterflies that stay inside them, the last stage through
+//              shared memory) and stores x = sm_scale log2(e) delta q_rot /
+//              qscale in fp16 hi and lo parts as the tensor-memory A operand.
+//              Per tile each half reads its 64 score columns, applies the key
+//              norms, the causal mask and a lazy running max (the two halves'
+//              tile maxima are exchanged; the max is raised only when a score
+//              beats it by more than 8 in log2 units, so p <= 2^8; a tile with
+//              a value scale above 255 takes the exact max; a raise rescales
+//              the half's 64 output columns), and writes the weights
+//              p * scale in fp16 hi and lo parts over its scores as the A
+//              operand of PV.  The two halves' sums meet at the end.
+//   warps 8-11 producers: thread = token of the tile.  They unpack the key
 //              codes through a 256-entry table into the two-level centroid
 //              operand C[c] / delta = N[c] + rem2[c] / delta (N an integer of
 //              magnitude <= 2047, |rem2 / delta| <= 1/2, both exact enough in
 //              fp16), the value codes into exact fp16 subnormals, and the
 //              norms, scales and zero points into shared memory.
-//   warp 8     lane 0 loads the pages (bulk async copies into a four-tile
+//   warp 12    lane 0 loads the pages (bulk async copies into a four-tile
 //              ring) and issues the MMAs: scores S [128 rows x 128 tokens] =
 //              q_hi . N + q_lo . N + q_hi . rem2/delta (24 kind::f16 MMAs,
 //              K = 16), and O [128 rows x 128 dims] += w_hi . V + w_lo . V (16
