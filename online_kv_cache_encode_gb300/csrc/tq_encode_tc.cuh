@@ -18,15 +18,18 @@
 //  (cell-devlog) -- Step 1 (RHT), Step 3 (value codes); Bit-Axon --
 //  quantization function; "OCTOPUS ..." -- methodology steps 1, 2]
 //
-// CTA: four warpgroups, two per tile slot.  A slot has its own input buffers
-// in shared memory (the tile's key and value rows in the K-major core-matrix
-// layout with the 128-byte swizzle, filled by TMA tile copies of 64
-// coordinates x 128 rows, two per operand) and 256 tensor-memory columns
-// (U_k, U_v).  Each warpgroup of a slot takes one half of the columns: it sums
-// the squares and finds the minimum and maximum over its half, the two halves
-// exchange these through shared memory, and each codes its half.  A slot takes every other tile of the CTA's share: the copies of
-// its next tile run while it codes the current one, and the other slot's work
-// fills the gaps.  One CTA per SM, persistent over the tiles.
+// CTA: four independent warpgroups, one per tile in flight, persistent over
+// the CTA's tiles (taken in turn from a shared-memory counter).  A warpgroup
+// has one 32 KB input buffer in shared memory (one operand of a tile in the
+// K-major core-matrix layout with the 128-byte swizzle, filled by two TMA tile
+// copies of 64 coordinates x 128 rows) and 128 tensor-memory columns; each of
+// its threads takes one row of the tile, so every per-row reduction stays in
+// one thread.  Per tile it rotates the keys, starts the copy of the values
+// into the buffer the key MMAs have just read and codes the keys while that
+// copy runs, then rotates the values, starts the copy of its next tile's keys
+// and codes the values: the buffer is refilled during every half of the
+// epilogue, so four copies per SM are in flight most of the time.  One CTA per
+// SM.
 #pragma once
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -39,7 +42,8 @@
 namespace tq {
 
 constexpr int kEtRows = 128;                   // rows (token, KV head) per tile
-constexpr int kEtThreads = 512;                // two slots x two column halves, one warpgroup each
+constexpr int kEtGroups = 4;                   // independent warpgroups (tiles in flight)
+constexpr int kEtThreads = kEtGroups * 128;
 // H: K-major core matrices without swizzle, along K adjacent, 8-row groups
 // 2 KB apart.  The inputs: the TMA boxes' 128-byte-swizzled K-major layout
 // (row r of a box at 128 r, its 16-byte pieces permuted by r % 8; 8-row groups
@@ -48,11 +52,11 @@ constexpr uint32_t kEtLbo = 128, kEtSbo = 2048;
 constexpr uint32_t kEtXSbo = 1024, kEtXBox = 16384;
 constexpr int kEtOp = kEtRows * kHeadDim * 2;  // one 128 x 128 16-bit operand: 32 KB
 constexpr int kEtH = 0;                        // H [n][k]
-constexpr int kEtX = kEtOp;                    // slot s: keys at kEtX + 2 s kEtOp, values kEtOp further
-constexpr int kEtXchg = kEtX + 4 * kEtOp;      // [slot][half][row] (sum of squares, min, max, finite)
-constexpr int kEtBsd = kEtXchg + 2 * 2 * kEtRows * 16;  // key widths above 4 bits: sqrt(d) t_b of the positive half
-constexpr int kEtBars = kEtBsd + 4 * (kMaxLevels / 2);  // per slot: MMAs done, inputs landed
-constexpr int kEtTaddr = kEtBars + 32;
+constexpr int kEtX = kEtOp;                    // warpgroup w's buffer at kEtX + w kEtOp
+constexpr int kEtBsd = kEtX + kEtGroups * kEtOp;        // key widths above 4 bits: sqrt(d) t_b of the positive half
+constexpr int kEtBars = kEtBsd + 4 * (kMaxLevels / 2);  // per warpgroup: MMAs done, copy landed
+constexpr int kEtNext = kEtBars + 16 * kEtGroups;       // tile counter, next tile per warpgroup
+constexpr int kEtTaddr = kEtNext + 4 * (1 + kEtGroups);
 constexpr int kEtSmem = kEtTaddr + 16 + 1024;  // + room to align the base to 1 KB (swizzle atoms)
 
 // Box (x, y) of a 2-D tensor map into shared memory, completing on `bar`.
@@ -63,11 +67,11 @@ __device__ __forceinline__ void et_tma_2d(uint32_t dst, const CUtensorMap* map, 
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
-// OR of `v` over the 256 threads of a tile slot (named barrier `id`)
-__device__ __forceinline__ bool et_any256(bool v, int id) {
+// OR of `v` over the 128 threads of a warpgroup (named barrier `id`)
+__device__ __forceinline__ bool et_any128(bool v, int id) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
         : "r"((uint32_t)v), "r"(id)
         : "memory");
@@ -126,53 +130,86 @@ __device__ __forceinline__ void et_pack_biased(const uint32_t (&f)[32], uint32_t
 
 // Key codes (widths up to 4 bits) of 32 rotated coordinates x against the
 // positive thresholds scaled by F (T[b] = F sqrt(d) t_{HALF+b} gamma), with F a
-// power of two such that (|x| - thr_b) F >= 2 whenever |x| > thr_b: then
-// sat(|x| F - T[b]) is exactly [|x| > thr_b].  n = #{b : |x| > thr_b} comes from
-// a binary search over the thresholds whose steps are such saturated
-// differences, the next threshold picked by the exact select
-// fma(s, A, fma(s, -B, B)) = (s ? A : B) for s in {0, 1} (two coordinates per
-// packed instruction); the code is HALF + n for x > 0 and HALF - 1 - n
-// otherwise, i.e. n ^ HALF or n ^ (HALF - 1) for n < HALF.
+// power of two such that T[0] lies in [2^24, 2^25).  Every threshold, and every
+// float near one, is then an even integer, and so is |x| F once it reaches
+// 2^24; the saturated difference sat(|x| F - t) is therefore exactly
+// [|x| F > t] for any such t.  n = #{b : |x| > thr_b} comes from a binary
+// search whose steps are these differences, two coordinates per packed
+// instruction where the arithmetic allows it.  The next threshold is picked
+// arithmetically, t = T[lo] + s (T[hi] - T[lo]) for a step s in {0, 1}: for
+// s = 0 it is T[lo] exactly, and for s = 1 it is T[hi] up to the rounding of the
+// difference (an ulp), which can move a decision only for a coordinate within
+// 2^-23 (relative) of a boundary.  The sign: sg = sat(x 2^127) is [x > 0] for
+// every x of magnitude 2^-127 or more, and the code HALF + n (x > 0) or
+// HALF - 1 - n (otherwise) is formed as c + sg + (2 sg - 1) n with the
+// rounding constant in c, so the code is an integer even for a smaller x
+// (fractional sg; n is 0 there).
 template <int KB>
-__device__ __forceinline__ void et_key_codes(const float (&x)[32], const float (&T)[(1 << (KB - 1)) > 1 ? (1 << (KB - 1)) - 1 : 1],
-                                             float F, uint32_t (&f)[32]) {
+struct EtKeySearch {
+    static constexpr int HALF = 1 << (KB - 1);
+    uint64_t F2;            // the scale, twice
+    float t1;               // first step: T[HALF / 2 - 1]
+    uint64_t lo2, d2;       // second step: T[lo] and T[hi] - T[lo] (HALF >= 4)
+    uint64_t l3, d3a, d3b, d3ab;  // third step (HALF == 8): T0 + sa (T2 - T0) + sb (T4 - T0) + sa sb (T6 - T4 - T2 + T0)
+    __device__ __forceinline__ EtKeySearch(const float* T, float F) {
+        F2 = f2_pack(F, F);
+        t1 = 0.f;
+        lo2 = d2 = l3 = d3a = d3b = d3ab = 0ull;
+        if constexpr (HALF == 8) {
+            t1 = T[3];
+            lo2 = f2_pack(T[1], T[1]);
+            d2 = f2_pack(T[5] - T[1], T[5] - T[1]);
+            const float a = T[2] - T[0], b = T[4] - T[0], ab = (T[6] - T[4]) - a;
+            l3 = f2_pack(T[0], T[0]);
+            d3a = f2_pack(a, a);
+            d3b = f2_pack(b, b);
+            d3ab = f2_pack(ab, ab);
+        } else if constexpr (HALF == 4) {
+            t1 = T[1];
+            lo2 = f2_pack(T[0], T[0]);
+            d2 = f2_pack(T[2] - T[0], T[2] - T[0]);
+        } else if constexpr (HALF == 2) {
+            t1 = T[0];
+        }
+    }
+};
+
+template <int KB>
+__device__ __forceinline__ void et_key_codes(const float (&x)[32], const EtKeySearch<KB>& ks, uint32_t (&f)[32]) {
     constexpr int HALF = 1 << (KB - 1);
-    const uint64_t MG2 = f2_pack(kEtMagic, kEtMagic);
-    // the select constants: (A, -B, B) pairs per select of constant thresholds
     auto c2 = [](float v) { return f2_pack(v, v); };
+    const uint64_t C = c2(kEtMagic + (float)(HALF - 1));
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
-        const float X0 = fabsf(x[j]) * F, X1 = fabsf(x[j + 1]) * F;
-        uint64_t N;
-        if constexpr (HALF == 8) {
-            const float a0 = __saturatef(X0 - T[3]), a1 = __saturatef(X1 - T[3]);
-            const uint64_t S4 = f2_pack(a0, a1);
-            float tA0, tA1;
-            f2_unpack(f2_fma(S4, c2(T[5]), f2_fma(S4, c2(-T[1]), c2(T[1]))), tA0, tA1);
-            const float b0 = __saturatef(X0 - tA0), b1 = __saturatef(X1 - tA1);
-            const uint64_t S2 = f2_pack(b0, b1), NS2 = f2_pack(-b0, -b1);
-            const uint64_t U = f2_fma(S4, c2(T[6]), f2_fma(S4, c2(-T[2]), c2(T[2])));
-            const uint64_t L = f2_fma(S4, c2(T[4]), f2_fma(S4, c2(-T[0]), c2(T[0])));
-            float tB0, tB1;
-            f2_unpack(f2_fma(S2, U, f2_fma(NS2, L, L)), tB0, tB1);
-            const uint64_t S1 = f2_pack(__saturatef(X0 - tB0), __saturatef(X1 - tB1));
-            N = f2_fma(S4, c2(4.f), f2_fma(S2, c2(2.f), S1));
-        } else if constexpr (HALF == 4) {
-            const float a0 = __saturatef(X0 - T[1]), a1 = __saturatef(X1 - T[1]);
-            const uint64_t S2 = f2_pack(a0, a1);
-            float tA0, tA1;
-            f2_unpack(f2_fma(S2, c2(T[2]), f2_fma(S2, c2(-T[0]), c2(T[0]))), tA0, tA1);
-            const uint64_t S1 = f2_pack(__saturatef(X0 - tA0), __saturatef(X1 - tA1));
-            N = f2_fma(S2, c2(2.f), S1);
-        } else if constexpr (HALF == 2) {
-            N = f2_pack(__saturatef(X0 - T[0]), __saturatef(X1 - T[0]));
-        } else {
-            N = 0ull;
+        float X0, X1;
+        f2_unpack(f2_mul(f2_pack(x[j], x[j + 1]), ks.F2), X0, X1);
+        const uint64_t SG = f2_pack(__saturatef(x[j] * 0x1p127f), __saturatef(x[j + 1] * 0x1p127f));
+        uint64_t N = 0ull;
+        if constexpr (HALF >= 2) {
+            const uint64_t S1 = f2_pack(__saturatef(fabsf(X0) - ks.t1), __saturatef(fabsf(X1) - ks.t1));
+            if constexpr (HALF == 2) {
+                N = S1;
+            } else {
+                float a0, a1;
+                f2_unpack(f2_fma(S1, ks.d2, ks.lo2), a0, a1);
+                const uint64_t S2 = f2_pack(__saturatef(fabsf(X0) - a0), __saturatef(fabsf(X1) - a1));
+                if constexpr (HALF == 4) {
+                    N = f2_fma(S1, c2(2.f), S2);
+                } else {
+                    // S1 picks the upper half (T4 .. T6), S2 the upper quarter of it
+                    float b0, b1;
+                    f2_unpack(f2_fma(S2, f2_fma(S1, ks.d3ab, ks.d3a), f2_fma(S1, ks.d3b, ks.l3)), b0, b1);
+                    const uint64_t S3 = f2_pack(__saturatef(fabsf(X0) - b0), __saturatef(fabsf(X1) - b1));
+                    N = f2_fma(S1, c2(4.f), f2_fma(S2, c2(2.f), S3));
+                }
+            }
         }
-        float n0, n1;
-        f2_unpack(f2_add(N, MG2), n0, n1);
-        f[j] = __float_as_uint(n0) ^ (uint32_t)((x[j] > 0.f) ? HALF : HALF - 1);
-        f[j + 1] = __float_as_uint(n1) ^ (uint32_t)((x[j + 1] > 0.f) ? HALF : HALF - 1);
+        // c + sg + (2 sg - 1) n
+        const uint64_t SGN = f2_fma(SG, c2(2.f), c2(-1.f));
+        float k0, k1;
+        f2_unpack(f2_fma(SGN, N, f2_add(SG, C)), k0, k1);
+        f[j] = __float_as_uint(k0);
+        f[j + 1] = __float_as_uint(k1);
     }
 }
 
@@ -192,7 +229,7 @@ __device__ __forceinline__ void et_value_codes(const float (&x)[32], float mn, f
         for (int j = 0; j < 32; ++j) f[j] = kEtMagicBits;
         return;
     }
-    bool near = false;
+    float emax[2] = {0.f, 0.f};  // the largest |q - rint(q)|, two chains
     const uint64_t C2 = f2_pack(inv_sqrt_d, inv_sqrt_d), NMN2 = f2_pack(-mn, -mn), RS2 = f2_pack(rs, rs),
                    MG2 = f2_pack(kEtMagic, kEtMagic);
 #pragma unroll
@@ -203,31 +240,25 @@ __device__ __forceinline__ void et_value_codes(const float (&x)[32], float mn, f
         float e0, e1, t0, t1;
         f2_unpack(f2_sub(q, f2_sub(t, MG2)), e0, e1);
         f2_unpack(t, t0, t1);
-        near = near || fabsf(e0) > kTie || fabsf(e1) > kTie;
+        emax[(j >> 1) & 1] = fmax3(emax[(j >> 1) & 1], fabsf(e0), fabsf(e1));
         f[j] = __float_as_uint(t0);
         f[j + 1] = __float_as_uint(t1);
     }
-    if (near) {
+    if (fmaxf(emax[0], emax[1]) > kTie) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             f[j] = __float_as_uint(fminf(fmaxf(rintf(fmaf(x[j], inv_sqrt_d, -mn) / scale), 0.f), VMAX) + kEtMagic);
     }
 }
 
-// This thread's row of tensor memory, 32 columns at ta and 32 at tb, with one
-// wait for both loads.
-__device__ __forceinline__ void et_load2x32(uint32_t ta, uint32_t tb, float (&xa)[32], float (&xb)[32]) {
-    uint32_t ra[32], rb[32];
-    tc::ld_32x32b_x32(ta, ra);
-    tc::ld_32x32b_x32(tb, rb);
+// This thread's row of tensor memory, 32 columns at ta.
+__device__ __forceinline__ void et_load32(uint32_t ta, float (&x)[32]) {
+    uint32_t r[32];
+    tc::ld_32x32b_x32(ta, r);
     tc::wait_ld();
-    tc::reg_fence(ra);
-    tc::reg_fence(rb);
+    tc::reg_fence(r);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        xa[j] = __uint_as_float(ra[j]);
-        xb[j] = __uint_as_float(rb[j]);
-    }
+    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
 }
 
 template <int KB, int VB>
@@ -238,20 +269,22 @@ __global__ void __launch_bounds__(kEtThreads, 1)
     constexpr int D = kHeadDim;
     constexpr int HALF = 1 << (KB - 1);
     constexpr int VMAX = (1 << VB) - 1;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int wg = tid >> 7, tw = tid & 127;
     const Geometry& g = a.g;
     // the swizzled layout repeats every 1 KB and is anchored at 1 KB boundaries
     uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     float* bsd_s = reinterpret_cast<float*>(sm + kEtBsd);
+    int* next_s = reinterpret_cast<int*>(sm + kEtNext);  // [0]: tile counter; [1 + w]: warpgroup w's next tile
 
     // The set-up up to the H matrix reads only kernel parameters and shared
     // memory, so it runs before the wait for the previous grid (programmatic
     // dependent launch) and overlaps that grid's last CTAs.
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(sbase + kEtBars + 8 * b, 1);
+        for (int b = 0; b < 2 * kEtGroups; ++b) mbar_init(sbase + kEtBars + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        next_s[0] = kEtGroups;
     }
     if (warp == 0) tc::tmem_alloc<512>(sbase + kEtTaddr);
     {
@@ -289,50 +322,46 @@ __global__ void __launch_bounds__(kEtThreads, 1)
     // take the tensor-memory columns this CTA waits for
     grid_launch_dependents();
 
-    const int slot = wg >> 1, half = wg & 1;  // tile slot; column half this warpgroup codes
-    const int ts = tid & 255;                   // thread of the slot
-    const uint32_t xk = sbase + kEtX + slot * 2 * kEtOp, xv = xk + kEtOp;
-    const uint32_t tcol = tmem + 256u * slot;                                        // U_k at +0, U_v at +128
-    const uint32_t tk = tcol + ((uint32_t)((warp & 3) * 32) << 16), tv = tk + 128;  // this warp's lanes
-    const uint32_t mbar = sbase + kEtBars + 8 * slot;
-    const uint32_t full = sbase + kEtBars + 16 + 8 * slot;
-    // the rows of `tile` into this slot's buffers (thread 0 of the slot): box
-    // k8 holds coordinates 8 k8 .. 8 k8 + 7 of the 128 rows, rows past the last
+    const uint32_t xb = sbase + kEtX + wg * kEtOp;                                  // this warpgroup's buffer
+    const uint32_t tcol = tmem + 128u * (uint32_t)wg;                                // its columns
+    const uint32_t trow = tcol + ((uint32_t)((warp & 3) * 32) << 16);                // this warp's lanes
+    const uint32_t done = sbase + kEtBars + 16 * wg, full = done + 8;
+    const int bar_id = 1 + wg;  // named barrier of the warpgroup
+    // one operand of `tile` into the buffer (thread 0 of the warpgroup): box j
+    // holds coordinates 64 j .. 64 j + 63 of the 128 rows, rows past the last
     // item zero-filled
-    auto load = [&](int tile) {
-        mbar_arrive_tx(full, 2u * kEtOp);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            et_tma_2d(xk + j * kEtXBox, &tmk, 64 * j, tile * kEtRows, full);
-            et_tma_2d(xv + j * kEtXBox, &tmv, 64 * j, tile * kEtRows, full);
-        }
+    auto load = [&](const CUtensorMap* map, int tile) {
+        mbar_arrive_tx(full, (uint32_t)kEtOp);
+        et_tma_2d(xb, map, 0, tile * kEtRows, full);
+        et_tma_2d(xb + kEtXBox, map, 64, tile * kEtRows, full);
     };
+    // 8 MMAs: U = X H^T of the operand in the buffer into the columns
     const uint32_t idesc = (a.dtype == TQ_BF16) ? tc::idesc_bf16_f32(kEtRows, D) : tc::idesc_f16_f32(kEtRows, D);
+    auto rotate = [&]() {
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s)
+            tc::mma_f16_ss(tcol, tc::smem_desc_sw128(xb + (s >> 2) * kEtXBox + 32 * (s & 3), kEtXSbo),
+                           tc::smem_desc(sbase + kEtH + 256 * s, kEtLbo, kEtSbo), idesc, s > 0 ? 1u : 0u);
+        tc::commit(done);
+    };
     const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
     const int hkv = g.hkv;
     const int64_t cap = g.num_blocks * kBlockSize;
+    // the CTA's tiles are blockIdx.x + k gridDim.x; warpgroup w starts with k = w
+    const int nk = (num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    int k = wg;
     bool bad = false;
-    int tile = blockIdx.x + slot * gridDim.x;
-    if (ts == 0 && tile < num_tiles) load(tile);
-    for (int i = 0; tile < num_tiles; ++i) {
-        // the slot's threads are done reading the tensor-memory columns the
-        // MMAs are about to overwrite
-        tc::fence_before_sync();
-        asm volatile("bar.sync %0, 256;" ::"r"(1 + slot) : "memory");
-        if (ts == 0) {
-            // the tile's rows have landed (a wait that gives up issues nothing:
-            // the MMA wait below then gives up too)
-            if (mbar_wait(full, (uint32_t)(i & 1))) {
+    uint32_t ph = 0;  // phase of both barriers: each completes twice per tile
+    if (tw == 0 && k < nk) load(&tmk, (int)blockIdx.x + k * (int)gridDim.x);
+    while (k < nk) {
+        const int tile = (int)blockIdx.x + k * (int)gridDim.x;
+        // ---- keys (the barrier at the end of the previous tile ordered the
+        // threads' reads of the columns before these MMAs) ----
+        if (tw == 0) {
+            // a copy wait that gives up issues nothing: the MMA wait below then gives up too
+            if (mbar_wait(full, ph)) {
                 tc::fence_after_sync();
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s)
-                    tc::mma_f16_ss(tcol, tc::smem_desc_sw128(xk + (s >> 2) * kEtXBox + 32 * (s & 3), kEtXSbo),
-                                   tc::smem_desc(sbase + kEtH + 256 * s, kEtLbo, kEtSbo), idesc, s > 0 ? 1u : 0u);
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s)
-                    tc::mma_f16_ss(tcol + 128, tc::smem_desc_sw128(xv + (s >> 2) * kEtXBox + 32 * (s & 3), kEtXSbo),
-                                   tc::smem_desc(sbase + kEtH + 256 * s, kEtLbo, kEtSbo), idesc, s > 0 ? 1u : 0u);
-                tc::commit(mbar);
+                rotate();
             }
         }
         // this row's (token, KV head) item and its slot, loaded while the MMAs run
@@ -342,93 +371,71 @@ __global__ void __launch_bounds__(kEtThreads, 1)
         const uint32_t t = itu / (uint32_t)hkv;
         const int hc = (int)(itu - t * (uint32_t)hkv);
         const int64_t sl = live ? __ldg(a.slot_mapping + t) : -1;
-        // a wait that gives up ends the slot's loop for all its threads
-        // together (the named barriers need all 256)
-        bad = et_any256(!mbar_wait(mbar, (uint32_t)(i & 1)), 1 + slot);
+        // a wait that gives up ends the warpgroup's loop for all its threads
+        // together (its named barrier needs all 128)
+        bad = et_any128(!mbar_wait(done, ph), bar_id);
         if (bad) break;
         tc::fence_after_sync();
-        const int next = tile + 2 * (int)gridDim.x;
-        if (ts == 0 && next < num_tiles) load(next);  // the buffers are free: the MMAs have read them
+        if (tw == 0) load(&tmv, tile);  // the key MMAs have read the buffer
 
-        // ---- row tw of the tile ----
-        if (half == 0 && live && sl >= cap) flag(a.status, TQ_FLAG_BAD_SLOT);
+        if (live && sl >= cap) flag(a.status, TQ_FLAG_BAD_SLOT);
         const bool store = live && sl >= 0 && sl < cap;
         static_assert(kBlockSize == 16, "page index by shift");
         const int64_t blk = store ? (sl >> 4) : 0;
         const int off = (int)(sl & (kBlockSize - 1));
         uint8_t* page = a.pool + (blk * hkv + hc) * g.page_bytes;
+        float x[32];
 
-        float xk_[32], xv_[32];
-        // ---- this half's sum of squares of U_k (||U_k||^2 = d ||k||^2, d = 128:
-        // an exact scaling), minimum and maximum of U_v ----
+        // gamma = ||U_k|| / sqrt(d) (||U_k||^2 = d ||k||^2, d = 128: an exact scaling)
         uint64_t ss2[2] = {0ull, 0ull};  // four partial sums of squares, two per register
-        float lo4[4] = {3.4e38f, 3.4e38f, 3.4e38f, 3.4e38f}, hi4[4] = {-3.4e38f, -3.4e38f, -3.4e38f, -3.4e38f};
         bool finite = true;
 #pragma unroll 1
-        for (int c = 2 * half; c < 2 * half + 2; ++c) {
-            et_load2x32(tk + 32 * c, tv + 32 * c, xk_, xv_);
+        for (int c = 0; c < 4; ++c) {
+            et_load32(trow + 32 * c, x);
             // a non-finite input coordinate makes every rotated coordinate inf
             // or NaN (H has no zero entry), so one coordinate tells
-            finite = finite && isfinite(xk_[0]) && isfinite(xv_[0]);
+            finite = finite && isfinite(x[0]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if ((j & 1) == 0) {
-                    const uint64_t p = f2_pack(xk_[j], xk_[j + 1]);
-                    ss2[(j >> 1) & 1] = f2_fma(p, p, ss2[(j >> 1) & 1]);
-                }
-                lo4[j & 3] = fminf(lo4[j & 3], xv_[j]);
-                hi4[j & 3] = fmaxf(hi4[j & 3], xv_[j]);
+            for (int j = 0; j < 32; j += 2) {
+                const uint64_t p = f2_pack(x[j], x[j + 1]);
+                ss2[(j >> 1) & 1] = f2_fma(p, p, ss2[(j >> 1) & 1]);
             }
         }
-        float4* xchg = reinterpret_cast<float4*>(sm + kEtXchg) + slot * 2 * kEtRows;
         float s4[4];
         f2_unpack(ss2[0], s4[0], s4[1]);
         f2_unpack(ss2[1], s4[2], s4[3]);
-        xchg[half * kEtRows + tw] = make_float4((s4[0] + s4[1]) + (s4[2] + s4[3]),
-                                                fminf(fminf(lo4[0], lo4[1]), fminf(lo4[2], lo4[3])),
-                                                fmaxf(fmaxf(hi4[0], hi4[1]), fmaxf(hi4[2], hi4[3])), finite ? 1.f : 0.f);
-        asm volatile("bar.sync %0, 256;" ::"r"(1 + slot) : "memory");
-        // both halves combine the two records in the same order: the same gamma,
-        // min and max
-        const float4 e0 = xchg[tw], e1 = xchg[kEtRows + tw];
-        const float gamma = sqrtf((e0.x + e1.x) * (1.f / 128.f));
-        // the scaling by 1/sqrt(d) is monotone, so min and max commute with it
-        const float mn = fminf(e0.y, e1.y) * inv_sqrt_d;
-        const float mx = fmaxf(e0.z, e1.z) * inv_sqrt_d;
-        finite = e0.w != 0.f && e1.w != 0.f;
-        const float scale = (mx - mn) / (float)VMAX;
-        const float rs = 1.f / scale;
+        const float gamma = sqrtf(((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / 128.f));
         {
             uint8_t* krow = page + g.kcode_off + off * (D * KB / 8);
-            uint8_t* vrow = page + g.vcode_off + off * (D * VB / 8);
             const KeyThresholds<KB <= 4 ? KB : 1> kt(a.c, gamma);
             // T = F thr: F = 2^(24 - e) with 2^e <= thr_0 < 2^(e + 1), so that
-            // (|x| - thr_b) F >= 2 when |x| > thr_b (the difference of two floats
-            // at least thr_0 apart in exponent is a multiple of 2^(e - 23));
-            // |x| F stays below 2^25 / t_{HALF} (|x| <= sqrt(d) gamma)
+            // T[0] lies in [2^24, 2^25) and the search's steps are exact; |x| F
+            // stays below 2^25 / t_{HALF} (|x| <= sqrt(d) gamma)
             constexpr int NT = (KB <= 4 && HALF > 1) ? HALF - 1 : 1;
-            float T[NT];
+            float T[NT] = {};
             float F = 1.f;
-            const int e0 = (int)((__float_as_uint(kt.thr[0]) >> 23) & 0xFFu) - 127;
-            const bool fast = KB <= 4 && gamma > 0.f && e0 > -100 && e0 < 100;
+            bool fast = KB <= 4 && gamma > 0.f;
             if constexpr (KB <= 4 && HALF > 1) {
+                const int e0 = (int)((__float_as_uint(kt.thr[0]) >> 23) & 0xFFu) - 127;
+                fast = fast && e0 > -100 && e0 < 100;
                 F = __uint_as_float((uint32_t)(127 + 24 - e0) << 23);
 #pragma unroll
                 for (int b = 0; b < NT; ++b) T[b] = kt.thr[b] * F;
             }
+            const EtKeySearch<(KB <= 4) ? KB : 1> ks(T, F);
 #pragma unroll 1
-            for (int c = 2 * half; c < 2 * half + 2; ++c) {
-                et_load2x32(tk + 32 * c, tv + 32 * c, xk_, xv_);
+            for (int c = 0; c < 4; ++c) {
+                et_load32(trow + 32 * c, x);
                 uint32_t fk[32];
                 if (fast) {
-                    if constexpr (KB <= 4) et_key_codes<KB>(xk_, T, F, fk);
+                    if constexpr (KB <= 4) et_key_codes<KB>(x, ks, fk);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         int code = HALF - 1;  // a zero key (gamma = 0)
                         if (gamma > 0.f) {
-                            if constexpr (KB <= 4) code = key_code_bsearch<KB>(kt, xk_[j]);
-                            else code = key_code_search<KB>(xk_[j], gamma, bsd_s);
+                            if constexpr (KB <= 4) code = key_code_bsearch<KB>(kt, x[j]);
+                            else code = key_code_search<KB>(x[j], gamma, bsd_s);
                         }
                         fk[j] = kEtMagicBits + (uint32_t)code;
                     }
@@ -436,14 +443,56 @@ __global__ void __launch_bounds__(kEtThreads, 1)
                 uint32_t wk[KB];
                 et_pack_biased<KB>(fk, wk);
                 if (store) et_store_words<KB>(krow + c * 4 * KB, wk);
+            }
+        }
+
+        // ---- values: the threads are done reading the key columns ----
+        tc::fence_before_sync();
+        asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+        if (tw == 0) {
+            if (mbar_wait(full, ph ^ 1u)) {
+                tc::fence_after_sync();
+                rotate();
+            }
+        }
+        bad = et_any128(!mbar_wait(done, ph ^ 1u), bar_id);
+        if (bad) break;
+        tc::fence_after_sync();
+        if (tw == 0) {
+            // the value MMAs have read the buffer: the keys of this warpgroup's next tile
+            const int kn = atomicAdd(next_s, 1);
+            next_s[1 + wg] = kn;
+            if (kn < nk) load(&tmk, (int)blockIdx.x + kn * (int)gridDim.x);
+        }
+        // v_rot = U_v / sqrt(d): the scaling is monotone, so min and max commute with it
+        float lo2[2] = {3.4e38f, 3.4e38f}, hi2[2] = {-3.4e38f, -3.4e38f};
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            et_load32(trow + 32 * c, x);
+            finite = finite && isfinite(x[0]);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                lo2[(j >> 1) & 1] = fmin3(lo2[(j >> 1) & 1], x[j], x[j + 1]);
+                hi2[(j >> 1) & 1] = fmax3(hi2[(j >> 1) & 1], x[j], x[j + 1]);
+            }
+        }
+        const float mn = fminf(lo2[0], lo2[1]) * inv_sqrt_d;
+        const float mx = fmaxf(hi2[0], hi2[1]) * inv_sqrt_d;
+        const float scale = (mx - mn) / (float)VMAX;
+        const float rs = 1.f / scale;
+        {
+            uint8_t* vrow = page + g.vcode_off + off * (D * VB / 8);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                et_load32(trow + 32 * c, x);
                 uint32_t fv[32];
-                et_value_codes<VB>(xv_, mn, scale, rs, fv);
+                et_value_codes<VB>(x, mn, scale, rs, fv);
                 uint32_t wv[VB];
                 et_pack_biased<VB>(fv, wv);
                 if (store) et_store_words<VB>(vrow + c * 4 * VB, wv);
             }
         }
-        if (store && half == 0) {
+        if (store) {
             if (!finite) flag(a.status, TQ_FLAG_NONFINITE);
             const uint16_t hg = f16_bits(gamma), hs = f16_bits(scale), hz = f16_bits(mn);
             reinterpret_cast<uint16_t*>(page + g.gam_off)[off] = hg;
@@ -452,9 +501,13 @@ __global__ void __launch_bounds__(kEtThreads, 1)
             const bool ovf = ((hg & 0x7FFF) == 0x7C00) || ((hs & 0x7FFF) == 0x7C00) || ((hz & 0x7FFF) == 0x7C00);
             if (ovf && finite) flag(a.status, TQ_FLAG_OVERFLOW);
         }
-        tile = next;
+        // the next tile, published by thread 0 before the barrier below; every
+        // thread reads it after that barrier (at the top of the keys)
+        tc::fence_before_sync();
+        asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+        k = next_s[1 + wg];
     }
-    if (bad && ts == 0) flag(a.status, TQ_FLAG_TIMEOUT);
+    if (bad && tw == 0) flag(a.status, TQ_FLAG_TIMEOUT);
     // every MMA of the CTA has completed (each warpgroup waited for its last)
     tc::fence_before_sync();
     __syncthreads();
