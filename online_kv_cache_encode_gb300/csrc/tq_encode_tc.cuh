@@ -11,7 +11,9 @@
 // memory for the whole kernel.  The rest of the encode reads one row per
 // thread from tensor memory and needs no cross-lane traffic:
 //   key:   gamma = ||U_k|| / sqrt(d) = ||k||; code_j = #{boundaries < u_j} with
-//          u = U_k / (sqrt(d) gamma), decided as U_k against sqrt(d) t_b gamma;
+//          u = U_k / (sqrt(d) gamma), decided as U_k against sqrt(d) t_b gamma
+//          (widths up to 4) or as |U_k| / gamma against sqrt(d) t_b on a grid
+//          (wider keys);
 //   value: v_rot = U_v / sqrt(d); per-token min / max;
 //          code = clamp(rint((v_rot - min) / scale), 0, 2^b - 1).
 // ["TurboQuant: KV Cache Vector Quantization" -- three steps; deep dive
@@ -53,11 +55,18 @@ constexpr uint32_t kEtXSbo = 1024, kEtXBox = 16384;
 constexpr int kEtOp = kEtRows * kHeadDim * 2;  // one 128 x 128 16-bit operand: 32 KB
 constexpr int kEtH = 0;                        // H [n][k]
 constexpr int kEtX = kEtOp;                    // warpgroup w's buffer at kEtX + w kEtOp
-constexpr int kEtBsd = kEtX + kEtGroups * kEtOp;        // key widths above 4 bits: sqrt(d) t_b of the positive half
-constexpr int kEtBars = kEtBsd + 4 * (kMaxLevels / 2);  // per warpgroup: MMAs done, copy landed
-constexpr int kEtNext = kEtBars + 16 * kEtGroups;       // tile counter, next tile per warpgroup
-constexpr int kEtTaddr = kEtNext + 4 * (1 + kEtGroups);
-constexpr int kEtSmem = kEtTaddr + 16 + 1024;  // + room to align the base to 1 KB (swizzle atoms)
+// key widths above 4 bits: the decision grid over z = |u| / gamma in [0, sqrt(d)],
+// 128 cells per unit (cell c: z 128 in [c - 1/2, c + 1/2]), indexed up to z = 16
+constexpr int kEtCells = 2049;
+constexpr int kEtGrid = kEtX + kEtGroups * kEtOp;        // [cell] (-tau 2^40 or -inf, count below)
+// the rest of the layout; the grid takes space only for key widths above 4 bits
+template <int KB>
+struct EtLayout {
+    static constexpr int bars = kEtGrid + (KB > 4 ? 8 * kEtCells + 8 : 0);  // per warpgroup: MMAs done, copy landed
+    static constexpr int next = bars + 16 * kEtGroups;   // tile counter, next tile per warpgroup
+    static constexpr int taddr = next + 4 * (1 + kEtGroups);
+    static constexpr int smem = taddr + 16 + 1024;       // + room to align the base to 1 KB (swizzle atoms)
+};
 
 // Box (x, y) of a 2-D tensor map into shared memory, completing on `bar`.
 __device__ __forceinline__ void et_tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
@@ -76,6 +85,19 @@ __device__ __forceinline__ bool et_any128(bool v, int id) {
         : "r"((uint32_t)v), "r"(id)
         : "memory");
     return r != 0;
+}
+
+// Three-input minimum and maximum of sm_100 and later: one instruction where
+// two-input ones take two.
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 // B words at p (4-byte aligned; 8-byte when B is even, 16-byte when B % 4 == 0)
@@ -213,6 +235,42 @@ __device__ __forceinline__ void et_key_codes(const float (&x)[32], const EtKeySe
     }
 }
 
+// Key codes (widths above 4 bits) of 32 rotated coordinates x through the
+// decision grid.  With z = |x| / gamma, taken as y = sat(z / 16) (a NaN or inf
+// lands on an end of the grid), the cell c = rint(128 z) spans z in
+// [(c - 1/2) / 128, (c + 1/2) / 128]; no two positive boundaries tau_b =
+// sqrt(d) t_b lie that close, so the count n = #{b : z > tau_b} is the cell's
+// count below it plus [z > tau] for the one boundary tau that may lie in the
+// cell, decided as sat(2^40 z - 2^40 tau) (exact: z - tau is at least an ulp of
+// tau, and 2^40 of that is at least 1).  The cell's entry is (-2^40 tau, or
+// -inf for none, and the count below) at grid + 8 c; its address comes from
+// the biased field of rint(128 z) by one integer multiply-add.  The sign and
+// the code are formed as in et_key_codes.
+template <int KB>
+__device__ __forceinline__ void et_key_codes_grid(const float (&x)[32], float ig16, uint32_t grid,
+                                                  uint32_t (&f)[32]) {
+    constexpr int HALF = 1 << (KB - 1);
+    auto c2 = [](float v) { return f2_pack(v, v); };
+    const uint64_t C = c2(kEtMagic + (float)(HALF - 1)), MG = c2(kEtMagic), W = c2(2048.f);
+    const uint32_t adj = grid - (kEtMagicBits << 3);  // wraps: 8 bits(rint) + adj = grid + 8 c
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float y0 = __saturatef(fabsf(x[j]) * ig16), y1 = __saturatef(fabsf(x[j + 1]) * ig16);
+        float r0, r1;
+        f2_unpack(f2_fma(f2_pack(y0, y1), W, MG), r0, r1);
+        float nt0, n00, nt1, n01;
+        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(nt0), "=f"(n00) : "r"(__float_as_uint(r0) * 8u + adj));
+        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(nt1), "=f"(n01) : "r"(__float_as_uint(r1) * 8u + adj));
+        const uint64_t S = f2_pack(__saturatef(fmaf(y0, 0x1p44f, nt0)), __saturatef(fmaf(y1, 0x1p44f, nt1)));
+        const uint64_t N = f2_add(f2_pack(n00, n01), S);
+        const uint64_t SG = f2_pack(__saturatef(x[j] * 0x1p127f), __saturatef(x[j + 1] * 0x1p127f));
+        float k0, k1;
+        f2_unpack(f2_fma(f2_fma(SG, c2(2.f), c2(-1.f)), N, f2_add(SG, C)), k0, k1);
+        f[j] = __float_as_uint(k0);
+        f[j + 1] = __float_as_uint(k1);
+    }
+}
+
 // Value codes of 32 coordinates x (rotated, unnormalised) of one row, biased:
 // rint((x / sqrt(d) - mn) / scale), the quotient formed as a product with
 // rs = 1 / scale.  That product is within VMAX 2^-22 of the exact quotient,
@@ -275,18 +333,18 @@ __global__ void __launch_bounds__(kEtThreads, 1)
     // the swizzled layout repeats every 1 KB and is anchored at 1 KB boundaries
     uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
-    float* bsd_s = reinterpret_cast<float*>(sm + kEtBsd);
-    int* next_s = reinterpret_cast<int*>(sm + kEtNext);  // [0]: tile counter; [1 + w]: warpgroup w's next tile
+    using LY = EtLayout<KB>;
+    int* next_s = reinterpret_cast<int*>(sm + LY::next);  // [0]: tile counter; [1 + w]: warpgroup w's next tile
 
     // The set-up up to the H matrix reads only kernel parameters and shared
     // memory, so it runs before the wait for the previous grid (programmatic
     // dependent launch) and overlaps that grid's last CTAs.
     if (tid == 0) {
-        for (int b = 0; b < 2 * kEtGroups; ++b) mbar_init(sbase + kEtBars + 8 * b, 1);
+        for (int b = 0; b < 2 * kEtGroups; ++b) mbar_init(sbase + LY::bars + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         next_s[0] = kEtGroups;
     }
-    if (warp == 0) tc::tmem_alloc<512>(sbase + kEtTaddr);
+    if (warp == 0) tc::tmem_alloc<512>(sbase + LY::taddr);
     {
         // H[n][k] = (-1)^(popcount(n & k) + [s_k = -1]) in the input type, K-major:
         // element (n, k) at (n / 8) 2048 + (k / 8) 128 + (n % 8) 16 + (k % 8) 2
@@ -310,14 +368,33 @@ __global__ void __launch_bounds__(kEtThreads, 1)
         }
     }
     grid_dependency_wait();  // the previous grid's writes (inputs, pool) are visible
+    int grid_bad = 0;
     if constexpr (KB > 4) {
-        for (int i = tid; i < HALF - 1; i += kEtThreads) bsd_s[i] = a.tab->boundary_sd_pos[i];
+        // the decision grid: per cell the count of positive boundaries below it
+        // and the one boundary inside it, if any
+        const float* bp = a.tab->boundary_sd_pos;  // HALF - 1 increasing values
+        float2* grid = reinterpret_cast<float2*>(sm + kEtGrid);
+        for (int c = tid; c < kEtCells; c += kEtThreads) {
+            const float lo = ((float)c - 0.5f) * (1.f / 128.f), hi = ((float)c + 0.5f) * (1.f / 128.f);
+            int n0 = 0;  // #{b : bp[b] < lo}
+#pragma unroll
+            for (int step = HALF / 2; step >= 1; step >>= 1)
+                if (n0 + step <= HALF - 1 && bp[n0 + step - 1] < lo) n0 += step;
+            float nt = -INFINITY;
+            if (n0 < HALF - 1 && bp[n0] <= hi) {
+                nt = -bp[n0] * 0x1p40f;
+                if (n0 + 1 < HALF - 1 && bp[n0 + 1] <= hi) grid_bad = 1;
+            }
+            grid[c] = make_float2(nt, (float)n0);
+        }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // H: generic writes -> tensor-core reads
     tc::fence_before_sync();
-    __syncthreads();
+    // a grid cell with two boundaries (none for the codebooks of d = 128) sends
+    // the wide-key decisions to the search over the boundaries
+    grid_bad = __syncthreads_or(grid_bad);
     tc::fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kEtTaddr);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + LY::taddr);
     // only now may a dependent grid start: one of its CTAs on this SM must not
     // take the tensor-memory columns this CTA waits for
     grid_launch_dependents();
@@ -325,7 +402,7 @@ __global__ void __launch_bounds__(kEtThreads, 1)
     const uint32_t xb = sbase + kEtX + wg * kEtOp;                                  // this warpgroup's buffer
     const uint32_t tcol = tmem + 128u * (uint32_t)wg;                                // its columns
     const uint32_t trow = tcol + ((uint32_t)((warp & 3) * 32) << 16);                // this warp's lanes
-    const uint32_t done = sbase + kEtBars + 16 * wg, full = done + 8;
+    const uint32_t done = sbase + LY::bars + 16 * wg, full = done + 8;
     const int bar_id = 1 + wg;  // named barrier of the warpgroup
     // one operand of `tile` into the buffer (thread 0 of the warpgroup): box j
     // holds coordinates 64 j .. 64 j + 63 of the 128 rows, rows past the last
@@ -423,19 +500,23 @@ __global__ void __launch_bounds__(kEtThreads, 1)
                 for (int b = 0; b < NT; ++b) T[b] = kt.thr[b] * F;
             }
             const EtKeySearch<(KB <= 4) ? KB : 1> ks(T, F);
+            // wide keys: z / 16 = |x| / (16 gamma)
+            const float ig16 = (KB > 4 && gamma > 0.f) ? 0.0625f / gamma : 0.f;
+            if constexpr (KB > 4) fast = !grid_bad && gamma > 1e-30f && ig16 < 3.0e38f;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 et_load32(trow + 32 * c, x);
                 uint32_t fk[32];
                 if (fast) {
                     if constexpr (KB <= 4) et_key_codes<KB>(x, ks, fk);
+                    else et_key_codes_grid<KB>(x, ig16, sbase + kEtGrid, fk);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         int code = HALF - 1;  // a zero key (gamma = 0)
                         if (gamma > 0.f) {
                             if constexpr (KB <= 4) code = key_code_bsearch<KB>(kt, x[j]);
-                            else code = key_code_search<KB>(x[j], gamma, bsd_s);
+                            else code = key_code_search<KB>(x[j], gamma, a.tab->boundary_sd_pos);
                         }
                         fk[j] = kEtMagicBits + (uint32_t)code;
                     }
@@ -557,11 +638,11 @@ int launch_encode_tc(const EncodeArgs& a, int64_t items, int num_sms, cudaStream
     if (!et_tensor_map(&tmk, a.K, items) || !et_tensor_map(&tmv, a.V, items)) return -1;
     auto kern = encode_tc_kernel<KB, VB>;
     static int done[64] = {};
-    cudaError_t e = ensure_smem_limit(kern, kEtSmem, done);
+    cudaError_t e = ensure_smem_limit(kern, EtLayout<KB>::smem, done);
     if (e != cudaSuccess) return (int)e;
     const int num_tiles = (int)((items + kEtRows - 1) / kEtRows);
     const int grid = num_tiles < num_sms ? num_tiles : num_sms;
-    return (int)launch_programmatic(kern, dim3((unsigned)grid), dim3(kEtThreads), (size_t)kEtSmem, s, a, tmk, tmv,
+    return (int)launch_programmatic(kern, dim3((unsigned)grid), dim3(kEtThreads), (size_t)EtLayout<KB>::smem, s, a, tmk, tmv,
                                     items, num_tiles);
 }
 
