@@ -110,3 +110,73 @@ def test_bulk_encode_flags(tq, oracle):
     for base, nbytes in [(L.k, 64), (L.v, 64), (L.g, 2), (L.s, 2), (L.z, 2)]:
         for p in page:
             assert np.all(pool[p + base + off * nbytes: p + base + (off + 1) * nbytes] == 0xAB)
+
+
+@pytest.mark.parametrize("kb,vb", [(4, 4), (3, 2), (6, 6), (8, 8)])
+def test_bulk_encode_structured_rows(tq, oracle, kb, vb):
+    """Rows the random inputs do not produce, on the tensor-core path: a zero
+    key, keys with two equal coordinates (half of their rotated coordinates
+    exactly 0: the sign decision at 0 must give 2^(kb-1) - 1, as x > 0 does),
+    a key on one coordinate (every rotated coordinate of one magnitude), keys
+    scaled by 2^-12, 2^-20 and 2^10 (other threshold scales), a zero value row
+    (scale 0) and a value row of a tiny spread."""
+    import torch
+    dev = "cuda"
+    n = _bulk_tokens(8)
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(n,), hkv=8, hq=16, key_bits=kb, value_bits=vb)
+    K = W.kv_tokens(w, 0, 0, 0, n).copy()
+    V = W.kv_tokens(w, 1, 0, 0, n).copy()
+    K[10] = 0.0
+    K[12] = 0.0
+    K[12, :, 5] = 1.0
+    K[12, :, 77] = 1.0
+    K[13] *= 2.0 ** -12
+    K[14] *= 2.0 ** 10
+    K[15] = 0.0
+    K[15, :, 3] = -3.0
+    K[16] *= 2.0 ** -20
+    V[11] = 0.0
+    V[17] = 0.0
+    V[17, :, 9] = 2.0 ** -14
+    bt = W.block_table(w)
+    nb = w.num_blocks()
+    slots = W.slots(w, bt, 0, 0, n)
+    oc = oracle.Cache(w.d, kb, vb, 0, w.block_size, w.hkv, nb, w.seed)
+    pool_o = oc.new_pool()
+    st_o = oc.encode(K, V, slots, pool_o)
+    gc = tq.Cache(nb, w.hkv, kb, vb, 0, w.seed, w.block_size, w.d)
+    st = tq.new_status()
+    gc.encode(torch.from_numpy(K).to(dev, torch.bfloat16), torch.from_numpy(V).to(dev, torch.bfloat16),
+              torch.from_numpy(slots).to(dev), st)
+    torch.cuda.synchronize()
+    pool_g = gc.pool.cpu().numpy()
+    L = parity.Layout(w.d, kb, vb, 0, w.block_size, w.hkv, oc.page_bytes)
+    all_slots = np.repeat(slots, w.hkv)
+    all_heads = np.tile(np.arange(w.hkv), n)
+    fo = parity.unpack(pool_o, L, all_slots, all_heads)
+    fg = parity.unpack(pool_g, L, all_slots, all_heads)
+    half = 1 << (kb - 1)
+    rows = lambda t: slice(t * w.hkv, (t + 1) * w.hkv)  # noqa: E731
+    # the exactly-zero rotated coordinates of the two-coordinate keys take the
+    # lower code of the tie (the upper one is for x > 0 only); the oracle's middle
+    # boundary is 0 only up to its rounding (-5e-17 at 3 bits), so its code
+    # there may be either, and those 512 ties stay out of the mismatch budget
+    zero = np.abs(oracle.rotate(oc.s, K[12, 0].astype(np.float64))) == 0.0
+    assert zero.sum() == 64
+    assert np.all(fg["k"][rows(12)][:, zero] == half - 1)
+    ties = np.ix_(np.arange(12 * w.hkv, 13 * w.hkv), np.where(zero)[0])
+    fo["k"][ties] = fg["k"][ties]
+    enc = parity.compare_encode(fo, fg, K.reshape(-1, w.d).astype(np.float64), V.reshape(-1, w.d).astype(np.float64),
+                                oc, oracle)
+    enc["status_oracle"], enc["status_gpu"] = st_o, int(st.item())
+    enc["other_bytes_equal"] = True
+    parity.assert_encode_parity(dict(enc=enc))
+    assert np.all(fg["k"][rows(10)] == half - 1) and np.all(fo["k"][rows(10)] == half - 1)
+    assert np.all(fg["v"][rows(11)] == 0) and np.all(fo["v"][rows(11)] == 0)
+    # rows with no coordinate near a boundary agree with the oracle code for code
+    for t in (10, 11, 17):
+        np.testing.assert_array_equal(fg["k"][rows(t)], fo["k"][rows(t)], err_msg=f"token {t}")
+        np.testing.assert_array_equal(fg["v"][rows(t)], fo["v"][rows(t)], err_msg=f"token {t}")
+    assert set(np.unique(fg["v"][rows(17)])) <= {0, (1 << vb) - 1}
+    # one coordinate: every rotated coordinate has one magnitude, so one code per sign
+    assert all(len(np.unique(r)) <= 2 for r in fg["k"][rows(15)])
