@@ -588,7 +588,16 @@ __global__ void __launch_bounds__(kEtThreads, 1)
         asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
         k = next_s[1 + wg];
     }
-    if (bad && tw == 0) flag(a.status, TQ_FLAG_TIMEOUT);
+    if (bad && tw == 0) {
+        flag(a.status, TQ_FLAG_TIMEOUT);
+        // a copy or MMAs this warpgroup started may still be in flight: wait (a
+        // short bound each) for the current phase of both barriers, whichever
+        // parity it has, before the CTA releases its memory
+        for (uint32_t par = 0; par < 2; ++par) {
+            mbar_wait_for(full, par, 100000000ll);
+            mbar_wait_for(done, par, 100000000ll);
+        }
+    }
     // every MMA of the CTA has completed (each warpgroup waited for its last)
     tc::fence_before_sync();
     __syncthreads();
