@@ -7,7 +7,7 @@
 // unpacked once for all of them.  Grid (split, row block, KV head): a CTA
 // takes 128 query rows (row r = position index * G + query in group) and the
 // 128-token tiles of its split of the token range (tiles past the block's last
-// position are skipped).  Its 13 warps:
+// position are skipped).  Its 15 warps:
 //   warps 0-7  softmax, two warps per query row: thread = (column half, query
 //              row = tensor-memory lane).  Before the tiles the pair rotates
 //              its query (q_rot = R q: each half takes 64 dimensions through
@@ -22,12 +22,14 @@
 //              the half's 64 output columns), and writes the weights
 //              p * scale in fp16 hi and lo parts over its scores as the A
 //              operand of PV.  The two halves' sums meet at the end.
-//   warps 8-11 producers: thread = token of the tile.  They unpack the key
-//              codes through a 256-entry table into the two-level centroid
+//   warps 8-11 key producers: thread = token of the tile.  They unpack the
+//              key codes through a 256-entry table into the two-level centroid
 //              operand C[c] / delta = N[c] + rem2[c] / delta (N an integer of
 //              magnitude <= 2047, |rem2 / delta| <= 1/2, both exact enough in
-//              fp16), the value codes into exact fp16 subnormals, and the
-//              norms, scales and zero points into shared memory.
+//              fp16).
+//   warps 13-14 value producers: thread = two tokens of the tile.  They unpack
+//              the value codes into exact fp16 subnormals, and the norms,
+//              scales, zero points and masks into shared memory.
 //   warp 12    lane 0 loads the pages (bulk async copies into a four-tile
 //              ring) and issues the MMAs: scores S [128 rows x 128 tokens] =
 //              q_hi . N + q_lo . N + q_hi . rem2/delta (24 kind::f16 MMAs,
@@ -59,7 +61,7 @@ namespace {
 constexpr int kPfRows = 128;                    // query rows per CTA (tensor-memory lanes)
 constexpr int kPfTile = 128;                    // tokens per tile
 constexpr int kPfPages = kPfTile / kBlockSize;  // pages per tile
-constexpr int kPfWarps = 13;                    // softmax 0-7 (two per row), producers 8-11, issuer 12
+constexpr int kPfWarps = 15;                    // softmax 0-7 (two per row), key producers 8-11, issuer 12, value producers 13-14
 constexpr int kPfSoftmax = 256;                 // softmax threads (named barrier 1)
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPartRow = 4 + kHeadDim;          // partial record: max, sum, 2 pad, acc[128]
@@ -102,8 +104,8 @@ struct PfLayout {
     static constexpr int msk = gam + 4 * kPfTile * 4;
     static constexpr int scl = msk + 4 * kPfTile * 4;
     static constexpr int zer = scl + 2 * kPfTile * 4;
-    static constexpr int big = zer + 2 * kPfTile * 4;   // per tile parity and producer warp: a scale > kBigScale
-    static constexpr int inv = big + 2 * 4 * 4;         // per tile (u & 3) and producer warp: a token not there
+    static constexpr int big = zer + 2 * kPfTile * 4;   // per tile parity and value producer warp: a scale > kBigScale
+    static constexpr int inv = big + 2 * 4 * 4;         // per tile (u & 3) and value producer warp: a token not there
     static constexpr int xch = inv + 4 * 4 * 4;         // softmax pair exchange: [2][2][128] floats x 2
     static constexpr int lut = xch + 4 * 2 * kPfRows * 4;   // 256 entries x (N pair, rem2/delta pair)
     static constexpr int bars = lut + 256 * 8;
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         for (int i = 0; i < kRing * kPfPages; ++i) mbar_init(bar(i), 1);
         mbar_init(bar(kBarBk), 4);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(kBarBv + b), 4);
+            mbar_init(bar(kBarBv + b), 2);
             mbar_init(bar(kBarS + b), 1);
             mbar_init(bar(kBarP + b), 8);
             mbar_init(bar(kBarO + b), 1);
@@ -186,6 +188,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tc::tmem_alloc<kTmemCols>(sbase + L::taddr);
+    // the flags: two of the four entries per tile are written (two value producer warps)
+    for (int i = tid; i < 2 * 4 + 4 * 4; i += kPfThreads) big_s[i] = 0;  // big and inv are adjacent
     {
         // byte e (codes e & 15, e >> 4) -> (N[e & 15], N[e >> 4]), (rem2/delta[e & 15], rem2/delta[e >> 4])
         uint32_t* lut = reinterpret_cast<uint32_t*>(sm + L::lut);
@@ -314,13 +318,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             }
         }
         __syncwarp();
-    } else if (warp >= 8) {
-        // ================= producers: thread = token of the tile =================
+    } else if (warp >= 8 && warp < 12) {
+        // ================= key producers: thread = token of the tile =================
         const int t = tid - 256;          // token of the tile
         const int j = t >> 4, slot = t & 15;
         const uint32_t* lut = reinterpret_cast<const uint32_t*>(sm + L::lut);
         for (int u = 0; u < U; ++u) {
-            const int half = u & 1;
             const int si = (u & (kRing - 1)) * kPfPages + j;
             pf_wait(bar(si), (u / kRing) & 1, bad);
             const int pok = page_ok[si];
@@ -331,42 +334,55 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
             if (u > 0) pf_wait(bar(kBarS + ((u - 1) & 1)), ((u - 1) >> 1) & 1, bad);
             // the softmax warps use the key operand's space for the query rotation
             else pf_wait(bar(kBarQ), 0, bad);
-            {
-                // 16 code bytes (32 dims) at a time; the loop is not unrolled (nine
-                // warps in three roles share the instruction cache)
+            // 16 code bytes (32 dims) at a time; the loop is not unrolled (the
+            // warps of four roles share the instruction cache)
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 v4 = valid ? lds128(pg + F::kcode + slot * 64 + 16 * c) : make_uint4(0, 0, 0, 0);
-                    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+            for (int c = 0; c < 4; ++c) {
+                const uint4 v4 = valid ? lds128(pg + F::kcode + slot * 64 + 16 * c) : make_uint4(0, 0, 0, 0);
+                const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        // dims 8 dg .. 8 dg + 7 = code bytes 4 dg .. 4 dg + 3 = word q
-                        const int dg = 4 * c + q;
-                        uint32_t nn[4], rr[4];
+                for (int q = 0; q < 4; ++q) {
+                    // dims 8 dg .. 8 dg + 7 = code bytes 4 dg .. 4 dg + 3 = word q
+                    const int dg = 4 * c + q;
+                    uint32_t nn[4], rr[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t e = (w4[q] >> (8 * k)) & 0xFFu;
-                            const uint2 v = valid ? *reinterpret_cast<const uint2*>(lut + 2 * e) : make_uint2(0u, 0u);
-                            nn[k] = v.x;
-                            rr[k] = v.y;
-                        }
-                        sts128(sbase + L::bn + key_chunk(t, dg), nn[0], nn[1], nn[2], nn[3]);
-                        sts128(sbase + L::br + key_chunk(t, dg), rr[0], rr[1], rr[2], rr[3]);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t e = (w4[q] >> (8 * k)) & 0xFFu;
+                        const uint2 v = valid ? *reinterpret_cast<const uint2*>(lut + 2 * e) : make_uint2(0u, 0u);
+                        nn[k] = v.x;
+                        rr[k] = v.y;
                     }
+                    sts128(sbase + L::bn + key_chunk(t, dg), nn[0], nn[1], nn[2], nn[3]);
+                    sts128(sbase + L::br + key_chunk(t, dg), rr[0], rr[1], rr[2], rr[3]);
                 }
-                float gm = 0.f;
-                if (valid) gm = lds_h2f(pg + F::gam + 2 * slot);
-                gam_s[(u & 3) * kPfTile + t] = gm;
-                msk_s[(u & 3) * kPfTile + t] = valid ? 0.f : -INFINITY;
-                const bool any_inv = __any_sync(0xffffffffu, !valid);
-                if (lane == 0) inv_s[(u & 3) * 4 + (warp - 8)] = any_inv ? 1 : 0;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarBk));
+        }
+    } else if (warp >= 13) {
+        // ================= value producers: thread = two tokens of the tile =================
+        // Tokens v and v + 64 of the tile: their value operand rows, scales, zero
+        // points, norms and masks, and the tile's flags (a token not there, a
+        // scale above kBigScale), all written before the arrival on the value
+        // barrier the softmax waits on.
+        const int vw = warp - 13;
+        const int v = tid - 13 * 32;      // 0 .. 63
+        for (int u = 0; u < U; ++u) {
+            const int half = u & 1;
             // ---- values: PV of tile u - 2 has read this value buffer ----
             if (u > 1) pf_wait(bar(kBarO + half), ((u - 2) >> 1) & 1, bad);
-            {
+            bool any_inv = false, bg = false;
+#pragma unroll 1
+            for (int i = 0; i < 2; ++i) {
+                const int t = v + 64 * i;
+                const int j = t >> 4, slot = t & 15;
+                const int si = (u & (kRing - 1)) * kPfPages + j;
+                pf_wait(bar(si), (u / kRing) & 1, bad);
+                const int pok = page_ok[si];
+                const int tok = (t_first + u) * kPfTile + t;
+                const bool valid = pok == 1 && tok <= p_hi && !bad;
+                const uint32_t pg = sbase + L::ring + si * L::stride;
                 constexpr int VROW = D * VB / 8;
                 const uint32_t bvb = sbase + L::bv + half * L::bv_size;
                 if constexpr (VB == 3) {
@@ -409,17 +425,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const Prefill
                         }
                     }
                 }
-                float sc = 0.f, zr = 0.f;
+                float sc = 0.f, zr = 0.f, gm = 0.f;
                 if (valid) {
                     sc = lds_h2f(pg + F::scl + 2 * slot);
                     zr = lds_h2f(pg + F::zer + 2 * slot);
+                    gm = lds_h2f(pg + F::gam + 2 * slot);
                 }
                 scl_s[half * kPfTile + t] = sc;
                 zer_s[half * kPfTile + t] = zr;
+                gam_s[(u & 3) * kPfTile + t] = gm;
+                msk_s[(u & 3) * kPfTile + t] = valid ? 0.f : -INFINITY;
+                any_inv = any_inv || !valid;
                 // a scale above kBigScale makes this tile take the exact max, so
                 // that p * scale (p <= 1 then) stays inside the fp16 range
-                const bool bg = __any_sync(0xffffffffu, sc > kBigScale);
-                if (lane == 0) big_s[half * 4 + (warp - 8)] = bg ? 1 : 0;
+                bg = bg || sc > kBigScale;
+            }
+            any_inv = __any_sync(0xffffffffu, any_inv);
+            bg = __any_sync(0xffffffffu, bg);
+            if (lane == 0) {
+                inv_s[(u & 3) * 4 + vw] = any_inv ? 1 : 0;
+                big_s[half * 4 + vw] = bg ? 1 : 0;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
