@@ -57,14 +57,14 @@ def test_host_codebook_matches_scipy(tq):
 @pytest.mark.parametrize("b", [5, 6, 7, 8])
 def test_wide_key_boundaries_fit_the_encode_grid(tq, b):
     """The tensor-core encode decides keys wider than 4 bits on a grid of
-    128 cells per unit of z = |u| / gamma, each cell holding at most one
+    64 cells per unit of z = |u| / gamma, each cell holding at most one
     positive boundary sqrt(d) t_b: the boundaries (and the first one from 0)
     must lie more than a cell apart, as they do for every d = 128 codebook."""
     cb = tq.Codebook(128, b)
     half = 1 << (b - 1)
     pos = np.sqrt(128.0) * cb.boundaries[half:]
     assert cb.boundaries[half - 1] == 0.0
-    assert np.diff(np.concatenate([[0.0], pos])).min() > 1.0 / 128
+    assert np.diff(np.concatenate([[0.0], pos])).min() > 1.0 / 64
     assert pos[-1] < 16.0  # inside the grid's range
 
 
