@@ -164,6 +164,31 @@ __device__ __forceinline__ void et_store_words(uint8_t* p, const uint32_t (&w)[B
     }
 }
 
+// 32 bytes to global memory at p (32-byte aligned): one store instruction.
+__device__ __forceinline__ void et_stg256(uint8_t* p, const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a[0]), "r"(a[1]), "r"(a[2]),
+                 "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3])
+                 : "memory");
+}
+// The codes of one 32-code chunk c of a row.  An 8-bit chunk is one 32-byte
+// sector: one store when the pool is 32-byte aligned (rows and chunks then are:
+// pages, row offsets and chunk offsets are multiples of 32 B), 3.8 % faster
+// per encode at 8/8 than two 16-byte stores.  Pairing two 4-bit chunks into
+// one such store (the even chunk's words kept until the odd one) was 3 %
+// slower at 4/4, so the other widths store 16, 8 or 4 bytes at a time.
+template <int B>
+__device__ __forceinline__ void et_store_chunk(uint8_t* row, int c, bool a32, const uint32_t (&w)[B]) {
+    if constexpr (B == 8) {
+        if (a32) {
+            const uint32_t lo[4] = {w[0], w[1], w[2], w[3]}, hi[4] = {w[4], w[5], w[6], w[7]};
+            et_stg256(row + 32 * c, lo, hi);
+            return;
+        }
+    }
+    et_store_words<B>(row + c * 4 * B, w);
+}
+
+
 // Codes are formed in the fp32 add pipe rather than with compares, selects and
 // conversions: for |q| < 2^22, q + 1.5 2^23 rounds q to the nearest integer
 // (ties to even) and holds it in its low mantissa bits above the constant
@@ -452,6 +477,8 @@ __global__ void __launch_bounds__(kEtThreads, 1)
     const uint32_t trow = tcol + ((uint32_t)((warp & 3) * 32) << 16);                // this warp's lanes
     const uint32_t done = sbase + LY::bars + 16 * wg, full = done + 8;
     const uint32_t rowbuf = sbase + LY::rows + (uint32_t)((wg * kEtRows + tw) * LY::rs);  // this thread's staged row
+    // 8-bit code rows start on 32-byte boundaries (see et_store_chunk)
+    const bool a32 = ((reinterpret_cast<uintptr_t>(a.pool) | (uintptr_t)g.page_bytes | (uintptr_t)g.vcode_off) & 31u) == 0;
     const int bar_id = 1 + wg;  // named barrier of the warpgroup
     // one operand of `tile` into the buffer (thread 0 of the warpgroup): box j
     // holds coordinates 64 j .. 64 j + 63 of the 128 rows, rows past the last
@@ -575,7 +602,7 @@ __global__ void __launch_bounds__(kEtThreads, 1)
                 uint32_t wk[KB];
                 et_pack_biased<KB>(fk, wk);
                 if constexpr (et_bulk(KB)) et_sts_words<KB>(rowbuf + c * 4 * KB, wk);
-                else if (store) et_store_words<KB>(krow + c * 4 * KB, wk);
+                else if (store) et_store_chunk<KB>(krow, c, a32, wk);
             }
             if constexpr (et_bulk(KB)) {
                 if (store) {
@@ -633,7 +660,7 @@ __global__ void __launch_bounds__(kEtThreads, 1)
                 uint32_t wv[VB];
                 et_pack_biased<VB>(fv, wv);
                 if constexpr (et_bulk(VB)) et_sts_words<VB>(rowbuf + c * 4 * VB, wv);
-                else if (store) et_store_words<VB>(vrow + c * 4 * VB, wv);
+                else if (store) et_store_chunk<VB>(vrow, c, a32, wv);
             }
             if constexpr (et_bulk(VB)) {
                 if (store) {
