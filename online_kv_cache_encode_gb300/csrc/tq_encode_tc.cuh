@@ -96,6 +96,23 @@ __device__ __forceinline__ void et_bulk_commit() { asm volatile("cp.async.bulk.c
 __device__ __forceinline__ void et_bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void et_bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Rows of 1 to 3 bits are stored a group of chunks at a time: 1 bit, the whole
+// 16-byte row; 2 bits, two chunks (16 bytes); 3 bits, two chunks (24 bytes, as
+// three 8-byte stores).  Rows are 16 B per code bit on 16-byte aligned pages,
+// so each group starts 16-byte (1, 2 bits) or 8-byte (3 bits) aligned.  At 3/3
+// this took 43.8 -> 39.2 us per encode against one 4- or 8-byte store per word.
+__host__ __device__ constexpr int et_group(int B) { return B == 1 ? 4 : 2; }
+template <int B>
+__device__ __forceinline__ void et_store_group(uint8_t* p, const uint32_t (&w)[et_group(B) * B]) {
+    if constexpr (B == 3) {
+        reinterpret_cast<uint2*>(p)[0] = make_uint2(w[0], w[1]);
+        reinterpret_cast<uint2*>(p)[1] = make_uint2(w[2], w[3]);
+        reinterpret_cast<uint2*>(p)[2] = make_uint2(w[4], w[5]);
+    } else {
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // B words to shared memory at a (4-byte aligned; 8-byte when B is even,
 // 16-byte when B % 4 == 0)
 template <int B>
@@ -581,8 +598,8 @@ __global__ void __launch_bounds__(kEtThreads, 1)
             if constexpr (KB > 4) fast = !grid_bad && gamma > 1e-30f && ig16 < 3.0e38f;
             // the staged row's last bulk copy (the previous tile's values) has read it
             if constexpr (et_bulk(KB)) et_bulk_wait_read();
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            // the packed key words of chunk c
+            auto key_chunk = [&](int c, uint32_t (&wk)[KB]) {
                 et_load32(trow + 32 * c, x);
                 uint32_t fk[32];
                 if (fast) {
@@ -599,10 +616,31 @@ __global__ void __launch_bounds__(kEtThreads, 1)
                         fk[j] = kEtMagicBits + (uint32_t)code;
                     }
                 }
-                uint32_t wk[KB];
                 et_pack_biased<KB>(fk, wk);
-                if constexpr (et_bulk(KB)) et_sts_words<KB>(rowbuf + c * 4 * KB, wk);
-                else if (store) et_store_chunk<KB>(krow, c, a32, wk);
+            };
+            if constexpr (KB <= 3) {
+                // narrow rows: a group of chunks per step, stored in wider pieces
+                constexpr int NG = et_group(KB);
+#pragma unroll 1
+                for (int c = 0; c < 4; c += NG) {
+                    uint32_t wg_[NG * KB];
+#pragma unroll
+                    for (int h = 0; h < NG; ++h) {
+                        uint32_t wk[KB];
+                        key_chunk(c + h, wk);
+#pragma unroll
+                        for (int i = 0; i < KB; ++i) wg_[h * KB + i] = wk[i];
+                    }
+                    if (store) et_store_group<KB>(krow + 4 * KB * c, wg_);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t wk[KB];
+                    key_chunk(c, wk);
+                    if constexpr (et_bulk(KB)) et_sts_words<KB>(rowbuf + c * 4 * KB, wk);
+                    else if (store) et_store_chunk<KB>(krow, c, a32, wk);
+                }
             }
             if constexpr (et_bulk(KB)) {
                 if (store) {
@@ -652,15 +690,35 @@ __global__ void __launch_bounds__(kEtThreads, 1)
             uint8_t* vrow = page + g.vcode_off + off * (D * VB / 8);
             // the staged row's key copy has read it
             if constexpr (et_bulk(VB)) et_bulk_wait_read();
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            // the packed value words of chunk c
+            auto value_chunk = [&](int c, uint32_t (&wv)[VB]) {
                 et_load32(trow + 32 * c, x);
                 uint32_t fv[32];
                 et_value_codes<VB>(x, mn, scale, rs, fv);
-                uint32_t wv[VB];
                 et_pack_biased<VB>(fv, wv);
-                if constexpr (et_bulk(VB)) et_sts_words<VB>(rowbuf + c * 4 * VB, wv);
-                else if (store) et_store_chunk<VB>(vrow, c, a32, wv);
+            };
+            if constexpr (VB <= 3) {
+                constexpr int NG = et_group(VB);
+#pragma unroll 1
+                for (int c = 0; c < 4; c += NG) {
+                    uint32_t wg_[NG * VB];
+#pragma unroll
+                    for (int h = 0; h < NG; ++h) {
+                        uint32_t wv[VB];
+                        value_chunk(c + h, wv);
+#pragma unroll
+                        for (int i = 0; i < VB; ++i) wg_[h * VB + i] = wv[i];
+                    }
+                    if (store) et_store_group<VB>(vrow + 4 * VB * c, wg_);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t wv[VB];
+                    value_chunk(c, wv);
+                    if constexpr (et_bulk(VB)) et_sts_words<VB>(rowbuf + c * 4 * VB, wv);
+                    else if (store) et_store_chunk<VB>(vrow, c, a32, wv);
+                }
             }
             if constexpr (et_bulk(VB)) {
                 if (store) {

@@ -180,3 +180,54 @@ def test_bulk_encode_structured_rows(tq, oracle, kb, vb):
     assert set(np.unique(fg["v"][rows(17)])) <= {0, (1 << vb) - 1}
     # one coordinate: every rotated coordinate has one magnitude, so one code per sign
     assert all(len(np.unique(r)) <= 2 for r in fg["k"][rows(15)])
+
+
+@pytest.mark.parametrize("kb,vb", [(5, 7), (6, 6), (8, 8), (3, 1)])
+def test_bulk_encode_leaves_other_bytes(tq, oracle, kb, vb):
+    """Every width's code stores (direct, 32-byte, or staged rows written by
+    one bulk copy each) write exactly the slots they encode: a pool of 0xAB
+    keeps every byte outside them, skipped tokens (slot -1) included, and the
+    written rows match the oracle's."""
+    import torch
+    dev = "cuda"
+    n = _bulk_tokens(8)
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(n,), hkv=8, hq=16, key_bits=kb, value_bits=vb)
+    K = W.kv_tokens(w, 0, 0, 0, n)
+    V = W.kv_tokens(w, 1, 0, 0, n)
+    bt = W.block_table(w)
+    nb = w.num_blocks()
+    slots = W.slots(w, bt, 0, 0, n).copy()
+    skipped = np.arange(5, n, 97)
+    slots[skipped] = -1
+    gc = tq.Cache(nb, w.hkv, kb, vb, 0, w.seed, w.block_size, w.d)
+    gc.pool.fill_(0xAB)
+    st = tq.new_status()
+    gc.encode(torch.from_numpy(K).to(dev, torch.bfloat16), torch.from_numpy(V).to(dev, torch.bfloat16),
+              torch.from_numpy(slots).to(dev), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    oc = oracle.Cache(w.d, kb, vb, 0, w.block_size, w.hkv, nb, w.seed)
+    pool_o = oc.new_pool()
+    pool_o[:] = 0xAB
+    oc.encode(K, V, slots, pool_o)
+    pool_g = gc.pool.cpu().numpy()
+    L = parity.Layout(w.d, kb, vb, 0, w.block_size, w.hkv, oc.page_bytes)
+    written = slots >= 0
+    all_slots = np.repeat(slots[written], w.hkv)
+    all_heads = np.tile(np.arange(w.hkv), int(written.sum()))
+    # outside the written slots both pools hold the fill byte
+    mask = np.ones(pool_g.size, dtype=bool)
+    page = (all_slots // L.bs * L.hkv + all_heads) * L.page_bytes
+    for base, nbytes in [(L.k, w.d * kb // 8), (L.v, w.d * vb // 8), (L.g, 2), (L.s, 2), (L.z, 2)]:
+        idx = (page + base + (all_slots % L.bs) * nbytes)[:, None] + np.arange(nbytes)[None, :]
+        mask[idx.ravel()] = False
+    assert np.all(pool_g[mask] == 0xAB)
+    assert np.all(pool_o[mask] == 0xAB)
+    fo = parity.unpack(pool_o, L, all_slots, all_heads)
+    fg = parity.unpack(pool_g, L, all_slots, all_heads)
+    kin = K[written].reshape(-1, w.d).astype(np.float64)
+    vin = V[written].reshape(-1, w.d).astype(np.float64)
+    enc = parity.compare_encode(fo, fg, kin, vin, oc, oracle)
+    enc["status_oracle"], enc["status_gpu"] = 0, 0
+    enc["other_bytes_equal"] = True
+    parity.assert_encode_parity(dict(enc=enc))
