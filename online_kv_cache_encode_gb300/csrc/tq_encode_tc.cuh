@@ -96,22 +96,6 @@ __device__ __forceinline__ void et_bulk_commit() { asm volatile("cp.async.bulk.c
 __device__ __forceinline__ void et_bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void et_bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Rows of 1 to 3 bits are stored a group of chunks at a time: 1 bit, the whole
-// 16-byte row; 2 bits, two chunks (16 bytes); 3 bits, two chunks (24 bytes, as
-// three 8-byte stores).  Rows are 16 B per code bit on 16-byte aligned pages,
-// so each group starts 16-byte (1, 2 bits) or 8-byte (3 bits) aligned.  At 3/3
-// this took 43.8 -> 39.2 us per encode against one 4- or 8-byte store per word.
-__host__ __device__ constexpr int et_group(int B) { return B == 1 ? 4 : 2; }
-template <int B>
-__device__ __forceinline__ void et_store_group(uint8_t* p, const uint32_t (&w)[et_group(B) * B]) {
-    if constexpr (B == 3) {
-        reinterpret_cast<uint2*>(p)[0] = make_uint2(w[0], w[1]);
-        reinterpret_cast<uint2*>(p)[1] = make_uint2(w[2], w[3]);
-        reinterpret_cast<uint2*>(p)[2] = make_uint2(w[4], w[5]);
-    } else {
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
 
 // B words to shared memory at a (4-byte aligned; 8-byte when B is even,
 // 16-byte when B % 4 == 0)
@@ -190,9 +174,8 @@ __device__ __forceinline__ void et_stg256(uint8_t* p, const uint32_t (&a)[4], co
 // The codes of one 32-code chunk c of a row.  An 8-bit chunk is one 32-byte
 // sector: one store when the pool is 32-byte aligned (rows and chunks then are:
 // pages, row offsets and chunk offsets are multiples of 32 B), 3.8 % faster
-// per encode at 8/8 than two 16-byte stores.  Pairing two 4-bit chunks into
-// one such store (the even chunk's words kept until the odd one) was 3 %
-// slower at 4/4, so the other widths store 16, 8 or 4 bytes at a time.
+// per encode at 8/8 than two 16-byte stores.  Other widths stored chunk by
+// chunk take 16, 8 or 4 bytes at a time.
 template <int B>
 __device__ __forceinline__ void et_store_chunk(uint8_t* row, int c, bool a32, const uint32_t (&w)[B]) {
     if constexpr (B == 8) {
@@ -203,6 +186,33 @@ __device__ __forceinline__ void et_store_chunk(uint8_t* row, int c, bool a32, co
         }
     }
     et_store_words<B>(row + c * 4 * B, w);
+}
+
+// Rows of 1 to 4 bits are stored a group of chunks at a time: 1 bit, the whole
+// 16-byte row; 2 bits, two chunks (16 bytes); 3 bits, two chunks (24 bytes, as
+// three 8-byte stores); 4 bits, two chunks (one 32-byte store when the pool is
+// 32-byte aligned).  Rows are 16 B per code bit on 16-byte aligned pages, so
+// each group starts 16-byte (1, 2 bits), 8-byte (3 bits) or 32-byte (4 bits,
+// aligned pool) aligned.  At 3/3 this took 43.8 -> 39.2 us per encode against
+// one 4- or 8-byte store per word.
+__host__ __device__ constexpr int et_group(int B) { return B == 1 ? 4 : 2; }
+template <int B>
+__device__ __forceinline__ void et_store_group(uint8_t* p, const uint32_t (&w)[et_group(B) * B], bool a32) {
+    if constexpr (B == 4) {
+        const uint32_t lo[4] = {w[0], w[1], w[2], w[3]}, hi[4] = {w[4], w[5], w[6], w[7]};
+        if (a32) {
+            et_stg256(p, lo, hi);
+        } else {
+            *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(p + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    } else if constexpr (B == 3) {
+        reinterpret_cast<uint2*>(p)[0] = make_uint2(w[0], w[1]);
+        reinterpret_cast<uint2*>(p)[1] = make_uint2(w[2], w[3]);
+        reinterpret_cast<uint2*>(p)[2] = make_uint2(w[4], w[5]);
+    } else {
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
 }
 
 
@@ -618,7 +628,7 @@ __global__ void __launch_bounds__(kEtThreads, 1)
                 }
                 et_pack_biased<KB>(fk, wk);
             };
-            if constexpr (KB <= 3) {
+            if constexpr (KB <= 4) {
                 // narrow rows: a group of chunks per step, stored in wider pieces
                 constexpr int NG = et_group(KB);
 #pragma unroll 1
@@ -631,7 +641,7 @@ __global__ void __launch_bounds__(kEtThreads, 1)
 #pragma unroll
                         for (int i = 0; i < KB; ++i) wg_[h * KB + i] = wk[i];
                     }
-                    if (store) et_store_group<KB>(krow + 4 * KB * c, wg_);
+                    if (store) et_store_group<KB>(krow + 4 * KB * c, wg_, a32);
                 }
             } else {
 #pragma unroll 1
@@ -697,7 +707,7 @@ __global__ void __launch_bounds__(kEtThreads, 1)
                 et_value_codes<VB>(x, mn, scale, rs, fv);
                 et_pack_biased<VB>(fv, wv);
             };
-            if constexpr (VB <= 3) {
+            if constexpr (VB <= 4) {
                 constexpr int NG = et_group(VB);
 #pragma unroll 1
                 for (int c = 0; c < 4; c += NG) {
@@ -709,7 +719,7 @@ __global__ void __launch_bounds__(kEtThreads, 1)
 #pragma unroll
                         for (int i = 0; i < VB; ++i) wg_[h * VB + i] = wv[i];
                     }
-                    if (store) et_store_group<VB>(vrow + 4 * VB * c, wg_);
+                    if (store) et_store_group<VB>(vrow + 4 * VB * c, wg_, a32);
                 }
             } else {
 #pragma unroll 1
