@@ -231,3 +231,32 @@ def test_bulk_encode_leaves_other_bytes(tq, oracle, kb, vb):
     enc["status_oracle"], enc["status_gpu"] = 0, 0
     enc["other_bytes_equal"] = True
     parity.assert_encode_parity(dict(enc=enc))
+
+
+@pytest.mark.parametrize("kb,vb", [(4, 4), (8, 8), (4, 2)])
+def test_bulk_encode_pool_16_byte_aligned(tq, oracle, kb, vb):
+    """A pool that is 16-byte but not 32-byte aligned (the API asks for 16):
+    the 4- and 8-bit rows fall back from 32-byte to 16-byte stores and the
+    pool bytes come out the same as on an aligned pool."""
+    import torch
+    dev = "cuda"
+    n = _bulk_tokens(8)
+    w = W.scaled(W.WORKLOADS["gqa32k"], lens=(n,), hkv=8, hq=16, key_bits=kb, value_bits=vb)
+    K = torch.from_numpy(W.kv_tokens(w, 0, 0, 0, n)).to(dev, torch.bfloat16)
+    V = torch.from_numpy(W.kv_tokens(w, 1, 0, 0, n)).to(dev, torch.bfloat16)
+    bt = W.block_table(w)
+    nb = w.num_blocks()
+    slots = torch.from_numpy(W.slots(w, bt, 0, 0, n)).to(dev)
+    a = tq.Cache(nb, w.hkv, kb, vb, 0, w.seed, w.block_size, w.d)
+    nbytes = a.pool.numel()
+    big = torch.zeros(nbytes + 64, dtype=torch.uint8, device=dev)
+    assert big.data_ptr() % 32 == 0
+    b = tq.Cache(nb, w.hkv, kb, vb, 0, w.seed, w.block_size, w.d, pool=big[16:16 + nbytes])
+    assert b.pool.data_ptr() % 32 == 16
+    st = tq.new_status()
+    a.encode(K, V, slots, st)
+    b.encode(K, V, slots, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(a.pool, b.pool)
+    assert torch.all(big[:16] == 0) and torch.all(big[16 + nbytes:] == 0)
